@@ -1,0 +1,258 @@
+"""ctypes front end of the C oracle (``wmtp_oracle.c``).
+
+Test infrastructure only; see the package docstring.  Each wrapper names the
+passage of "Windowed-MTP: Removing the Full-Context Draft-KV Tax at
+Million-Token Context" (arXiv 2607.21535) that the C function follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+ORC_OK = 0
+ORC_EINVAL = -1
+ORC_ECAPACITY = -2
+ORC_EBOUNDS = -4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "wmtp_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C11, -O2, OpenMP over output rows).
+
+    No -ffast-math: every floating-point operation keeps the order written in
+    the C source.
+    """
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-fopenmp", "-fPIC",
+               "-shared", "-Wall", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        lib.orc_num_threads.restype = ctypes.c_int
+        lib.orc_keep.restype = _i64
+        lib.orc_keep.argtypes = [_i64, _i64, _i64, ctypes.c_int, _i64p]
+        lib.orc_ring_slot.restype = _i64
+        lib.orc_ring_slot.argtypes = [_i64] * 7
+        lib.orc_ring_map.restype = ctypes.c_int
+        lib.orc_ring_map.argtypes = [_i32p, _i32p, _i32p, _i32p, _i64, _i64,
+                                     _i64, _i64, _i64, _i32p]
+        lib.orc_build_draft_indices.restype = ctypes.c_int
+        lib.orc_build_draft_indices.argtypes = [
+            _i32p, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
+            _i32p, _i32p, _i64, _i32p, _i32p, _i64, _i32p]
+        lib.orc_append_kv.restype = ctypes.c_int
+        lib.orc_append_kv.argtypes = [_u16p, _u16p, _i32p, _i64, _i64, _i64,
+                                      _u16p, _u16p, _i64]
+        lib.orc_draft_decode_attn.restype = ctypes.c_int
+        lib.orc_draft_decode_attn.argtypes = [
+            _u16p, _i64, _i64, _i64, _i64, _i64, _u16p, _u16p, _i64, _i32p,
+            _i64, _i32p, ctypes.c_double, _i64p, _i64, _f64p, _f64p, _f64p,
+            _i64, ctypes.c_int]
+        lib.orc_tree_draft_attn.restype = ctypes.c_int
+        lib.orc_tree_draft_attn.argtypes = [
+            _u16p, _i64, _i64, _i64, _i64, _u16p, _u16p, _i64, _i32p, _i32p,
+            _i64, _i64, _i64, _i64, ctypes.c_double, _i64p, _i64, _f64p,
+            _f64p, ctypes.c_int]
+        lib.orc_acceptance_length.restype = ctypes.c_double
+        lib.orc_acceptance_length.argtypes = [_f64p, _i64, _f64p]
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray | None, ctype):
+    if a is None:
+        return ctypes.cast(None, ctypes.POINTER(ctype))
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _as(a, dtype) -> np.ndarray | None:
+    if a is None:
+        return None
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def _check(status: int, what: str) -> None:
+    if status != ORC_OK:
+        raise ValueError(f"oracle {what} failed with status {status}")
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops use by default."""
+    return int(_load().orc_num_threads())
+
+
+def keep(s_kv: int, n_sink: int, window: int, windowed: bool = True) -> np.ndarray:
+    """Positions a draft step with kv length ``s_kv`` attends (App. A
+    pseudocode): sinks then the last ``window`` positions, or all of them."""
+    lib = _load()
+    n = lib.orc_keep(s_kv, n_sink, window, int(windowed), None)
+    out = np.empty(max(n, 0), dtype=np.int64)
+    lib.orc_keep(s_kv, n_sink, window, int(windowed), _ptr(out, ctypes.c_int64))
+    return out
+
+
+def ring_slot(ring_base: int, p: int, branch: int, n_sink: int, window: int,
+              depth: int, tree_k: int = 1) -> int:
+    """Ring slot of logical position ``p`` (App. A; §7 tree sizing)."""
+    return int(_load().orc_ring_slot(ring_base, p, branch, n_sink, window,
+                                     depth, tree_k))
+
+
+def ring_map(ring_base, pos, req_of, n_sink, window, depth, tree_k=1,
+             branch=None) -> np.ndarray:
+    """Vector form of :func:`ring_slot` over (request, position, branch)."""
+    rb = _as(ring_base, np.int32)
+    p = _as(pos, np.int32)
+    r = _as(req_of, np.int32)
+    br = _as(branch, np.int32)
+    out = np.empty(p.shape[0], dtype=np.int32)
+    _check(_load().orc_ring_map(_ptr(rb, ctypes.c_int32), _ptr(p, ctypes.c_int32),
+                                _ptr(br, ctypes.c_int32), _ptr(r, ctypes.c_int32),
+                                p.shape[0], n_sink, window, depth, tree_k,
+                                _ptr(out, ctypes.c_int32)), "ring_map")
+    return out
+
+
+def build_draft_indices(seq_lens, gamma, n_sink, window, depth, tree_k=1,
+                        windowed=True, req_to_token=None, req_pool_idx=None,
+                        ring_base=None, stride=None):
+    """Draft KV-index tables for ``gamma`` draft steps (§4 Mechanism; App. A).
+
+    Returns ``(table[gamma, B, stride] int32, lens[gamma, B] int32)``; entries
+    past ``lens`` are left at -1.
+    """
+    sl = _as(seq_lens, np.int32)
+    B = sl.shape[0]
+    rtt = _as(req_to_token, np.int32)
+    rpi = _as(req_pool_idx, np.int32)
+    rb = _as(ring_base, np.int32)
+    if rtt is not None and rpi is None:
+        rpi = np.arange(B, dtype=np.int32)
+    if stride is None:
+        stride = max([int(len(keep(int(s) + j + 1, n_sink, window, windowed)))
+                      for s in sl for j in range(gamma)] + [1])
+    table = np.full((gamma, B, stride), -1, dtype=np.int32)
+    lens = np.zeros((gamma, B), dtype=np.int32)
+    rtt_stride = rtt.shape[1] if rtt is not None else 0
+    _check(_load().orc_build_draft_indices(
+        _ptr(sl, ctypes.c_int32), B, gamma, n_sink, window, depth, tree_k,
+        int(windowed), _ptr(rtt, ctypes.c_int32), _ptr(rpi, ctypes.c_int32),
+        rtt_stride, _ptr(rb, ctypes.c_int32), _ptr(table, ctypes.c_int32),
+        stride, _ptr(lens, ctypes.c_int32)), "build_draft_indices")
+    return table, lens
+
+
+def append_kv(k_new, v_new, slots, k_pool, v_pool) -> None:
+    """Copy each new token's K/V rows into pool slot ``slots[i]`` (in place)."""
+    kn = _as(k_new, np.uint16)
+    vn = _as(v_new, np.uint16)
+    sl = _as(slots, np.int32)
+    assert k_pool.dtype == np.uint16 and k_pool.flags["C_CONTIGUOUS"]
+    assert v_pool.dtype == np.uint16 and v_pool.flags["C_CONTIGUOUS"]
+    n, H_kv, D = kn.shape
+    _check(_load().orc_append_kv(_ptr(kn, ctypes.c_uint16), _ptr(vn, ctypes.c_uint16),
+                                 _ptr(sl, ctypes.c_int32), n, H_kv, D,
+                                 _ptr(k_pool, ctypes.c_uint16),
+                                 _ptr(v_pool, ctypes.c_uint16), k_pool.shape[0]),
+           "append_kv")
+
+
+def draft_decode_attn(q, k_pool, v_pool, table, lens, scale, rows=None,
+                      nthreads=None):
+    """fp64 softmax attention over a block table (§4 Mechanism).
+
+    q: [B, n_q, H_q, D] bf16 bits; k_pool/v_pool: [num_slots, H_kv, D] bf16
+    bits; table: [B, stride] int32; lens: [B].  ``rows`` optionally selects
+    flattened (b*n_q + t)*H_q + h rows; the others come back as NaN.
+    Returns ``(out[B, n_q, H_q, D] float64, lse[B, n_q, H_q] float64)``.
+    """
+    q = _as(q, np.uint16)
+    kp = _as(k_pool, np.uint16)
+    vp = _as(v_pool, np.uint16)
+    tb = _as(table, np.int32)
+    ln = _as(lens, np.int32)
+    B, n_q, H_q, D = q.shape
+    num_slots, H_kv, _ = kp.shape
+    rws = _as(rows, np.int64)
+    nthreads = nthreads or num_threads()
+    out = np.full((B, n_q, H_q, D), np.nan, dtype=np.float64)
+    lse = np.full((B, n_q, H_q), np.nan, dtype=np.float64)
+    scratch_len = max(int(ln.max()) if ln.size else 0, 1)
+    scratch = np.empty(scratch_len * nthreads, dtype=np.float64)
+    _check(_load().orc_draft_decode_attn(
+        _ptr(q, ctypes.c_uint16), B, n_q, H_q, H_kv, D, _ptr(kp, ctypes.c_uint16),
+        _ptr(vp, ctypes.c_uint16), num_slots, _ptr(tb, ctypes.c_int32),
+        tb.shape[-1], _ptr(ln, ctypes.c_int32), float(scale),
+        _ptr(rws, ctypes.c_int64), 0 if rws is None else rws.shape[0],
+        _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double),
+        _ptr(scratch, ctypes.c_double), scratch_len, nthreads),
+        "draft_decode_attn")
+    return out, lse
+
+
+def tree_draft_attn(q, k_pool, v_pool, seq_lens, ring_base, n_sink, window,
+                    depth, tree_k, scale, rows=None, nthreads=None):
+    """fp64 tree-draft attention over the ring (§7 tree speculation).
+
+    q: [B, tree_k*depth, H_q, D]; node t = branch*depth + i.
+    Returns ``(out float64, lse float64)`` shaped like q without / with D.
+    """
+    q = _as(q, np.uint16)
+    kp = _as(k_pool, np.uint16)
+    vp = _as(v_pool, np.uint16)
+    sl = _as(seq_lens, np.int32)
+    rb = _as(ring_base, np.int32)
+    B, n_nodes, H_q, D = q.shape
+    assert n_nodes == tree_k * depth
+    num_slots, H_kv, _ = kp.shape
+    rws = _as(rows, np.int64)
+    nthreads = nthreads or num_threads()
+    out = np.full((B, n_nodes, H_q, D), np.nan, dtype=np.float64)
+    lse = np.full((B, n_nodes, H_q), np.nan, dtype=np.float64)
+    _check(_load().orc_tree_draft_attn(
+        _ptr(q, ctypes.c_uint16), B, H_q, H_kv, D, _ptr(kp, ctypes.c_uint16),
+        _ptr(vp, ctypes.c_uint16), num_slots, _ptr(sl, ctypes.c_int32),
+        _ptr(rb, ctypes.c_int32), n_sink, window, depth, tree_k, float(scale),
+        _ptr(rws, ctypes.c_int64), 0 if rws is None else rws.shape[0],
+        _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double), nthreads),
+        "tree_draft_attn")
+    return out, lse
+
+
+def acceptance_length(hist):
+    """(alpha[1..gamma], AL) from an acceptance histogram (§5, Eq. 4)."""
+    h = _as(hist, np.float64)
+    gamma = h.shape[0] - 1
+    alpha = np.zeros(max(gamma, 0), dtype=np.float64)
+    al = _load().orc_acceptance_length(_ptr(h, ctypes.c_double), gamma,
+                                       _ptr(alpha, ctypes.c_double))
+    return alpha, float(al)
