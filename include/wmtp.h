@@ -1,0 +1,194 @@
+/*
+ * wmtp.h -- C ABI of the GB300 (sm_103a) library for the Windowed-MTP draft
+ * attention hot path.
+ *
+ * Method: "Windowed-MTP: Removing the Full-Context Draft-KV Tax at
+ * Million-Token Context" (arXiv 2607.21535).  The MTP/NEXTN draft head's
+ * decode attention reads only [n_sink sink positions] || [the most recent W
+ * positions] of the KV cache (§4 "Method", Mechanism), and the draft KV lives
+ * in a compact per-request ring of n_sink + W + d*k slots (App. A "The
+ * windowing change"; §6 Memory; §7 "Compatibility with tree speculation").
+ *
+ * Conventions shared by every call:
+ *   - All pointers marked "device" point to memory of the current CUDA device;
+ *     the caller owns every buffer.  The library allocates nothing and never
+ *     synchronises; every call is asynchronous on `stream` (a cudaStream_t,
+ *     NULL = the legacy default stream) and may be captured in a CUDA graph.
+ *   - bf16 values travel as their 16-bit patterns (uint16_t).
+ *   - Positions and slots are 0-based.  A request's KV pool has the layout
+ *     [num_slots][H_kv][D]: the K (or V) row of KV head g for slot s starts at
+ *     element (s * H_kv + g) * D.
+ *   - Host-side argument checks run before any launch and return
+ *     WMTP_EINVAL / WMTP_ECAPACITY without touching memory.  A failed launch
+ *     returns WMTP_ECUDA.  Checks that need device data (a slot outside the
+ *     pool, a table longer than its row) are done in the kernels: the access is
+ *     skipped, the first such error code is latched in a device word, and
+ *     wmtp_get_device_error() returns it.  No kernel traps or spins without a
+ *     time limit.
+ *   - Draft depth d = gamma + 1 ("Windowed-MTP", §3 Eq. (1): d is the engine's
+ *     num_draft_tokens and gamma = d - 1 draft forwards per decode step);
+ *     tree_k = 1 is a chain.
+ */
+#ifndef WMTP_H
+#define WMTP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t wmtp_status;
+
+#define WMTP_OK 0
+#define WMTP_EINVAL (-1)     /* bad argument (null pointer, bad size, bad config) */
+#define WMTP_ECAPACITY (-2)  /* an output or workspace is too small */
+#define WMTP_ECUDA (-3)      /* a CUDA launch or runtime call failed */
+#define WMTP_EDEVICE (-4)    /* wmtp_get_device_error(): a device-side check failed */
+
+/* Device-side error codes latched by the kernels (first one wins). */
+#define WMTP_DEV_OK 0
+#define WMTP_DEV_SLOT_RANGE 1    /* a slot index outside [0, num_slots) */
+#define WMTP_DEV_TABLE_OVERFLOW 2 /* a table row needs more than `stride` entries */
+#define WMTP_DEV_LEN_RANGE 3     /* a lens[] entry is negative or above the row stride */
+#define WMTP_DEV_WAIT_TIMEOUT 4  /* a pipeline wait ran out of time; results invalid */
+#define WMTP_DEV_ARG_RANGE 5     /* a device-side position, branch or length is out of range */
+
+/* Library version, e.g. 1000 for 0.1.0. */
+int32_t wmtp_version(void);
+
+/* Short English text for a wmtp_status or a device error code. */
+const char *wmtp_status_string(int32_t status);
+
+/* Reads (and, if `clear` is non-zero, resets) the device error word of the
+ * current device.  Synchronises the device.  *code receives a WMTP_DEV_* code.
+ * Returns WMTP_OK, or WMTP_ECUDA if the copy failed. */
+wmtp_status wmtp_get_device_error(int32_t *code, int32_t clear);
+
+/* ------------------------------------------------------------------------
+ * Draft KV-index builder.
+ * "Windowed-MTP", App. A "The windowing change (pseudocode)" and §4
+ * Mechanism: for draft step j (0 <= j < gamma) of request b the draft sees
+ * kv_len = seq_lens[b] + j + 1 positions (its own token appended before it
+ * attends).  Windowed mode (windowed != 0) and kv_len > n_sink + W:
+ * positions [0, n_sink) then [kv_len - W, kv_len); otherwise (or full mode)
+ * positions [0, kv_len).  Each position p becomes a physical slot:
+ *   paged layout (req_to_token != NULL): req_to_token[req_pool_idx[b] *
+ *     rtt_stride + p] (req_pool_idx == NULL means request b uses row b);
+ *   ring layout  (req_to_token == NULL): the ring slot of p on branch 0
+ *     (see wmtp_ring_map) for ring_base[b].
+ *
+ * seq_lens      device int32 [B]: committed length S of each request.
+ * table         device int32 [gamma][B][stride], written for i < lens only.
+ * lens          device int32 [gamma][B]: entries written per row.
+ * depth, tree_k ring geometry (used by the ring layout only).
+ * Errors: WMTP_EINVAL for null pointers, B < 0, gamma < 0, n_sink < 0,
+ * W < 1, depth < 1, tree_k < 1, stride < 1 or gamma * B > 65535.
+ * Row lengths depend on device data, so capacity is checked in the kernel:
+ * a row that needs more than `stride` entries writes `stride` entries,
+ * stores its true length in lens and latches WMTP_DEV_TABLE_OVERFLOW. */
+wmtp_status wmtp_build_draft_indices(const int32_t *seq_lens, int32_t B,
+                                     int32_t gamma, int32_t n_sink,
+                                     int32_t window, int32_t depth,
+                                     int32_t tree_k, int32_t windowed,
+                                     const int32_t *req_to_token,
+                                     const int32_t *req_pool_idx,
+                                     int64_t rtt_stride,
+                                     const int32_t *ring_base, int32_t *table,
+                                     int64_t stride, int32_t *lens,
+                                     void *stream);
+
+/* ------------------------------------------------------------------------
+ * Ring slot mapper.
+ * "Windowed-MTP", App. A: slot = ring_base(r) + logical position, with a
+ * ring of n_sink + W + d slots per request; §7: a tree of width k reserves
+ * n_sink + W + d*k and its candidates diverge only over the last d positions.
+ * This library pins the sink slots and rolls the rest:
+ *   branch == 0 and p < n_sink : ring_base + p
+ *   otherwise                  : ring_base + n_sink
+ *                                + ((p - n_sink + branch * d) mod (W + d*k))
+ * (non-negative modulo).  Below n_sink + W + d*k this equals the pages'
+ * literal ring_base + p; above it, live sinks are never overwritten.
+ *
+ * ring_base device int32 [number of requests]; pos, req_of device int32 [n];
+ * branch device int32 [n] or NULL (all 0); slots device int32 [n] (output).
+ * Errors: WMTP_EINVAL for null pointers, n < 0, n_sink < 0, W < 1, depth < 1,
+ * tree_k < 1. */
+wmtp_status wmtp_ring_map(const int32_t *ring_base, const int32_t *pos,
+                          const int32_t *branch, const int32_t *req_of,
+                          int32_t n, int32_t n_sink, int32_t window,
+                          int32_t depth, int32_t tree_k, int32_t *slots,
+                          void *stream);
+
+/* ------------------------------------------------------------------------
+ * Draft KV append: each draft forward writes its own token's K and V before
+ * attending ("Windowed-MTP", §3: the draft re-reads the cache it extends).
+ * Copies k_new[i] and v_new[i] (each [H_kv][D] bf16) into pool slot
+ * slots[i].  k_new, v_new device bf16 [n][H_kv][D]; slots device int32 [n];
+ * k_pool, v_pool device bf16 [num_slots][H_kv][D].
+ * A slot outside [0, num_slots) is skipped and latches WMTP_DEV_SLOT_RANGE.
+ * Errors: WMTP_EINVAL for null pointers, n < 0, H_kv < 1, D < 1, D % 8 != 0
+ * or pointers not 16-byte aligned. */
+wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
+                           const int32_t *slots, int32_t n, int32_t H_kv,
+                           int32_t D, uint16_t *k_pool, uint16_t *v_pool,
+                           int64_t num_slots, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Split-KV flash-decode draft attention with a log-sum-exp merge.
+ * Computes, for every request b, query token t < n_q and query head h
+ * (KV head g = h / (H_q / H_kv)), softmax attention over the keys listed in
+ * table row b ("Windowed-MTP", §4 Mechanism: the reduced table is the key
+ * set, no extra mask):
+ *   s_i = scale * <q[b,t,h,:], K[table[b,i], g, :]>,  i < lens[b]
+ *   out[b,t,h,:] = sum_i softmax(s)_i V[table[b,i], g, :]
+ *   lse[b,t,h]   = log sum_i exp(s_i)        (natural log)
+ * Each row is cut into n_split contiguous chunks whose size depends only on
+ * lens[b] and n_split, so results depend on the logical key order and not
+ * on the physical slots.  Partials (o, lse) are merged in split order.
+ * An empty row gives out = 0, lse = -inf.
+ *
+ * q        device bf16 [B][n_q][H_q][D], D in {128, 256}, H_q / H_kv <= 8.
+ * table    device int32, row b at table + b * table_stride.
+ * lens     device int32 [B]; each must be <= table_stride.
+ * out      device fp32 [B][n_q][H_q][D];  lse device fp32 [B][n_q][H_q] or NULL.
+ * workspace device, >= wmtp_attn_workspace_bytes(...) bytes, 256-byte
+ *          aligned.  Its first bytes hold one merge counter per (request,
+ *          query token, KV head); they must be zero when a call starts.
+ *          wmtp_attn_workspace_init() zeroes them, and every completed call
+ *          leaves its own counters at zero, so a workspace serves any number
+ *          of calls with the same B * n_q * H_kv.  Initialise again before
+ *          using it for a larger B * n_q * H_kv.  Calls that share a
+ *          workspace must not overlap on the GPU.  Unused when n_split == 1.
+ * n_split  1 .. 1024; wmtp_attn_num_splits() gives a good value.
+ * Errors: WMTP_EINVAL for null pointers, bad sizes, D not 128/256,
+ * H_q % H_kv != 0, group > 8, misaligned pool/q pointers;
+ * WMTP_ECAPACITY if workspace_bytes is too small. */
+size_t wmtp_attn_workspace_bytes(int32_t B, int32_t n_q, int32_t H_q,
+                                 int32_t H_kv, int32_t D, int32_t n_split);
+
+/* Zeroes the workspace's merge counters (an async memset on `stream`). */
+wmtp_status wmtp_attn_workspace_init(void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
+/* Split count for rows of up to max_len keys on the current device: enough
+ * CTAs to fill the SMs once, but no split shorter than one key tile. */
+int32_t wmtp_attn_num_splits(int32_t B, int32_t n_q, int32_t H_kv,
+                             int64_t max_len);
+
+wmtp_status wmtp_draft_decode_attn(const uint16_t *q, int32_t B, int32_t n_q,
+                                   int32_t H_q, int32_t H_kv, int32_t D,
+                                   const uint16_t *k_pool,
+                                   const uint16_t *v_pool, int64_t num_slots,
+                                   const int32_t *table, int64_t table_stride,
+                                   const int32_t *lens, float scale,
+                                   float *out, float *lse, void *workspace,
+                                   size_t workspace_bytes, int32_t n_split,
+                                   void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WMTP_H */

@@ -1,0 +1,309 @@
+"""GB300 (sm_103a) library for the Windowed-MTP draft-attention hot path.
+
+Method: "Windowed-MTP: Removing the Full-Context Draft-KV Tax at Million-Token
+Context" (arXiv 2607.21535).  The compute runs in the CUDA library
+``_lib/libwmtp.so`` (C ABI: ``include/wmtp.h``).  This module only marshals
+torch tensors into pointers, sizes and the current CUDA stream; it performs no
+arithmetic of the method and has no CPU fallback: if the library is missing it
+raises.
+
+Calls (same names as the C ABI without the ``wmtp_`` prefix):
+  build_draft_indices  draft KV-index tables (sink + window, or full context)
+  ring_map             logical position -> ring slot
+  append_kv            write draft K/V rows into the pool
+  draft_decode_attn    split-KV flash-decode attention with LSE merge
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "WmtpError", "load", "build", "version", "device_error",
+    "build_draft_indices", "ring_map", "append_kv", "draft_decode_attn",
+    "attn_workspace_bytes", "attn_num_splits", "AttnWorkspace",
+]
+
+WMTP_OK = 0
+WMTP_EINVAL = -1
+WMTP_ECAPACITY = -2
+WMTP_ECUDA = -3
+WMTP_EDEVICE = -4
+
+DEV_ERRORS = {0: "ok", 1: "slot out of range", 2: "table overflow", 3: "lens out of range",
+              4: "pipeline wait timeout", 5: "device argument out of range"}
+
+
+class WmtpError(RuntimeError):
+    def __init__(self, what: str, status: int):
+        super().__init__(f"{what}: status {status} ({_STATUS.get(status, 'unknown')})")
+        self.status = status
+
+
+_STATUS = {WMTP_OK: "ok", WMTP_EINVAL: "invalid argument", WMTP_ECAPACITY: "capacity",
+           WMTP_ECUDA: "CUDA error", WMTP_EDEVICE: "device check failed"}
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile ``libwmtp.so`` for sm_103a (nvcc) if it is missing or stale."""
+    return _build.build(force=force, verbose=verbose)
+
+
+def load():
+    """Load the CUDA library; raises if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise ImportError(f"libwmtp.so is not built ({path}); run "
+                              "speculative_decoding_draft_build_gb300.build()")
+        lib = ctypes.CDLL(path)
+        lib.wmtp_version.restype = _i32
+        lib.wmtp_status_string.restype = ctypes.c_char_p
+        lib.wmtp_status_string.argtypes = [_i32]
+        lib.wmtp_get_device_error.restype = _i32
+        lib.wmtp_get_device_error.argtypes = [ctypes.POINTER(_i32), _i32]
+        lib.wmtp_build_draft_indices.restype = _i32
+        lib.wmtp_build_draft_indices.argtypes = [
+            _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp]
+        lib.wmtp_ring_map.restype = _i32
+        lib.wmtp_ring_map.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]
+        lib.wmtp_append_kv.restype = _i32
+        lib.wmtp_append_kv.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _vp]
+        lib.wmtp_attn_workspace_bytes.restype = ctypes.c_size_t
+        lib.wmtp_attn_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+        lib.wmtp_attn_workspace_init.restype = _i32
+        lib.wmtp_attn_workspace_init.argtypes = [_vp, ctypes.c_size_t, _vp]
+        lib.wmtp_attn_num_splits.restype = _i32
+        lib.wmtp_attn_num_splits.argtypes = [_i32, _i32, _i32, _i64]
+        lib.wmtp_draft_decode_attn.restype = _i32
+        lib.wmtp_draft_decode_attn.argtypes = [
+            _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, ctypes.c_float,
+            _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
+        _lib = lib
+        return lib
+
+
+def version() -> int:
+    return int(load().wmtp_version())
+
+
+def _check(status: int, what: str) -> None:
+    if status != WMTP_OK:
+        raise WmtpError(what, int(status))
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, device=None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def device_error(clear: bool = True) -> int:
+    """Device-side error code latched by the kernels (0 = none). Synchronises."""
+    code = _i32(0)
+    _check(load().wmtp_get_device_error(ctypes.byref(code), int(clear)), "get_device_error")
+    return int(code.value)
+
+
+# ---------------------------------------------------------------- a1
+def build_draft_indices(seq_lens: torch.Tensor, gamma: int, n_sink: int, window: int,
+                        depth: int, tree_k: int = 1, windowed: bool = True,
+                        req_to_token: torch.Tensor | None = None,
+                        req_pool_idx: torch.Tensor | None = None,
+                        ring_base: torch.Tensor | None = None, stride: int | None = None,
+                        table: torch.Tensor | None = None, lens: torch.Tensor | None = None,
+                        stream=None):
+    """Draft KV-index tables for ``gamma`` draft steps (``wmtp_build_draft_indices``).
+
+    Returns ``(table[gamma, B, stride] int32, lens[gamma, B] int32)``.  When
+    ``stride`` is omitted it is ``n_sink + window`` (windowed) or
+    ``req_to_token.shape[1]`` (full, paged layout).
+    """
+    _need(seq_lens, "seq_lens", torch.int32)
+    dev = seq_lens.device
+    B = seq_lens.shape[0]
+    if req_to_token is not None:
+        _need(req_to_token, "req_to_token", torch.int32, dev)
+        if req_pool_idx is not None:
+            _need(req_pool_idx, "req_pool_idx", torch.int32, dev)
+    if ring_base is not None:
+        _need(ring_base, "ring_base", torch.int32, dev)
+    if stride is None:
+        if table is not None:
+            stride = table.shape[-1]
+        elif windowed:
+            stride = n_sink + window
+        elif req_to_token is not None:
+            stride = req_to_token.shape[1]
+        else:
+            raise ValueError("stride is required for a full-context ring table")
+    if table is None:
+        table = torch.empty((gamma, B, stride), dtype=torch.int32, device=dev)
+    if lens is None:
+        lens = torch.empty((gamma, B), dtype=torch.int32, device=dev)
+    _need(table, "table", torch.int32, dev)
+    _need(lens, "lens", torch.int32, dev)
+    rtt_stride = req_to_token.shape[1] if req_to_token is not None else 0
+    with torch.cuda.device(dev):
+        _check(load().wmtp_build_draft_indices(
+            _ptr(seq_lens), B, gamma, n_sink, window, depth, tree_k, int(bool(windowed)),
+            _ptr(req_to_token), _ptr(req_pool_idx), rtt_stride, _ptr(ring_base), _ptr(table),
+            stride, _ptr(lens), _stream(stream)), "build_draft_indices")
+    return table, lens
+
+
+# ---------------------------------------------------------------- a2
+def ring_map(ring_base: torch.Tensor, pos: torch.Tensor, req_of: torch.Tensor, n_sink: int,
+             window: int, depth: int, tree_k: int = 1, branch: torch.Tensor | None = None,
+             slots: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Ring slots of logical positions (``wmtp_ring_map``)."""
+    _need(ring_base, "ring_base", torch.int32)
+    dev = ring_base.device
+    _need(pos, "pos", torch.int32, dev)
+    _need(req_of, "req_of", torch.int32, dev)
+    if branch is not None:
+        _need(branch, "branch", torch.int32, dev)
+    n = pos.numel()
+    if slots is None:
+        slots = torch.empty(n, dtype=torch.int32, device=dev)
+    _need(slots, "slots", torch.int32, dev)
+    with torch.cuda.device(dev):
+        _check(load().wmtp_ring_map(_ptr(ring_base), _ptr(pos), _ptr(branch), _ptr(req_of), n,
+                                    n_sink, window, depth, tree_k, _ptr(slots), _stream(stream)),
+               "ring_map")
+    return slots
+
+
+def append_kv(k_new: torch.Tensor, v_new: torch.Tensor, slots: torch.Tensor,
+              k_pool: torch.Tensor, v_pool: torch.Tensor, stream=None) -> None:
+    """Write each new token's K/V rows into pool slot ``slots[i]`` (``wmtp_append_kv``)."""
+    _need(k_pool, "k_pool", torch.bfloat16)
+    dev = k_pool.device
+    for t, nm in ((v_pool, "v_pool"), (k_new, "k_new"), (v_new, "v_new")):
+        _need(t, nm, torch.bfloat16, dev)
+    _need(slots, "slots", torch.int32, dev)
+    n, H_kv, D = k_new.shape
+    if v_new.shape != k_new.shape or k_pool.shape[1:] != (H_kv, D) or v_pool.shape != k_pool.shape:
+        raise ValueError("append_kv: shape mismatch")
+    with torch.cuda.device(dev):
+        _check(load().wmtp_append_kv(_ptr(k_new), _ptr(v_new), _ptr(slots), n, H_kv, D,
+                                     _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _stream(stream)),
+               "append_kv")
+
+
+# ---------------------------------------------------------------- a3 + a4
+def attn_workspace_bytes(B: int, n_q: int, H_q: int, H_kv: int, D: int, n_split: int) -> int:
+    return int(load().wmtp_attn_workspace_bytes(B, n_q, H_q, H_kv, D, n_split))
+
+
+def attn_num_splits(B: int, n_q: int, H_kv: int, max_len: int, device=None) -> int:
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        return int(load().wmtp_attn_num_splits(B, n_q, H_kv, int(max_len)))
+
+
+class AttnWorkspace:
+    """Device scratch for the split-KV partials, zeroed once at creation.
+
+    Every completed ``draft_decode_attn`` call leaves the merge counters at
+    zero, so one workspace serves any number of calls (not concurrent ones).
+    """
+
+    def __init__(self, nbytes: int, device, stream=None):
+        self.nbytes = int(nbytes)
+        self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+        with torch.cuda.device(self.buf.device):
+            _check(load().wmtp_attn_workspace_init(_ptr(self.buf), self.nbytes, _stream(stream)),
+                   "attn_workspace_init")
+
+    def ensure(self, nbytes: int, stream=None) -> "AttnWorkspace":
+        if nbytes <= self.nbytes:
+            return self
+        return AttnWorkspace(nbytes, self.buf.device, stream)
+
+
+_ws_cache: dict = {}
+
+
+def draft_decode_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                      table: torch.Tensor, lens: torch.Tensor, scale: float,
+                      out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                      n_split: int | None = None, max_len: int | None = None,
+                      workspace: AttnWorkspace | None = None, stream=None):
+    """Split-KV flash-decode attention over a block table (``wmtp_draft_decode_attn``).
+
+    q: [B, n_q, H_q, D] bf16; k_pool/v_pool: [num_slots, H_kv, D] bf16;
+    table: [B, stride] int32 (or [..., stride] with B rows); lens: [B] int32.
+    ``n_split`` defaults to ``attn_num_splits`` for ``max_len`` (default: the
+    table stride).  Returns ``(out [B, n_q, H_q, D] fp32, lse [B, n_q, H_q] fp32)``.
+    """
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    for t, nm in ((k_pool, "k_pool"), (v_pool, "v_pool")):
+        _need(t, nm, torch.bfloat16, dev)
+    _need(table, "table", torch.int32, dev)
+    _need(lens, "lens", torch.int32, dev)
+    B, n_q, H_q, D = q.shape
+    num_slots, H_kv, Dk = k_pool.shape
+    if Dk != D or v_pool.shape != k_pool.shape:
+        raise ValueError("draft_decode_attn: pool shape mismatch")
+    stride = table.shape[-1]
+    if table.numel() < B * stride or lens.numel() < B:
+        raise ValueError("draft_decode_attn: table/lens smaller than B rows")
+    if out is None:
+        out = torch.empty((B, n_q, H_q, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, n_q, H_q), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev)
+    _need(lse, "lse", torch.float32, dev)
+    if n_split is None:
+        n_split = attn_num_splits(B, n_q, H_kv, max_len if max_len is not None else stride, dev)
+    need = attn_workspace_bytes(B, n_q, H_q, H_kv, D, n_split)
+    if workspace is None:
+        # one zero-initialised workspace per (device, stream, layout): the merge
+        # counters sit at layout-dependent offsets
+        sid = torch.cuda.current_stream(dev).cuda_stream if stream is None else stream.cuda_stream
+        key = (dev, sid, B * n_q * H_kv, H_q, D, n_split)
+        ws = _ws_cache.get(key)
+        if ws is None:
+            ws = AttnWorkspace(need, dev, stream)
+            _ws_cache[key] = ws
+        workspace = ws
+    elif workspace.nbytes < need:
+        raise ValueError(f"workspace holds {workspace.nbytes} bytes, {need} needed")
+    with torch.cuda.device(dev):
+        _check(load().wmtp_draft_decode_attn(
+            _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
+            stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf),
+            workspace.nbytes, n_split, _stream(stream)), "draft_decode_attn")
+    return out, lse

@@ -1,0 +1,526 @@
+// wmtp_attn.cu -- split-KV flash-decode draft attention for sm_103a.
+//
+// Method: "Windowed-MTP: Removing the Full-Context Draft-KV Tax at
+// Million-Token Context" (arXiv 2607.21535), §4 Mechanism: the draft's
+// decode attention reads exactly the keys its (reduced) block table lists,
+// with no further mask.  The split-KV partition and the log-sum-exp merge are
+// textbook flash-decoding: exact in exact arithmetic, so the result does not
+// depend on how the row is split.
+//
+// Kernel design (one CTA = one chunk of one table row for one KV head):
+//   * warp 4 is the producer: it reads the chunk's slot numbers from the table
+//     and gathers each key's K row and V row (D bf16 each) with one bulk
+//     copy per row on the TMA engine into a padded shared-memory tile,
+//     signalling an mbarrier per stage.  Rows of keys past the chunk end (or
+//     with a bad slot) are zeroed instead and masked.
+//   * warps 0-3 are consumers: each owns 16 keys of every 64-key tile.  QK^T
+//     runs on the tensor cores with the keys as the M dimension and the (up to
+//     8) query heads of the GQA group as N, so one K/V read serves the whole
+//     group and no MMA rows are padding.  The score fragment is converted to
+//     bf16 and transposed in registers (movmatrix) into the B operand of the
+//     PV product, which accumulates O^T (D x 8) in fp32 registers.  Online
+//     softmax in base 2, max/sum across lanes with warp shuffles.
+//   * at the end the four consumer warps combine through shared memory; the
+//     CTA writes its partial (o, lse) and takes a ticket; the last CTA of the
+//     (row, KV head) merges all partials in split order.  No CTA ever waits
+//     for another, and every mbarrier wait has a time limit.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "wmtp.h"
+#include "wmtp_internal.h"
+#include "wmtp_ptx.cuh"
+
+namespace wmtp {
+namespace {
+
+__device__ int32_t g_attn_error = 0;
+
+__device__ __forceinline__ void latch(int32_t code) { atomicCAS(&g_attn_error, 0, code); }
+
+constexpr int kConsumerWarps = 4;
+constexpr int kKeysPerWarp = 16;
+constexpr int kTileKeys = kConsumerWarps * kKeysPerWarp;  // 64 keys per stage
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kMaxGroup = 8;  // query heads per KV head handled by one CTA
+constexpr int kMaxSplits = 1024;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D>
+struct Cfg {
+    static constexpr int kRowBytes = D * 2;        // one K (or V) row of one head
+    static constexpr int kPitch = kRowBytes + 16;  // padded: conflict-free ldmatrix
+    static constexpr int kStages = 3;
+    static constexpr int kTileBytes = kTileKeys * kPitch;
+    static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
+    static constexpr int kOPitch = D + 4;               // fp32 combine rows
+    static constexpr int kCombineBytes =
+        kConsumerWarps * kMaxGroup * kOPitch * 4 + 2 * kConsumerWarps * kMaxGroup * 4;
+    static constexpr int kMergeBytes = kMaxGroup * kMaxSplits * 4;
+    static_assert(kCombineBytes <= kStages * kStageBytes, "combine area must fit");
+    static_assert(kMergeBytes + kCombineBytes <= kStages * kStageBytes, "merge area must fit");
+    static constexpr int kBarOffset = kStages * kStageBytes;
+    // full[kStages], empty[kStages] (8 B each), valid masks[kStages] (8 B),
+    // two int flags.
+    static constexpr int kSmemBytes = kBarOffset + 3 * kStages * 8 + 16;
+};
+
+struct WorkspaceView {
+    int32_t *counters;  // [B*n_q*H_kv]
+    float *lse_part;    // [B*n_q*H_q*n_split], base-2 units
+    float *o_part;      // [B*n_q*H_q*n_split*D]
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline size_t workspace_bytes(int64_t rows_q, int64_t rows_kv, int D, int n_split) {
+    if (n_split <= 1) return 0;
+    return align256(rows_kv * 4) + align256(rows_q * n_split * 4) +
+           (size_t)rows_q * n_split * D * 4;
+}
+
+inline WorkspaceView carve(void *ws, int64_t rows_q, int64_t rows_kv, int n_split) {
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    WorkspaceView v;
+    v.counters = reinterpret_cast<int32_t *>(p);
+    p += align256(rows_kv * 4);
+    v.lse_part = reinterpret_cast<float *>(p);
+    p += align256(rows_q * n_split * 4);
+    v.o_part = reinterpret_cast<float *>(p);
+    return v;
+}
+
+__device__ __forceinline__ void consumer_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
+    const __nv_bfloat16 *__restrict__ q, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t G,
+    const __nv_bfloat16 *__restrict__ k_pool, const __nv_bfloat16 *__restrict__ v_pool,
+    int64_t num_slots, const int32_t *__restrict__ table, int64_t table_stride,
+    const int32_t *__restrict__ lens, float scale_log2, float *__restrict__ out,
+    float *__restrict__ lse, WorkspaceView ws, int32_t n_split) {
+    using C = Cfg<D>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *vmask = empty + C::kStages;
+    volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(vmask + C::kStages);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int split = blockIdx.x;
+    const int g = blockIdx.y;
+    const int64_t bt = blockIdx.z;  // request * n_q + query token
+    const int64_t b = bt / n_q;
+
+    // Chunk of this split: a multiple of the key tile, fixed by L and n_split.
+    int64_t L = lens[b];
+    if (L < 0 || L > table_stride) {
+        if (threadIdx.x == 0 && split == 0 && g == 0) latch(WMTP_DEV_LEN_RANGE);
+        L = L < 0 ? 0 : table_stride;
+    }
+    int64_t chunk = (L + n_split - 1) / n_split;
+    chunk = (chunk + kTileKeys - 1) / kTileKeys * kTileKeys;
+    const int64_t start = (int64_t)split * chunk;
+    const int64_t cnt = L - start < 0 ? 0 : (L - start < chunk ? L - start : chunk);
+    const int n_tiles = (int)((cnt + kTileKeys - 1) / kTileKeys);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), kConsumerWarps);
+        }
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        const int32_t *__restrict__ trow = table + b * table_stride + start;
+        const uint64_t policy = l2_policy_evict_first();
+        const size_t slot_bytes = (size_t)H_kv * C::kRowBytes;
+        const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * C::kRowBytes;
+        const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * C::kRowBytes;
+        int32_t s0 = lane < cnt ? __ldg(trow + lane) : 0;
+        int32_t s1 = lane + 32 < cnt ? __ldg(trow + lane + 32) : 0;
+        int armed = 0;
+        for (int it = 0; it < n_tiles; ++it) {
+            const int st = it % C::kStages;
+            const int64_t nb = (int64_t)(it + 1) * kTileKeys;
+            const int32_t n0 = nb + lane < cnt ? __ldg(trow + nb + lane) : 0;
+            const int32_t n1 = nb + lane + 32 < cnt ? __ldg(trow + nb + lane + 32) : 0;
+            if (it >= C::kStages &&
+                !mbar_wait_bounded(smem_addr(&empty[st]), ((it / C::kStages) - 1) & 1,
+                                   kWaitLimitNs)) {
+                if (lane == 0) latch(WMTP_DEV_WAIT_TIMEOUT);
+                flags[0] = 1;
+                break;
+            }
+            if (flags[0]) break;
+            const int64_t k0 = (int64_t)it * kTileKeys + lane;
+            const bool in0 = k0 < cnt, in1 = k0 + 32 < cnt;
+            const bool v0 = in0 && s0 >= 0 && s0 < num_slots;
+            const bool v1 = in1 && s1 >= 0 && s1 < num_slots;
+            if ((in0 && !v0) || (in1 && !v1)) latch(WMTP_DEV_SLOT_RANGE);
+            const uint32_t m0 = __ballot_sync(0xffffffffu, v0);
+            const uint32_t m1 = __ballot_sync(0xffffffffu, v1);
+            const uint64_t vm = (uint64_t)m0 | ((uint64_t)m1 << 32);
+            uint8_t *kst = smem + st * C::kStageBytes;
+            uint8_t *vst = kst + C::kTileBytes;
+            // Keys without a row get zero V (weight 0 * finite value = 0).
+            uint64_t inv = ~vm;
+            while (inv) {
+                const int key = __ffsll((long long)inv) - 1;
+                inv &= inv - 1;
+                uint4 *row = reinterpret_cast<uint4 *>(vst + key * C::kPitch);
+                for (int e = lane; e < C::kRowBytes / 16; e += 32) row[e] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            const uint32_t full_bar = smem_addr(&full[st]);
+            if (lane == 0) {
+                vmask[st] = vm;
+                const uint32_t bytes = (uint32_t)(__popcll(vm) * 2 * C::kRowBytes);
+                mbar_arrive_expect_tx(full_bar, bytes);
+            }
+            __syncwarp();
+            if (v0) {
+                bulk_g2s(smem_addr(kst + lane * C::kPitch), kbase + (size_t)s0 * slot_bytes,
+                         C::kRowBytes, full_bar, policy);
+                bulk_g2s(smem_addr(vst + lane * C::kPitch), vbase + (size_t)s0 * slot_bytes,
+                         C::kRowBytes, full_bar, policy);
+            }
+            if (v1) {
+                bulk_g2s(smem_addr(kst + (lane + 32) * C::kPitch), kbase + (size_t)s1 * slot_bytes,
+                         C::kRowBytes, full_bar, policy);
+                bulk_g2s(smem_addr(vst + (lane + 32) * C::kPitch), vbase + (size_t)s1 * slot_bytes,
+                         C::kRowBytes, full_bar, policy);
+            }
+            armed = it + 1;
+            s0 = n0;
+            s1 = n1;
+        }
+        // Never leave while our copies can still land: wait (bounded) for the
+        // last phase armed on every stage.
+        for (int st = 0; st < C::kStages && st < armed; ++st) {
+            const int last = ((armed - 1 - st) / C::kStages) * C::kStages + st;
+            if (!mbar_wait_bounded(smem_addr(&full[st]), (last / C::kStages) & 1, kWaitLimitNs)) {
+                if (lane == 0) latch(WMTP_DEV_WAIT_TIMEOUT);
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------- consumers
+    const int r = lane >> 2;  // MMA group: key row (QK) / output dim row (PV)
+    const int c = lane & 3;   // thread in group: query-head pair 2c, 2c+1
+    constexpr int KD = D / 16;
+
+    uint32_t qf[KD][2];
+    {
+        const bool live = r < G;
+        const __nv_bfloat16 *qrow = q + (bt * H_q + (int64_t)g * G + (live ? r : 0)) * D;
+#pragma unroll
+        for (int kd = 0; kd < KD; ++kd) {
+            qf[kd][0] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c)) : 0u;
+            qf[kd][1] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c + 8)) : 0u;
+        }
+    }
+
+    float o[KD][4];
+#pragma unroll
+    for (int dt = 0; dt < KD; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY;  // running max, rows 2c and 2c+1 (base 2)
+    float l0 = 0.f, l1 = 0.f;              // this thread's share of the running sums
+    bool aborted = false;
+
+    const uint32_t k_off = (uint32_t)((warp * kKeysPerWarp + (lane & 15)) * C::kPitch + (lane >> 4) * 16);
+    const uint32_t v_off = (uint32_t)((warp * kKeysPerWarp + (lane & 7) + ((lane >> 4) << 3)) * C::kPitch +
+                                      ((lane >> 3) & 1) * 16);
+    const uint32_t tiles_base = smem_addr(smem);
+
+    for (int it = 0; it < n_tiles; ++it) {
+        const int st = it % C::kStages;
+        if (!mbar_wait_bounded(smem_addr(&full[st]), (it / C::kStages) & 1, kWaitLimitNs)) {
+            if (lane == 0) latch(WMTP_DEV_WAIT_TIMEOUT);
+            flags[0] = 1;
+            aborted = true;
+            break;
+        }
+        const uint32_t wm = (uint32_t)(vmask[st] >> (warp * kKeysPerWarp)) & 0xffffu;
+        if (wm) {
+            const uint32_t kaddr = tiles_base + st * C::kStageBytes + k_off;
+            const uint32_t vaddr = tiles_base + st * C::kStageBytes + C::kTileBytes + v_off;
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kd = 0; kd < KD; ++kd) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kaddr + kd * 32, a0, a1, a2, a3);
+                if (kd & 1)
+                    mma_bf16_16816(sb, a0, a1, a2, a3, qf[kd][0], qf[kd][1]);
+                else
+                    mma_bf16_16816(sa, a0, a1, a2, a3, qf[kd][0], qf[kd][1]);
+            }
+            // s[0]: key r, head 2c; s[1]: key r, head 2c+1; s[2], s[3]: key r+8.
+            const bool ok_lo = (wm >> r) & 1u, ok_hi = (wm >> (r + 8)) & 1u;
+            const float x0 = ok_lo ? (sa[0] + sb[0]) * scale_log2 : -INFINITY;
+            const float x1 = ok_lo ? (sa[1] + sb[1]) * scale_log2 : -INFINITY;
+            const float x2 = ok_hi ? (sa[2] + sb[2]) * scale_log2 : -INFINITY;
+            const float x3 = ok_hi ? (sa[3] + sb[3]) * scale_log2 : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: wm != 0
+            const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+            const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+            const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+            l0 = l0 * al0 + (p0 + p2);
+            l1 = l1 * al1 + (p1 + p3);
+            m0 = mn0;
+            m1 = mn1;
+#pragma unroll
+            for (int dt = 0; dt < KD; ++dt) {
+                o[dt][0] *= al0;
+                o[dt][1] *= al1;
+                o[dt][2] *= al0;
+                o[dt][3] *= al1;
+            }
+            // P^T as the B operand: keys 2c,2c+1 (and +8) for query head r.
+            const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+            const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+#pragma unroll
+            for (int dt = 0; dt < KD; ++dt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_trans(vaddr + dt * 32, a0, a1, a2, a3);
+                mma_bf16_16816(o[dt], a0, a1, a2, a3, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+    }
+
+    // Row sums: add the shares of the 8 lanes that hold the same query heads.
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
+    }
+
+    // ---------------------------------------------- combine the four warps
+    consumer_bar();  // every consumer is done with the stage tiles
+    if (flags[0]) aborted = true;
+    float *ow = reinterpret_cast<float *>(smem);                       // [warp][head][kOPitch]
+    float *mw = ow + kConsumerWarps * kMaxGroup * C::kOPitch;          // [warp][head]
+    float *lw = mw + kConsumerWarps * kMaxGroup;                       // [warp][head]
+    float *wts = lw + kConsumerWarps * kMaxGroup;                      // merge weights
+    {
+        float *o_lo = ow + (warp * kMaxGroup + 2 * c) * C::kOPitch;
+        float *o_hi = o_lo + C::kOPitch;
+#pragma unroll
+        for (int dt = 0; dt < KD; ++dt) {
+            o_lo[dt * 16 + r] = o[dt][0];
+            o_hi[dt * 16 + r] = o[dt][1];
+            o_lo[dt * 16 + r + 8] = o[dt][2];
+            o_hi[dt * 16 + r + 8] = o[dt][3];
+        }
+        if (r == 0) {
+            mw[warp * kMaxGroup + 2 * c] = m0;
+            mw[warp * kMaxGroup + 2 * c + 1] = m1;
+            lw[warp * kMaxGroup + 2 * c] = l0;
+            lw[warp * kMaxGroup + 2 * c + 1] = l1;
+        }
+    }
+    consumer_bar();
+
+    const int tid = threadIdx.x;  // 0 .. kConsumerThreads-1
+    const int64_t row_q0 = bt * H_q + (int64_t)g * G;  // first query row of the group
+    for (int e = tid; e < G * D; e += kConsumerThreads) {
+        const int h = e / D, dim = e - h * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w * kMaxGroup + h]);
+        float Ls = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float f = exp2f(mw[w * kMaxGroup + h] - M);
+                Ls += lw[w * kMaxGroup + h] * f;
+                O += ow[(w * kMaxGroup + h) * C::kOPitch + dim] * f;
+            }
+        }
+        const bool empty_part = !(Ls > 0.f);
+        const float o_val = aborted ? NAN : (empty_part ? 0.f : O / Ls);
+        const float lse2 = aborted ? NAN : (empty_part ? -INFINITY : M + log2f(Ls));
+        if (n_split == 1) {
+            out[(row_q0 + h) * D + dim] = o_val;
+            if (lse && dim == 0) lse[row_q0 + h] = lse2 * kLn2;
+        } else {
+            ws.o_part[((row_q0 + h) * n_split + split) * D + dim] = o_val;
+            if (dim == 0) ws.lse_part[(row_q0 + h) * n_split + split] = lse2;
+        }
+    }
+    if (n_split == 1) return;
+
+    // ------------------------------------------ ticket; the last CTA merges
+    __threadfence();
+    consumer_bar();
+    if (tid == 0) {
+        const int32_t ticket = atomicAdd(&ws.counters[bt * H_kv + g], 1);
+        flags[1] = (ticket == n_split - 1);
+    }
+    consumer_bar();
+    if (!flags[1]) return;
+    __threadfence();
+
+    // Per query head: lse = log2 sum_s 2^lse_s; weights 2^(lse_s - lse).
+    for (int e = tid; e < G * n_split; e += kConsumerThreads) {
+        const int h = e / n_split, s = e - h * n_split;
+        wts[h * n_split + s] = __ldcg(ws.lse_part + (row_q0 + h) * n_split + s);
+    }
+    consumer_bar();
+    for (int h = warp; h < G; h += kConsumerWarps) {
+        float M = -INFINITY;
+        for (int s = lane; s < n_split; s += 32) M = fmaxf(M, wts[h * n_split + s]);
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
+        float sum = 0.f;
+        if (M != -INFINITY && !isnan(M)) {
+            // fixed order: lane-strided partial sums, then a fixed shuffle tree
+            for (int s = lane; s < n_split; s += 32) {
+                const float x = wts[h * n_split + s];
+                sum += x == -INFINITY ? 0.f : exp2f(x - M);
+            }
+        }
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+        const float lse_tot = (sum > 0.f) ? M + log2f(sum) : (isnan(M) ? NAN : -INFINITY);
+        __syncwarp();
+        for (int s = lane; s < n_split; s += 32) {
+            const float x = wts[h * n_split + s];
+            wts[h * n_split + s] = (sum > 0.f && x != -INFINITY) ? exp2f(x - lse_tot) : 0.f;
+        }
+        if (lane == 0 && lse) lse[row_q0 + h] = lse_tot * kLn2;
+    }
+    consumer_bar();
+    for (int e = tid; e < G * D; e += kConsumerThreads) {
+        const int h = e / D, dim = e - h * D;
+        const float *op = ws.o_part + (row_q0 + h) * n_split * D + dim;
+        float acc = 0.f;
+        for (int s = 0; s < n_split; ++s) {
+            const float w = wts[h * n_split + s];
+            if (w != 0.f) acc += w * __ldcg(op + (int64_t)s * D);
+        }
+        out[(row_q0 + h) * D + dim] = acc;
+    }
+    if (tid == 0) ws.counters[bt * H_kv + g] = 0;  // ready for the next call
+}
+
+template <int D>
+wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
+                                int32_t H_kv, const uint16_t *k_pool, const uint16_t *v_pool,
+                                int64_t num_slots, const int32_t *table, int64_t table_stride,
+                                const int32_t *lens, float scale, float *out, float *lse,
+                                void *workspace, int32_t n_split, cudaStream_t stream) {
+    using C = Cfg<D>;
+    const int64_t rows_q = (int64_t)B * n_q * H_q;
+    const int64_t rows_kv = (int64_t)B * n_q * H_kv;
+    WorkspaceView ws{nullptr, nullptr, nullptr};
+    if (n_split > 1) ws = carve(workspace, rows_q, rows_kv, n_split);
+    if (cudaFuncSetAttribute(split_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+        return WMTP_ECUDA;
+    const float scale_log2 = scale * 1.4426950408889634f;
+    dim3 grid((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q));
+    split_decode_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(
+        reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q, H_kv, H_q / H_kv,
+        reinterpret_cast<const __nv_bfloat16 *>(k_pool),
+        reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, table, table_stride, lens,
+        scale_log2, out, lse, ws, n_split);
+    return launch_status();
+}
+
+}  // namespace
+
+cudaError_t read_attn_error(int32_t *code, bool clear) {
+    cudaError_t err = cudaMemcpyFromSymbol(code, g_attn_error, sizeof(int32_t));
+    if (err != cudaSuccess || !clear) return err;
+    const int32_t zero = 0;
+    return cudaMemcpyToSymbol(g_attn_error, &zero, sizeof(int32_t));
+}
+
+}  // namespace wmtp
+
+using namespace wmtp;
+
+extern "C" {
+
+size_t wmtp_attn_workspace_bytes(int32_t B, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t D,
+                                 int32_t n_split) {
+    if (B < 0 || n_q < 0 || H_q < 0 || H_kv < 1 || D < 1 || n_split < 1) return 0;
+    return workspace_bytes((int64_t)B * n_q * H_q, (int64_t)B * n_q * H_kv, D, n_split);
+}
+
+wmtp_status wmtp_attn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+    if (workspace_bytes == 0) return WMTP_OK;
+    if (!workspace) return WMTP_EINVAL;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, as_stream(stream)) == cudaSuccess
+               ? WMTP_OK
+               : WMTP_ECUDA;
+}
+
+int32_t wmtp_attn_num_splits(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_len) {
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t rows = (int64_t)(B > 0 ? B : 1) * (n_q > 0 ? n_q : 1) * (H_kv > 0 ? H_kv : 1);
+    const int64_t tiles = (max_len + kTileKeys - 1) / kTileKeys;
+    int64_t by_sms = sms / rows;                  // one CTA per SM, one wave
+    int64_t by_len = tiles / 4;                   // at least four key tiles per split
+    int64_t n = by_sms < by_len ? by_sms : by_len;
+    if (n < 1) n = 1;
+    if (n > kMaxSplits) n = kMaxSplits;
+    return (int32_t)n;
+}
+
+wmtp_status wmtp_draft_decode_attn(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
+                                   int32_t H_kv, int32_t D, const uint16_t *k_pool,
+                                   const uint16_t *v_pool, int64_t num_slots,
+                                   const int32_t *table, int64_t table_stride,
+                                   const int32_t *lens, float scale, float *out, float *lse,
+                                   void *workspace, size_t workspace_bytes_, int32_t n_split,
+                                   void *stream) {
+    if (B < 0 || n_q < 0 || H_q < 1 || H_kv < 1 || (H_q % H_kv) != 0) return WMTP_EINVAL;
+    if (H_q / H_kv > kMaxGroup) return WMTP_EINVAL;
+    if (D != 128 && D != 256) return WMTP_EINVAL;
+    if (n_split < 1 || n_split > kMaxSplits || table_stride < 1 || num_slots < 0)
+        return WMTP_EINVAL;
+    if ((int64_t)B * n_q > 65535 || H_kv > 65535) return WMTP_EINVAL;
+    if (B == 0 || n_q == 0) return WMTP_OK;
+    if (!q || !k_pool || !v_pool || !table || !lens || !out) return WMTP_EINVAL;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || (reinterpret_cast<uintptr_t>(q) & 3u))
+        return WMTP_EINVAL;
+    if (n_split > 1) {
+        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return WMTP_EINVAL;
+        if (workspace_bytes_ < wmtp_attn_workspace_bytes(B, n_q, H_q, H_kv, D, n_split))
+            return WMTP_ECAPACITY;
+    }
+    cudaStream_t s = as_stream(stream);
+    if (D == 256)
+        return launch_split_decode<256>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
+                                        table_stride, lens, scale, out, lse, workspace, n_split, s);
+    return launch_split_decode<128>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
+                                    table_stride, lens, scale, out, lse, workspace, n_split, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,211 @@
+// wmtp_index.cu -- draft KV-index builder, ring slot mapper and draft KV
+// append for sm_103a, plus the library's status and device-error calls.
+//
+// Method: "Windowed-MTP: Removing the Full-Context Draft-KV Tax at
+// Million-Token Context" (arXiv 2607.21535), §4 Mechanism and App. A "The
+// windowing change (pseudocode)"; ring sizing from §6 Memory and §7
+// "Compatibility with tree speculation".
+//
+// All three kernels move int32 / bf16 rows and are bandwidth- or
+// launch-bound: coalesced loads and stores, no shared memory.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "wmtp.h"
+#include "wmtp_internal.h"
+
+namespace wmtp {
+namespace {
+
+__device__ int32_t g_index_error = 0;
+
+__device__ __forceinline__ void latch(int32_t code) { atomicCAS(&g_index_error, 0, code); }
+
+// Ring slot of logical position p on tree branch `branch` (see wmtp_ring_map
+// in wmtp.h): sinks pinned on branch 0, everything else rolls over
+// W + d*k slots after them, each branch shifted by branch * d.
+__device__ __forceinline__ int64_t ring_slot(int64_t base, int64_t p, int64_t branch,
+                                             int64_t n_sink, int64_t window,
+                                             int64_t depth, int64_t tree_k) {
+    if (p < n_sink && branch == 0) return base + p;
+    const int64_t m = window + depth * tree_k;
+    int64_t r = (p - n_sink + branch * depth) % m;
+    if (r < 0) r += m;
+    return base + n_sink + r;
+}
+
+// One grid row (blockIdx.y) per (draft step j, request b); the x dimension
+// strides over the row's entries.  Entry e of a windowed row is position e
+// for the sinks and e + (kv_len - W - n_sink) for the window.
+__global__ void __launch_bounds__(256) build_indices_kernel(
+    const int32_t *__restrict__ seq_lens, int32_t B, int32_t n_sink, int32_t window,
+    int32_t depth, int32_t tree_k, int32_t windowed,
+    const int32_t *__restrict__ req_to_token, const int32_t *__restrict__ req_pool_idx,
+    int64_t rtt_stride, const int32_t *__restrict__ ring_base, int32_t *__restrict__ table,
+    int64_t stride, int32_t *__restrict__ lens) {
+    const int32_t row = blockIdx.y;
+    const int32_t j = row / B;
+    const int32_t b = row - j * B;
+    const int64_t kv_len = (int64_t)seq_lens[b] + j + 1;
+    const bool win = windowed && kv_len > (int64_t)n_sink + window;
+    const int64_t n = kv_len <= 0 ? 0 : (win ? (int64_t)n_sink + window : kv_len);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        lens[row] = (int32_t)n;
+        if (n > stride) latch(WMTP_DEV_TABLE_OVERFLOW);
+    }
+    const int64_t n_write = n < stride ? n : stride;
+    const int64_t shift = win ? kv_len - window - n_sink : 0;
+    int32_t *__restrict__ out = table + (int64_t)row * stride;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    if (req_to_token) {
+        const int32_t pool_row = req_pool_idx ? req_pool_idx[b] : b;
+        const int32_t *__restrict__ src = req_to_token + (int64_t)pool_row * rtt_stride;
+        for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n_write; e += step) {
+            const int64_t p = (win && e >= n_sink) ? e + shift : e;
+            if (p >= rtt_stride) {
+                latch(WMTP_DEV_ARG_RANGE);
+                continue;
+            }
+            out[e] = __ldg(src + p);
+        }
+    } else {
+        const int64_t base = ring_base[b];
+        for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n_write; e += step) {
+            const int64_t p = (win && e >= n_sink) ? e + shift : e;
+            out[e] = (int32_t)ring_slot(base, p, 0, n_sink, window, depth, tree_k);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) ring_map_kernel(
+    const int32_t *__restrict__ ring_base, const int32_t *__restrict__ pos,
+    const int32_t *__restrict__ branch, const int32_t *__restrict__ req_of, int32_t n,
+    int32_t n_sink, int32_t window, int32_t depth, int32_t tree_k, int32_t *__restrict__ slots) {
+    const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int32_t br = branch ? branch[i] : 0;
+    const int32_t p = pos[i];
+    if (br < 0 || br >= tree_k || p < 0) {
+        latch(WMTP_DEV_ARG_RANGE);
+        slots[i] = -1;
+        return;
+    }
+    slots[i] = (int32_t)ring_slot(ring_base[req_of[i]], p, br, n_sink, window, depth, tree_k);
+}
+
+// One thread per 16-byte chunk of a token's K row set and V row set.
+__global__ void __launch_bounds__(256) append_kv_kernel(
+    const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+    const int32_t *__restrict__ slots, int64_t total, int32_t chunks_per_token,
+    uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, int64_t num_slots) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const int64_t i = idx / chunks_per_token;
+    const int64_t e = idx - i * chunks_per_token;
+    const int64_t slot = slots[i];
+    if (slot < 0 || slot >= num_slots) {
+        latch(WMTP_DEV_SLOT_RANGE);
+        return;
+    }
+    k_pool[slot * chunks_per_token + e] = k_new[idx];
+    v_pool[slot * chunks_per_token + e] = v_new[idx];
+}
+
+}  // namespace
+
+cudaError_t read_index_error(int32_t *code, bool clear) {
+    cudaError_t err = cudaMemcpyFromSymbol(code, g_index_error, sizeof(int32_t));
+    if (err != cudaSuccess || !clear) return err;
+    const int32_t zero = 0;
+    return cudaMemcpyToSymbol(g_index_error, &zero, sizeof(int32_t));
+}
+
+}  // namespace wmtp
+
+using namespace wmtp;
+
+extern "C" {
+
+int32_t wmtp_version(void) { return 1000; }
+
+const char *wmtp_status_string(int32_t status) {
+    switch (status) {
+        case WMTP_OK: return "ok";
+        case WMTP_EINVAL: return "invalid argument";
+        case WMTP_ECAPACITY: return "output or workspace too small";
+        case WMTP_ECUDA: return "CUDA launch or runtime error";
+        case WMTP_EDEVICE: return "device-side check failed";
+        default: return "unknown status";
+    }
+}
+
+wmtp_status wmtp_get_device_error(int32_t *code, int32_t clear) {
+    if (!code) return WMTP_EINVAL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return WMTP_ECUDA;
+    int32_t a = 0, b = 0;
+    if (read_index_error(&a, clear != 0) != cudaSuccess) return WMTP_ECUDA;
+    if (read_attn_error(&b, clear != 0) != cudaSuccess) return WMTP_ECUDA;
+    *code = a ? a : b;
+    return WMTP_OK;
+}
+
+wmtp_status wmtp_build_draft_indices(const int32_t *seq_lens, int32_t B, int32_t gamma,
+                                     int32_t n_sink, int32_t window, int32_t depth,
+                                     int32_t tree_k, int32_t windowed,
+                                     const int32_t *req_to_token,
+                                     const int32_t *req_pool_idx, int64_t rtt_stride,
+                                     const int32_t *ring_base, int32_t *table,
+                                     int64_t stride, int32_t *lens, void *stream) {
+    if (B < 0 || gamma < 0 || n_sink < 0 || window < 1 || depth < 1 || tree_k < 1 ||
+        stride < 1)
+        return WMTP_EINVAL;
+    if ((int64_t)gamma * B > 65535) return WMTP_EINVAL;
+    if (B == 0 || gamma == 0) return WMTP_OK;
+    if (!seq_lens || !table || !lens) return WMTP_EINVAL;
+    if (!req_to_token && !ring_base) return WMTP_EINVAL;
+    if (req_to_token && rtt_stride < 1) return WMTP_EINVAL;
+    constexpr int kThreads = 256;
+    constexpr int64_t kPerCta = kThreads * 4;
+    int64_t gx = (stride + kPerCta - 1) / kPerCta;
+    if (gx > 8192) gx = 8192;
+    dim3 grid((unsigned)gx, (unsigned)(gamma * B));
+    build_indices_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(
+        seq_lens, B, n_sink, window, depth, tree_k, windowed, req_to_token, req_pool_idx,
+        rtt_stride, ring_base, table, stride, lens);
+    return launch_status();
+}
+
+wmtp_status wmtp_ring_map(const int32_t *ring_base, const int32_t *pos,
+                          const int32_t *branch, const int32_t *req_of, int32_t n,
+                          int32_t n_sink, int32_t window, int32_t depth, int32_t tree_k,
+                          int32_t *slots, void *stream) {
+    if (n < 0 || n_sink < 0 || window < 1 || depth < 1 || tree_k < 1) return WMTP_EINVAL;
+    if (n == 0) return WMTP_OK;
+    if (!ring_base || !pos || !req_of || !slots) return WMTP_EINVAL;
+    constexpr int kThreads = 256;
+    ring_map_kernel<<<(n + kThreads - 1) / kThreads, kThreads, 0, as_stream(stream)>>>(
+        ring_base, pos, branch, req_of, n, n_sink, window, depth, tree_k, slots);
+    return launch_status();
+}
+
+wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
+                           const int32_t *slots, int32_t n, int32_t H_kv, int32_t D,
+                           uint16_t *k_pool, uint16_t *v_pool, int64_t num_slots,
+                           void *stream) {
+    if (n < 0 || H_kv < 1 || D < 1 || (D % 8) != 0 || num_slots < 0) return WMTP_EINVAL;
+    if (n == 0) return WMTP_OK;
+    if (!k_new || !v_new || !slots || !k_pool || !v_pool) return WMTP_EINVAL;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+        return WMTP_EINVAL;
+    const int32_t chunks = H_kv * D / 8;
+    const int64_t total = (int64_t)n * chunks;
+    constexpr int kThreads = 256;
+    const int64_t blocks = (total + kThreads - 1) / kThreads;
+    append_kv_kernel<<<(unsigned)blocks, kThreads, 0, as_stream(stream)>>>(
+        reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), slots,
+        total, chunks, reinterpret_cast<uint4 *>(k_pool), reinterpret_cast<uint4 *>(v_pool),
+        num_slots);
+    return launch_status();
+}
+
+}  // extern "C"
