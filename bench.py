@@ -1,0 +1,655 @@
+#!/usr/bin/env python
+"""Benchmark of the Windowed-MTP draft-attention hot path on one GB300 per rank.
+
+Workload (default): the million-token draft step of "Windowed-MTP: Removing
+the Full-Context Draft-KV Tax at Million-Token Context" (§6 setup: B=1, 1M
+context, 2 KV heads, head_dim 256, bf16 KV, n_sink 64, W 4032, d 7 = gamma 6
+draft forwards) on seeded synthetic data: K/V ~ N(0,1) with 1% of K rows x4,
+a seeded random permutation as the page table.
+
+One timed step = one decode step's draft-attention phase for both arms:
+  full arm     : full-context index build + 6 x (append_kv + attention over
+                 the whole table, 1,048,577.. keys)
+  windowed arm : sink+window index build + 6 x (append_kv + attention over
+                 64 + 4032 keys)
+The full arm is launched directly (its attention launches are each bracketed
+by CUDA events for the roofline); the windowed arm, whose kernels take a few
+microseconds, is replayed from a CUDA graph.  L2 is flushed (256 MiB write)
+before each arm, outside the events.
+
+Prints ONE JSON line (rank 0).  `value` is the windowed arm's microseconds
+per decode step (lower is better); both arms' numbers are under "arms".
+`--impl reference` times the fp64 CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "draft-attn μs/step and KV GB/s (% of HBM peak), windowed vs full, at 1M ctx"
+UNIT = "us/step"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "1m": dict(name="million-token draft step", B=1, S=1_048_576, H_q=16, H_kv=2, D=256,
+               n_sink=64, W=4032, gamma=6, outlier_frac=0.01, seed=1002),
+    "131k": dict(name="131K-context draft step", B=1, S=131_072, H_q=16, H_kv=2, D=256,
+                 n_sink=64, W=4032, gamma=6, outlier_frac=0.0, seed=1001),
+}
+
+
+# ------------------------------------------------------------------ helpers
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def attn_bytes(L, n_q, H_q, H_kv, D):
+    """Algorithmic bytes of one attention launch over a table row of L keys:
+    K and V rows of every KV head (bf16), the int32 table, q (bf16), out and
+    lse (fp32)."""
+    return L * H_kv * D * 2 * 2 + 4 * L + n_q * H_q * D * 2 + n_q * H_q * (D + 1) * 4
+
+
+def source_hash():
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "speculative_decoding_draft_build_gb300", "csrc", "wmtp_attn.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current attention source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(kernel_key)
+        if ent and ent.get("source_hash") == source_hash():
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Polls SM clock and clock-event reasons through NVML (read-only) while
+    the timed region runs; falls back to nvidia-smi."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.period = period_s
+        self.samples = []  # (sm_mhz, reasons_mask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._h = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            props = torch.cuda.get_device_properties(device_index)
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0".encode()
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index), ctypes.byref(h)) != 0:
+                    raise OSError("no NVML handle")
+            self._nvml, self._h = nv, h
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            try:
+                self._reasons_fn = nv.nvmlDeviceGetCurrentClocksEventReasons
+            except AttributeError:
+                self._reasons_fn = nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception:
+            self._nvml = None
+
+    def _sample_nvml(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        ok1 = self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0
+        ok2 = self._reasons_fn(self._h, ctypes.byref(rs)) == 0
+        if ok1:
+            self.samples.append((int(clk.value), int(rs.value) if ok2 else 0))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample_nvml()
+            time.sleep(self.period)
+
+    def start(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            self._sample_nvml()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "unavailable"}
+        mhz = [s[0] for s in self.samples]
+        mask = 0
+        for _, m in self.samples:
+            mask |= m
+        reasons = [n for b, n in self.REASONS.items() if mask & b]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(mhz), "source": "nvml"}
+
+
+class Dist:
+    def __init__(self, n_gpus: int):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, values):
+        """Elementwise max of a list of floats over ranks."""
+        if self.pg is None:
+            return list(values)
+        dev = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
+        t = torch.tensor(values, dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return t.cpu().tolist()
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ workload
+class Workload:
+    """Inputs resident on the device; tables, outputs and workspaces preallocated."""
+
+    def __init__(self, cfg, dev):
+        from speculative_decoding_draft_build_gb300 import synth
+        import speculative_decoding_draft_build_gb300 as wm
+        self.cfg = cfg
+        self.dev = dev
+        B, S, H_q, H_kv, D, g = cfg["B"], cfg["S"], cfg["H_q"], cfg["H_kv"], cfg["D"], cfg["gamma"]
+        seed = cfg["seed"]
+        self.scale = 1.0 / math.sqrt(D)
+        pool = B * (S + g)
+        self.kp = synth.normal_bf16((pool, H_kv, D), seed, dev)
+        if cfg["outlier_frac"] > 0:
+            synth.scale_random_rows_(self.kp, cfg["outlier_frac"], 4.0, seed + 1)
+        self.vp = synth.normal_bf16((pool, H_kv, D), seed + 2, dev)
+        self.kn = synth.normal_bf16((g, B, H_kv, D), seed + 3, dev)
+        self.vn = synth.normal_bf16((g, B, H_kv, D), seed + 4, dev)
+        self.q = synth.normal_bf16((g, B, 1, H_q, D), seed + 5, dev)
+        self.rtt = synth.permutation(pool, seed + 6, dev).view(B, S + g)
+        self.seq = torch.full((B,), S, dtype=torch.int32, device=dev)
+        self.slots = torch.stack([self.rtt[:, S + j] for j in range(g)]).contiguous()  # [g, B]
+        self.full_stride = S + g
+        self.win_stride = cfg["n_sink"] + cfg["W"]
+        self.tab_full = torch.empty((g, B, self.full_stride), dtype=torch.int32, device=dev)
+        self.len_full = torch.empty((g, B), dtype=torch.int32, device=dev)
+        self.tab_win = torch.empty((g, B, self.win_stride), dtype=torch.int32, device=dev)
+        self.len_win = torch.empty((g, B), dtype=torch.int32, device=dev)
+        self.out_full = torch.empty((g, B, 1, H_q, D), dtype=torch.float32, device=dev)
+        self.lse_full = torch.empty((g, B, 1, H_q), dtype=torch.float32, device=dev)
+        self.out_win = torch.empty_like(self.out_full)
+        self.lse_win = torch.empty_like(self.lse_full)
+        self.ns_full = wm.attn_num_splits(B, 1, H_kv, S + g, dev)
+        self.ns_win = wm.attn_num_splits(B, 1, H_kv, self.win_stride, dev)
+        self.ws_full = wm.AttnWorkspace(wm.attn_workspace_bytes(B, 1, H_q, H_kv, D, self.ns_full), dev)
+        self.ws_win = wm.AttnWorkspace(wm.attn_workspace_bytes(B, 1, H_q, H_kv, D, self.ns_win), dev)
+        self.flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize(dev)
+
+    def full_arm(self, events=None):
+        import speculative_decoding_draft_build_gb300 as wm
+        c = self.cfg
+        wm.build_draft_indices(self.seq, c["gamma"], c["n_sink"], c["W"], c["gamma"] + 1,
+                               windowed=False, req_to_token=self.rtt, table=self.tab_full,
+                               lens=self.len_full)
+        for j in range(c["gamma"]):
+            wm.append_kv(self.kn[j], self.vn[j], self.slots[j], self.kp, self.vp)
+            if events is not None:
+                events[j][0].record()
+            wm.draft_decode_attn(self.q[j], self.kp, self.vp, self.tab_full[j], self.len_full[j],
+                                 self.scale, out=self.out_full[j], lse=self.lse_full[j],
+                                 n_split=self.ns_full, workspace=self.ws_full)
+            if events is not None:
+                events[j][1].record()
+
+    def win_arm(self, events=None):
+        import speculative_decoding_draft_build_gb300 as wm
+        c = self.cfg
+        wm.build_draft_indices(self.seq, c["gamma"], c["n_sink"], c["W"], c["gamma"] + 1,
+                               windowed=True, req_to_token=self.rtt, table=self.tab_win,
+                               lens=self.len_win)
+        for j in range(c["gamma"]):
+            wm.append_kv(self.kn[j], self.vn[j], self.slots[j], self.kp, self.vp)
+            if events is not None:
+                events[j][0].record()
+            wm.draft_decode_attn(self.q[j], self.kp, self.vp, self.tab_win[j], self.len_win[j],
+                                 self.scale, out=self.out_win[j], lse=self.lse_win[j],
+                                 n_split=self.ns_win, workspace=self.ws_win)
+            if events is not None:
+                events[j][1].record()
+
+    def bytes_full_attn(self, j):
+        c = self.cfg
+        return c["B"] * attn_bytes(c["S"] + j + 1, 1, c["H_q"], c["H_kv"], c["D"])
+
+    def bytes_win_attn(self, j):
+        c = self.cfg
+        L = min(c["S"] + j + 1, c["n_sink"] + c["W"])
+        return c["B"] * attn_bytes(L, 1, c["H_q"], c["H_kv"], c["D"])
+
+
+def _external_event():
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, dist_ctx):
+    import speculative_decoding_draft_build_gb300 as wm
+    wm.build()
+    wm.load()
+    dev = torch.device("cuda", dist_ctx.local)
+    torch.cuda.set_device(dev)
+    cfg = WORKLOADS[args.workload]
+    w = Workload(cfg, dev)
+    g = cfg["gamma"]
+    stream = torch.cuda.current_stream(dev)
+
+    # warm-up (also sets kernel attributes before capture)
+    for _ in range(max(args.warmup, 1)):
+        w.full_arm()
+        w.win_arm()
+    torch.cuda.synchronize(dev)
+
+    # windowed arm as a CUDA graph (timed loop), plus a second capture with
+    # timing events around each attention launch when this torch supports
+    # events inside a capture (used after the timed loop)
+    cap_stream = torch.cuda.Stream(dev)
+
+    def capture(events=None):
+        gr = torch.cuda.CUDAGraph()
+        cap_stream.wait_stream(stream)
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(gr, stream=cap_stream):
+                w.win_arm(events)
+        stream.wait_stream(cap_stream)
+        return gr
+
+    graph = capture()
+    for _ in range(max(args.warmup, 1)):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    e_full = [[ev(), ev()] for _ in range(K)]
+    e_win = [[ev(), ev()] for _ in range(K)]
+    e_attn = [[[ev(), ev()] for _ in range(g)] for _ in range(K)]
+    sampler = ClockSampler(dev.index)
+    dist_ctx.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    t0 = time.perf_counter()
+    for k in range(K):
+        w.flush.zero_()
+        e_full[k][0].record()
+        w.full_arm(e_attn[k])
+        e_full[k][1].record()
+        w.flush.zero_()
+        e_win[k][0].record()
+        graph.replay()
+        e_win[k][1].record()
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    dist_ctx.barrier()
+    sampler.stop()
+
+    full_ms = [a.elapsed_time(b) for a, b in e_full]
+    win_ms = [a.elapsed_time(b) for a, b in e_win]
+    attn_full_ms = [[e_attn[k][j][0].elapsed_time(e_attn[k][j][1]) for j in range(g)] for k in range(K)]
+    full_attn_mean_ms = statistics.mean(x for row in attn_full_ms for x in row)
+
+    # windowed attention per launch, on the same graph with inner events
+    win_attn_ms = []
+    win_attn_source = "cuda-graph replays with timing events around each attention node"
+    inner = [[_external_event(), _external_event()] for _ in range(g)]
+    if inner[0][0] is not None:
+        try:
+            g_ev = capture(inner)
+            for k in range(K):
+                w.flush.zero_()
+                g_ev.replay()
+                torch.cuda.synchronize(dev)
+                win_attn_ms.extend(a.elapsed_time(b) for a, b in inner)
+        except Exception:
+            win_attn_ms = []
+    if not win_attn_ms:
+        win_attn_source = "graph of the windowed attention launches alone, mean per node"
+        cap_stream.wait_stream(stream)
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(g2, stream=cap_stream):
+                for j in range(g):
+                    wm.draft_decode_attn(w.q[j], w.kp, w.vp, w.tab_win[j], w.len_win[j], w.scale,
+                                         out=w.out_win[j], lse=w.lse_win[j], n_split=w.ns_win,
+                                         workspace=w.ws_win)
+        stream.wait_stream(cap_stream)
+        for k in range(K):
+            a, b = ev(), ev()
+            w.flush.zero_()
+            a.record()
+            g2.replay()
+            b.record()
+            torch.cuda.synchronize(dev)
+            win_attn_ms.append(a.elapsed_time(b) / g)
+    win_attn_mean_ms = statistics.mean(win_attn_ms)
+
+    full_bytes = sum(w.bytes_full_attn(j) for j in range(g))
+    win_bytes = sum(w.bytes_win_attn(j) for j in range(g))
+    stats = [statistics.median(full_ms), statistics.median(win_ms), full_attn_mean_ms,
+             win_attn_mean_ms, wall]
+    stats = dist_ctx.max(stats)
+    full_step_ms, win_step_ms, full_attn_ms_max, win_attn_ms_max, wall_max = stats
+
+    peak, peak_kind = hbm_peak()
+    full_gbs = (full_bytes / g) / (full_attn_ms_max * 1e-3) / 1e9
+    win_gbs = (win_bytes / g) / (win_attn_ms_max * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC,
+        "value": round(win_step_ms * 1e3, 3),
+        "unit": UNIT,
+        "n_gpus": dist_ctx.world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(full_step_ms + win_step_ms, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{cfg['name']}: B={cfg['B']}, S={cfg['S']}, H_q={cfg['H_q']}, "
+                        f"H_kv={cfg['H_kv']}, D={cfg['D']}, n_sink={cfg['n_sink']}, W={cfg['W']}, "
+                        f"gamma={g}, d={g + 1}, permuted page table"
+                        + (f", {cfg['outlier_frac']:.0%} of K rows x4" if cfg["outlier_frac"] else ""),
+            "B": cfg["B"], "S": cfg["S"], "gamma": g, "n_sink": cfg["n_sink"], "W": cfg["W"],
+            "H_q": cfg["H_q"], "H_kv": cfg["H_kv"], "D": cfg["D"],
+            "l2": "flushed before each arm (256 MiB write, outside the event brackets)",
+            "parallelism": "replicas" if dist_ctx.world > 1 else "single GPU",
+            "value_is": "windowed arm: index build + 6 x (append_kv + draft attention), us per decode step",
+        },
+        "arms": {
+            "windowed": {
+                "us_per_step": round(win_step_ms * 1e3, 3),
+                "attn_us_per_launch": round(win_attn_ms_max * 1e3, 3),
+                "attn_us_per_step": round(win_attn_ms_max * 1e3 * g, 3),
+                "keys_per_launch": min(cfg["S"] + 1, cfg["n_sink"] + cfg["W"]),
+                "kv_gbs": round(win_gbs, 1),
+                "frac_of_hbm": round(win_gbs / peak, 4),
+                "n_split": w.ns_win,
+                "launch": "cuda graph",
+                "attn_timing": win_attn_source,
+            },
+            "full": {
+                "us_per_step": round(full_step_ms * 1e3, 3),
+                "attn_us_per_launch": round(full_attn_ms_max * 1e3, 3),
+                "attn_us_per_step": round(full_attn_ms_max * 1e3 * g, 3),
+                "keys_per_launch": cfg["S"] + 1,
+                "kv_gbs": round(full_gbs, 1),
+                "frac_of_hbm": round(full_gbs / peak, 4),
+                "n_split": w.ns_full,
+                "launch": "direct",
+            },
+        },
+        "roofline": {
+            "kernel": "split_decode_kernel<256> (full-context draft attention)",
+            "bound": "hbm",
+            "achieved": round(full_gbs, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(full_gbs / peak, 4),
+            "peak_kind": peak_kind,
+            "bytes_per_launch": int(full_bytes / g),
+            "traffic": profiled_traffic("full_1m"),
+        },
+        "roofline_windowed": {
+            "kernel": "split_decode_kernel<256> (windowed draft attention)",
+            "bound": "hbm",
+            "achieved": round(win_gbs, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(win_gbs / peak, 4),
+            "peak_kind": peak_kind,
+            "bytes_per_launch": int(win_bytes / g),
+            "traffic": None,
+        },
+        "gpu_launches": K * 2 * (1 + 2 * g),
+        "clocks": sampler.summary(),
+        "timed_region_s": round(wall_max, 4),
+    }
+
+    result["e2e"] = measure_e2e(w, args, dev)
+    if dist_ctx.rank == 0 and dist_ctx.world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, args)
+    return result
+
+
+def measure_e2e(w, args, dev):
+    """Windowed arm through the Python binding with host buffers: every step
+    copies its inputs (q, new K/V, seq_lens) from pinned host memory, runs
+    the arm with direct calls, and reads the outputs back; timed on the host
+    around a stream synchronisation."""
+    c = w.cfg
+    g = c["gamma"]
+    q_h = w.q.cpu().pin_memory()
+    kn_h = w.kn.cpu().pin_memory()
+    vn_h = w.vn.cpu().pin_memory()
+    seq_h = w.seq.cpu().pin_memory()
+    out_h = torch.empty(w.out_win.shape, dtype=torch.float32).pin_memory()
+    lse_h = torch.empty(w.lse_win.shape, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    h2d = q_h.numel() * 2 + kn_h.numel() * 2 + vn_h.numel() * 2 + seq_h.numel() * 4
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+
+    def step():
+        w.q.copy_(q_h, non_blocking=True)
+        w.kn.copy_(kn_h, non_blocking=True)
+        w.vn.copy_(vn_h, non_blocking=True)
+        w.seq.copy_(seq_h, non_blocking=True)
+        w.win_arm()
+        out_h.copy_(w.out_win, non_blocking=True)
+        lse_h.copy_(w.lse_win, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t)
+    return {"value": round(statistics.median(times) * 1e6, 3), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "how": "windowed arm via the Python binding (direct calls), pinned host I/O, host-timed"}
+
+
+# ------------------------------------------------------------------ oracle legs
+def _oracle_inputs(w):
+    import numpy as np
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return dict(kp=bits(w.kp), vp=bits(w.vp), kn=bits(w.kn), vn=bits(w.vn), q=bits(w.q),
+                rtt=w.rtt.cpu().numpy(), slots=w.slots.cpu().numpy(), seq=w.seq.cpu().numpy())
+
+
+def oracle_windowed_step(o, w, host):
+    """One windowed decode step in the oracle: tables, then per draft step the
+    append and the attention of every query head."""
+    c = w.cfg
+    g = c["gamma"]
+    table, lens = o.build_draft_indices(host["seq"], g, c["n_sink"], c["W"], g + 1, windowed=True,
+                                        req_to_token=host["rtt"], stride=c["n_sink"] + c["W"])
+    for j in range(g):
+        o.append_kv(host["kn"][j], host["vn"][j], host["slots"][j], host["kp"], host["vp"])
+        o.draft_decode_attn(host["q"][j], host["kp"], host["vp"], table[j], lens[j], w.scale)
+
+
+def cpu_baseline(w, args):
+    import oracle as o
+    o.build()
+    host = _oracle_inputs(w)
+    t = time.perf_counter()
+    oracle_windowed_step(o, w, host)
+    first = time.perf_counter() - t
+    reps = max(1, min(5, int(5.0 / max(first, 1e-3))))
+    ts = [first]
+    for _ in range(reps):
+        t = time.perf_counter()
+        oracle_windowed_step(o, w, host)
+        ts.append(time.perf_counter() - t)
+    win_us = statistics.median(ts) * 1e6
+    # full arm: one draft forward over the whole table, all query heads
+    c = w.cfg
+    g = c["gamma"]
+    t = time.perf_counter()
+    table, lens = o.build_draft_indices(host["seq"], 1, c["n_sink"], c["W"], g + 1, windowed=False,
+                                        req_to_token=host["rtt"], stride=c["S"] + g)
+    t_build = time.perf_counter() - t
+    t = time.perf_counter()
+    o.draft_decode_attn(host["q"][0], host["kp"], host["vp"], table[0], lens[0], w.scale)
+    t_fwd = time.perf_counter() - t
+    return {"value": round(win_us, 1), "unit": UNIT, "cores": o.num_threads(), "kind": "oracle",
+            "sample": f"windowed decode step (gamma={g}, all {c['H_q']} heads) x{len(ts)}, median; "
+                      f"full arm estimated from one full-context forward ({c['S'] + 1} keys, all heads) "
+                      f"x{g} + one table build",
+            "full_us_per_step_est": round((t_fwd * g + t_build * g) * 1e6, 1)}
+
+
+def run_reference(args, dist_ctx):
+    """The fp64 CPU oracle as the reference arm, timed on the host cores on
+    the same workload; each step is one windowed decode step."""
+    import oracle as o
+    o.build()
+    cfg = WORKLOADS[args.workload]
+    dev = torch.device("cuda", dist_ctx.local) if torch.cuda.is_available() else torch.device("cpu")
+    w = Workload.__new__(Workload)
+    # inputs only (same seeds as our arm); no CUDA library involved
+    from speculative_decoding_draft_build_gb300 import synth
+    B, S, H_q, H_kv, D, g = cfg["B"], cfg["S"], cfg["H_q"], cfg["H_kv"], cfg["D"], cfg["gamma"]
+    seed = cfg["seed"]
+    w.cfg = cfg
+    w.scale = 1.0 / math.sqrt(D)
+    pool = B * (S + g)
+    w.kp = synth.normal_bf16((pool, H_kv, D), seed, dev)
+    if cfg["outlier_frac"] > 0:
+        synth.scale_random_rows_(w.kp, cfg["outlier_frac"], 4.0, seed + 1)
+    w.vp = synth.normal_bf16((pool, H_kv, D), seed + 2, dev)
+    w.kn = synth.normal_bf16((g, B, H_kv, D), seed + 3, dev)
+    w.vn = synth.normal_bf16((g, B, H_kv, D), seed + 4, dev)
+    w.q = synth.normal_bf16((g, B, 1, H_q, D), seed + 5, dev)
+    w.rtt = synth.permutation(pool, seed + 6, dev).view(B, S + g)
+    w.seq = torch.full((B,), S, dtype=torch.int32, device=dev)
+    w.slots = torch.stack([w.rtt[:, S + j] for j in range(g)]).contiguous()
+    host = _oracle_inputs(w)
+    for _ in range(args.warmup):
+        oracle_windowed_step(o, w, host)
+    ts = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle_windowed_step(o, w, host)
+        ts.append(time.perf_counter() - t)
+    wall = time.perf_counter() - t0
+    val = statistics.median(ts) * 1e6
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(val, 1), "unit": UNIT,
+        "n_gpus": dist_ctx.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(val / 1e3, 4), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{cfg['name']}: B={B}, S={S}, H_q={H_q}, H_kv={H_kv}, D={D}, "
+                               f"n_sink={cfg['n_sink']}, W={cfg['W']}, gamma={g}, windowed arm",
+                   "B": B, "S": S, "gamma": g},
+        "cpu_baseline": {"kind": "oracle", "cores": o.num_threads(), "value": round(val, 1),
+                         "unit": UNIT,
+                         "sample": f"{args.steps} windowed decode steps (index build + {g} x "
+                                   f"(append + attention, all {H_q} heads)), median"},
+        "e2e": {"value": round(val, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "timed_region_s": round(wall, 3),
+    }
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="1m")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    dist_ctx = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            if dist_ctx.rank != 0:
+                return 0
+            res = run_reference(args, dist_ctx)
+        else:
+            res = run_ours(args, dist_ctx)
+        if dist_ctx.rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        dist_ctx.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -16,10 +16,10 @@
 //   * warps 0-3 are consumers: each owns 16 keys of every 64-key tile.  QK^T
 //     runs on the tensor cores with the keys as the M dimension and the (up to
 //     8) query heads of the GQA group as N, so one K/V read serves the whole
-//     group and no MMA rows are padding.  The score fragment is converted to
-//     bf16 and transposed in registers (movmatrix) into the B operand of the
-//     PV product, which accumulates O^T (D x 8) in fp32 registers.  Online
-//     softmax in base 2, max/sum across lanes with warp shuffles.
+//     group and no MMA rows are padding.  The weights are split into bf16
+//     head + tail and transposed in registers (movmatrix) into the B operand
+//     of the PV product, which accumulates O^T (D x 8) in fp32 registers.
+//     Online softmax in base 2, max/sum across lanes with warp shuffles.
 //   * at the end the four consumer warps combine through shared memory; the
 //     CTA writes its partial (o, lse) and takes a ticket; the last CTA of the
 //     (row, KV head) merges all partials in split order.  No CTA ever waits
@@ -297,13 +297,20 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
                 o[dt][3] *= al1;
             }
             // P^T as the B operand: keys 2c,2c+1 (and +8) for query head r.
-            const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-            const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+            // P is split into a bf16 head and a bf16 tail (p = hi + lo to about
+            // 16 significant bits) so that rounding the weights to bf16 does
+            // not cost accuracy; both halves share the same V fragment.
+            const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+            const uint32_t t01 = pack_bf16x2(p0 - bf16_lo_to_f32(h01), p1 - bf16_hi_to_f32(h01));
+            const uint32_t t23 = pack_bf16x2(p2 - bf16_lo_to_f32(h23), p3 - bf16_hi_to_f32(h23));
+            const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
+            const uint32_t pl0 = movmatrix_trans(t01), pl1 = movmatrix_trans(t23);
 #pragma unroll
             for (int dt = 0; dt < KD; ++dt) {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_trans(vaddr + dt * 32, a0, a1, a2, a3);
-                mma_bf16_16816(o[dt], a0, a1, a2, a3, pb0, pb1);
+                mma_bf16_16816(o[dt], a0, a1, a2, a3, ph0, ph1);
+                mma_bf16_16816(o[dt], a0, a1, a2, a3, pl0, pl1);
             }
         }
         __syncwarp();
@@ -437,9 +444,17 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     const int64_t rows_kv = (int64_t)B * n_q * H_kv;
     WorkspaceView ws{nullptr, nullptr, nullptr};
     if (n_split > 1) ws = carve(workspace, rows_q, rows_kv, n_split);
-    if (cudaFuncSetAttribute(split_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
-        return WMTP_ECUDA;
+    // Opt in to the large shared-memory carve-out once per device (outside
+    // any later stream capture of the launches).
+    static int opted_in[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WMTP_ECUDA;
+    if (!opted_in[dev]) {
+        if (cudaFuncSetAttribute(split_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes) != cudaSuccess)
+            return WMTP_ECUDA;
+        opted_in[dev] = 1;
+    }
     const float scale_log2 = scale * 1.4426950408889634f;
     dim3 grid((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q));
     split_decode_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(

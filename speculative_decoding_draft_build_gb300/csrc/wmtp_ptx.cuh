@@ -129,6 +129,10 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     return y;
 }
 
+// The two bf16 halves of a packed pair, widened exactly to fp32.
+__device__ __forceinline__ float bf16_lo_to_f32(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi_to_f32(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
