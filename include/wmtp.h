@@ -152,7 +152,9 @@ wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
  * q        device bf16 [B][n_q][H_q][D], D in {128, 256}, H_q / H_kv <= 8.
  * table    device int32, row b at table + b * table_stride.
  * lens     device int32 [B]; each must be <= table_stride.
- * out      device fp32 [B][n_q][H_q][D];  lse device fp32 [B][n_q][H_q] or NULL.
+ * out      device fp32 [B][n_q][H_q][D], 16-byte aligned;
+ * lse      device fp32 [B][n_q][H_q] or NULL.
+ * k_pool, v_pool 16-byte aligned; q 4-byte aligned.
  * workspace device, >= wmtp_attn_workspace_bytes(...) bytes, 256-byte
  *          aligned.  Its first bytes hold one merge counter per (request,
  *          query token, KV head); they must be zero when a call starts.

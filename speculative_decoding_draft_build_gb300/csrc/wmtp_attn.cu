@@ -8,22 +8,25 @@
 // depend on how the row is split.
 //
 // Kernel design (one CTA = one chunk of one table row for one KV head):
-//   * warp 4 is the producer: it reads the chunk's slot numbers from the table
-//     and gathers each key's K row and V row (D bf16 each) with one bulk
-//     copy per row on the TMA engine into a padded shared-memory tile,
-//     signalling an mbarrier per stage.  Rows of keys past the chunk end (or
-//     with a bad slot) are zeroed instead and masked.
-//   * warps 0-3 are consumers: each owns 16 keys of every 64-key tile.  QK^T
-//     runs on the tensor cores with the keys as the M dimension and the (up to
-//     8) query heads of the GQA group as N, so one K/V read serves the whole
-//     group and no MMA rows are padding.  The weights are split into bf16
-//     head + tail and transposed in registers (movmatrix) into the B operand
-//     of the PV product, which accumulates O^T (D x 8) in fp32 registers.
-//     Online softmax in base 2, max/sum across lanes with warp shuffles.
-//   * at the end the four consumer warps combine through shared memory; the
-//     CTA writes its partial (o, lse) and takes a ticket; the last CTA of the
-//     (row, KV head) merges all partials in split order.  No CTA ever waits
-//     for another, and every mbarrier wait has a time limit.
+//   * four warps; each warp owns 16 keys of every 64-key tile and runs its
+//     own multi-stage copy pipeline for them: lanes 0-15 fetch the 16 slot
+//     numbers from the table one tile ahead, then the warp gathers each key's
+//     K row and V row (D bf16) with 16-byte cp.async copies -- one 512-byte
+//     row per warp instruction, fully coalesced -- into a padded shared-memory
+//     tile.  Keys past the chunk end (or with a bad slot) are zero-filled by
+//     the copy itself (source size 0) and masked.  Warps never wait for each
+//     other inside the loop.
+//   * QK^T runs on the tensor cores with the keys as the M dimension and the
+//     (up to 8) query heads of the GQA group as N, so one K/V read serves the
+//     whole group and no MMA rows are padding.  The weights are split into
+//     bf16 head + tail and transposed in registers (movmatrix) into the B
+//     operand of the PV product, which accumulates O^T (D x 8) in fp32
+//     registers.  Online softmax in base 2, max/sum across lanes with warp
+//     shuffles.
+//   * at the end the four warps combine through shared memory; the CTA writes
+//     its partial (o, lse) and takes a ticket; the last CTA of the (row, KV
+//     head) merges all partials in split order with vectorised, unrolled L2
+//     reads.  No CTA ever waits for another.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -42,12 +45,10 @@ __device__ __forceinline__ void latch(int32_t code) { atomicCAS(&g_attn_error, 0
 
 constexpr int kConsumerWarps = 4;
 constexpr int kKeysPerWarp = 16;
-constexpr int kTileKeys = kConsumerWarps * kKeysPerWarp;  // 64 keys per stage
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kTileKeys = kConsumerWarps * kKeysPerWarp;  // 64 keys per tile
+constexpr int kThreads = kConsumerWarps * 32;
 constexpr int kMaxGroup = 8;  // query heads per KV head handled by one CTA
 constexpr int kMaxSplits = 1024;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
@@ -55,18 +56,18 @@ struct Cfg {
     static constexpr int kRowBytes = D * 2;        // one K (or V) row of one head
     static constexpr int kPitch = kRowBytes + 16;  // padded: conflict-free ldmatrix
     static constexpr int kStages = 3;
-    static constexpr int kTileBytes = kTileKeys * kPitch;
-    static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
-    static constexpr int kOPitch = D + 4;               // fp32 combine rows
+    static constexpr int kWarpTile = kKeysPerWarp * kPitch;     // 16 rows of K (or V)
+    static constexpr int kWarpStage = 2 * kWarpTile;            // K rows then V rows
+    static constexpr int kWarpBytes = kStages * kWarpStage;     // one warp's pipeline
+    static constexpr int kTilesBytes = kConsumerWarps * kWarpBytes;
+    static constexpr int kOPitch = D + 4;                       // fp32 combine rows
     static constexpr int kCombineBytes =
         kConsumerWarps * kMaxGroup * kOPitch * 4 + 2 * kConsumerWarps * kMaxGroup * 4;
     static constexpr int kMergeBytes = kMaxGroup * kMaxSplits * 4;
-    static_assert(kCombineBytes <= kStages * kStageBytes, "combine area must fit");
-    static_assert(kMergeBytes + kCombineBytes <= kStages * kStageBytes, "merge area must fit");
-    static constexpr int kBarOffset = kStages * kStageBytes;
-    // full[kStages], empty[kStages] (8 B each), valid masks[kStages] (8 B),
-    // two int flags.
-    static constexpr int kSmemBytes = kBarOffset + 3 * kStages * 8 + 16;
+    static_assert(kMergeBytes + kCombineBytes <= kTilesBytes, "merge area must fit");
+    static constexpr int kMaskOffset = kTilesBytes;              // uint32 [warps][stages]
+    static constexpr int kFlagOffset = kMaskOffset + kConsumerWarps * kStages * 4;
+    static constexpr int kSmemBytes = kFlagOffset + 16;
 };
 
 struct WorkspaceView {
@@ -94,10 +95,6 @@ inline WorkspaceView carve(void *ws, int64_t rows_q, int64_t rows_kv, int n_spli
     return v;
 }
 
-__device__ __forceinline__ void consumer_bar() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const __nv_bfloat16 *__restrict__ q, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t G,
@@ -106,11 +103,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const int32_t *__restrict__ lens, float scale_log2, float *__restrict__ out,
     float *__restrict__ lse, WorkspaceView ws, int32_t n_split) {
     using C = Cfg<D>;
+    constexpr int S = C::kStages;
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
-    uint64_t *empty = full + C::kStages;
-    uint64_t *vmask = empty + C::kStages;
-    volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(vmask + C::kStages);
+    uint32_t *masks = reinterpret_cast<uint32_t *>(smem + C::kMaskOffset);
+    volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(smem + C::kFlagOffset);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -131,95 +127,59 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const int64_t cnt = L - start < 0 ? 0 : (L - start < chunk ? L - start : chunk);
     const int n_tiles = (int)((cnt + kTileKeys - 1) / kTileKeys);
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_addr(&full[s]), 1);
-            mbar_init(smem_addr(&empty[s]), kConsumerWarps);
-        }
-        flags[0] = 0;
-        flags[1] = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
+    // ------------------------------------------------ per-warp copy pipeline
+    const int32_t *__restrict__ trow = table + b * table_stride + start;
+    const uint64_t policy = l2_policy_evict_first();
+    const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * C::kRowBytes;
+    const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * C::kRowBytes;
+    const size_t slot_bytes = (size_t)H_kv * C::kRowBytes;
+    uint8_t *wsm = smem + warp * C::kWarpBytes;
+    const uint32_t wsm_addr = smem_addr(wsm);
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------ producer
-        const int32_t *__restrict__ trow = table + b * table_stride + start;
-        const uint64_t policy = l2_policy_evict_first();
-        const size_t slot_bytes = (size_t)H_kv * C::kRowBytes;
-        const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * C::kRowBytes;
-        const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * C::kRowBytes;
-        int32_t s0 = lane < cnt ? __ldg(trow + lane) : 0;
-        int32_t s1 = lane + 32 < cnt ? __ldg(trow + lane + 32) : 0;
-        int armed = 0;
-        for (int it = 0; it < n_tiles; ++it) {
-            const int st = it % C::kStages;
-            const int64_t nb = (int64_t)(it + 1) * kTileKeys;
-            const int32_t n0 = nb + lane < cnt ? __ldg(trow + nb + lane) : 0;
-            const int32_t n1 = nb + lane + 32 < cnt ? __ldg(trow + nb + lane + 32) : 0;
-            if (it >= C::kStages &&
-                !mbar_wait_bounded(smem_addr(&empty[st]), ((it / C::kStages) - 1) & 1,
-                                   kWaitLimitNs)) {
-                if (lane == 0) latch(WMTP_DEV_WAIT_TIMEOUT);
-                flags[0] = 1;
-                break;
-            }
-            if (flags[0]) break;
-            const int64_t k0 = (int64_t)it * kTileKeys + lane;
-            const bool in0 = k0 < cnt, in1 = k0 + 32 < cnt;
-            const bool v0 = in0 && s0 >= 0 && s0 < num_slots;
-            const bool v1 = in1 && s1 >= 0 && s1 < num_slots;
-            if ((in0 && !v0) || (in1 && !v1)) latch(WMTP_DEV_SLOT_RANGE);
-            const uint32_t m0 = __ballot_sync(0xffffffffu, v0);
-            const uint32_t m1 = __ballot_sync(0xffffffffu, v1);
-            const uint64_t vm = (uint64_t)m0 | ((uint64_t)m1 << 32);
-            uint8_t *kst = smem + st * C::kStageBytes;
-            uint8_t *vst = kst + C::kTileBytes;
-            // Keys without a row get zero V (weight 0 * finite value = 0).
-            uint64_t inv = ~vm;
-            while (inv) {
-                const int key = __ffsll((long long)inv) - 1;
-                inv &= inv - 1;
-                uint4 *row = reinterpret_cast<uint4 *>(vst + key * C::kPitch);
-                for (int e = lane; e < C::kRowBytes / 16; e += 32) row[e] = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            const uint32_t full_bar = smem_addr(&full[st]);
-            if (lane == 0) {
-                vmask[st] = vm;
-                const uint32_t bytes = (uint32_t)(__popcll(vm) * 2 * C::kRowBytes);
-                mbar_arrive_expect_tx(full_bar, bytes);
-            }
-            __syncwarp();
-            if (v0) {
-                bulk_g2s(smem_addr(kst + lane * C::kPitch), kbase + (size_t)s0 * slot_bytes,
-                         C::kRowBytes, full_bar, policy);
-                bulk_g2s(smem_addr(vst + lane * C::kPitch), vbase + (size_t)s0 * slot_bytes,
-                         C::kRowBytes, full_bar, policy);
-            }
-            if (v1) {
-                bulk_g2s(smem_addr(kst + (lane + 32) * C::kPitch), kbase + (size_t)s1 * slot_bytes,
-                         C::kRowBytes, full_bar, policy);
-                bulk_g2s(smem_addr(vst + (lane + 32) * C::kPitch), vbase + (size_t)s1 * slot_bytes,
-                         C::kRowBytes, full_bar, policy);
-            }
-            armed = it + 1;
-            s0 = n0;
-            s1 = n1;
+    // Slot of key (tile t, this warp's key `lane`) for lanes 0-15.
+    auto load_slot = [&](int t) -> int32_t {
+        const int64_t k = (int64_t)t * kTileKeys + warp * kKeysPerWarp + (lane & 15);
+        return (lane < kKeysPerWarp && k < cnt) ? __ldg(trow + k) : 0;
+    };
+    // Issue the copies of tile t (stage t % S) from the slots held by lanes 0-15.
+    auto issue = [&](int t, int32_t my_slot) {
+        const int st = t % S;
+        const int64_t k = (int64_t)t * kTileKeys + warp * kKeysPerWarp + (lane & 15);
+        const bool in = lane < kKeysPerWarp && k < cnt;
+        const bool ok = in && my_slot >= 0 && my_slot < num_slots;
+        if (in && !ok) latch(WMTP_DEV_SLOT_RANGE);
+        const uint32_t vm = __ballot_sync(0xffffffffu, ok) & 0xffffu;
+        if (lane == 0) masks[warp * S + st] = vm;
+        const uint32_t kdst = wsm_addr + st * C::kWarpStage;
+        const uint32_t vdst = kdst + C::kWarpTile;
+        constexpr int kLanesPerRow = C::kRowBytes / 16;  // 32 (D=256) or 16 (D=128)
+        constexpr int kRowsPerInst = 32 / kLanesPerRow;
+        const int sub = lane / kLanesPerRow;
+        const int col = (lane % kLanesPerRow) * 16;
+#pragma unroll
+        for (int r0 = 0; r0 < kKeysPerWarp; r0 += kRowsPerInst) {
+            const int r = r0 + sub;
+            const int32_t slot = __shfl_sync(0xffffffffu, my_slot, r);
+            const bool rv = (vm >> r) & 1u;
+            const size_t off = rv ? (size_t)slot * slot_bytes + col : 0;
+            cp_async_16(kdst + r * C::kPitch + col, kbase + off, rv ? 16u : 0u, policy);
+            cp_async_16(vdst + r * C::kPitch + col, vbase + off, rv ? 16u : 0u, policy);
         }
-        // Never leave while our copies can still land: wait (bounded) for the
-        // last phase armed on every stage.
-        for (int st = 0; st < C::kStages && st < armed; ++st) {
-            const int last = ((armed - 1 - st) / C::kStages) * C::kStages + st;
-            if (!mbar_wait_bounded(smem_addr(&full[st]), (last / C::kStages) & 1, kWaitLimitNs)) {
-                if (lane == 0) latch(WMTP_DEV_WAIT_TIMEOUT);
-            }
-        }
-        return;
-    }
+    };
 
-    // -------------------------------------------------------------- consumers
+    {
+        int32_t pro[S - 1];
+#pragma unroll
+        for (int t = 0; t < S - 1; ++t) pro[t] = load_slot(t);
+#pragma unroll
+        for (int t = 0; t < S - 1; ++t) {
+            if (t < n_tiles) issue(t, pro[t]);
+            cp_async_commit();
+        }
+    }
+    int32_t next_slot = load_slot(S - 1);
+
+    // -------------------------------------------------------------- compute
     const int r = lane >> 2;  // MMA group: key row (QK) / output dim row (PV)
     const int c = lane & 3;   // thread in group: query-head pair 2c, 2c+1
     constexpr int KD = D / 16;
@@ -240,25 +200,21 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     for (int dt = 0; dt < KD; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY;  // running max, rows 2c and 2c+1 (base 2)
     float l0 = 0.f, l1 = 0.f;              // this thread's share of the running sums
-    bool aborted = false;
 
-    const uint32_t k_off = (uint32_t)((warp * kKeysPerWarp + (lane & 15)) * C::kPitch + (lane >> 4) * 16);
-    const uint32_t v_off = (uint32_t)((warp * kKeysPerWarp + (lane & 7) + ((lane >> 4) << 3)) * C::kPitch +
-                                      ((lane >> 3) & 1) * 16);
-    const uint32_t tiles_base = smem_addr(smem);
+    const uint32_t k_off = (uint32_t)((lane & 15) * C::kPitch + (lane >> 4) * 16);
+    const uint32_t v_off = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * C::kPitch + ((lane >> 3) & 1) * 16);
 
     for (int it = 0; it < n_tiles; ++it) {
-        const int st = it % C::kStages;
-        if (!mbar_wait_bounded(smem_addr(&full[st]), (it / C::kStages) & 1, kWaitLimitNs)) {
-            if (lane == 0) latch(WMTP_DEV_WAIT_TIMEOUT);
-            flags[0] = 1;
-            aborted = true;
-            break;
-        }
-        const uint32_t wm = (uint32_t)(vmask[st] >> (warp * kKeysPerWarp)) & 0xffffu;
+        if (it + S - 1 < n_tiles) issue(it + S - 1, next_slot);
+        cp_async_commit();
+        next_slot = load_slot(it + S);
+        cp_async_wait<S - 1>();
+        __syncwarp();
+        const int st = it % S;
+        const uint32_t wm = masks[warp * S + st];
         if (wm) {
-            const uint32_t kaddr = tiles_base + st * C::kStageBytes + k_off;
-            const uint32_t vaddr = tiles_base + st * C::kStageBytes + C::kTileBytes + v_off;
+            const uint32_t kaddr = wsm_addr + st * C::kWarpStage + k_off;
+            const uint32_t vaddr = wsm_addr + st * C::kWarpStage + C::kWarpTile + v_off;
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kd = 0; kd < KD; ++kd) {
@@ -314,8 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
     }
+    cp_async_wait<0>();
 
     // Row sums: add the shares of the 8 lanes that hold the same query heads.
 #pragma unroll
@@ -325,8 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     }
 
     // ---------------------------------------------- combine the four warps
-    consumer_bar();  // every consumer is done with the stage tiles
-    if (flags[0]) aborted = true;
+    __syncthreads();  // every warp is done with its tiles
     float *ow = reinterpret_cast<float *>(smem);                       // [warp][head][kOPitch]
     float *mw = ow + kConsumerWarps * kMaxGroup * C::kOPitch;          // [warp][head]
     float *lw = mw + kConsumerWarps * kMaxGroup;                       // [warp][head]
@@ -348,11 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
             lw[warp * kMaxGroup + 2 * c + 1] = l1;
         }
     }
-    consumer_bar();
+    __syncthreads();
 
-    const int tid = threadIdx.x;  // 0 .. kConsumerThreads-1
+    const int tid = threadIdx.x;
     const int64_t row_q0 = bt * H_q + (int64_t)g * G;  // first query row of the group
-    for (int e = tid; e < G * D; e += kConsumerThreads) {
+    for (int e = tid; e < G * D; e += kThreads) {
         const int h = e / D, dim = e - h * D;
         float M = -INFINITY;
 #pragma unroll
@@ -367,8 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
             }
         }
         const bool empty_part = !(Ls > 0.f);
-        const float o_val = aborted ? NAN : (empty_part ? 0.f : O / Ls);
-        const float lse2 = aborted ? NAN : (empty_part ? -INFINITY : M + log2f(Ls));
+        const float o_val = empty_part ? 0.f : O / Ls;
+        const float lse2 = empty_part ? -INFINITY : M + log2f(Ls);
         if (n_split == 1) {
             out[(row_q0 + h) * D + dim] = o_val;
             if (lse && dim == 0) lse[row_q0 + h] = lse2 * kLn2;
@@ -381,54 +336,75 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
 
     // ------------------------------------------ ticket; the last CTA merges
     __threadfence();
-    consumer_bar();
+    __syncthreads();
     if (tid == 0) {
         const int32_t ticket = atomicAdd(&ws.counters[bt * H_kv + g], 1);
-        flags[1] = (ticket == n_split - 1);
+        flags[0] = (ticket == n_split - 1);
     }
-    consumer_bar();
-    if (!flags[1]) return;
+    __syncthreads();
+    if (!flags[0]) return;
     __threadfence();
 
     // Per query head: lse = log2 sum_s 2^lse_s; weights 2^(lse_s - lse).
-    for (int e = tid; e < G * n_split; e += kConsumerThreads) {
-        const int h = e / n_split, s = e - h * n_split;
-        wts[h * n_split + s] = __ldcg(ws.lse_part + (row_q0 + h) * n_split + s);
+    for (int e = tid; e < G * n_split; e += kThreads) {
+        const int h = e / n_split, s2 = e - h * n_split;
+        wts[h * n_split + s2] = __ldcg(ws.lse_part + (row_q0 + h) * n_split + s2);
     }
-    consumer_bar();
+    __syncthreads();
     for (int h = warp; h < G; h += kConsumerWarps) {
         float M = -INFINITY;
-        for (int s = lane; s < n_split; s += 32) M = fmaxf(M, wts[h * n_split + s]);
+        for (int s2 = lane; s2 < n_split; s2 += 32) M = fmaxf(M, wts[h * n_split + s2]);
 #pragma unroll
         for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
         float sum = 0.f;
-        if (M != -INFINITY && !isnan(M)) {
+        if (M != -INFINITY) {
             // fixed order: lane-strided partial sums, then a fixed shuffle tree
-            for (int s = lane; s < n_split; s += 32) {
-                const float x = wts[h * n_split + s];
+            for (int s2 = lane; s2 < n_split; s2 += 32) {
+                const float x = wts[h * n_split + s2];
                 sum += x == -INFINITY ? 0.f : exp2f(x - M);
             }
         }
 #pragma unroll
         for (int sh = 16; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
-        const float lse_tot = (sum > 0.f) ? M + log2f(sum) : (isnan(M) ? NAN : -INFINITY);
+        const float lse_tot = (sum > 0.f) ? M + log2f(sum) : -INFINITY;
         __syncwarp();
-        for (int s = lane; s < n_split; s += 32) {
-            const float x = wts[h * n_split + s];
-            wts[h * n_split + s] = (sum > 0.f && x != -INFINITY) ? exp2f(x - lse_tot) : 0.f;
+        for (int s2 = lane; s2 < n_split; s2 += 32) {
+            const float x = wts[h * n_split + s2];
+            wts[h * n_split + s2] = (sum > 0.f && x != -INFINITY) ? exp2f(x - lse_tot) : 0.f;
         }
         if (lane == 0 && lse) lse[row_q0 + h] = lse_tot * kLn2;
     }
-    consumer_bar();
-    for (int e = tid; e < G * D; e += kConsumerThreads) {
-        const int h = e / D, dim = e - h * D;
-        const float *op = ws.o_part + (row_q0 + h) * n_split * D + dim;
-        float acc = 0.f;
-        for (int s = 0; s < n_split; ++s) {
-            const float w = wts[h * n_split + s];
-            if (w != 0.f) acc += w * __ldcg(op + (int64_t)s * D);
+    __syncthreads();
+    constexpr int D4 = D / 4;
+    constexpr int kUnroll = 8;
+    for (int e = tid; e < G * D4; e += kThreads) {
+        const int h = e / D4, d4 = e - h * D4;
+        const float4 *op = reinterpret_cast<const float4 *>(ws.o_part + (row_q0 + h) * n_split * D) + d4;
+        const float *wh = wts + h * n_split;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int s2 = 0;
+        for (; s2 + kUnroll <= n_split; s2 += kUnroll) {
+            float4 v[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) v[u] = __ldcg(op + (int64_t)(s2 + u) * D4);
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const float w = wh[s2 + u];
+                acc.x += w * v[u].x;
+                acc.y += w * v[u].y;
+                acc.z += w * v[u].z;
+                acc.w += w * v[u].w;
+            }
         }
-        out[(row_q0 + h) * D + dim] = acc;
+        for (; s2 < n_split; ++s2) {
+            const float4 v = __ldcg(op + (int64_t)s2 * D4);
+            const float w = wh[s2];
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
+        reinterpret_cast<float4 *>(out + (row_q0 + h) * D)[d4] = acc;
     }
     if (tid == 0) ws.counters[bt * H_kv + g] = 0;  // ready for the next call
 }
@@ -523,7 +499,8 @@ wmtp_status wmtp_draft_decode_attn(const uint16_t *q, int32_t B, int32_t n_q, in
     if ((int64_t)B * n_q > 65535 || H_kv > 65535) return WMTP_EINVAL;
     if (B == 0 || n_q == 0) return WMTP_OK;
     if (!q || !k_pool || !v_pool || !table || !lens || !out) return WMTP_EINVAL;
-    if (!aligned16(k_pool) || !aligned16(v_pool) || (reinterpret_cast<uintptr_t>(q) & 3u))
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(q) & 3u))
         return WMTP_EINVAL;
     if (n_split > 1) {
         if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return WMTP_EINVAL;
