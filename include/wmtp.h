@@ -146,7 +146,9 @@ wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
  *   lse[b,t,h]   = log sum_i exp(s_i)        (natural log)
  * Each row is cut into n_split contiguous chunks whose size depends only on
  * lens[b] and n_split, so results depend on the logical key order and not
- * on the physical slots.  Partials (o, lse) are merged in split order.
+ * on the physical slots.  Partials (o, lse) are merged in split order:
+ * through distributed shared memory of a thread-block cluster when
+ * n_split <= 16, else through the workspace by the last CTA to finish.
  * An empty row gives out = 0, lse = -inf.
  *
  * q        device bf16 [B][n_q][H_q][D], D in {128, 256}, H_q / H_kv <= 8.
@@ -162,7 +164,9 @@ wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
  *          leaves its own counters at zero, so a workspace serves any number
  *          of calls with the same B * n_q * H_kv.  Initialise again before
  *          using it for a larger B * n_q * H_kv.  Calls that share a
- *          workspace must not overlap on the GPU.  Unused when n_split == 1.
+ *          workspace must not overlap on the GPU.  Unused when n_split == 1,
+ *          and when the splits merge through a thread-block cluster (up to
+ *          16 splits, where the device can hold such a cluster).
  * n_split  1 .. 1024; wmtp_attn_num_splits() gives a good value.
  * Errors: WMTP_EINVAL for null pointers, bad sizes, D not 128/256,
  * H_q % H_kv != 0, group > 8, misaligned pool/q pointers;

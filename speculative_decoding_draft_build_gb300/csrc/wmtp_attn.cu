@@ -9,24 +9,29 @@
 //
 // Kernel design (one CTA = one chunk of one table row for one KV head):
 //   * four warps; each warp owns 16 keys of every 64-key tile and runs its
-//     own multi-stage copy pipeline for them: lanes 0-15 fetch the 16 slot
-//     numbers from the table one tile ahead, then the warp gathers each key's
-//     K row and V row (D bf16) with 16-byte cp.async copies -- one 512-byte
-//     row per warp instruction, fully coalesced -- into a padded shared-memory
-//     tile.  Keys past the chunk end (or with a bad slot) are zero-filled by
-//     the copy itself (source size 0) and masked.  Warps never wait for each
-//     other inside the loop.
+//     own three-stage copy pipeline for them.  The chunk's slot numbers are
+//     fetched from the table into a per-warp shared-memory ring with cp.async
+//     five tiles ahead; each key's K row and V row (D bf16) is then gathered
+//     with 16-byte cp.async copies -- one 512-byte row per warp instruction,
+//     fully coalesced -- into a padded shared-memory tile.  Keys past the
+//     chunk end (or with a bad slot) are zero-filled by the copy itself
+//     (source size 0) and masked.  Warps never wait for each other inside
+//     the loop, and no issue ever waits on a global load.
 //   * QK^T runs on the tensor cores with the keys as the M dimension and the
 //     (up to 8) query heads of the GQA group as N, so one K/V read serves the
 //     whole group and no MMA rows are padding.  The weights are split into
 //     bf16 head + tail and transposed in registers (movmatrix) into the B
 //     operand of the PV product, which accumulates O^T (D x 8) in fp32
 //     registers.  Online softmax in base 2, max/sum across lanes with warp
-//     shuffles.
-//   * at the end the four warps combine through shared memory; the CTA writes
-//     its partial (o, lse) and takes a ticket; the last CTA of the (row, KV
-//     head) merges all partials in split order with vectorised, unrolled L2
-//     reads.  No CTA ever waits for another.
+//     shuffles; the accumulator is rescaled only when a running max moves.
+//   * at the end the four warps combine through shared memory (per-head
+//     factors computed once).  Up to 16 splits of a (row, KV head) run as one
+//     thread-block cluster and merge through distributed shared memory;
+//     larger split counts write partials to the workspace, take a ticket, and
+//     the last CTA merges them in split order.  No CTA ever spins on another.
+//   * every kernel waits on its predecessor with griddepcontrol.wait before
+//     touching global memory and is launched with programmatic stream
+//     serialization, so consecutive launches overlap only their start-up.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -49,6 +54,7 @@ constexpr int kTileKeys = kConsumerWarps * kKeysPerWarp;  // 64 keys per tile
 constexpr int kThreads = kConsumerWarps * 32;
 constexpr int kMaxGroup = 8;  // query heads per KV head handled by one CTA
 constexpr int kMaxSplits = 1024;
+constexpr int kMaxClusterMerge = 16;  // splits merged through a cluster (non-portable size)
 constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
@@ -63,9 +69,12 @@ struct Cfg {
     static constexpr int kOPitch = D + 4;                       // fp32 combine rows
     static constexpr int kCombineBytes =
         kConsumerWarps * kMaxGroup * kOPitch * 4 + 2 * kConsumerWarps * kMaxGroup * 4;
-    static constexpr int kMergeBytes = kMaxGroup * kMaxSplits * 4;
-    static_assert(kMergeBytes + kCombineBytes <= kTilesBytes, "merge area must fit");
-    static constexpr int kMaskOffset = kTilesBytes;              // uint32 [warps][stages]
+    static constexpr int kPartBytes = kMaxGroup * D * 4 + kMaxGroup * 4;  // cluster merge
+    static constexpr int kMergeBytes = kMaxGroup * kMaxSplits * 4;        // ticket merge
+    static_assert(kCombineBytes + kPartBytes + kMergeBytes <= kTilesBytes, "merge areas must fit");
+    static constexpr int kRingTiles = 2 * kStages;   // slot tiles held per warp
+    static constexpr int kRingOffset = kTilesBytes;  // int32 [warps][ring tiles][16]
+    static constexpr int kMaskOffset = kRingOffset + kConsumerWarps * kRingTiles * kKeysPerWarp * 4;
     static constexpr int kFlagOffset = kMaskOffset + kConsumerWarps * kStages * 4;
     static constexpr int kSmemBytes = kFlagOffset + 16;
 };
@@ -101,12 +110,16 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const __nv_bfloat16 *__restrict__ k_pool, const __nv_bfloat16 *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ table, int64_t table_stride,
     const int32_t *__restrict__ lens, float scale_log2, float *__restrict__ out,
-    float *__restrict__ lse, WorkspaceView ws, int32_t n_split) {
+    float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t cluster_merge) {
     using C = Cfg<D>;
     constexpr int S = C::kStages;
+    constexpr int R = C::kRingTiles;
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *masks = reinterpret_cast<uint32_t *>(smem + C::kMaskOffset);
     volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(smem + C::kFlagOffset);
+
+    griddep_launch_dependents();
+    griddep_wait();
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -114,6 +127,22 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const int g = blockIdx.y;
     const int64_t bt = blockIdx.z;  // request * n_q + query token
     const int64_t b = bt / n_q;
+    const int r = lane >> 2;  // MMA group: key row (QK) / output dim row (PV)
+    const int c = lane & 3;   // thread in group: query-head pair 2c, 2c+1
+    constexpr int KD = D / 16;
+
+    // Query fragments (B operand of QK^T), loaded first so that their latency
+    // overlaps the table fetch.
+    uint32_t qf[KD][2];
+    {
+        const bool live = r < G;
+        const __nv_bfloat16 *qrow = q + (bt * H_q + (int64_t)g * G + (live ? r : 0)) * D;
+#pragma unroll
+        for (int kd = 0; kd < KD; ++kd) {
+            qf[kd][0] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c)) : 0u;
+            qf[kd][1] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c + 8)) : 0u;
+        }
+    }
 
     // Chunk of this split: a multiple of the key tile, fixed by L and n_split.
     int64_t L = lens[b];
@@ -133,17 +162,26 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * C::kRowBytes;
     const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * C::kRowBytes;
     const size_t slot_bytes = (size_t)H_kv * C::kRowBytes;
-    uint8_t *wsm = smem + warp * C::kWarpBytes;
-    const uint32_t wsm_addr = smem_addr(wsm);
+    const uint32_t wsm_addr = smem_addr(smem + warp * C::kWarpBytes);
 
-    // Slot of key (tile t, this warp's key `lane`) for lanes 0-15.
-    auto load_slot = [&](int t) -> int32_t {
-        const int64_t k = (int64_t)t * kTileKeys + warp * kKeysPerWarp + (lane & 15);
-        return (lane < kKeysPerWarp && k < cnt) ? __ldg(trow + k) : 0;
+    // Slot numbers travel through a per-warp shared-memory ring, fetched with
+    // cp.async 2S-1 tiles ahead inside the same commit groups as the K/V
+    // rows, so issuing a tile's gathers never waits on a global load.
+    const int32_t *ring = reinterpret_cast<const int32_t *>(smem + C::kRingOffset) + warp * R * kKeysPerWarp;
+    const uint32_t ring_addr = smem_addr(ring);
+    auto fetch_slots = [&](int t) {
+        if (lane < kKeysPerWarp) {
+            const int64_t k = (int64_t)t * kTileKeys + warp * kKeysPerWarp + lane;
+            const bool in = k < cnt;
+            cp_async_4(ring_addr + ((t % R) * kKeysPerWarp + lane) * 4,
+                       in ? static_cast<const void *>(trow + k) : static_cast<const void *>(table),
+                       in ? 4u : 0u);
+        }
     };
-    // Issue the copies of tile t (stage t % S) from the slots held by lanes 0-15.
-    auto issue = [&](int t, int32_t my_slot) {
+    // Issue the K/V gathers of tile t (stage t % S); its slots are in the ring.
+    auto issue = [&](int t) {
         const int st = t % S;
+        const int32_t my_slot = lane < kKeysPerWarp ? ring[(t % R) * kKeysPerWarp + lane] : 0;
         const int64_t k = (int64_t)t * kTileKeys + warp * kKeysPerWarp + (lane & 15);
         const bool in = lane < kKeysPerWarp && k < cnt;
         const bool ok = in && my_slot >= 0 && my_slot < num_slots;
@@ -158,43 +196,27 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         const int col = (lane % kLanesPerRow) * 16;
 #pragma unroll
         for (int r0 = 0; r0 < kKeysPerWarp; r0 += kRowsPerInst) {
-            const int r = r0 + sub;
-            const int32_t slot = __shfl_sync(0xffffffffu, my_slot, r);
-            const bool rv = (vm >> r) & 1u;
-            const size_t off = rv ? (size_t)slot * slot_bytes + col : 0;
-            cp_async_16(kdst + r * C::kPitch + col, kbase + off, rv ? 16u : 0u, policy);
-            cp_async_16(vdst + r * C::kPitch + col, vbase + off, rv ? 16u : 0u, policy);
+            const int key = r0 + sub;
+            const int32_t slot = __shfl_sync(0xffffffffu, my_slot, key);
+            const bool kv = (vm >> key) & 1u;
+            const size_t off = kv ? (size_t)slot * slot_bytes + col : 0;
+            cp_async_16(kdst + key * C::kPitch + col, kbase + off, kv ? 16u : 0u, policy);
+            cp_async_16(vdst + key * C::kPitch + col, vbase + off, kv ? 16u : 0u, policy);
         }
     };
 
-    {
-        int32_t pro[S - 1];
+    // Prologue: slots of the first 2S-1 tiles, then K/V of the first S-1.
+    for (int t = 0; t < 2 * S - 1 && t < n_tiles; ++t) fetch_slots(t);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
 #pragma unroll
-        for (int t = 0; t < S - 1; ++t) pro[t] = load_slot(t);
-#pragma unroll
-        for (int t = 0; t < S - 1; ++t) {
-            if (t < n_tiles) issue(t, pro[t]);
-            cp_async_commit();
-        }
+    for (int t = 0; t < S - 1; ++t) {
+        if (t < n_tiles) issue(t);
+        cp_async_commit();
     }
-    int32_t next_slot = load_slot(S - 1);
 
     // -------------------------------------------------------------- compute
-    const int r = lane >> 2;  // MMA group: key row (QK) / output dim row (PV)
-    const int c = lane & 3;   // thread in group: query-head pair 2c, 2c+1
-    constexpr int KD = D / 16;
-
-    uint32_t qf[KD][2];
-    {
-        const bool live = r < G;
-        const __nv_bfloat16 *qrow = q + (bt * H_q + (int64_t)g * G + (live ? r : 0)) * D;
-#pragma unroll
-        for (int kd = 0; kd < KD; ++kd) {
-            qf[kd][0] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c)) : 0u;
-            qf[kd][1] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c + 8)) : 0u;
-        }
-    }
-
     float o[KD][4];
 #pragma unroll
     for (int dt = 0; dt < KD; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
@@ -205,9 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const uint32_t v_off = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * C::kPitch + ((lane >> 3) & 1) * 16);
 
     for (int it = 0; it < n_tiles; ++it) {
-        if (it + S - 1 < n_tiles) issue(it + S - 1, next_slot);
+        // Groups committed so far: slots, K/V of tiles 0..S-2, then one group
+        // per iteration; waiting for all but the newest S-1 makes tile `it`
+        // (and the slots of tile it+S) resident.
+        if (it + S - 1 < n_tiles) issue(it + S - 1);
+        if (it + 2 * S - 1 < n_tiles) fetch_slots(it + 2 * S - 1);
         cp_async_commit();
-        next_slot = load_slot(it + S);
         cp_async_wait<S - 1>();
         __syncwarp();
         const int st = it % S;
@@ -215,22 +240,23 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         if (wm) {
             const uint32_t kaddr = wsm_addr + st * C::kWarpStage + k_off;
             const uint32_t vaddr = wsm_addr + st * C::kWarpStage + C::kWarpTile + v_off;
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            // Four independent accumulation chains over the head dimension.
+            float sacc[4][4] = {};
 #pragma unroll
             for (int kd = 0; kd < KD; ++kd) {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(kaddr + kd * 32, a0, a1, a2, a3);
-                if (kd & 1)
-                    mma_bf16_16816(sb, a0, a1, a2, a3, qf[kd][0], qf[kd][1]);
-                else
-                    mma_bf16_16816(sa, a0, a1, a2, a3, qf[kd][0], qf[kd][1]);
+                mma_bf16_16816(sacc[kd & 3], a0, a1, a2, a3, qf[kd][0], qf[kd][1]);
             }
-            // s[0]: key r, head 2c; s[1]: key r, head 2c+1; s[2], s[3]: key r+8.
+            float sc[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sc[i] = (sacc[0][i] + sacc[1][i]) + (sacc[2][i] + sacc[3][i]);
+            // sc[0]: key r, head 2c; sc[1]: key r, head 2c+1; sc[2], sc[3]: key r+8.
             const bool ok_lo = (wm >> r) & 1u, ok_hi = (wm >> (r + 8)) & 1u;
-            const float x0 = ok_lo ? (sa[0] + sb[0]) * scale_log2 : -INFINITY;
-            const float x1 = ok_lo ? (sa[1] + sb[1]) * scale_log2 : -INFINITY;
-            const float x2 = ok_hi ? (sa[2] + sb[2]) * scale_log2 : -INFINITY;
-            const float x3 = ok_hi ? (sa[3] + sb[3]) * scale_log2 : -INFINITY;
+            const float x0 = ok_lo ? sc[0] * scale_log2 : -INFINITY;
+            const float x1 = ok_lo ? sc[1] * scale_log2 : -INFINITY;
+            const float x2 = ok_hi ? sc[2] * scale_log2 : -INFINITY;
+            const float x3 = ok_hi ? sc[3] * scale_log2 : -INFINITY;
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
             for (int sh = 4; sh < 32; sh <<= 1) {
@@ -245,12 +271,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
             l1 = l1 * al1 + (p1 + p3);
             m0 = mn0;
             m1 = mn1;
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {  // a running max moved
 #pragma unroll
-            for (int dt = 0; dt < KD; ++dt) {
-                o[dt][0] *= al0;
-                o[dt][1] *= al1;
-                o[dt][2] *= al0;
-                o[dt][3] *= al1;
+                for (int dt = 0; dt < KD; ++dt) {
+                    o[dt][0] *= al0;
+                    o[dt][1] *= al1;
+                    o[dt][2] *= al0;
+                    o[dt][3] *= al1;
+                }
             }
             // P^T as the B operand: keys 2c,2c+1 (and +8) for query head r.
             // P is split into a bf16 head and a bf16 tail (p = hi + lo to about
@@ -285,7 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     float *ow = reinterpret_cast<float *>(smem);                       // [warp][head][kOPitch]
     float *mw = ow + kConsumerWarps * kMaxGroup * C::kOPitch;          // [warp][head]
     float *lw = mw + kConsumerWarps * kMaxGroup;                       // [warp][head]
-    float *wts = lw + kConsumerWarps * kMaxGroup;                      // merge weights
+    float *part_o = lw + kConsumerWarps * kMaxGroup;                   // [head][D] (cluster)
+    float *part_lse = part_o + kMaxGroup * D;                          // [head]
+    float *wts = part_lse + kMaxGroup;                                 // scratch for merges
     {
         float *o_lo = ow + (warp * kMaxGroup + 2 * c) * C::kOPitch;
         float *o_hi = o_lo + C::kOPitch;
@@ -307,32 +337,86 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
 
     const int tid = threadIdx.x;
     const int64_t row_q0 = bt * H_q + (int64_t)g * G;  // first query row of the group
-    for (int e = tid; e < G * D; e += kThreads) {
-        const int h = e / D, dim = e - h * D;
+    // Per query head: the CTA max, each warp's factor 2^(m_w - M) / L and the
+    // CTA's lse, computed once; then every output element is four FMAs.
+    float *fac = wts;                                    // [head][warp]
+    float *cta_lse = fac + kMaxGroup * kConsumerWarps;   // [head]
+    if (tid < G) {
+        const int h = tid;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w * kMaxGroup + h]);
-        float Ls = 0.f, O = 0.f;
-        if (M != -INFINITY) {
+        float f[kConsumerWarps], Ls = 0.f;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float f = exp2f(mw[w * kMaxGroup + h] - M);
-                Ls += lw[w * kMaxGroup + h] * f;
-                O += ow[(w * kMaxGroup + h) * C::kOPitch + dim] * f;
-            }
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            f[w] = M == -INFINITY ? 0.f : exp2f(mw[w * kMaxGroup + h] - M);
+            Ls += lw[w * kMaxGroup + h] * f[w];
         }
-        const bool empty_part = !(Ls > 0.f);
-        const float o_val = empty_part ? 0.f : O / Ls;
-        const float lse2 = empty_part ? -INFINITY : M + log2f(Ls);
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) fac[h * kConsumerWarps + w] = f[w] * inv;
+        cta_lse[h] = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
+    }
+    __syncthreads();
+    for (int e = tid; e < G * D; e += kThreads) {
+        const int h = e / D, dim = e - h * D;
+        float o_val = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w)
+            o_val += ow[(w * kMaxGroup + h) * C::kOPitch + dim] * fac[h * kConsumerWarps + w];
+        const float lse2 = cta_lse[h];
         if (n_split == 1) {
             out[(row_q0 + h) * D + dim] = o_val;
             if (lse && dim == 0) lse[row_q0 + h] = lse2 * kLn2;
+        } else if (cluster_merge) {
+            part_o[h * D + dim] = o_val;
+            if (dim == 0) part_lse[h] = lse2;
         } else {
             ws.o_part[((row_q0 + h) * n_split + split) * D + dim] = o_val;
             if (dim == 0) ws.lse_part[(row_q0 + h) * n_split + split] = lse2;
         }
     }
     if (n_split == 1) return;
+
+    if (cluster_merge) {
+        // ---------------------------------- merge through distributed smem
+        // The n_split CTAs of this (row, KV head) form one cluster; CTA `rank`
+        // merges a slice of the G x D outputs, reading every CTA's partial
+        // in split order.  The second barrier keeps each CTA's shared memory
+        // alive until all peers have read it.
+        cluster_sync();
+        const int rank = (int)cluster_ctarank();
+        const int total = G * D;
+        const int per = (total + n_split - 1) / n_split;
+        const int lo = rank * per;
+        const int hi = lo + per < total ? lo + per : total;
+        const uint32_t po_addr = smem_addr(part_o), pl_addr = smem_addr(part_lse);
+        for (int e = lo + tid; e < hi; e += kThreads) {
+            const int h = e / D, dim = e - h * D;
+            float ls[kMaxClusterMerge];
+            float M = -INFINITY;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxClusterMerge; ++s2) {
+                ls[s2] = s2 < n_split ? ld_dsmem_f32(map_to_rank(pl_addr + h * 4, s2)) : -INFINITY;
+                M = fmaxf(M, ls[s2]);
+            }
+            float sum = 0.f, acc = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxClusterMerge; ++s2) {
+                    if (s2 < n_split && ls[s2] != -INFINITY) {
+                        const float w = exp2f(ls[s2] - M);
+                        sum += w;
+                        acc += w * ld_dsmem_f32(map_to_rank(po_addr + e * 4, s2));
+                    }
+                }
+            }
+            out[(row_q0 + h) * D + dim] = sum > 0.f ? acc / sum : 0.f;
+            if (lse && dim == 0) lse[row_q0 + h] = sum > 0.f ? (M + log2f(sum)) * kLn2 : -INFINITY;
+        }
+        cluster_sync();
+        return;
+    }
 
     // ------------------------------------------ ticket; the last CTA merges
     __threadfence();
@@ -409,6 +493,36 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     if (tid == 0) ws.counters[bt * H_kv + g] = 0;  // ready for the next call
 }
 
+// Whether a cluster of `n` CTAs of this kernel can be resident on device
+// `dev` (cached per device and size).
+template <int D>
+bool cluster_merge_ok(int dev, int n) {
+    static int8_t known[64][kMaxClusterMerge + 1] = {};
+    if (n < 2 || n > kMaxClusterMerge || dev < 0 || dev >= 64) return false;
+    if (known[dev][n]) return known[dev][n] > 0;
+    bool ok = cudaFuncSetAttribute(split_decode_kernel<D>,
+                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    if (ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)n, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = (unsigned)n;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        ok = cudaOccupancyMaxActiveClusters(&clusters, split_decode_kernel<D>, &cfg) == cudaSuccess &&
+             clusters > 0;
+    }
+    cudaGetLastError();  // a refused query is not an error of this call
+    known[dev][n] = ok ? 1 : -1;
+    return ok;
+}
+
 template <int D>
 wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
                                 int32_t H_kv, const uint16_t *k_pool, const uint16_t *v_pool,
@@ -418,8 +532,6 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     using C = Cfg<D>;
     const int64_t rows_q = (int64_t)B * n_q * H_q;
     const int64_t rows_kv = (int64_t)B * n_q * H_kv;
-    WorkspaceView ws{nullptr, nullptr, nullptr};
-    if (n_split > 1) ws = carve(workspace, rows_q, rows_kv, n_split);
     // Opt in to the large shared-memory carve-out once per device (outside
     // any later stream capture of the launches).
     static int opted_in[64] = {0};
@@ -431,14 +543,19 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
             return WMTP_ECUDA;
         opted_in[dev] = 1;
     }
+    const bool use_cluster = n_split > 1 && cluster_merge_ok<D>(dev, n_split);
+    WorkspaceView ws{nullptr, nullptr, nullptr};
+    if (n_split > 1 && !use_cluster) ws = carve(workspace, rows_q, rows_kv, n_split);
     const float scale_log2 = scale * 1.4426950408889634f;
-    dim3 grid((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q));
-    split_decode_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(
-        reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q, H_kv, H_q / H_kv,
-        reinterpret_cast<const __nv_bfloat16 *>(k_pool),
+    PdlLaunch launch(dim3((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q)), dim3(kThreads),
+                     C::kSmemBytes, stream);
+    if (use_cluster) launch.add_cluster((unsigned)n_split);
+    const cudaError_t err = cudaLaunchKernelEx(
+        &launch.cfg, split_decode_kernel<D>, reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q,
+        H_kv, H_q / H_kv, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
         reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, table, table_stride, lens,
-        scale_log2, out, lse, ws, n_split);
-    return launch_status();
+        scale_log2, out, lse, ws, n_split, (int32_t)(use_cluster ? 1 : 0));
+    return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
 }  // namespace

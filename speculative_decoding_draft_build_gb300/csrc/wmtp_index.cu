@@ -13,6 +13,7 @@
 
 #include "wmtp.h"
 #include "wmtp_internal.h"
+#include "wmtp_ptx.cuh"
 
 namespace wmtp {
 namespace {
@@ -43,6 +44,8 @@ __global__ void __launch_bounds__(256) build_indices_kernel(
     const int32_t *__restrict__ req_to_token, const int32_t *__restrict__ req_pool_idx,
     int64_t rtt_stride, const int32_t *__restrict__ ring_base, int32_t *__restrict__ table,
     int64_t stride, int32_t *__restrict__ lens) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int32_t row = blockIdx.y;
     const int32_t j = row / B;
     const int32_t b = row - j * B;
@@ -81,6 +84,8 @@ __global__ void __launch_bounds__(256) ring_map_kernel(
     const int32_t *__restrict__ ring_base, const int32_t *__restrict__ pos,
     const int32_t *__restrict__ branch, const int32_t *__restrict__ req_of, int32_t n,
     int32_t n_sink, int32_t window, int32_t depth, int32_t tree_k, int32_t *__restrict__ slots) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const int32_t br = branch ? branch[i] : 0;
@@ -98,6 +103,8 @@ __global__ void __launch_bounds__(256) append_kv_kernel(
     const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
     const int32_t *__restrict__ slots, int64_t total, int32_t chunks_per_token,
     uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, int64_t num_slots) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= total) return;
     const int64_t i = idx / chunks_per_token;
@@ -168,11 +175,12 @@ wmtp_status wmtp_build_draft_indices(const int32_t *seq_lens, int32_t B, int32_t
     constexpr int64_t kPerCta = kThreads * 4;
     int64_t gx = (stride + kPerCta - 1) / kPerCta;
     if (gx > 8192) gx = 8192;
-    dim3 grid((unsigned)gx, (unsigned)(gamma * B));
-    build_indices_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(
-        seq_lens, B, n_sink, window, depth, tree_k, windowed, req_to_token, req_pool_idx,
-        rtt_stride, ring_base, table, stride, lens);
-    return launch_status();
+    PdlLaunch L(dim3((unsigned)gx, (unsigned)(gamma * B)), dim3(kThreads), 0, as_stream(stream));
+    return cudaLaunchKernelEx(&L.cfg, build_indices_kernel, seq_lens, B, n_sink, window, depth,
+                              tree_k, windowed, req_to_token, req_pool_idx, rtt_stride, ring_base,
+                              table, stride, lens) == cudaSuccess
+               ? WMTP_OK
+               : WMTP_ECUDA;
 }
 
 wmtp_status wmtp_ring_map(const int32_t *ring_base, const int32_t *pos,
@@ -183,9 +191,11 @@ wmtp_status wmtp_ring_map(const int32_t *ring_base, const int32_t *pos,
     if (n == 0) return WMTP_OK;
     if (!ring_base || !pos || !req_of || !slots) return WMTP_EINVAL;
     constexpr int kThreads = 256;
-    ring_map_kernel<<<(n + kThreads - 1) / kThreads, kThreads, 0, as_stream(stream)>>>(
-        ring_base, pos, branch, req_of, n, n_sink, window, depth, tree_k, slots);
-    return launch_status();
+    PdlLaunch L(dim3((unsigned)((n + kThreads - 1) / kThreads)), dim3(kThreads), 0, as_stream(stream));
+    return cudaLaunchKernelEx(&L.cfg, ring_map_kernel, ring_base, pos, branch, req_of, n, n_sink,
+                              window, depth, tree_k, slots) == cudaSuccess
+               ? WMTP_OK
+               : WMTP_ECUDA;
 }
 
 wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
@@ -201,11 +211,13 @@ wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
     const int64_t total = (int64_t)n * chunks;
     constexpr int kThreads = 256;
     const int64_t blocks = (total + kThreads - 1) / kThreads;
-    append_kv_kernel<<<(unsigned)blocks, kThreads, 0, as_stream(stream)>>>(
-        reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), slots,
-        total, chunks, reinterpret_cast<uint4 *>(k_pool), reinterpret_cast<uint4 *>(v_pool),
-        num_slots);
-    return launch_status();
+    PdlLaunch L(dim3((unsigned)blocks), dim3(kThreads), 0, as_stream(stream));
+    return cudaLaunchKernelEx(&L.cfg, append_kv_kernel, reinterpret_cast<const uint4 *>(k_new),
+                              reinterpret_cast<const uint4 *>(v_new), slots, total, chunks,
+                              reinterpret_cast<uint4 *>(k_pool), reinterpret_cast<uint4 *>(v_pool),
+                              num_slots) == cudaSuccess
+               ? WMTP_OK
+               : WMTP_ECUDA;
 }
 
 }  // extern "C"

@@ -22,4 +22,30 @@ inline wmtp_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
+// Launch configuration with programmatic stream serialization: the kernel may
+// begin launching while the previous kernel in the stream drains; every
+// kernel of this library calls griddepcontrol.wait before touching global
+// memory, so ordering is unchanged and only launch latency is hidden.
+struct PdlLaunch {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attrs[2]{};
+    PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attrs;
+        cfg.numAttrs = 1;
+    }
+    void add_cluster(unsigned x) {
+        attrs[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attrs[cfg.numAttrs].val.clusterDim.x = x;
+        attrs[cfg.numAttrs].val.clusterDim.y = 1;
+        attrs[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
+    }
+};
+
 }  // namespace wmtp

@@ -50,7 +50,9 @@ def test_attn_sizes_and_splits(D, H_q, H_kv):
         q = synth.normal_bf16((B, 1, H_q, D), seed + L, DEV)
         table = torch.stack([synth.permutation(num_slots, seed + L + b, DEV) for b in range(B)])
         lens = torch.tensor([L, max(L - 7, 0), min(L + 5, num_slots)], dtype=torch.int32, device=DEV)
-        for n_split in (1, 2, 3, 7, None):
+        # n_split <= 16 merges through a thread-block cluster, larger counts
+        # through the workspace ticket; both paths are covered
+        for n_split in (1, 2, 3, 7, 16, 20, 37, None):
             out, lse, ro, rl = _run_both(q, kp, vp, table, lens, 1 / math.sqrt(D), n_split)
             assert_attn_close(out, lse, ro, rl, what=f"D={D} G={H_q // H_kv} L={L} split={n_split}")
 
@@ -64,7 +66,7 @@ def test_attn_many_query_tokens_and_empty_rows():
     q = synth.normal_bf16((B, n_q, H_q, D), 23, DEV)
     table = torch.stack([synth.permutation(num_slots, 24 + b, DEV) for b in range(B)])
     lens = torch.tensor([0, 700, 1, 333], dtype=torch.int32, device=DEV)
-    for n_split in (1, 4, 11):
+    for n_split in (1, 4, 11, 17):
         out, lse, ro, rl = _run_both(q, kp, vp, table, lens, 0.0625, n_split)
         assert_attn_close(out, lse, ro, rl, what=f"n_q=3 split={n_split}")
         assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
@@ -95,6 +97,10 @@ def test_attn_deterministic_and_split_consistent():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
     c = wm.draft_decode_attn(q, kp, vp, table, lens, 0.0625, n_split=2)
     torch.testing.assert_close(a[0], c[0], atol=2e-3, rtol=1e-2)
+    d1 = wm.draft_decode_attn(q, kp, vp, table, lens, 0.0625, n_split=40)
+    d2 = wm.draft_decode_attn(q, kp, vp, table, lens, 0.0625, n_split=40)
+    assert torch.equal(d1[0], d2[0]) and torch.equal(d1[1], d2[1])
+    torch.testing.assert_close(a[0], d1[0], atol=2e-3, rtol=1e-2)
 
 
 def test_attn_tiny_windowed_workload():
