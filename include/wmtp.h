@@ -193,6 +193,39 @@ wmtp_status wmtp_draft_decode_attn(const uint16_t *q, int32_t B, int32_t n_q,
                                    size_t workspace_bytes, int32_t n_split,
                                    void *stream);
 
+/* ------------------------------------------------------------------------
+ * Draft attention without a caller-provided workspace.
+ * The paper has no counterpart to this call; it exists for callers that
+ * cannot hand the library a workspace: an engine that has reserved nearly
+ * all device memory for its KV pool and its own allocator (a cudaMalloc
+ * there fails, or stalls the device while it runs), or a plugin boundary
+ * that passes only input and output pointers.
+ *
+ * Same computation, arguments and checks as wmtp_draft_decode_attn minus
+ * the workspace.  With n_split > 1 the partials always merge through the
+ * "last CTA merges" path, in a scratch array that the library holds in
+ * device memory: WMTP_NOALLOC_SCRATCH_BYTES per device that loads the
+ * library, kept until the process exits.  The call allocates nothing.
+ *   - A call needing more scratch than that -- B * n_q * H_kv merge
+ *     counters above WMTP_NOALLOC_MAX_COUNTERS, or partials of
+ *     B * n_q * H_q * n_split * (D + 1) floats beyond the rest of the
+ *     array -- returns WMTP_ECAPACITY before launching anything.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make that first call before any stream
+ *     capture.  A failed lookup returns WMTP_ECUDA.
+ *   - Every call shares the one array and it keeps the last call's
+ *     contents; each call first zeroes the merge counters it uses (an
+ *     async memset on `stream`).  Calls that overlap on the GPU (other
+ *     streams, other threads) race on the array: serialise them. */
+#define WMTP_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define WMTP_NOALLOC_MAX_COUNTERS 4096
+wmtp_status wmtp_draft_decode_attn_noalloc(
+    const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q, int32_t H_kv,
+    int32_t D, const uint16_t *k_pool, const uint16_t *v_pool,
+    int64_t num_slots, const int32_t *table, int64_t table_stride,
+    const int32_t *lens, float scale, float *out, float *lse, int32_t n_split,
+    void *stream);
+
 #ifdef __cplusplus
 }
 #endif

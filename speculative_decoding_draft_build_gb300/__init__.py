@@ -26,7 +26,7 @@ from . import _build
 __all__ = [
     "WmtpError", "load", "build", "version", "device_error",
     "build_draft_indices", "ring_map", "append_kv", "draft_decode_attn",
-    "attn_workspace_bytes", "attn_num_splits", "AttnWorkspace",
+    "attn_workspace_bytes", "attn_num_splits", "AttnWorkspace", "draft_decode_attn_noalloc",
 ]
 
 WMTP_OK = 0
@@ -93,6 +93,10 @@ def load():
         lib.wmtp_draft_decode_attn.argtypes = [
             _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, ctypes.c_float,
             _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
+        lib.wmtp_draft_decode_attn_noalloc.restype = _i32
+        lib.wmtp_draft_decode_attn_noalloc.argtypes = [
+            _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, ctypes.c_float,
+            _vp, _vp, _i32, _vp]
         _lib = lib
         return lib
 
@@ -306,4 +310,31 @@ def draft_decode_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
             _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
             stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf),
             workspace.nbytes, n_split, _stream(stream)), "draft_decode_attn")
+    return out, lse
+
+
+def draft_decode_attn_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                              table: torch.Tensor, lens: torch.Tensor, scale: float,
+                              out: torch.Tensor, lse: torch.Tensor, n_split: int, stream=None):
+    """``wmtp_draft_decode_attn_noalloc``: the same attention as
+    :func:`draft_decode_attn`, for callers that cannot provide a workspace
+    (the library uses a fixed scratch array it holds on the device).  The
+    outputs must be passed in; nothing is allocated on this path.  The first
+    call on a device looks up the scratch address: make it before any stream
+    capture.  Calls that overlap on the GPU share the scratch and race."""
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    for t, nm in ((k_pool, "k_pool"), (v_pool, "v_pool")):
+        _need(t, nm, torch.bfloat16, dev)
+    _need(table, "table", torch.int32, dev)
+    _need(lens, "lens", torch.int32, dev)
+    _need(out, "out", torch.float32, dev)
+    _need(lse, "lse", torch.float32, dev)
+    B, n_q, H_q, D = q.shape
+    num_slots, H_kv, _ = k_pool.shape
+    with torch.cuda.device(dev):
+        _check(load().wmtp_draft_decode_attn_noalloc(
+            _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
+            table.shape[-1], _ptr(lens), float(scale), _ptr(out), _ptr(lse), n_split,
+            _stream(stream)), "draft_decode_attn_noalloc")
     return out, lse

@@ -558,6 +558,72 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
+// ------------------------------------------------ scratch without allocation
+// Device scratch for wmtp_draft_decode_attn_noalloc: a fixed region of merge
+// counters, then the split partials (lse, then o).  Every device that loads
+// the library holds it until the process exits.
+constexpr size_t kNoAllocBytes = WMTP_NOALLOC_SCRATCH_BYTES;
+constexpr size_t kNoAllocCounterBytes = (size_t)WMTP_NOALLOC_MAX_COUNTERS * 4;
+static_assert(kNoAllocCounterBytes % 256 == 0, "partials must stay 256-byte aligned");
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
+
+// Device address of the scratch array on the current device `dev`, looked up
+// once per device (host code cannot use the symbol itself as an address).
+void *noalloc_scratch(int dev) {
+    static void *addr[64] = {};
+    if (dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+// Bytes of partials (after the counter region) a call needs.
+inline size_t noalloc_partial_bytes(int64_t rows_q, int D, int n_split) {
+    return align256((size_t)rows_q * n_split * 4) + (size_t)rows_q * n_split * D * 4;
+}
+
+template <int D>
+wmtp_status launch_split_decode_noalloc(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
+                                        int32_t H_kv, const uint16_t *k_pool,
+                                        const uint16_t *v_pool, int64_t num_slots,
+                                        const int32_t *table, int64_t table_stride,
+                                        const int32_t *lens, float scale, float *out, float *lse,
+                                        int32_t n_split, cudaStream_t stream) {
+    using C = Cfg<D>;
+    const int64_t rows_q = (int64_t)B * n_q * H_q;
+    const int64_t rows_kv = (int64_t)B * n_q * H_kv;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WMTP_ECUDA;
+    WorkspaceView ws{nullptr, nullptr, nullptr};
+    if (n_split > 1) {
+        uint8_t *base = static_cast<uint8_t *>(noalloc_scratch(dev));
+        if (!base) return WMTP_ECUDA;
+        ws.counters = reinterpret_cast<int32_t *>(base);
+        ws.lse_part = reinterpret_cast<float *>(base + kNoAllocCounterBytes);
+        ws.o_part = reinterpret_cast<float *>(base + kNoAllocCounterBytes +
+                                              align256((size_t)rows_q * n_split * 4));
+        // The array keeps the previous call's contents: the counters this
+        // call uses must start at zero.
+        if (cudaMemsetAsync(ws.counters, 0, (size_t)rows_kv * 4, stream) != cudaSuccess)
+            return WMTP_ECUDA;
+    }
+    if (cudaFuncSetAttribute(split_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+        return WMTP_ECUDA;
+    const float scale_log2 = scale * 1.4426950408889634f;
+    PdlLaunch launch(dim3((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q)), dim3(kThreads),
+                     C::kSmemBytes, stream);
+    const cudaError_t err = cudaLaunchKernelEx(
+        &launch.cfg, split_decode_kernel<D>, reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q,
+        H_kv, H_q / H_kv, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
+        reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, table, table_stride, lens,
+        scale_log2, out, lse, ws, n_split, (int32_t)0);
+    return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
+}
+
 }  // namespace
 
 cudaError_t read_attn_error(int32_t *code, bool clear) {
@@ -630,6 +696,38 @@ wmtp_status wmtp_draft_decode_attn(const uint16_t *q, int32_t B, int32_t n_q, in
                                         table_stride, lens, scale, out, lse, workspace, n_split, s);
     return launch_split_decode<128>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
                                     table_stride, lens, scale, out, lse, workspace, n_split, s);
+}
+
+wmtp_status wmtp_draft_decode_attn_noalloc(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
+                                           int32_t H_kv, int32_t D, const uint16_t *k_pool,
+                                           const uint16_t *v_pool, int64_t num_slots,
+                                           const int32_t *table, int64_t table_stride,
+                                           const int32_t *lens, float scale, float *out,
+                                           float *lse, int32_t n_split, void *stream) {
+    if (B < 0 || n_q < 0 || H_q < 1 || H_kv < 1 || (H_q % H_kv) != 0) return WMTP_EINVAL;
+    if (H_q / H_kv > kMaxGroup) return WMTP_EINVAL;
+    if (D != 128 && D != 256) return WMTP_EINVAL;
+    if (n_split < 1 || n_split > kMaxSplits || table_stride < 1 || num_slots < 0)
+        return WMTP_EINVAL;
+    if ((int64_t)B * n_q > 65535 || H_kv > 65535) return WMTP_EINVAL;
+    if (B == 0 || n_q == 0) return WMTP_OK;
+    if (!q || !k_pool || !v_pool || !table || !lens || !out) return WMTP_EINVAL;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(q) & 3u))
+        return WMTP_EINVAL;
+    if (n_split > 1) {
+        const int64_t rows_q = (int64_t)B * n_q * H_q;
+        const int64_t rows_kv = (int64_t)B * n_q * H_kv;
+        if (rows_kv > WMTP_NOALLOC_MAX_COUNTERS ||
+            noalloc_partial_bytes(rows_q, D, n_split) > kNoAllocBytes - kNoAllocCounterBytes)
+            return WMTP_ECAPACITY;
+    }
+    cudaStream_t s = as_stream(stream);
+    if (D == 256)
+        return launch_split_decode_noalloc<256>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots,
+                                                table, table_stride, lens, scale, out, lse, n_split, s);
+    return launch_split_decode_noalloc<128>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
+                                            table_stride, lens, scale, out, lse, n_split, s);
 }
 
 }  // extern "C"
