@@ -456,7 +456,7 @@ def run_ours(args, dist_ctx):
             "frac": round(full_gbs / peak, 4),
             "peak_kind": peak_kind,
             "bytes_per_launch": int(full_bytes / g),
-            "traffic": profiled_traffic("full_1m"),
+            "traffic": profiled_traffic("full_1m") if args.workload == "1m" else None,
         },
         "roofline_windowed": {
             "kernel": "split_decode_kernel<256> (windowed draft attention)",
@@ -467,7 +467,7 @@ def run_ours(args, dist_ctx):
             "frac": round(win_gbs / peak, 4),
             "peak_kind": peak_kind,
             "bytes_per_launch": int(win_bytes / g),
-            "traffic": None,
+            "traffic": profiled_traffic("windowed_4096") if args.workload == "1m" else None,
         },
         "gpu_launches": K * 2 * (1 + 2 * g),
         "clocks": sampler.summary(),
