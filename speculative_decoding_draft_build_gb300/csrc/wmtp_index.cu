@@ -14,6 +14,7 @@
 #include "wmtp.h"
 #include "wmtp_internal.h"
 #include "wmtp_ptx.cuh"
+#include "wmtp_ring.cuh"
 
 namespace wmtp {
 namespace {
@@ -21,19 +22,6 @@ namespace {
 __device__ int32_t g_index_error = 0;
 
 __device__ __forceinline__ void latch(int32_t code) { atomicCAS(&g_index_error, 0, code); }
-
-// Ring slot of logical position p on tree branch `branch` (see wmtp_ring_map
-// in wmtp.h): sinks pinned on branch 0, everything else rolls over
-// W + d*k slots after them, each branch shifted by branch * d.
-__device__ __forceinline__ int64_t ring_slot(int64_t base, int64_t p, int64_t branch,
-                                             int64_t n_sink, int64_t window,
-                                             int64_t depth, int64_t tree_k) {
-    if (p < n_sink && branch == 0) return base + p;
-    const int64_t m = window + depth * tree_k;
-    int64_t r = (p - n_sink + branch * depth) % m;
-    if (r < 0) r += m;
-    return base + n_sink + r;
-}
 
 // One grid row (blockIdx.y) per (draft step j, request b); the x dimension
 // strides over the row's entries.  Entry e of a windowed row is position e
