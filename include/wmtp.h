@@ -194,6 +194,50 @@ wmtp_status wmtp_draft_decode_attn(const uint16_t *q, int32_t B, int32_t n_q,
                                    void *stream);
 
 /* ------------------------------------------------------------------------
+ * Tree-draft attention over the ring.
+ * "Windowed-MTP" §7 "Compatibility with tree speculation": windowing changes
+ * only which KV the draft reads, not the tree; a tree of width k reserves
+ * n_sink + W + d*k ring slots per request and its candidates share the
+ * sink + window prefix, diverging over the last d positions.  This library's
+ * reading (the pages leave the tree open): node (branch b, depth i), b < k,
+ * i < d, of a request with committed length S sits at logical position S + i
+ * and attends the positions App. A's keep rule gives for kv length S + i + 1,
+ * where positions below S are committed tokens (ring branch 0) and positions
+ * S..S+i are the nodes of its own branch (ring branch b, see wmtp_ring_map).
+ * For k = 1 this is exactly the chain of wmtp_build_draft_indices +
+ * wmtp_draft_decode_attn.  Slots are computed in the kernel from ring_base:
+ * no table is read.
+ *
+ * q         device bf16 [B][k*d][H_q][D], node t = b*d + i; 16-byte aligned.
+ * seq_lens  device int32 [B] (committed length S); ring_base device int32 [B].
+ * out       device fp32 [B][k*d][H_q][D], 16-byte aligned; lse fp32 [B][k*d][H_q]
+ *           or NULL.
+ * workspace >= wmtp_tree_workspace_bytes(...), 256-byte aligned; its merge
+ *           counters must be zero at the first call (wmtp_attn_workspace_init
+ *           zeroes a whole workspace) and every completed call leaves them
+ *           zero.  Unused when n_split == 1.
+ * n_split   1 .. 64 key chunks per request; wmtp_tree_num_splits() gives one.
+ * Errors: WMTP_EINVAL for null or misaligned pointers, bad sizes, D not
+ * 128/256, H_q % H_kv != 0, W < 1, d < 1, k < 1; WMTP_ECAPACITY for a small
+ * workspace; slots outside the pool latch WMTP_DEV_SLOT_RANGE. */
+size_t wmtp_tree_workspace_bytes(int32_t B, int32_t H_q, int32_t H_kv,
+                                 int32_t D, int32_t depth, int32_t tree_k,
+                                 int32_t n_split);
+int32_t wmtp_tree_num_splits(int32_t B, int32_t H_q, int32_t H_kv,
+                             int32_t depth, int32_t tree_k, int32_t n_sink,
+                             int32_t window);
+wmtp_status wmtp_tree_draft_attn(const uint16_t *q, int32_t B, int32_t H_q,
+                                 int32_t H_kv, int32_t D,
+                                 const uint16_t *k_pool,
+                                 const uint16_t *v_pool, int64_t num_slots,
+                                 const int32_t *seq_lens,
+                                 const int32_t *ring_base, int32_t n_sink,
+                                 int32_t window, int32_t depth, int32_t tree_k,
+                                 float scale, float *out, float *lse,
+                                 void *workspace, size_t workspace_bytes,
+                                 int32_t n_split, void *stream);
+
+/* ------------------------------------------------------------------------
  * Draft attention without a caller-provided workspace.
  * The paper has no counterpart to this call; it exists for callers that
  * cannot hand the library a workspace: an engine that has reserved nearly

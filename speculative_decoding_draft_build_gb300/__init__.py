@@ -12,6 +12,7 @@ Calls (same names as the C ABI without the ``wmtp_`` prefix):
   ring_map             logical position -> ring slot
   append_kv            write draft K/V rows into the pool
   draft_decode_attn    split-KV flash-decode attention with LSE merge
+  tree_draft_attn      tree-draft attention over the ring (tree-causal mask)
 """
 from __future__ import annotations
 
@@ -27,6 +28,7 @@ __all__ = [
     "WmtpError", "load", "build", "version", "device_error",
     "build_draft_indices", "ring_map", "append_kv", "draft_decode_attn",
     "attn_workspace_bytes", "attn_num_splits", "AttnWorkspace", "draft_decode_attn_noalloc",
+    "tree_draft_attn", "tree_workspace_bytes", "tree_num_splits",
 ]
 
 WMTP_OK = 0
@@ -93,6 +95,14 @@ def load():
         lib.wmtp_draft_decode_attn.argtypes = [
             _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, ctypes.c_float,
             _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
+        lib.wmtp_tree_workspace_bytes.restype = ctypes.c_size_t
+        lib.wmtp_tree_workspace_bytes.argtypes = [_i32] * 7
+        lib.wmtp_tree_num_splits.restype = _i32
+        lib.wmtp_tree_num_splits.argtypes = [_i32] * 7
+        lib.wmtp_tree_draft_attn.restype = _i32
+        lib.wmtp_tree_draft_attn.argtypes = [
+            _vp, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32,
+            ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
         lib.wmtp_draft_decode_attn_noalloc.restype = _i32
         lib.wmtp_draft_decode_attn_noalloc.argtypes = [
             _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, ctypes.c_float,
@@ -337,4 +347,65 @@ def draft_decode_attn_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: tor
             _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
             table.shape[-1], _ptr(lens), float(scale), _ptr(out), _ptr(lse), n_split,
             _stream(stream)), "draft_decode_attn_noalloc")
+    return out, lse
+
+
+def tree_workspace_bytes(B: int, H_q: int, H_kv: int, D: int, depth: int, tree_k: int,
+                         n_split: int) -> int:
+    return int(load().wmtp_tree_workspace_bytes(B, H_q, H_kv, D, depth, tree_k, n_split))
+
+
+def tree_num_splits(B: int, H_q: int, H_kv: int, depth: int, tree_k: int, n_sink: int,
+                    window: int, device=None) -> int:
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        return int(load().wmtp_tree_num_splits(B, H_q, H_kv, depth, tree_k, n_sink, window))
+
+
+def tree_draft_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                    seq_lens: torch.Tensor, ring_base: torch.Tensor, n_sink: int, window: int,
+                    depth: int, tree_k: int, scale: float, out: torch.Tensor | None = None,
+                    lse: torch.Tensor | None = None, n_split: int | None = None,
+                    workspace: AttnWorkspace | None = None, stream=None):
+    """Tree-draft attention over the ring (``wmtp_tree_draft_attn``).
+
+    q: [B, tree_k*depth, H_q, D] bf16 (node t = branch*depth + i); k_pool /
+    v_pool: [num_slots, H_kv, D] bf16 holding each request's ring at
+    ``ring_base``; seq_lens: committed lengths [B] int32.
+    Returns ``(out [B, k*d, H_q, D] fp32, lse [B, k*d, H_q] fp32)``.
+    """
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    for t, nm in ((k_pool, "k_pool"), (v_pool, "v_pool")):
+        _need(t, nm, torch.bfloat16, dev)
+    _need(seq_lens, "seq_lens", torch.int32, dev)
+    _need(ring_base, "ring_base", torch.int32, dev)
+    B, n_nodes, H_q, D = q.shape
+    if n_nodes != tree_k * depth:
+        raise ValueError("q must hold tree_k * depth nodes per request")
+    num_slots, H_kv, _ = k_pool.shape
+    if out is None:
+        out = torch.empty((B, n_nodes, H_q, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, n_nodes, H_q), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev)
+    _need(lse, "lse", torch.float32, dev)
+    if n_split is None:
+        n_split = tree_num_splits(B, H_q, H_kv, depth, tree_k, n_sink, window, dev)
+    need = tree_workspace_bytes(B, H_q, H_kv, D, depth, tree_k, n_split)
+    if workspace is None:
+        sid = torch.cuda.current_stream(dev).cuda_stream if stream is None else stream.cuda_stream
+        key = ("tree", dev, sid, B, H_q, H_kv, D, depth, tree_k, n_split)
+        ws = _ws_cache.get(key)
+        if ws is None:
+            ws = AttnWorkspace(need, dev, stream)
+            _ws_cache[key] = ws
+        workspace = ws
+    elif workspace.nbytes < need:
+        raise ValueError(f"workspace holds {workspace.nbytes} bytes, {need} needed")
+    with torch.cuda.device(dev):
+        _check(load().wmtp_tree_draft_attn(
+            _ptr(q), B, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(seq_lens),
+            _ptr(ring_base), n_sink, window, depth, tree_k, float(scale), _ptr(out), _ptr(lse),
+            _ptr(workspace.buf), workspace.nbytes, n_split, _stream(stream)), "tree_draft_attn")
     return out, lse

@@ -137,10 +137,11 @@ const char *wmtp_status_string(int32_t status) {
 wmtp_status wmtp_get_device_error(int32_t *code, int32_t clear) {
     if (!code) return WMTP_EINVAL;
     if (cudaDeviceSynchronize() != cudaSuccess) return WMTP_ECUDA;
-    int32_t a = 0, b = 0;
+    int32_t a = 0, b = 0, t = 0;
     if (read_index_error(&a, clear != 0) != cudaSuccess) return WMTP_ECUDA;
     if (read_attn_error(&b, clear != 0) != cudaSuccess) return WMTP_ECUDA;
-    *code = a ? a : b;
+    if (read_tree_error(&t, clear != 0) != cudaSuccess) return WMTP_ECUDA;
+    *code = a ? a : (b ? b : t);
     return WMTP_OK;
 }
 

@@ -13,6 +13,7 @@ namespace wmtp {
 // device code is needed); these read-and-optionally-clear them.
 cudaError_t read_index_error(int32_t *code, bool clear);
 cudaError_t read_attn_error(int32_t *code, bool clear);
+cudaError_t read_tree_error(int32_t *code, bool clear);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
