@@ -63,6 +63,14 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def attn_bytes(L, n_q, H_q, H_kv, D):
     """Algorithmic bytes of one attention launch over a table row of L keys:
     K and V rows of every KV head (bf16), the int32 table, q (bf16), out and
@@ -475,9 +483,66 @@ def run_ours(args, dist_ctx):
     }
 
     result["e2e"] = measure_e2e(w, args, dev)
+    if args.workload == "1m" and not args.no_tree:
+        result["tree"] = measure_tree(args, dev)
     if dist_ctx.rank == 0 and dist_ctx.world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args)
     return result
+
+
+def measure_tree(args, dev):
+    """Tree-draft attention (k=4 branches x d=7, B=8 requests with contexts
+    log-uniform in [32K, 1M], H_q=16, H_kv=2, D=256, n_sink=64) for each
+    window W: event-timed launches with L2 flushed before each, algorithmic
+    bytes (each ring key row once per KV head, q, out, lse) and useful flops
+    (4*D per visible key per query row)."""
+    import speculative_decoding_draft_build_gb300 as wm
+    from speculative_decoding_draft_build_gb300 import synth
+    B, k, d, H_q, H_kv, D, n_sink = 8, 4, 7, 16, 2, 256, 64
+    S_list = synth.log_uniform_lengths(B, 32_768, 1_048_576, 5000)
+    seq = torch.tensor(S_list, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    peak_hbm, _ = hbm_peak()
+    peak_tf = bf16_peak()
+    res = {}
+    reps = max(5, min(args.steps, 30))
+    for W in (1024, 2048, 4096, 8192):
+        R = n_sink + W + d * k
+        rb = torch.tensor(synth.ring_bases(B, R, B + 2, 5000 + W), dtype=torch.int32, device=dev)
+        kp = synth.normal_bf16(((B + 2) * R, H_kv, D), 5001 + W, dev)
+        vp = synth.normal_bf16(((B + 2) * R, H_kv, D), 5002 + W, dev)
+        q = synth.normal_bf16((B, k * d, H_q, D), 5003 + W, dev)
+        out = torch.empty((B, k * d, H_q, D), dtype=torch.float32, device=dev)
+        lse = torch.empty((B, k * d, H_q), dtype=torch.float32, device=dev)
+        ns = wm.tree_num_splits(B, H_q, H_kv, d, k, n_sink, W, dev)
+        ws = wm.AttnWorkspace(wm.tree_workspace_bytes(B, H_q, H_kv, D, d, k, ns), dev)
+        for _ in range(3):
+            wm.tree_draft_attn(q, kp, vp, seq, rb, n_sink, W, d, k, 1 / 16, out=out, lse=lse,
+                               n_split=ns, workspace=ws)
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            wm.tree_draft_attn(q, kp, vp, seq, rb, n_sink, W, d, k, 1 / 16, out=out, lse=lse,
+                               n_split=ns, workspace=ws)
+            b.record()
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b) * 1e-3)
+        t = statistics.median(ts)
+        keys = n_sink + W - 1 + k * d  # key list per request (contexts exceed the window)
+        nbytes = B * keys * H_kv * D * 2 * 2 + B * k * d * H_q * (D * 2 + (D + 1) * 4)
+        flops = B * k * d * H_q * (n_sink + W) * 4 * D
+        res[f"W={W}"] = {"us_per_launch": round(t * 1e6, 2), "kv_gbs": round(nbytes / t / 1e9, 1),
+                         "frac_of_hbm": round(nbytes / t / 1e9 / peak_hbm, 4),
+                         "tflops": round(flops / t / 1e12, 2),
+                         "frac_of_bf16_peak": round(flops / t / 1e12 / peak_tf, 4),
+                         "n_split": ns, "bytes_per_launch": int(nbytes), "flops_per_launch": int(flops)}
+        del kp, vp
+    return {"workload": "tree drafter: B=8, contexts log-uniform [32K, 1M], k=4, d=7 (28 nodes), "
+                        "H_q=16, H_kv=2, D=256, n_sink=64, ring of n_sink+W+d*k slots",
+            "timing": "CUDA events per launch, L2 flushed before each, median", "windows": res,
+            "kernel": "tree_decode_kernel<256> (mma.sync bf16)", "bf16_peak_tflops": peak_tf}
 
 
 def measure_e2e(w, args, dev):
@@ -633,6 +698,7 @@ def main(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="1m")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-tree", action="store_true", help="skip the tree-drafter measurement")
     args = p.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
