@@ -14,6 +14,13 @@ namespace wmtp {
 cudaError_t read_index_error(int32_t *code, bool clear);
 cudaError_t read_attn_error(int32_t *code, bool clear);
 cudaError_t read_tree_error(int32_t *code, bool clear);
+cudaError_t read_tree_tc_error(int32_t *code, bool clear);
+size_t tree_tc_workspace_bytes(int64_t B, int64_t H_kv, int64_t R, int D, int n_split);
+wmtp_status tree_tc_launch(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_kv, int32_t D,
+                           const uint16_t *k_pool, const uint16_t *v_pool, int64_t num_slots,
+                           const int32_t *seq_lens, const int32_t *ring_base, int32_t n_sink,
+                           int32_t window, int32_t depth, int32_t tree_k, float scale, float *out,
+                           float *lse, void *workspace, int32_t n_split, cudaStream_t stream);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

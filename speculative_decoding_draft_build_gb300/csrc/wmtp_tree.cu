@@ -47,6 +47,7 @@ constexpr int kRowsPerCta = kWarps * 16;  // query rows (node, head) per CTA
 constexpr int kTileKeys = 64;
 constexpr int kStages = 2;
 constexpr int kMaxTreeSplits = 64;
+constexpr int kTcRows = 128;  // query rows per CTA of the tcgen05 kernel
 constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
@@ -478,8 +479,7 @@ size_t wmtp_tree_workspace_bytes(int32_t B, int32_t H_q, int32_t H_kv, int32_t D
                                  int32_t tree_k, int32_t n_split) {
     if (B < 0 || H_kv < 1 || H_q < H_kv || D < 1 || depth < 1 || tree_k < 1 || n_split < 1) return 0;
     const int64_t R = (int64_t)tree_k * depth * (H_q / H_kv);
-    const int64_t n_rb = (R + kRowsPerCta - 1) / kRowsPerCta;
-    return tree_ws_bytes(B, H_kv, R, n_rb, D, n_split);
+    return tree_tc_workspace_bytes(B, H_kv, R, D, n_split);
 }
 
 int32_t wmtp_tree_num_splits(int32_t B, int32_t H_q, int32_t H_kv, int32_t depth, int32_t tree_k,
@@ -489,7 +489,7 @@ int32_t wmtp_tree_num_splits(int32_t B, int32_t H_q, int32_t H_kv, int32_t depth
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (B < 1 || H_kv < 1 || H_q < H_kv || depth < 1 || tree_k < 1) return 1;
     const int64_t R = (int64_t)tree_k * depth * (H_q / H_kv);
-    const int64_t n_rb = (R + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t n_rb = (R + kTcRows - 1) / kTcRows;
     const int64_t per_split = (int64_t)B * H_kv * n_rb;
     const int64_t keys = (int64_t)n_sink + window + (int64_t)tree_k * depth;
     int64_t n = sms / per_split;
@@ -511,8 +511,9 @@ wmtp_status wmtp_tree_draft_attn(const uint16_t *q, int32_t B, int32_t H_q, int3
     if (D != 128 && D != 256) return WMTP_EINVAL;
     if (n_sink < 0 || window < 1 || depth < 1 || tree_k < 1) return WMTP_EINVAL;
     if (n_split < 1 || n_split > kMaxTreeSplits || num_slots < 0) return WMTP_EINVAL;
+    if (depth > 255) return WMTP_EINVAL;
     const int64_t R = (int64_t)tree_k * depth * (H_q / H_kv);
-    const int64_t n_rb = (R + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t n_rb = (R + kTcRows - 1) / kTcRows;
     if (R > (1 << 20) || (int64_t)H_kv * n_rb > 65535 || B > 65535) return WMTP_EINVAL;
     if (B == 0) return WMTP_OK;
     if (!q || !k_pool || !v_pool || !seq_lens || !ring_base || !out) return WMTP_EINVAL;
@@ -520,15 +521,11 @@ wmtp_status wmtp_tree_draft_attn(const uint16_t *q, int32_t B, int32_t H_q, int3
         return WMTP_EINVAL;
     if (n_split > 1) {
         if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return WMTP_EINVAL;
-        if (workspace_bytes < tree_ws_bytes(B, H_kv, R, n_rb, D, n_split)) return WMTP_ECAPACITY;
+        if (workspace_bytes < tree_tc_workspace_bytes(B, H_kv, R, D, n_split)) return WMTP_ECAPACITY;
     }
-    cudaStream_t s = as_stream(stream);
-    if (D == 256)
-        return launch_tree<256>(q, B, H_q, H_kv, k_pool, v_pool, num_slots, seq_lens, ring_base,
-                                n_sink, window, depth, tree_k, scale, out, lse, workspace, n_split,
-                                s);
-    return launch_tree<128>(q, B, H_q, H_kv, k_pool, v_pool, num_slots, seq_lens, ring_base, n_sink,
-                            window, depth, tree_k, scale, out, lse, workspace, n_split, s);
+    return tree_tc_launch(q, B, H_q, H_kv, D, k_pool, v_pool, num_slots, seq_lens, ring_base,
+                          n_sink, window, depth, tree_k, scale, out, lse, workspace, n_split,
+                          as_stream(stream));
 }
 
 }  // extern "C"

@@ -1,0 +1,550 @@
+// wmtp_tree_tc.cu -- tree-draft attention on the 5th-generation tensor cores
+// (tcgen05, accumulators in tensor memory) for sm_103a.
+//
+// Same computation as the tree kernel described in wmtp_tree.cu ("Windowed-
+// MTP" §7 tree speculation; node (branch b, depth i) attends keep(S + i + 1)
+// of App. A with its own branch's draft nodes), built for the dense case:
+// the 224 query rows of a KV head (28 nodes x 8 heads at k = 4, d = 7) meet
+// every key of the request's window.
+//
+// One CTA = 128 query rows (the MMA's M) x one key chunk of one request and
+// KV head.  Warp roles:
+//   warps 0-3  softmax: thread i owns query row i = tensor-memory lane i.  It
+//              reads its row of S = Q K^T from tensor memory, applies the
+//              tree-causal mask, keeps a running reference max (the O
+//              accumulator is rescaled in tensor memory only when the max
+//              grows by more than 2^8), writes P as bf16 head + tail into
+//              shared memory, and at the end reads its row of O.
+//   warps 4-5  gather: slots from the ring rule (no table), 16-byte cp.async
+//              of each key's K and V rows into the no-swizzle core-matrix
+//              layouts the MMA reads (K K-major, V MN-major), two stages.
+//   warp 6     one thread issues the MMAs: S(t) = Q K(t)^T (M=128, N=64,
+//              K=D) into one of two S buffers, then O += P_hi V + P_lo V
+//              (M=128, N=D, K=64); completion is signalled through mbarriers
+//              with tcgen05.commit.
+// Key chunks are split over CTAs; the last CTA of a (request, KV head, row
+// block) merges the partials from the workspace in split order.  Every wait
+// has a time limit; tensor memory is always released.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "wmtp.h"
+#include "wmtp_internal.h"
+#include "wmtp_ptx.cuh"
+#include "wmtp_ring.cuh"
+#include "wmtp_tc.cuh"
+
+namespace wmtp {
+namespace {
+
+__device__ int32_t g_tree_tc_error = 0;
+
+__device__ __forceinline__ void latch(int32_t code) { atomicCAS(&g_tree_tc_error, 0, code); }
+
+constexpr int kRows = 128;  // query rows per CTA (MMA M)
+constexpr int kKeys = 64;   // keys per tile (N of QK^T, K of PV)
+constexpr int kSoftWarps = 4;
+constexpr int kLoadWarps = 2;
+constexpr int kMmaWarp = kSoftWarps + kLoadWarps;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kMaxSplits = 64;
+constexpr float kLazyRescale = 8.f;  // log2 of the growth tolerated before rescaling O
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+// Barrier slots.
+enum { kKvFull = 0, kKvEmpty = 2, kSFull = 4, kSEmpty = 6, kPFull = 8, kPvDone = 9, kNumBars = 10 };
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 8;                    // 16-byte chunks per row
+    static constexpr int kRowSbo = kChunks * 128;            // 8-row group stride (Q, K, V)
+    static constexpr int kQBytes = kRows / 8 * kRowSbo;
+    static constexpr int kTileBytes = kKeys / 8 * kRowSbo;   // K (or V) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kPSbo = kKeys / 8 * 128;            // P: 8-row group stride
+    static constexpr int kPBytes = kRows / 8 * kPSbo;        // one of P_hi / P_lo
+    static constexpr int kQOff = 0;
+    static constexpr int kKvOff = kQBytes;
+    static constexpr int kPOff = kKvOff + 2 * kStageBytes;
+    static constexpr int kInfoOff = kPOff + 2 * kPBytes;     // int2 [2][kKeys]
+    static constexpr int kBarOff = kInfoOff + 2 * kKeys * 8;
+    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16;
+    static constexpr int kOCol = 2 * kKeys;                  // O after the two S buffers
+    static constexpr int kTmemCols = (kOCol + D <= 256) ? 256 : 512;
+    static_assert(kRows * kMaxSplits * 4 <= 2 * kStageBytes, "merge weights must fit");
+};
+
+struct TreeWs {
+    int32_t *counters;
+    float *lse_part;
+    float *o_part;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Geo {
+    int64_t S, ns, lo0, Uc, U;
+};
+
+__device__ __forceinline__ Geo geometry(int64_t S, int n_sink, int window, int n_nodes) {
+    Geo g;
+    g.S = S;
+    g.ns = S < n_sink ? S : n_sink;
+    const bool windowed0 = S + 1 > (int64_t)n_sink + window;
+    g.lo0 = windowed0 ? S + 1 - window : g.ns;
+    g.Uc = g.ns + (S - g.lo0);
+    g.U = g.Uc + n_nodes;
+    return g;
+}
+
+// Key info for the mask: logical position and a code (-2 no key, -1 a
+// committed key, else branch << 8 | depth of a draft node).
+__device__ __forceinline__ int2 key_info(const Geo &g, int64_t e, int depth) {
+    if (e < g.Uc) return make_int2((int)(e < g.ns ? e : g.lo0 + (e - g.ns)), -1);
+    const int64_t n = e - g.Uc;
+    const int br = (int)(n / depth);
+    const int dep = (int)(n - (int64_t)br * depth);
+    return make_int2((int)(g.S + dep), (br << 8) | dep);
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int32_t *abort) {
+    if (mbar_wait_bounded(smem_addr(bar), parity, kWaitNs)) return true;
+    latch(WMTP_DEV_WAIT_TIMEOUT);
+    *abort = 1;
+    return false;
+}
+
+// Warp-uniform wait: the whole warp proceeds only if every lane saw the phase
+// (tensor-memory loads and stores that follow are warp-collective).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int32_t *abort) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
+    const __nv_bfloat16 *__restrict__ q, int32_t H_q, int32_t H_kv, int32_t G, int32_t n_nodes,
+    const __nv_bfloat16 *__restrict__ k_pool, const __nv_bfloat16 *__restrict__ v_pool,
+    int64_t num_slots, const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ ring_base,
+    int32_t n_sink, int32_t window, int32_t depth, int32_t tree_k, float scale_log2,
+    float *__restrict__ out, float *__restrict__ lse, TreeWs ws, int32_t n_split, int32_t n_rb) {
+    using C = Cfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);  // [0] abort [1] ticket
+    int2 *info = reinterpret_cast<int2 *>(smem + C::kInfoOff);
+
+    griddep_launch_dependents();
+    griddep_wait();
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x;
+    const int g = blockIdx.y % H_kv;
+    const int rb = blockIdx.y / H_kv;
+    const int64_t b = blockIdx.z;
+    const int R = n_nodes * G;
+
+    int64_t S = seq_lens[b];
+    if (S < 0) {
+        if (tid == 0) latch(WMTP_DEV_ARG_RANGE);
+        S = 0;
+    }
+    const int64_t base = ring_base[b];
+    const Geo geo = geometry(S, n_sink, window, n_nodes);
+    int64_t chunk = (geo.U + n_split - 1) / n_split;
+    chunk = (chunk + kKeys - 1) / kKeys * kKeys;
+    const int64_t start = (int64_t)split * chunk;
+    const int64_t cnt = geo.U - start < 0 ? 0 : (geo.U - start < chunk ? geo.U - start : chunk);
+    const int n_tiles = (int)((cnt + kKeys - 1) / kKeys);
+
+    if (tid == 0) {
+        mbar_init(smem_addr(&bars[kKvFull]), kLoadWarps);
+        mbar_init(smem_addr(&bars[kKvFull + 1]), kLoadWarps);
+        mbar_init(smem_addr(&bars[kKvEmpty]), 1);
+        mbar_init(smem_addr(&bars[kKvEmpty + 1]), 1);
+        mbar_init(smem_addr(&bars[kSFull]), 1);
+        mbar_init(smem_addr(&bars[kSFull + 1]), 1);
+        mbar_init(smem_addr(&bars[kSEmpty]), kSoftWarps);
+        mbar_init(smem_addr(&bars[kSEmpty + 1]), kSoftWarps);
+        mbar_init(smem_addr(&bars[kPFull]), kSoftWarps);
+        mbar_init(smem_addr(&bars[kPvDone]), 1);
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tc_alloc(smem_addr(tmem_slot), C::kTmemCols);
+
+    // Q rows of this block -> shared memory (K-major core-matrix layout).
+    const uint32_t sbase = smem_addr(smem);
+    const uint64_t keep = l2_policy_evict_last();
+    for (int idx = tid; idx < kRows * C::kChunks; idx += kThreads) {
+        const int i = idx / C::kChunks, j = idx - i * C::kChunks;
+        const int rq = rb * kRows + i;
+        const bool live = rq < R;
+        const int t = live ? rq / G : 0;
+        const int h = g * G + (live ? rq % G : 0);
+        const __nv_bfloat16 *src = q + ((b * n_nodes + t) * H_q + h) * (int64_t)D + j * 8;
+        cp_async_16(sbase + C::kQOff + (i >> 3) * C::kRowSbo + j * 128 + (i & 7) * 16, src,
+                    live ? 16u : 0u, keep);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp >= kSoftWarps && warp < kMmaWarp) {
+        // ----------------------------------------------------------- gather
+        const int lw = warp - kSoftWarps;
+        const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * D * 2;
+        const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * D * 2;
+        const size_t slot_bytes = (size_t)H_kv * D * 2;
+        constexpr int kLanesPerRow = C::kChunks < 32 ? C::kChunks : 32;  // 16 (D=128) or 32
+        constexpr int kRowsPerInst = 32 / kLanesPerRow;
+        const int sub = lane / kLanesPerRow, col = lane % kLanesPerRow;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t & 1;
+            if (t >= 2 && !mbar_wait(&bars[kKvEmpty + st], ((t >> 1) - 1) & 1, flags)) break;
+            if (flags[0]) break;
+            // this lane's key (one of the warp's 32) and its slot
+            const int key = lw * 32 + lane;
+            const int64_t kk = (int64_t)t * kKeys + key;
+            int2 inf = make_int2(0, -2);
+            int64_t slot = 0;
+            bool ok = false;
+            if (kk < cnt) {
+                inf = key_info(geo, start + kk, depth);
+                const int br = inf.y < 0 ? 0 : (inf.y >> 8);
+                slot = ring_slot(base, inf.x, br, n_sink, window, depth, tree_k);
+                ok = slot >= 0 && slot < num_slots;
+                if (!ok) {
+                    latch(WMTP_DEV_SLOT_RANGE);
+                    inf.y = -2;
+                }
+            }
+            info[st * kKeys + key] = inf;
+            const uint32_t okm = __ballot_sync(0xffffffffu, ok);
+            const uint32_t kt = sbase + C::kKvOff + st * C::kStageBytes;
+            const uint32_t vt = kt + C::kTileBytes;
+            for (int r0 = 0; r0 < 32; r0 += kRowsPerInst) {
+                const int kr = r0 + sub;               // key within this warp's 32
+                const int kt_key = lw * 32 + kr;       // key within the tile
+                const int64_t sl = __shfl_sync(0xffffffffu, slot, kr);
+                const bool kok = (okm >> kr) & 1u;
+                const size_t off = kok ? (size_t)sl * slot_bytes + col * 16 : 0;
+                const uint32_t dst = (kt_key >> 3) * C::kRowSbo + col * 128 + (kt_key & 7) * 16;
+                cp_async_16(kt + dst, kbase + off, kok ? 16u : 0u, keep);
+                cp_async_16(vt + dst, vbase + off, kok ? 16u : 0u, keep);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bars[kKvFull + st]));
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = tc_idesc_bf16(kRows, kKeys, 0);
+            constexpr uint32_t idesc_pv = tc_idesc_bf16(kRows, D, 1);
+            const uint32_t q_s = sbase + C::kQOff;
+            const uint32_t p_hi = sbase + C::kPOff, p_lo = p_hi + C::kPBytes;
+            auto issue_qk = [&](int t) -> bool {
+                const int st = t & 1;
+                if (!mbar_wait(&bars[kKvFull + st], (t >> 1) & 1, flags)) return false;
+                if (t >= 2 && !mbar_wait(&bars[kSEmpty + st], ((t >> 1) - 1) & 1, flags)) return false;
+                tc_fence_after();
+                const uint32_t kt = sbase + C::kKvOff + st * C::kStageBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc_mma_bf16(tmem + st * kKeys, tc_smem_desc(q_s + kk * 256, 128, C::kRowSbo),
+                                tc_smem_desc(kt + kk * 256, 128, C::kRowSbo), idesc_qk, kk > 0);
+                tc_commit(smem_addr(&bars[kSFull + st]));
+                return true;
+            };
+            bool live = n_tiles == 0 || issue_qk(0);
+            for (int t = 0; live && t < n_tiles; ++t) {
+                if (t + 1 < n_tiles && !issue_qk(t + 1)) break;
+                if (!mbar_wait(&bars[kPFull], t & 1, flags)) break;
+                tc_fence_after();
+                const uint32_t vt = sbase + C::kKvOff + (t & 1) * C::kStageBytes + C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                    const uint64_t vd = tc_smem_desc(vt + 2 * kk * C::kRowSbo, C::kRowSbo, 128);
+                    tc_mma_bf16(tmem + C::kOCol, tc_smem_desc(p_hi + kk * 256, 128, C::kPSbo), vd,
+                                idesc_pv, (t > 0 || kk > 0));
+                    tc_mma_bf16(tmem + C::kOCol, tc_smem_desc(p_lo + kk * 256, 128, C::kPSbo), vd,
+                                idesc_pv, 1);
+                }
+                tc_commit(smem_addr(&bars[kPvDone]));
+                tc_commit(smem_addr(&bars[kKvEmpty + (t & 1)]));
+            }
+        }
+    } else {
+        // --------------------------------------------------------- softmax
+        const int i = tid;  // row = tensor-memory lane
+        const int rq = rb * kRows + i;
+        const bool row_live = rq < R;
+        const int node = row_live ? rq / G : 0;
+        const int rbr = node / depth, rdep = node - (node / depth) * depth;
+        const int64_t kv = S + rdep + 1;
+        const int64_t row_lo = kv > (int64_t)n_sink + window ? kv - window : 0;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        float m_ref = -INFINITY, l = 0.f;
+        bool o_live = false;  // O holds at least one PV product
+        uint8_t *ph = smem + C::kPOff + (i >> 3) * C::kPSbo + (i & 7) * 16;
+        uint8_t *pl = ph + C::kPBytes;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t & 1;
+            if (!warp_wait(&bars[kSFull + st], (t >> 1) & 1, flags)) break;
+            if (!warp_wait(&bars[kKvFull + st], (t >> 1) & 1, flags)) break;
+            tc_fence_after();
+            float x[kKeys];
+            {
+                uint32_t r0[32], r1[32];
+                tc_ld32(lane_base + st * kKeys, r0);
+                tc_ld32(lane_base + st * kKeys + 32, r1);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    x[k] = __uint_as_float(r0[k]);
+                    x[32 + k] = __uint_as_float(r1[k]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bars[kSEmpty + st]));
+            float mx = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kKeys; ++k) {
+                const int2 inf = info[st * kKeys + k];
+                bool vis = false;
+                if (row_live && inf.y != -2) {
+                    const bool in_win = inf.x < n_sink || inf.x >= row_lo;
+                    vis = inf.y == -1 ? in_win
+                                      : ((inf.y >> 8) == rbr && (inf.y & 255) <= rdep && in_win);
+                }
+                x[k] = vis ? x[k] * scale_log2 : -INFINITY;
+                mx = fmaxf(mx, x[k]);
+            }
+            // PV(t-1) must be done before O is rescaled or P is overwritten.
+            if (t >= 1 && !warp_wait(&bars[kPvDone], (t - 1) & 1, flags)) break;
+            tc_fence_after();
+            // Lazy rescale: the reference max moves only when a row's max grew
+            // by more than 2^8 (also the first time it becomes finite).  The
+            // rescale loop is warp-uniform; rows that keep their max use 1.
+            const bool need = mx > m_ref + kLazyRescale;
+            float alpha = 1.f;
+            if (need) {
+                alpha = exp2f(m_ref - mx);  // 0 when m_ref = -inf
+                l *= alpha;
+                m_ref = mx;
+            }
+            if (o_live && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t r[32];
+                    tc_ld32(lane_base + C::kOCol + c0, r);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+                    tc_st32(lane_base + C::kOCol + c0, r);
+                }
+            }
+            const float muse = m_ref == -INFINITY ? 0.f : m_ref;
+            float rs = 0.f;
+#pragma unroll
+            for (int k = 0; k < kKeys; ++k) {
+                x[k] = exp2f(x[k] - muse);
+                rs += x[k];
+            }
+            l += rs;
+            // P row as bf16 head and tail, 8 keys (16 bytes) per core-matrix row
+#pragma unroll
+            for (int j = 0; j < kKeys / 8; ++j) {
+                uint32_t hv[4], tv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float a = x[8 * j + 2 * u], c2 = x[8 * j + 2 * u + 1];
+                    hv[u] = pack_bf16x2(a, c2);
+                    tv[u] = pack_bf16x2(a - bf16_lo_to_f32(hv[u]), c2 - bf16_hi_to_f32(hv[u]));
+                }
+                *reinterpret_cast<uint4 *>(ph + j * 128) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                *reinterpret_cast<uint4 *>(pl + j * 128) = make_uint4(tv[0], tv[1], tv[2], tv[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bars[kPFull]));
+            o_live = true;
+        }
+        // ---------------------------------------------------- epilogue
+        bool have_o = n_tiles > 0 && !flags[0];
+        if (have_o) have_o = warp_wait(&bars[kPvDone], (n_tiles - 1) & 1, flags);
+        have_o = __all_sync(0xffffffffu, have_o);
+        tc_fence_after();
+        const int h = g * G + (row_live ? rq % G : 0);
+        const float inv = (have_o && l > 0.f) ? 1.f / l : 0.f;
+        const float lse2 = (have_o && l > 0.f) ? m_ref + log2f(l) : -INFINITY;
+        float *dst = nullptr;
+        if (row_live) {
+            if (n_split == 1) {
+                const int64_t orow = (b * n_nodes + node) * H_q + h;
+                dst = out + orow * D;
+                if (lse) lse[orow] = flags[0] ? NAN : lse2 * kLn2;
+            } else {
+                const int64_t prow = ((b * H_kv + g) * R + rq) * n_split + split;
+                dst = ws.o_part + prow * D;
+                ws.lse_part[prow] = flags[0] ? NAN : lse2;
+            }
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            if (have_o) tc_ld32(lane_base + C::kOCol + c0, r);  // warp-uniform
+            if (row_live) {
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    float4 v;
+                    v.x = have_o ? __uint_as_float(r[k]) * inv : 0.f;
+                    v.y = have_o ? __uint_as_float(r[k + 1]) * inv : 0.f;
+                    v.z = have_o ? __uint_as_float(r[k + 2]) * inv : 0.f;
+                    v.w = have_o ? __uint_as_float(r[k + 3]) * inv : 0.f;
+                    *reinterpret_cast<float4 *>(dst + c0 + k) = v;
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tc_dealloc(tmem, C::kTmemCols);
+    }
+    if (n_split == 1) return;
+
+    // ------------------------------------------ ticket; the last CTA merges
+    __threadfence();
+    __syncthreads();
+    const int64_t cidx = (b * H_kv + g) * n_rb + rb;
+    if (tid == 0) {
+        const int32_t ticket = atomicAdd(&ws.counters[cidx], 1);
+        flags[1] = (ticket == n_split - 1);
+    }
+    __syncthreads();
+    if (!flags[1]) return;
+    __threadfence();
+    const int row0 = rb * kRows;
+    const int n_rows = R - row0 < kRows ? R - row0 : kRows;
+    float *wts = reinterpret_cast<float *>(smem + C::kKvOff);  // [rows][n_split]
+    const int64_t prow0 = (b * H_kv + g) * R + row0;
+    for (int e = tid; e < n_rows * n_split; e += kThreads) wts[e] = __ldcg(ws.lse_part + prow0 * n_split + e);
+    __syncthreads();
+    for (int i = tid; i < n_rows; i += kThreads) {
+        float *w = wts + i * n_split;
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < n_split; ++s2) M = fmaxf(M, w[s2]);
+        float sum = 0.f;
+        if (M != -INFINITY)
+            for (int s2 = 0; s2 < n_split; ++s2) sum += w[s2] == -INFINITY ? 0.f : exp2f(w[s2] - M);
+        const float lt = sum > 0.f ? M + log2f(sum) : -INFINITY;
+        for (int s2 = 0; s2 < n_split; ++s2)
+            w[s2] = (sum > 0.f && w[s2] != -INFINITY) ? exp2f(w[s2] - lt) : 0.f;
+        const int rq = row0 + i;
+        if (lse) lse[(b * n_nodes + rq / G) * H_q + g * G + rq % G] = lt * kLn2;
+    }
+    __syncthreads();
+    constexpr int D4 = D / 4;
+    for (int e = tid; e < n_rows * D4; e += kThreads) {
+        const int i = e / D4, d4 = e - i * D4;
+        const float *w = wts + i * n_split;
+        const float4 *op = reinterpret_cast<const float4 *>(ws.o_part + (prow0 + i) * n_split * D) + d4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s2 = 0; s2 < n_split; ++s2) {
+            const float4 v = __ldcg(op + (int64_t)s2 * D4);
+            acc.x += w[s2] * v.x;
+            acc.y += w[s2] * v.y;
+            acc.z += w[s2] * v.z;
+            acc.w += w[s2] * v.w;
+        }
+        const int rq = row0 + i;
+        reinterpret_cast<float4 *>(out + ((b * n_nodes + rq / G) * H_q + g * G + rq % G) * D)[d4] = acc;
+    }
+    if (tid == 0) ws.counters[cidx] = 0;
+}
+
+template <int D>
+wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_kv,
+                           const uint16_t *k_pool, const uint16_t *v_pool, int64_t num_slots,
+                           const int32_t *seq_lens, const int32_t *ring_base, int32_t n_sink,
+                           int32_t window, int32_t depth, int32_t tree_k, float scale, float *out,
+                           float *lse, void *workspace, int32_t n_split, cudaStream_t stream) {
+    using C = Cfg<D>;
+    const int G = H_q / H_kv;
+    const int n_nodes = tree_k * depth;
+    const int R = n_nodes * G;
+    const int n_rb = (R + kRows - 1) / kRows;
+    static int opted_in[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WMTP_ECUDA;
+    if (!opted_in[dev]) {
+        if (cudaFuncSetAttribute(tree_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes) != cudaSuccess)
+            return WMTP_ECUDA;
+        opted_in[dev] = 1;
+    }
+    TreeWs ws{nullptr, nullptr, nullptr};
+    if (n_split > 1) {
+        uint8_t *p = static_cast<uint8_t *>(workspace);
+        ws.counters = reinterpret_cast<int32_t *>(p);
+        p += align256((size_t)B * H_kv * n_rb * 4);
+        ws.lse_part = reinterpret_cast<float *>(p);
+        p += align256((size_t)B * H_kv * R * n_split * 4);
+        ws.o_part = reinterpret_cast<float *>(p);
+    }
+    PdlLaunch launch(dim3((unsigned)n_split, (unsigned)(H_kv * n_rb), (unsigned)B), dim3(kThreads),
+                     C::kSmemBytes, stream);
+    const cudaError_t err = cudaLaunchKernelEx(
+        &launch.cfg, tree_tc_kernel<D>, reinterpret_cast<const __nv_bfloat16 *>(q), H_q, H_kv, G,
+        n_nodes, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
+        reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, seq_lens, ring_base, n_sink,
+        window, depth, tree_k, scale * 1.4426950408889634f, out, lse, ws, n_split, n_rb);
+    return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
+}
+
+}  // namespace
+
+cudaError_t read_tree_tc_error(int32_t *code, bool clear) {
+    cudaError_t err = cudaMemcpyFromSymbol(code, g_tree_tc_error, sizeof(int32_t));
+    if (err != cudaSuccess || !clear) return err;
+    const int32_t zero = 0;
+    return cudaMemcpyToSymbol(g_tree_tc_error, &zero, sizeof(int32_t));
+}
+
+size_t tree_tc_workspace_bytes(int64_t B, int64_t H_kv, int64_t R, int D, int n_split) {
+    if (n_split <= 1) return 0;
+    const int64_t n_rb = (R + kRows - 1) / kRows;
+    return align256((size_t)B * H_kv * n_rb * 4) + align256((size_t)B * H_kv * R * n_split * 4) +
+           (size_t)B * H_kv * R * n_split * D * 4;
+}
+
+wmtp_status tree_tc_launch(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_kv, int32_t D,
+                           const uint16_t *k_pool, const uint16_t *v_pool, int64_t num_slots,
+                           const int32_t *seq_lens, const int32_t *ring_base, int32_t n_sink,
+                           int32_t window, int32_t depth, int32_t tree_k, float scale, float *out,
+                           float *lse, void *workspace, int32_t n_split, cudaStream_t stream) {
+    if (D == 256)
+        return launch_tree_tc<256>(q, B, H_q, H_kv, k_pool, v_pool, num_slots, seq_lens, ring_base,
+                                   n_sink, window, depth, tree_k, scale, out, lse, workspace,
+                                   n_split, stream);
+    return launch_tree_tc<128>(q, B, H_q, H_kv, k_pool, v_pool, num_slots, seq_lens, ring_base,
+                               n_sink, window, depth, tree_k, scale, out, lse, workspace, n_split,
+                               stream);
+}
+
+}  // namespace wmtp
