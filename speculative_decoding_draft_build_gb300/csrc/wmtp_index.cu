@@ -140,10 +140,8 @@ wmtp_status wmtp_get_device_error(int32_t *code, int32_t clear) {
     int32_t a = 0, b = 0, t = 0;
     if (read_index_error(&a, clear != 0) != cudaSuccess) return WMTP_ECUDA;
     if (read_attn_error(&b, clear != 0) != cudaSuccess) return WMTP_ECUDA;
-    int32_t u = 0;
-    if (read_tree_error(&t, clear != 0) != cudaSuccess) return WMTP_ECUDA;
-    if (read_tree_tc_error(&u, clear != 0) != cudaSuccess) return WMTP_ECUDA;
-    *code = a ? a : (b ? b : (t ? t : u));
+    if (read_tree_tc_error(&t, clear != 0) != cudaSuccess) return WMTP_ECUDA;
+    *code = a ? a : (b ? b : t);
     return WMTP_OK;
 }
 

@@ -13,7 +13,6 @@ namespace wmtp {
 // device code is needed); these read-and-optionally-clear them.
 cudaError_t read_index_error(int32_t *code, bool clear);
 cudaError_t read_attn_error(int32_t *code, bool clear);
-cudaError_t read_tree_error(int32_t *code, bool clear);
 cudaError_t read_tree_tc_error(int32_t *code, bool clear);
 size_t tree_tc_workspace_bytes(int64_t B, int64_t H_kv, int64_t R, int D, int n_split);
 wmtp_status tree_tc_launch(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_kv, int32_t D,

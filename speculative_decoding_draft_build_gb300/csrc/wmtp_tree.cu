@@ -1,4 +1,5 @@
-// wmtp_tree.cu -- tree-draft attention over the ring for sm_103a.
+// wmtp_tree.cu -- tree-draft attention over the ring on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory) for sm_103a.
 //
 // Method: "Windowed-MTP: Removing the Full-Context Draft-KV Tax at
 // Million-Token Context" (arXiv 2607.21535), §7 "Compatibility with tree
@@ -9,21 +10,29 @@
 // (branch b, depth i) of a request with committed length S sits at position
 // S + i and attends keep(S + i + 1) of App. A's pseudocode, with the draft
 // positions S..S+i taken from its own branch.  For k = 1 this is the chain.
+// The request's key list is implicit -- sinks || committed window of the
+// shallowest node || the k*d draft nodes -- and ring slots are computed in
+// the kernel (no table read).  The 224 query rows of a KV head (28 nodes x 8
+// heads at k = 4, d = 7) meet every key of the window: a dense contraction.
 //
-// Kernel design (one CTA = 112 query rows x one key chunk of one request and
-// KV head):
-//   * the request's key list is implicit: sinks || committed window of the
-//     shallowest node || the k*d draft nodes, with ring slots computed in the
-//     kernel (no table read);
-//   * all 224 query rows of a KV head (28 nodes x 8 heads at k=4, d=7) form a
-//     dense contraction: rows are the MMA M dimension (16 per warp, 7 warps),
-//     keys N, head dim K, on mma.sync bf16 with fp32 accumulation;
-//   * K/V tiles of 64 keys are gathered by all warps with 16-byte cp.async
-//     into padded shared memory (two stages); Q rows stay in shared memory;
-//   * a per-(row, key) predicate applies the tree-causal mask; online softmax
-//     in base 2; the weights are split into bf16 head + tail for PV;
-//   * key chunks are split over CTAs; the last CTA of a (request, KV head,
-//     row block) merges the partials from the workspace in split order.
+// One CTA = 128 query rows (the MMA's M) x one key chunk of one request and
+// KV head.  Warp roles:
+//   warps 0-3  softmax: thread i owns query row i = tensor-memory lane i.  It
+//              reads its row of S = Q K^T from tensor memory, applies the
+//              tree-causal mask, keeps a running reference max (the O
+//              accumulator is rescaled in tensor memory only when the max
+//              grows by more than 2^8), writes P as bf16 head + tail into
+//              shared memory, and at the end reads its row of O.
+//   warps 4-5  gather: slots from the ring rule (no table), 16-byte cp.async
+//              of each key's K and V rows into the no-swizzle core-matrix
+//              layouts the MMA reads (K K-major, V MN-major), two stages.
+//   warp 6     one thread issues the MMAs: S(t) = Q K(t)^T (M=128, N=64,
+//              K=D) into one of two S buffers, then O += P_hi V + P_lo V
+//              (M=128, N=D, K=64); completion is signalled through mbarriers
+//              with tcgen05.commit.
+// Key chunks are split over CTAs; the last CTA of a (request, KV head, row
+// block) merges the partials from the workspace in split order.  Every wait
+// has a time limit; tensor memory is always released.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -33,53 +42,57 @@
 #include "wmtp_internal.h"
 #include "wmtp_ptx.cuh"
 #include "wmtp_ring.cuh"
+#include "wmtp_tc.cuh"
 
 namespace wmtp {
 namespace {
 
-__device__ int32_t g_tree_error = 0;
+__device__ int32_t g_tree_tc_error = 0;
 
-__device__ __forceinline__ void latch(int32_t code) { atomicCAS(&g_tree_error, 0, code); }
+__device__ __forceinline__ void latch(int32_t code) { atomicCAS(&g_tree_tc_error, 0, code); }
 
-constexpr int kWarps = 7;
-constexpr int kThreads = kWarps * 32;
-constexpr int kRowsPerCta = kWarps * 16;  // query rows (node, head) per CTA
-constexpr int kTileKeys = 64;
-constexpr int kStages = 2;
-constexpr int kMaxTreeSplits = 64;
-constexpr int kTcRows = 128;  // query rows per CTA of the tcgen05 kernel
+constexpr int kRows = 128;  // query rows per CTA (MMA M)
+constexpr int kKeys = 64;   // keys per tile (N of QK^T, K of PV)
+constexpr int kSoftWarps = 4;
+constexpr int kLoadWarps = 2;
+constexpr int kMmaWarp = kSoftWarps + kLoadWarps;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kMaxSplits = 64;
+constexpr float kLazyRescale = 8.f;  // log2 of the growth tolerated before rescaling O
+constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
 
+// Barrier slots.
+enum { kKvFull = 0, kKvEmpty = 2, kSFull = 4, kSEmpty = 6, kPFull = 8, kPvDone = 9, kNumBars = 10 };
+
 template <int D>
-struct TCfg {
-    static constexpr int kRowBytes = D * 2;
-    static constexpr int kPitch = kRowBytes + 16;  // padded: conflict-free ldmatrix
-    static constexpr int kQBytes = kRowsPerCta * kPitch;
-    static constexpr int kTileBytes = kTileKeys * kPitch;
-    static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
-    static constexpr int kKVOffset = kQBytes;
-    static constexpr int kFlagOffset = kKVOffset + kStages * kStageBytes;
-    static constexpr int kSmemBytes = kFlagOffset + 16;
-    static_assert(kRowsPerCta * kMaxTreeSplits * 4 <= kStages * kStageBytes, "merge weights must fit");
+struct Cfg {
+    static constexpr int kChunks = D / 8;                    // 16-byte chunks per row
+    static constexpr int kRowSbo = kChunks * 128;            // 8-row group stride (Q, K, V)
+    static constexpr int kQBytes = kRows / 8 * kRowSbo;
+    static constexpr int kTileBytes = kKeys / 8 * kRowSbo;   // K (or V) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kPSbo = kKeys / 8 * 128;            // P: 8-row group stride
+    static constexpr int kPBytes = kRows / 8 * kPSbo;        // one of P_hi / P_lo
+    static constexpr int kQOff = 0;
+    static constexpr int kKvOff = kQBytes;
+    static constexpr int kPOff = kKvOff + 2 * kStageBytes;
+    static constexpr int kInfoOff = kPOff + 2 * kPBytes;     // int2 [2][kKeys]
+    static constexpr int kBarOff = kInfoOff + 2 * kKeys * 8;
+    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16;
+    static constexpr int kOCol = 2 * kKeys;                  // O after the two S buffers
+    static constexpr int kTmemCols = (kOCol + D <= 256) ? 256 : 512;
+    static_assert(kRows * kMaxSplits * 4 <= 2 * kStageBytes, "merge weights must fit");
 };
 
 struct TreeWs {
-    int32_t *counters;  // [B][H_kv][row blocks]
-    float *lse_part;    // [B][H_kv][R][n_split], base 2
-    float *o_part;      // [B][H_kv][R][n_split][D]
+    int32_t *counters;
+    float *lse_part;
+    float *o_part;
 };
 
-__host__ __device__ inline size_t align256t(size_t x) { return (x + 255) & ~size_t(255); }
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline size_t tree_ws_bytes(int64_t B, int64_t H_kv, int64_t R, int64_t n_rb, int D, int n_split) {
-    if (n_split <= 1) return 0;
-    return align256t(B * H_kv * n_rb * 4) + align256t(B * H_kv * R * n_split * 4) +
-           (size_t)B * H_kv * R * n_split * D * 4;
-}
-
-// The request's key list: sinks [0, ns), committed window [lo0, S) of the
-// shallowest node (all of [0, S) when no node is windowed yet), then the
-// n_nodes draft nodes (branch-major).
 struct Geo {
     int64_t S, ns, lo0, Uc, U;
 };
@@ -95,53 +108,47 @@ __device__ __forceinline__ Geo geometry(int64_t S, int n_sink, int window, int n
     return g;
 }
 
-// Logical position and branch of entry e (< U) of the key list.
-__device__ __forceinline__ void entry_pos(const Geo &g, int64_t e, int depth, int64_t &p,
-                                          int &br, int &dep) {
-    if (e < g.Uc) {
-        p = e < g.ns ? e : g.lo0 + (e - g.ns);
-        br = 0;
-        dep = -1;
-    } else {
-        const int64_t n = e - g.Uc;
-        br = (int)(n / depth);
-        dep = (int)(n - (int64_t)br * depth);
-        p = g.S + dep;
-    }
+// Key info for the mask: logical position and a code (-2 no key, -1 a
+// committed key, else branch << 8 | depth of a draft node).
+__device__ __forceinline__ int2 key_info(const Geo &g, int64_t e, int depth) {
+    if (e < g.Uc) return make_int2((int)(e < g.ns ? e : g.lo0 + (e - g.ns)), -1);
+    const int64_t n = e - g.Uc;
+    const int br = (int)(n / depth);
+    const int dep = (int)(n - (int64_t)br * depth);
+    return make_int2((int)(g.S + dep), (br << 8) | dep);
 }
 
-// A query row: node (branch, depth); keys below `lo` other than sinks are
-// outside its window (lo = 0 when its key set is not windowed).
-struct RowInfo {
-    bool live;
-    int br, dep;
-    int64_t lo;
-};
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int32_t *abort) {
+    if (mbar_wait_bounded(smem_addr(bar), parity, kWaitNs)) return true;
+    latch(WMTP_DEV_WAIT_TIMEOUT);
+    *abort = 1;
+    return false;
+}
 
-__device__ __forceinline__ bool visible(const RowInfo &rw, int64_t p, int br, int dep, int n_sink) {
-    if (!rw.live) return false;
-    const bool in_window = p < n_sink || p >= rw.lo;
-    if (dep < 0) return in_window;                        // committed key
-    return br == rw.br && dep <= rw.dep && in_window;     // draft node on its own path
+// Warp-uniform wait: the whole warp proceeds only if every lane saw the phase
+// (tensor-memory loads and stores that follow are warp-collective).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int32_t *abort) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) tree_decode_kernel(
+__global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     const __nv_bfloat16 *__restrict__ q, int32_t H_q, int32_t H_kv, int32_t G, int32_t n_nodes,
     const __nv_bfloat16 *__restrict__ k_pool, const __nv_bfloat16 *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ ring_base,
     int32_t n_sink, int32_t window, int32_t depth, int32_t tree_k, float scale_log2,
     float *__restrict__ out, float *__restrict__ lse, TreeWs ws, int32_t n_split, int32_t n_rb) {
-    using C = TCfg<D>;
-    constexpr int KD = D / 16;
-    constexpr int kChunks = C::kRowBytes / 16;
-    extern __shared__ __align__(128) uint8_t smem[];
-    volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(smem + C::kFlagOffset);
+    using C = Cfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);  // [0] abort [1] ticket
+    int2 *info = reinterpret_cast<int2 *>(smem + C::kInfoOff);
 
     griddep_launch_dependents();
     griddep_wait();
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x;
     const int g = blockIdx.y % H_kv;
     const int rb = blockIdx.y / H_kv;
@@ -156,214 +163,276 @@ __global__ void __launch_bounds__(kThreads, 1) tree_decode_kernel(
     const int64_t base = ring_base[b];
     const Geo geo = geometry(S, n_sink, window, n_nodes);
     int64_t chunk = (geo.U + n_split - 1) / n_split;
-    chunk = (chunk + kTileKeys - 1) / kTileKeys * kTileKeys;
+    chunk = (chunk + kKeys - 1) / kKeys * kKeys;
     const int64_t start = (int64_t)split * chunk;
     const int64_t cnt = geo.U - start < 0 ? 0 : (geo.U - start < chunk ? geo.U - start : chunk);
-    const int n_tiles = (int)((cnt + kTileKeys - 1) / kTileKeys);
+    const int n_tiles = (int)((cnt + kKeys - 1) / kKeys);
 
-    // ------------------------------------------------- Q rows -> smem
-    const uint32_t q_addr = smem_addr(smem);
+    if (tid == 0) {
+        mbar_init(smem_addr(&bars[kKvFull]), kLoadWarps);
+        mbar_init(smem_addr(&bars[kKvFull + 1]), kLoadWarps);
+        mbar_init(smem_addr(&bars[kKvEmpty]), 1);
+        mbar_init(smem_addr(&bars[kKvEmpty + 1]), 1);
+        mbar_init(smem_addr(&bars[kSFull]), 1);
+        mbar_init(smem_addr(&bars[kSFull + 1]), 1);
+        mbar_init(smem_addr(&bars[kSEmpty]), kSoftWarps);
+        mbar_init(smem_addr(&bars[kSEmpty + 1]), kSoftWarps);
+        mbar_init(smem_addr(&bars[kPFull]), kSoftWarps);
+        mbar_init(smem_addr(&bars[kPvDone]), 1);
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tc_alloc(smem_addr(tmem_slot), C::kTmemCols);
+
+    // Q rows of this block -> shared memory (K-major core-matrix layout).
+    const uint32_t sbase = smem_addr(smem);
     const uint64_t keep = l2_policy_evict_last();
-    for (int idx = tid; idx < kRowsPerCta * kChunks; idx += kThreads) {
-        const int i = idx / kChunks, c16 = idx - i * kChunks;
-        const int rq = rb * kRowsPerCta + i;
+    for (int idx = tid; idx < kRows * C::kChunks; idx += kThreads) {
+        const int i = idx / C::kChunks, j = idx - i * C::kChunks;
+        const int rq = rb * kRows + i;
         const bool live = rq < R;
         const int t = live ? rq / G : 0;
         const int h = g * G + (live ? rq % G : 0);
-        const __nv_bfloat16 *src = q + ((b * n_nodes + t) * H_q + h) * (int64_t)D + c16 * 8;
-        cp_async_16(q_addr + i * C::kPitch + c16 * 16, src, live ? 16u : 0u, keep);
+        const __nv_bfloat16 *src = q + ((b * n_nodes + t) * H_q + h) * (int64_t)D + j * 8;
+        cp_async_16(sbase + C::kQOff + (i >> 3) * C::kRowSbo + j * 128 + (i & 7) * 16, src,
+                    live ? 16u : 0u, keep);
     }
-
-    // ------------------------------------------------- K/V gathers
-    const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * C::kRowBytes;
-    const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * C::kRowBytes;
-    const size_t slot_bytes = (size_t)H_kv * C::kRowBytes;
-    const uint32_t kv_addr = smem_addr(smem + C::kKVOffset);
-    auto issue = [&](int t, int st) {
-        const uint32_t kdst = kv_addr + st * C::kStageBytes;
-        const uint32_t vdst = kdst + C::kTileBytes;
-        for (int k = warp; k < kTileKeys; k += kWarps) {
-            const int64_t kk = (int64_t)t * kTileKeys + k;
-            bool ok = kk < cnt;
-            int64_t slot = 0;
-            if (ok) {
-                int64_t p;
-                int br, dep;
-                entry_pos(geo, start + kk, depth, p, br, dep);
-                slot = ring_slot(base, p, br, n_sink, window, depth, tree_k);
-                if (slot < 0 || slot >= num_slots) {
-                    ok = false;
-                    if (lane == 0) latch(WMTP_DEV_SLOT_RANGE);
-                }
-            }
-            const uint8_t *ks = kbase + (ok ? (size_t)slot * slot_bytes : 0);
-            const uint8_t *vs = vbase + (ok ? (size_t)slot * slot_bytes : 0);
-            for (int c16 = lane; c16 < kChunks; c16 += 32) {
-                cp_async_16(kdst + k * C::kPitch + c16 * 16, ks + c16 * 16, ok ? 16u : 0u, keep);
-                cp_async_16(vdst + k * C::kPitch + c16 * 16, vs + c16 * 16, ok ? 16u : 0u, keep);
-            }
-        }
-    };
-
-    if (n_tiles > 0) issue(0, 0);
-    cp_async_commit();  // Q rows + tile 0
-
-    // ------------------------------------------------- this thread's rows
-    const int r = lane >> 2, c = lane & 3;
-    RowInfo rows[2];
-#pragma unroll
-    for (int hi = 0; hi < 2; ++hi) {
-        const int rq = rb * kRowsPerCta + warp * 16 + r + 8 * hi;
-        RowInfo &rw = rows[hi];
-        rw.live = rq < R;
-        const int t = rw.live ? rq / G : 0;
-        rw.br = t / depth;
-        rw.dep = t - rw.br * depth;
-        const int64_t kv = S + rw.dep + 1;
-        rw.lo = kv > (int64_t)n_sink + window ? kv - window : 0;
-    }
-
-    float o[D / 8][4];
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-
-    const uint32_t a_base = q_addr + (warp * 16 + (lane & 15)) * C::kPitch + (lane >> 4) * 16;
-    const uint32_t kb_off = ((lane & 7) + ((lane >> 4) << 3)) * C::kPitch + ((lane >> 3) & 1) * 16;
-    const uint32_t vb_off = ((lane & 7) + (((lane >> 3) & 1) << 3)) * C::kPitch + (lane >> 4) * 16;
-
-    for (int it = 0; it < n_tiles; ++it) {
-        if (it + 1 < n_tiles) issue(it + 1, (it + 1) & 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        const uint32_t kt = kv_addr + (it & 1) * C::kStageBytes;
-        const uint32_t vt = kt + C::kTileBytes;
-
-        // S = Q K^T for 16 rows x 64 keys (8 n-tiles of 8 keys)
-        float s[8][4];
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-        for (int kd = 0; kd < KD; ++kd) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(a_base + kd * 32, a0, a1, a2, a3);
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t x0, x1, x2, x3;
-                ldsm_x4(kt + np * 16 * C::kPitch + kb_off + kd * 32, x0, x1, x2, x3);
-                mma_bf16_16816(s[2 * np], a0, a1, a2, a3, x0, x1);
-                mma_bf16_16816(s[2 * np + 1], a0, a1, a2, a3, x2, x3);
-            }
-        }
-
-        // tree-causal mask, online softmax (rows r and r+8 of this warp)
-        const int64_t tile_e0 = start + (int64_t)it * kTileKeys;
-        const int64_t tile_cnt = cnt - (int64_t)it * kTileKeys;
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int kk = nt * 8 + 2 * c + j;
-                bool v0 = false, v1 = false;
-                if (kk < tile_cnt) {
-                    int64_t p;
-                    int br, dep;
-                    entry_pos(geo, tile_e0 + kk, depth, p, br, dep);
-                    v0 = visible(rows[0], p, br, dep, n_sink);
-                    v1 = visible(rows[1], p, br, dep, n_sink);
-                }
-                s[nt][j] = v0 ? s[nt][j] * scale_log2 : -INFINITY;
-                s[nt][2 + j] = v1 ? s[nt][2 + j] * scale_log2 : -INFINITY;
-                mx[0] = fmaxf(mx[0], s[nt][j]);
-                mx[1] = fmaxf(mx[1], s[nt][2 + j]);
-            }
-        }
-        float alpha[2], muse[2];
-#pragma unroll
-        for (int hi = 0; hi < 2; ++hi) {
-            mx[hi] = fmaxf(mx[hi], __shfl_xor_sync(0xffffffffu, mx[hi], 1));
-            mx[hi] = fmaxf(mx[hi], __shfl_xor_sync(0xffffffffu, mx[hi], 2));
-            const float mn = fmaxf(m[hi], mx[hi]);
-            muse[hi] = mn == -INFINITY ? 0.f : mn;
-            alpha[hi] = exp2f(m[hi] - muse[hi]);
-            m[hi] = mn;
-        }
-        float rs[2] = {0.f, 0.f};
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            s[nt][0] = exp2f(s[nt][0] - muse[0]);
-            s[nt][1] = exp2f(s[nt][1] - muse[0]);
-            s[nt][2] = exp2f(s[nt][2] - muse[1]);
-            s[nt][3] = exp2f(s[nt][3] - muse[1]);
-            rs[0] += s[nt][0] + s[nt][1];
-            rs[1] += s[nt][2] + s[nt][3];
-        }
-        l[0] = l[0] * alpha[0] + rs[0];
-        l[1] = l[1] * alpha[1] + rs[1];
-        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-            for (int nt = 0; nt < D / 8; ++nt) {
-                o[nt][0] *= alpha[0];
-                o[nt][1] *= alpha[0];
-                o[nt][2] *= alpha[1];
-                o[nt][3] *= alpha[1];
-            }
-        }
-
-        // O += P V, P split into bf16 head + tail sharing each V fragment
-#pragma unroll
-        for (int kk16 = 0; kk16 < 4; ++kk16) {
-            const float *pa = s[2 * kk16], *pb = s[2 * kk16 + 1];
-            const uint32_t h0 = pack_bf16x2(pa[0], pa[1]), h1 = pack_bf16x2(pa[2], pa[3]);
-            const uint32_t h2 = pack_bf16x2(pb[0], pb[1]), h3 = pack_bf16x2(pb[2], pb[3]);
-            const uint32_t t0 = pack_bf16x2(pa[0] - bf16_lo_to_f32(h0), pa[1] - bf16_hi_to_f32(h0));
-            const uint32_t t1 = pack_bf16x2(pa[2] - bf16_lo_to_f32(h1), pa[3] - bf16_hi_to_f32(h1));
-            const uint32_t t2 = pack_bf16x2(pb[0] - bf16_lo_to_f32(h2), pb[1] - bf16_hi_to_f32(h2));
-            const uint32_t t3 = pack_bf16x2(pb[2] - bf16_lo_to_f32(h3), pb[3] - bf16_hi_to_f32(h3));
-#pragma unroll
-            for (int dp = 0; dp < D / 16; ++dp) {
-                uint32_t y0, y1, y2, y3;
-                ldsm_x4_trans(vt + kk16 * 16 * C::kPitch + vb_off + dp * 32, y0, y1, y2, y3);
-                mma_bf16_16816(o[2 * dp], h0, h1, h2, h3, y0, y1);
-                mma_bf16_16816(o[2 * dp + 1], h0, h1, h2, h3, y2, y3);
-                mma_bf16_16816(o[2 * dp], t0, t1, t2, t3, y0, y1);
-                mma_bf16_16816(o[2 * dp + 1], t0, t1, t2, t3, y2, y3);
-            }
-        }
-        __syncthreads();  // the stage is overwritten by the next issue
-    }
+    cp_async_commit();
     cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
+    if (warp >= kSoftWarps && warp < kMmaWarp) {
+        // ----------------------------------------------------------- gather
+        const int lw = warp - kSoftWarps;
+        const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * D * 2;
+        const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * D * 2;
+        const size_t slot_bytes = (size_t)H_kv * D * 2;
+        constexpr int kLanesPerRow = C::kChunks < 32 ? C::kChunks : 32;  // 16 (D=128) or 32
+        constexpr int kRowsPerInst = 32 / kLanesPerRow;
+        const int sub = lane / kLanesPerRow, col = lane % kLanesPerRow;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t & 1;
+            if (t >= 2 && !mbar_wait(&bars[kKvEmpty + st], ((t >> 1) - 1) & 1, flags)) break;
+            if (flags[0]) break;
+            // this lane's key (one of the warp's 32) and its slot
+            const int key = lw * 32 + lane;
+            const int64_t kk = (int64_t)t * kKeys + key;
+            int2 inf = make_int2(0, -2);
+            int64_t slot = 0;
+            bool ok = false;
+            if (kk < cnt) {
+                inf = key_info(geo, start + kk, depth);
+                const int br = inf.y < 0 ? 0 : (inf.y >> 8);
+                slot = ring_slot(base, inf.x, br, n_sink, window, depth, tree_k);
+                ok = slot >= 0 && slot < num_slots;
+                if (!ok) {
+                    latch(WMTP_DEV_SLOT_RANGE);
+                    inf.y = -2;
+                }
+            }
+            info[st * kKeys + key] = inf;
+            const uint32_t okm = __ballot_sync(0xffffffffu, ok);
+            const uint32_t kt = sbase + C::kKvOff + st * C::kStageBytes;
+            const uint32_t vt = kt + C::kTileBytes;
+            for (int r0 = 0; r0 < 32; r0 += kRowsPerInst) {
+                const int kr = r0 + sub;               // key within this warp's 32
+                const int kt_key = lw * 32 + kr;       // key within the tile
+                const int64_t sl = __shfl_sync(0xffffffffu, slot, kr);
+                const bool kok = (okm >> kr) & 1u;
+                const size_t off = kok ? (size_t)sl * slot_bytes + col * 16 : 0;
+                const uint32_t dst = (kt_key >> 3) * C::kRowSbo + col * 128 + (kt_key & 7) * 16;
+                cp_async_16(kt + dst, kbase + off, kok ? 16u : 0u, keep);
+                cp_async_16(vt + dst, vbase + off, kok ? 16u : 0u, keep);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bars[kKvFull + st]));
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = tc_idesc_bf16(kRows, kKeys, 0);
+            constexpr uint32_t idesc_pv = tc_idesc_bf16(kRows, D, 1);
+            const uint32_t q_s = sbase + C::kQOff;
+            const uint32_t p_hi = sbase + C::kPOff, p_lo = p_hi + C::kPBytes;
+            auto issue_qk = [&](int t) -> bool {
+                const int st = t & 1;
+                if (!mbar_wait(&bars[kKvFull + st], (t >> 1) & 1, flags)) return false;
+                if (t >= 2 && !mbar_wait(&bars[kSEmpty + st], ((t >> 1) - 1) & 1, flags)) return false;
+                tc_fence_after();
+                const uint32_t kt = sbase + C::kKvOff + st * C::kStageBytes;
 #pragma unroll
-    for (int hi = 0; hi < 2; ++hi) {
-        l[hi] += __shfl_xor_sync(0xffffffffu, l[hi], 1);
-        l[hi] += __shfl_xor_sync(0xffffffffu, l[hi], 2);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc_mma_bf16(tmem + st * kKeys, tc_smem_desc(q_s + kk * 256, 128, C::kRowSbo),
+                                tc_smem_desc(kt + kk * 256, 128, C::kRowSbo), idesc_qk, kk > 0);
+                tc_commit(smem_addr(&bars[kSFull + st]));
+                return true;
+            };
+            bool live = n_tiles == 0 || issue_qk(0);
+            for (int t = 0; live && t < n_tiles; ++t) {
+                if (t + 1 < n_tiles && !issue_qk(t + 1)) break;
+                if (!mbar_wait(&bars[kPFull], t & 1, flags)) break;
+                tc_fence_after();
+                const uint32_t vt = sbase + C::kKvOff + (t & 1) * C::kStageBytes + C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                    const uint64_t vd = tc_smem_desc(vt + 2 * kk * C::kRowSbo, C::kRowSbo, 128);
+                    tc_mma_bf16(tmem + C::kOCol, tc_smem_desc(p_hi + kk * 256, 128, C::kPSbo), vd,
+                                idesc_pv, (t > 0 || kk > 0));
+                    tc_mma_bf16(tmem + C::kOCol, tc_smem_desc(p_lo + kk * 256, 128, C::kPSbo), vd,
+                                idesc_pv, 1);
+                }
+                tc_commit(smem_addr(&bars[kPvDone]));
+                tc_commit(smem_addr(&bars[kKvEmpty + (t & 1)]));
+            }
+        }
+    } else {
+        // --------------------------------------------------------- softmax
+        const int i = tid;  // row = tensor-memory lane
+        const int rq = rb * kRows + i;
+        const bool row_live = rq < R;
+        const int node = row_live ? rq / G : 0;
+        const int rbr = node / depth, rdep = node - (node / depth) * depth;
+        const int64_t kv = S + rdep + 1;
+        const int64_t row_lo = kv > (int64_t)n_sink + window ? kv - window : 0;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        float m_ref = -INFINITY, l = 0.f;
+        bool o_live = false;  // O holds at least one PV product
+        uint8_t *ph = smem + C::kPOff + (i >> 3) * C::kPSbo + (i & 7) * 16;
+        uint8_t *pl = ph + C::kPBytes;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t & 1;
+            if (!warp_wait(&bars[kSFull + st], (t >> 1) & 1, flags)) break;
+            if (!warp_wait(&bars[kKvFull + st], (t >> 1) & 1, flags)) break;
+            tc_fence_after();
+            float x[kKeys];
+            {
+                uint32_t r0[32], r1[32];
+                tc_ld32(lane_base + st * kKeys, r0);
+                tc_ld32(lane_base + st * kKeys + 32, r1);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    x[k] = __uint_as_float(r0[k]);
+                    x[32 + k] = __uint_as_float(r1[k]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bars[kSEmpty + st]));
+            float mx = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kKeys; ++k) {
+                const int2 inf = info[st * kKeys + k];
+                bool vis = false;
+                if (row_live && inf.y != -2) {
+                    const bool in_win = inf.x < n_sink || inf.x >= row_lo;
+                    vis = inf.y == -1 ? in_win
+                                      : ((inf.y >> 8) == rbr && (inf.y & 255) <= rdep && in_win);
+                }
+                x[k] = vis ? x[k] * scale_log2 : -INFINITY;
+                mx = fmaxf(mx, x[k]);
+            }
+            // PV(t-1) must be done before O is rescaled or P is overwritten.
+            if (t >= 1 && !warp_wait(&bars[kPvDone], (t - 1) & 1, flags)) break;
+            tc_fence_after();
+            // Lazy rescale: the reference max moves only when a row's max grew
+            // by more than 2^8 (also the first time it becomes finite).  The
+            // rescale loop is warp-uniform; rows that keep their max use 1.
+            const bool need = mx > m_ref + kLazyRescale;
+            float alpha = 1.f;
+            if (need) {
+                alpha = exp2f(m_ref - mx);  // 0 when m_ref = -inf
+                l *= alpha;
+                m_ref = mx;
+            }
+            if (o_live && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t r[32];
+                    tc_ld32(lane_base + C::kOCol + c0, r);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+                    tc_st32(lane_base + C::kOCol + c0, r);
+                }
+            }
+            const float muse = m_ref == -INFINITY ? 0.f : m_ref;
+            float rs = 0.f;
+#pragma unroll
+            for (int k = 0; k < kKeys; ++k) {
+                x[k] = exp2f(x[k] - muse);
+                rs += x[k];
+            }
+            l += rs;
+            // P row as bf16 head and tail, 8 keys (16 bytes) per core-matrix row
+#pragma unroll
+            for (int j = 0; j < kKeys / 8; ++j) {
+                uint32_t hv[4], tv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float a = x[8 * j + 2 * u], c2 = x[8 * j + 2 * u + 1];
+                    hv[u] = pack_bf16x2(a, c2);
+                    tv[u] = pack_bf16x2(a - bf16_lo_to_f32(hv[u]), c2 - bf16_hi_to_f32(hv[u]));
+                }
+                *reinterpret_cast<uint4 *>(ph + j * 128) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                *reinterpret_cast<uint4 *>(pl + j * 128) = make_uint4(tv[0], tv[1], tv[2], tv[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bars[kPFull]));
+            o_live = true;
+        }
+        // ---------------------------------------------------- epilogue
+        bool have_o = n_tiles > 0 && !flags[0];
+        if (have_o) have_o = warp_wait(&bars[kPvDone], (n_tiles - 1) & 1, flags);
+        have_o = __all_sync(0xffffffffu, have_o);
+        tc_fence_after();
+        const int h = g * G + (row_live ? rq % G : 0);
+        const float inv = (have_o && l > 0.f) ? 1.f / l : 0.f;
+        const float lse2 = (have_o && l > 0.f) ? m_ref + log2f(l) : -INFINITY;
+        float *dst = nullptr;
+        if (row_live) {
+            if (n_split == 1) {
+                const int64_t orow = (b * n_nodes + node) * H_q + h;
+                dst = out + orow * D;
+                if (lse) lse[orow] = flags[0] ? NAN : lse2 * kLn2;
+            } else {
+                const int64_t prow = ((b * H_kv + g) * R + rq) * n_split + split;
+                dst = ws.o_part + prow * D;
+                ws.lse_part[prow] = flags[0] ? NAN : lse2;
+            }
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            if (have_o) tc_ld32(lane_base + C::kOCol + c0, r);  // warp-uniform
+            if (row_live) {
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    float4 v;
+                    v.x = have_o ? __uint_as_float(r[k]) * inv : 0.f;
+                    v.y = have_o ? __uint_as_float(r[k + 1]) * inv : 0.f;
+                    v.z = have_o ? __uint_as_float(r[k + 2]) * inv : 0.f;
+                    v.w = have_o ? __uint_as_float(r[k + 3]) * inv : 0.f;
+                    *reinterpret_cast<float4 *>(dst + c0 + k) = v;
+                }
+            }
+        }
     }
 
-    // ------------------------------------------------- partial or final rows
-#pragma unroll
-    for (int hi = 0; hi < 2; ++hi) {
-        if (!rows[hi].live) continue;
-        const int rq = rb * kRowsPerCta + warp * 16 + r + 8 * hi;
-        const int t = rq / G, h = g * G + rq % G;
-        const float inv = l[hi] > 0.f ? 1.f / l[hi] : 0.f;
-        const float lse2 = l[hi] > 0.f ? m[hi] + log2f(l[hi]) : -INFINITY;
-        float *dst;
-        if (n_split == 1) {
-            const int64_t orow = (b * n_nodes + t) * H_q + h;
-            dst = out + orow * D;
-            if (c == 0 && lse) lse[orow] = lse2 * kLn2;
-        } else {
-            const int64_t prow = ((b * H_kv + g) * R + rq) * n_split + split;
-            dst = ws.o_part + prow * D;
-            if (c == 0) ws.lse_part[prow] = lse2;
-        }
-#pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt)
-            *reinterpret_cast<float2 *>(dst + nt * 8 + 2 * c) =
-                make_float2(o[nt][2 * hi] * inv, o[nt][2 * hi + 1] * inv);
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tc_dealloc(tmem, C::kTmemCols);
     }
     if (n_split == 1) return;
 
@@ -373,18 +442,16 @@ __global__ void __launch_bounds__(kThreads, 1) tree_decode_kernel(
     const int64_t cidx = (b * H_kv + g) * n_rb + rb;
     if (tid == 0) {
         const int32_t ticket = atomicAdd(&ws.counters[cidx], 1);
-        flags[0] = (ticket == n_split - 1);
+        flags[1] = (ticket == n_split - 1);
     }
     __syncthreads();
-    if (!flags[0]) return;
+    if (!flags[1]) return;
     __threadfence();
-
-    const int row0 = rb * kRowsPerCta;
-    const int n_rows = R - row0 < kRowsPerCta ? R - row0 : kRowsPerCta;
-    float *wts = reinterpret_cast<float *>(smem + C::kKVOffset);  // [rows][n_split]
+    const int row0 = rb * kRows;
+    const int n_rows = R - row0 < kRows ? R - row0 : kRows;
+    float *wts = reinterpret_cast<float *>(smem + C::kKvOff);  // [rows][n_split]
     const int64_t prow0 = (b * H_kv + g) * R + row0;
-    for (int e = tid; e < n_rows * n_split; e += kThreads)
-        wts[e] = __ldcg(ws.lse_part + prow0 * n_split + e);
+    for (int e = tid; e < n_rows * n_split; e += kThreads) wts[e] = __ldcg(ws.lse_part + prow0 * n_split + e);
     __syncthreads();
     for (int i = tid; i < n_rows; i += kThreads) {
         float *w = wts + i * n_split;
@@ -397,8 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_decode_kernel(
         for (int s2 = 0; s2 < n_split; ++s2)
             w[s2] = (sum > 0.f && w[s2] != -INFINITY) ? exp2f(w[s2] - lt) : 0.f;
         const int rq = row0 + i;
-        const int64_t orow = (b * n_nodes + rq / G) * H_q + g * G + rq % G;
-        if (lse) lse[orow] = lt * kLn2;
+        if (lse) lse[(b * n_nodes + rq / G) * H_q + g * G + rq % G] = lt * kLn2;
     }
     __syncthreads();
     constexpr int D4 = D / 4;
@@ -415,28 +481,27 @@ __global__ void __launch_bounds__(kThreads, 1) tree_decode_kernel(
             acc.w += w[s2] * v.w;
         }
         const int rq = row0 + i;
-        const int64_t orow = (b * n_nodes + rq / G) * H_q + g * G + rq % G;
-        reinterpret_cast<float4 *>(out + orow * D)[d4] = acc;
+        reinterpret_cast<float4 *>(out + ((b * n_nodes + rq / G) * H_q + g * G + rq % G) * D)[d4] = acc;
     }
-    if (tid == 0) ws.counters[cidx] = 0;  // ready for the next call
+    if (tid == 0) ws.counters[cidx] = 0;
 }
 
 template <int D>
-wmtp_status launch_tree(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_kv,
-                        const uint16_t *k_pool, const uint16_t *v_pool, int64_t num_slots,
-                        const int32_t *seq_lens, const int32_t *ring_base, int32_t n_sink,
-                        int32_t window, int32_t depth, int32_t tree_k, float scale, float *out,
-                        float *lse, void *workspace, int32_t n_split, cudaStream_t stream) {
-    using C = TCfg<D>;
+wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_kv,
+                           const uint16_t *k_pool, const uint16_t *v_pool, int64_t num_slots,
+                           const int32_t *seq_lens, const int32_t *ring_base, int32_t n_sink,
+                           int32_t window, int32_t depth, int32_t tree_k, float scale, float *out,
+                           float *lse, void *workspace, int32_t n_split, cudaStream_t stream) {
+    using C = Cfg<D>;
     const int G = H_q / H_kv;
     const int n_nodes = tree_k * depth;
     const int R = n_nodes * G;
-    const int n_rb = (R + kRowsPerCta - 1) / kRowsPerCta;
+    const int n_rb = (R + kRows - 1) / kRows;
     static int opted_in[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WMTP_ECUDA;
     if (!opted_in[dev]) {
-        if (cudaFuncSetAttribute(tree_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(tree_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes) != cudaSuccess)
             return WMTP_ECUDA;
         opted_in[dev] = 1;
@@ -445,16 +510,16 @@ wmtp_status launch_tree(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_kv,
     if (n_split > 1) {
         uint8_t *p = static_cast<uint8_t *>(workspace);
         ws.counters = reinterpret_cast<int32_t *>(p);
-        p += align256t((size_t)B * H_kv * n_rb * 4);
+        p += align256((size_t)B * H_kv * n_rb * 4);
         ws.lse_part = reinterpret_cast<float *>(p);
-        p += align256t((size_t)B * H_kv * R * n_split * 4);
+        p += align256((size_t)B * H_kv * R * n_split * 4);
         ws.o_part = reinterpret_cast<float *>(p);
     }
     PdlLaunch launch(dim3((unsigned)n_split, (unsigned)(H_kv * n_rb), (unsigned)B), dim3(kThreads),
                      C::kSmemBytes, stream);
     const cudaError_t err = cudaLaunchKernelEx(
-        &launch.cfg, tree_decode_kernel<D>, reinterpret_cast<const __nv_bfloat16 *>(q), H_q, H_kv,
-        G, n_nodes, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
+        &launch.cfg, tree_tc_kernel<D>, reinterpret_cast<const __nv_bfloat16 *>(q), H_q, H_kv, G,
+        n_nodes, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
         reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, seq_lens, ring_base, n_sink,
         window, depth, tree_k, scale * 1.4426950408889634f, out, lse, ws, n_split, n_rb);
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
@@ -462,11 +527,32 @@ wmtp_status launch_tree(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_kv,
 
 }  // namespace
 
-cudaError_t read_tree_error(int32_t *code, bool clear) {
-    cudaError_t err = cudaMemcpyFromSymbol(code, g_tree_error, sizeof(int32_t));
+cudaError_t read_tree_tc_error(int32_t *code, bool clear) {
+    cudaError_t err = cudaMemcpyFromSymbol(code, g_tree_tc_error, sizeof(int32_t));
     if (err != cudaSuccess || !clear) return err;
     const int32_t zero = 0;
-    return cudaMemcpyToSymbol(g_tree_error, &zero, sizeof(int32_t));
+    return cudaMemcpyToSymbol(g_tree_tc_error, &zero, sizeof(int32_t));
+}
+
+size_t tree_tc_workspace_bytes(int64_t B, int64_t H_kv, int64_t R, int D, int n_split) {
+    if (n_split <= 1) return 0;
+    const int64_t n_rb = (R + kRows - 1) / kRows;
+    return align256((size_t)B * H_kv * n_rb * 4) + align256((size_t)B * H_kv * R * n_split * 4) +
+           (size_t)B * H_kv * R * n_split * D * 4;
+}
+
+wmtp_status tree_tc_launch(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_kv, int32_t D,
+                           const uint16_t *k_pool, const uint16_t *v_pool, int64_t num_slots,
+                           const int32_t *seq_lens, const int32_t *ring_base, int32_t n_sink,
+                           int32_t window, int32_t depth, int32_t tree_k, float scale, float *out,
+                           float *lse, void *workspace, int32_t n_split, cudaStream_t stream) {
+    if (D == 256)
+        return launch_tree_tc<256>(q, B, H_q, H_kv, k_pool, v_pool, num_slots, seq_lens, ring_base,
+                                   n_sink, window, depth, tree_k, scale, out, lse, workspace,
+                                   n_split, stream);
+    return launch_tree_tc<128>(q, B, H_q, H_kv, k_pool, v_pool, num_slots, seq_lens, ring_base,
+                               n_sink, window, depth, tree_k, scale, out, lse, workspace, n_split,
+                               stream);
 }
 
 }  // namespace wmtp
@@ -489,14 +575,14 @@ int32_t wmtp_tree_num_splits(int32_t B, int32_t H_q, int32_t H_kv, int32_t depth
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (B < 1 || H_kv < 1 || H_q < H_kv || depth < 1 || tree_k < 1) return 1;
     const int64_t R = (int64_t)tree_k * depth * (H_q / H_kv);
-    const int64_t n_rb = (R + kTcRows - 1) / kTcRows;
+    const int64_t n_rb = (R + kRows - 1) / kRows;
     const int64_t per_split = (int64_t)B * H_kv * n_rb;
     const int64_t keys = (int64_t)n_sink + window + (int64_t)tree_k * depth;
     int64_t n = sms / per_split;
-    const int64_t by_len = (keys + kTileKeys - 1) / kTileKeys / 4;  // >= four tiles per split
+    const int64_t by_len = (keys + kKeys - 1) / kKeys / 4;  // >= four tiles per split
     if (n > by_len) n = by_len;
     if (n < 1) n = 1;
-    if (n > kMaxTreeSplits) n = kMaxTreeSplits;
+    if (n > kMaxSplits) n = kMaxSplits;
     return (int32_t)n;
 }
 
@@ -510,10 +596,10 @@ wmtp_status wmtp_tree_draft_attn(const uint16_t *q, int32_t B, int32_t H_q, int3
     if (B < 0 || H_q < 1 || H_kv < 1 || (H_q % H_kv) != 0) return WMTP_EINVAL;
     if (D != 128 && D != 256) return WMTP_EINVAL;
     if (n_sink < 0 || window < 1 || depth < 1 || tree_k < 1) return WMTP_EINVAL;
-    if (n_split < 1 || n_split > kMaxTreeSplits || num_slots < 0) return WMTP_EINVAL;
+    if (n_split < 1 || n_split > kMaxSplits || num_slots < 0) return WMTP_EINVAL;
     if (depth > 255) return WMTP_EINVAL;
     const int64_t R = (int64_t)tree_k * depth * (H_q / H_kv);
-    const int64_t n_rb = (R + kTcRows - 1) / kTcRows;
+    const int64_t n_rb = (R + kRows - 1) / kRows;
     if (R > (1 << 20) || (int64_t)H_kv * n_rb > 65535 || B > 65535) return WMTP_EINVAL;
     if (B == 0) return WMTP_OK;
     if (!q || !k_pool || !v_pool || !seq_lens || !ring_base || !out) return WMTP_EINVAL;
