@@ -71,6 +71,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` inside the
+// instruction (it wakes as soon as the phase completes) instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait that sleeps in the barrier between checks.
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint32_t bar, uint32_t parity,
+                                                        uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 10000u)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` nanoseconds and returns false; never spins without a bound.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,

@@ -77,8 +77,7 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kKvOff = kQBytes;
     static constexpr int kPOff = kKvOff + 2 * kStageBytes;
-    static constexpr int kInfoOff = kPOff + 2 * kPBytes;     // int2 [2][kKeys]
-    static constexpr int kBarOff = kInfoOff + 2 * kKeys * 8;
+    static constexpr int kBarOff = kPOff + 2 * kPBytes;
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16;
     static constexpr int kOCol = 2 * kKeys;                  // O after the two S buffers
     static constexpr int kTmemCols = (kOCol + D <= 256) ? 256 : 512;
@@ -108,8 +107,8 @@ __device__ __forceinline__ Geo geometry(int64_t S, int n_sink, int window, int n
     return g;
 }
 
-// Key info for the mask: logical position and a code (-2 no key, -1 a
-// committed key, else branch << 8 | depth of a draft node).
+// Logical position and a code (-1 a committed key, else branch << 8 | depth
+// of a draft node) of entry e of the key list.
 __device__ __forceinline__ int2 key_info(const Geo &g, int64_t e, int depth) {
     if (e < g.Uc) return make_int2((int)(e < g.ns ? e : g.lo0 + (e - g.ns)), -1);
     const int64_t n = e - g.Uc;
@@ -119,7 +118,7 @@ __device__ __forceinline__ int2 key_info(const Geo &g, int64_t e, int depth) {
 }
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int32_t *abort) {
-    if (mbar_wait_bounded(smem_addr(bar), parity, kWaitNs)) return true;
+    if (mbar_wait_sleep_bounded(smem_addr(bar), parity, kWaitNs)) return true;
     latch(WMTP_DEV_WAIT_TIMEOUT);
     *abort = 1;
     return false;
@@ -143,7 +142,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);  // [0] abort [1] ticket
-    int2 *info = reinterpret_cast<int2 *>(smem + C::kInfoOff);
 
     griddep_launch_dependents();
     griddep_wait();
@@ -222,20 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             // this lane's key (one of the warp's 32) and its slot
             const int key = lw * 32 + lane;
             const int64_t kk = (int64_t)t * kKeys + key;
-            int2 inf = make_int2(0, -2);
             int64_t slot = 0;
             bool ok = false;
             if (kk < cnt) {
-                inf = key_info(geo, start + kk, depth);
+                const int2 inf = key_info(geo, start + kk, depth);
                 const int br = inf.y < 0 ? 0 : (inf.y >> 8);
                 slot = ring_slot(base, inf.x, br, n_sink, window, depth, tree_k);
                 ok = slot >= 0 && slot < num_slots;
-                if (!ok) {
-                    latch(WMTP_DEV_SLOT_RANGE);
-                    inf.y = -2;
-                }
+                if (!ok) latch(WMTP_DEV_SLOT_RANGE);
             }
-            info[st * kKeys + key] = inf;
             const uint32_t okm = __ballot_sync(0xffffffffu, ok);
             const uint32_t kt = sbase + C::kKvOff + st * C::kStageBytes;
             const uint32_t vt = kt + C::kTileBytes;
@@ -310,7 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         for (int t = 0; t < n_tiles; ++t) {
             const int st = t & 1;
             if (!warp_wait(&bars[kSFull + st], (t >> 1) & 1, flags)) break;
-            if (!warp_wait(&bars[kKvFull + st], (t >> 1) & 1, flags)) break;
             tc_fence_after();
             float x[kKeys];
             {
@@ -326,15 +318,26 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&bars[kSEmpty + st]));
+            // Tree-causal mask from the key index alone (the same for every
+            // lane, so the branches are warp-uniform): committed keys need a
+            // position, draft nodes a (branch, depth) as well.
             float mx = -INFINITY;
+            const int64_t e0 = start + (int64_t)t * kKeys;
+            const int64_t valid = cnt - (int64_t)t * kKeys;
 #pragma unroll
             for (int k = 0; k < kKeys; ++k) {
-                const int2 inf = info[st * kKeys + k];
+                const int64_t e = e0 + k;
                 bool vis = false;
-                if (row_live && inf.y != -2) {
-                    const bool in_win = inf.x < n_sink || inf.x >= row_lo;
-                    vis = inf.y == -1 ? in_win
-                                      : ((inf.y >> 8) == rbr && (inf.y & 255) <= rdep && in_win);
+                if (row_live && k < valid) {
+                    if (e < geo.Uc) {
+                        const int64_t p = e < geo.ns ? e : geo.lo0 + (e - geo.ns);
+                        vis = p < n_sink || p >= row_lo;
+                    } else {
+                        const int n = (int)(e - geo.Uc);
+                        const int br = n / depth, dep = n - (n / depth) * depth;
+                        const int64_t p = S + dep;
+                        vis = br == rbr && dep <= rdep && (p < n_sink || p >= row_lo);
+                    }
                 }
                 x[k] = vis ? x[k] * scale_log2 : -INFINITY;
                 mx = fmaxf(mx, x[k]);
