@@ -118,7 +118,7 @@ __device__ __forceinline__ int2 key_info(const Geo &g, int64_t e, int depth) {
 }
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int32_t *abort) {
-    if (mbar_wait_sleep_bounded(smem_addr(bar), parity, kWaitNs)) return true;
+    if (mbar_wait_bounded(smem_addr(bar), parity, kWaitNs)) return true;
     latch(WMTP_DEV_WAIT_TIMEOUT);
     *abort = 1;
     return false;
@@ -295,6 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         const int rbr = node / depth, rdep = node - (node / depth) * depth;
         const int64_t kv = S + rdep + 1;
         const int64_t row_lo = kv > (int64_t)n_sink + window ? kv - window : 0;
+        // Committed entry e (position e below ns, lo0 + e - ns after) is in the
+        // row's key set iff e < ns or its position >= row_lo; draft node n is
+        // iff it is on the row's branch at depth <= the row's depth and its
+        // position S + depth is a sink or >= row_lo.
+        const int Uc = (int)geo.Uc, ns = (int)geo.ns;
+        const int e_lo = ns + (int)(row_lo - geo.lo0 > 0 ? row_lo - geo.lo0 : 0);
+        const int n0 = rbr * depth, n_hi = n0 + rdep;
+        const int d_sink = (int)((int64_t)n_sink - S);
+        const int d_lo = (int)(row_lo - S);
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         float m_ref = -INFINITY, l = 0.f;
         bool o_live = false;  // O holds at least one PV product
@@ -318,27 +327,19 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&bars[kSEmpty + st]));
-            // Tree-causal mask from the key index alone (the same for every
-            // lane, so the branches are warp-uniform): committed keys need a
-            // position, draft nodes a (branch, depth) as well.
+            // Tree-causal mask from the key index alone, with per-row int32
+            // thresholds (no loads, no division): entry e is a committed key
+            // when e < Uc, else draft node n = e - Uc.
             float mx = -INFINITY;
-            const int64_t e0 = start + (int64_t)t * kKeys;
-            const int64_t valid = cnt - (int64_t)t * kKeys;
+            const int e0 = (int)(start + (int64_t)t * kKeys);
+            const int valid = (int)(cnt - (int64_t)t * kKeys);
 #pragma unroll
             for (int k = 0; k < kKeys; ++k) {
-                const int64_t e = e0 + k;
-                bool vis = false;
-                if (row_live && k < valid) {
-                    if (e < geo.Uc) {
-                        const int64_t p = e < geo.ns ? e : geo.lo0 + (e - geo.ns);
-                        vis = p < n_sink || p >= row_lo;
-                    } else {
-                        const int n = (int)(e - geo.Uc);
-                        const int br = n / depth, dep = n - (n / depth) * depth;
-                        const int64_t p = S + dep;
-                        vis = br == rbr && dep <= rdep && (p < n_sink || p >= row_lo);
-                    }
-                }
+                const int e = e0 + k;
+                const int n = e - Uc;
+                const bool vis_c = (e < ns) | (e >= e_lo);
+                const bool vis_n = (n >= n0) & (n <= n_hi) & (((n - n0) < d_sink) | ((n - n0) >= d_lo));
+                const bool vis = row_live & (k < valid) & (e < Uc ? vis_c : vis_n);
                 x[k] = vis ? x[k] * scale_log2 : -INFINITY;
                 mx = fmaxf(mx, x[k]);
             }
