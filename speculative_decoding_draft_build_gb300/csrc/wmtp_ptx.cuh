@@ -149,6 +149,12 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32
                  : "memory");
 }
 
+// Arrives on `bar` (without raising its expected count) once every cp.async
+// issued so far by this thread has completed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }

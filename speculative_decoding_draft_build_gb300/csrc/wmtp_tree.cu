@@ -52,9 +52,11 @@ __device__ int32_t g_tree_tc_error = 0;
 __device__ __forceinline__ void latch(int32_t code) { atomicCAS(&g_tree_tc_error, 0, code); }
 
 constexpr int kRows = 128;  // query rows per CTA (MMA M)
-constexpr int kKeys = 64;   // keys per tile (N of QK^T, K of PV)
+constexpr int kKeys = 32;   // keys per tile (N of QK^T, K of PV)
+constexpr int kKvStages = 4;
 constexpr int kSoftWarps = 4;
 constexpr int kLoadWarps = 2;
+constexpr int kLoadThreads = kLoadWarps * 32;
 constexpr int kMmaWarp = kSoftWarps + kLoadWarps;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr int kMaxSplits = 64;
@@ -62,8 +64,16 @@ constexpr float kLazyRescale = 8.f;  // log2 of the growth tolerated before resc
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// Barrier slots.
-enum { kKvFull = 0, kKvEmpty = 2, kSFull = 4, kSEmpty = 6, kPFull = 8, kPvDone = 9, kNumBars = 10 };
+// Barrier slots: K/V stages (4), S buffers (2), P buffers (2).
+enum {
+    kKvFull = 0,
+    kKvEmpty = kKvFull + kKvStages,
+    kSFull = kKvEmpty + kKvStages,
+    kSEmpty = kSFull + 2,
+    kPFull = kSEmpty + 2,
+    kPvDone = kPFull + 2,
+    kNumBars = kPvDone + 2
+};
 
 template <int D>
 struct Cfg {
@@ -74,14 +84,16 @@ struct Cfg {
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kPSbo = kKeys / 8 * 128;            // P: 8-row group stride
     static constexpr int kPBytes = kRows / 8 * kPSbo;        // one of P_hi / P_lo
+    static constexpr int kPBufBytes = 2 * kPBytes;           // P_hi then P_lo
     static constexpr int kQOff = 0;
     static constexpr int kKvOff = kQBytes;
-    static constexpr int kPOff = kKvOff + 2 * kStageBytes;
-    static constexpr int kBarOff = kPOff + 2 * kPBytes;
+    static constexpr int kPOff = kKvOff + kKvStages * kStageBytes;
+    static constexpr int kBarOff = kPOff + 2 * kPBufBytes;
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16;
     static constexpr int kOCol = 2 * kKeys;                  // O after the two S buffers
     static constexpr int kTmemCols = (kOCol + D <= 256) ? 256 : 512;
-    static_assert(kRows * kMaxSplits * 4 <= 2 * kStageBytes, "merge weights must fit");
+    static_assert(kRows * kMaxSplits * 4 <= kKvStages * kStageBytes, "merge weights must fit");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct TreeWs {
@@ -167,16 +179,16 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     const int n_tiles = (int)((cnt + kKeys - 1) / kKeys);
 
     if (tid == 0) {
-        mbar_init(smem_addr(&bars[kKvFull]), kLoadWarps);
-        mbar_init(smem_addr(&bars[kKvFull + 1]), kLoadWarps);
-        mbar_init(smem_addr(&bars[kKvEmpty]), 1);
-        mbar_init(smem_addr(&bars[kKvEmpty + 1]), 1);
-        mbar_init(smem_addr(&bars[kSFull]), 1);
-        mbar_init(smem_addr(&bars[kSFull + 1]), 1);
-        mbar_init(smem_addr(&bars[kSEmpty]), kSoftWarps);
-        mbar_init(smem_addr(&bars[kSEmpty + 1]), kSoftWarps);
-        mbar_init(smem_addr(&bars[kPFull]), kSoftWarps);
-        mbar_init(smem_addr(&bars[kPvDone]), 1);
+        for (int i = 0; i < kKvStages; ++i) {
+            mbar_init(smem_addr(&bars[kKvFull + i]), kLoadThreads);
+            mbar_init(smem_addr(&bars[kKvEmpty + i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&bars[kSFull + i]), 1);
+            mbar_init(smem_addr(&bars[kSEmpty + i]), kSoftWarps);
+            mbar_init(smem_addr(&bars[kPFull + i]), kSoftWarps);
+            mbar_init(smem_addr(&bars[kPvDone + i]), 1);
+        }
         flags[0] = 0;
         flags[1] = 0;
         fence_mbar_init();
@@ -206,23 +218,29 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
 
     if (warp >= kSoftWarps && warp < kMmaWarp) {
         // ----------------------------------------------------------- gather
+        // Each loader warp owns 16 keys of every 32-key tile; every loader
+        // thread arrives on the stage's barrier when its copies land, so up
+        // to four tiles are in flight.
         const int lw = warp - kSoftWarps;
         const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * D * 2;
         const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * D * 2;
         const size_t slot_bytes = (size_t)H_kv * D * 2;
-        constexpr int kLanesPerRow = C::kChunks < 32 ? C::kChunks : 32;  // 16 (D=128) or 32
+        constexpr int kKeysPerWarp = kKeys / kLoadWarps;                  // 16
+        constexpr int kLanesPerRow = C::kChunks < 32 ? C::kChunks : 32;   // 16 (D=128) or 32
         constexpr int kRowsPerInst = 32 / kLanesPerRow;
         const int sub = lane / kLanesPerRow, col = lane % kLanesPerRow;
         for (int t = 0; t < n_tiles; ++t) {
-            const int st = t & 1;
-            if (t >= 2 && !mbar_wait(&bars[kKvEmpty + st], ((t >> 1) - 1) & 1, flags)) break;
+            const int st = t % kKvStages;
+            if (t >= kKvStages &&
+                !mbar_wait(&bars[kKvEmpty + st], ((t / kKvStages) - 1) & 1, flags))
+                break;
             if (flags[0]) break;
-            // this lane's key (one of the warp's 32) and its slot
-            const int key = lw * 32 + lane;
+            // lanes 0-15 hold the slots of this warp's 16 keys
+            const int key = lw * kKeysPerWarp + (lane & (kKeysPerWarp - 1));
             const int64_t kk = (int64_t)t * kKeys + key;
             int64_t slot = 0;
             bool ok = false;
-            if (kk < cnt) {
+            if (lane < kKeysPerWarp && kk < cnt) {
                 const int2 inf = key_info(geo, start + kk, depth);
                 const int br = inf.y < 0 ? 0 : (inf.y >> 8);
                 slot = ring_slot(base, inf.x, br, n_sink, window, depth, tree_k);
@@ -232,48 +250,48 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             const uint32_t okm = __ballot_sync(0xffffffffu, ok);
             const uint32_t kt = sbase + C::kKvOff + st * C::kStageBytes;
             const uint32_t vt = kt + C::kTileBytes;
-            for (int r0 = 0; r0 < 32; r0 += kRowsPerInst) {
-                const int kr = r0 + sub;               // key within this warp's 32
-                const int kt_key = lw * 32 + kr;       // key within the tile
+#pragma unroll
+            for (int r0 = 0; r0 < kKeysPerWarp; r0 += kRowsPerInst) {
+                const int kr = r0 + sub;
+                const int tk = lw * kKeysPerWarp + kr;  // key within the tile
                 const int64_t sl = __shfl_sync(0xffffffffu, slot, kr);
                 const bool kok = (okm >> kr) & 1u;
                 const size_t off = kok ? (size_t)sl * slot_bytes + col * 16 : 0;
-                const uint32_t dst = (kt_key >> 3) * C::kRowSbo + col * 128 + (kt_key & 7) * 16;
+                const uint32_t dst = (tk >> 3) * C::kRowSbo + col * 128 + (tk & 7) * 16;
                 cp_async_16(kt + dst, kbase + off, kok ? 16u : 0u, keep);
                 cp_async_16(vt + dst, vbase + off, kok ? 16u : 0u, keep);
             }
-            cp_async_commit();
-            cp_async_wait<0>();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&bars[kKvFull + st]));
+            cp_async_mbar_arrive(smem_addr(&bars[kKvFull + st]));
         }
+        cp_async_wait<0>();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issue
         if (lane == 0) {
             constexpr uint32_t idesc_qk = tc_idesc_bf16(kRows, kKeys, 0);
             constexpr uint32_t idesc_pv = tc_idesc_bf16(kRows, D, 1);
             const uint32_t q_s = sbase + C::kQOff;
-            const uint32_t p_hi = sbase + C::kPOff, p_lo = p_hi + C::kPBytes;
             auto issue_qk = [&](int t) -> bool {
-                const int st = t & 1;
-                if (!mbar_wait(&bars[kKvFull + st], (t >> 1) & 1, flags)) return false;
-                if (t >= 2 && !mbar_wait(&bars[kSEmpty + st], ((t >> 1) - 1) & 1, flags)) return false;
+                const int st = t % kKvStages, sb = t & 1;
+                if (!mbar_wait(&bars[kKvFull + st], (t / kKvStages) & 1, flags)) return false;
+                if (t >= 2 && !mbar_wait(&bars[kSEmpty + sb], ((t >> 1) - 1) & 1, flags)) return false;
+                fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
                 tc_fence_after();
                 const uint32_t kt = sbase + C::kKvOff + st * C::kStageBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    tc_mma_bf16(tmem + st * kKeys, tc_smem_desc(q_s + kk * 256, 128, C::kRowSbo),
+                    tc_mma_bf16(tmem + sb * kKeys, tc_smem_desc(q_s + kk * 256, 128, C::kRowSbo),
                                 tc_smem_desc(kt + kk * 256, 128, C::kRowSbo), idesc_qk, kk > 0);
-                tc_commit(smem_addr(&bars[kSFull + st]));
+                tc_commit(smem_addr(&bars[kSFull + sb]));
                 return true;
             };
             bool live = n_tiles == 0 || issue_qk(0);
             for (int t = 0; live && t < n_tiles; ++t) {
                 if (t + 1 < n_tiles && !issue_qk(t + 1)) break;
-                if (!mbar_wait(&bars[kPFull], t & 1, flags)) break;
+                const int pb = t & 1;
+                if (!mbar_wait(&bars[kPFull + pb], (t >> 1) & 1, flags)) break;
                 tc_fence_after();
-                const uint32_t vt = sbase + C::kKvOff + (t & 1) * C::kStageBytes + C::kTileBytes;
+                const uint32_t vt = sbase + C::kKvOff + (t % kKvStages) * C::kStageBytes + C::kTileBytes;
+                const uint32_t p_hi = sbase + C::kPOff + pb * C::kPBufBytes, p_lo = p_hi + C::kPBytes;
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
                     const uint64_t vd = tc_smem_desc(vt + 2 * kk * C::kRowSbo, C::kRowSbo, 128);
@@ -282,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                     tc_mma_bf16(tmem + C::kOCol, tc_smem_desc(p_lo + kk * 256, 128, C::kPSbo), vd,
                                 idesc_pv, 1);
                 }
-                tc_commit(smem_addr(&bars[kPvDone]));
-                tc_commit(smem_addr(&bars[kKvEmpty + (t & 1)]));
+                tc_commit(smem_addr(&bars[kPvDone + pb]));
+                tc_commit(smem_addr(&bars[kKvEmpty + (t % kKvStages)]));
             }
         }
     } else {
@@ -307,45 +325,49 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         float m_ref = -INFINITY, l = 0.f;
         bool o_live = false;  // O holds at least one PV product
-        uint8_t *ph = smem + C::kPOff + (i >> 3) * C::kPSbo + (i & 7) * 16;
-        uint8_t *pl = ph + C::kPBytes;
+        const int poff = (i >> 3) * C::kPSbo + (i & 7) * 16;
         for (int t = 0; t < n_tiles; ++t) {
-            const int st = t & 1;
-            if (!warp_wait(&bars[kSFull + st], (t >> 1) & 1, flags)) break;
+            const int sb = t & 1, pb = t & 1;
+            if (!warp_wait(&bars[kSFull + sb], (t >> 1) & 1, flags)) break;
             tc_fence_after();
             float x[kKeys];
             {
-                uint32_t r0[32], r1[32];
-                tc_ld32(lane_base + st * kKeys, r0);
-                tc_ld32(lane_base + st * kKeys + 32, r1);
+                uint32_t r0[32];
+                tc_ld32(lane_base + sb * kKeys, r0);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    x[k] = __uint_as_float(r0[k]);
-                    x[32 + k] = __uint_as_float(r1[k]);
-                }
+                for (int k = 0; k < kKeys; ++k) x[k] = __uint_as_float(r0[k]);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&bars[kSEmpty + st]));
+            if (lane == 0) mbar_arrive(smem_addr(&bars[kSEmpty + sb]));
             // Tree-causal mask from the key index alone, with per-row int32
             // thresholds (no loads, no division): entry e is a committed key
-            // when e < Uc, else draft node n = e - Uc.
-            float mx = -INFINITY;
+            // when e < Uc, else draft node n = e - Uc.  Tiles whose keys every
+            // row of the warp sees skip the mask.
             const int e0 = (int)(start + (int64_t)t * kKeys);
             const int valid = (int)(cnt - (int64_t)t * kKeys);
+            const bool lane_all = !row_live || e0 + kKeys <= ns || e0 >= e_lo;
+            const bool fast = valid >= kKeys && e0 + kKeys <= Uc && __all_sync(0xffffffffu, lane_all);
+            float mx = -INFINITY;
+            if (fast) {
 #pragma unroll
-            for (int k = 0; k < kKeys; ++k) {
-                const int e = e0 + k;
-                const int n = e - Uc;
-                const bool vis_c = (e < ns) | (e >= e_lo);
-                const bool vis_n = (n >= n0) & (n <= n_hi) & (((n - n0) < d_sink) | ((n - n0) >= d_lo));
-                const bool vis = row_live & (k < valid) & (e < Uc ? vis_c : vis_n);
-                x[k] = vis ? x[k] * scale_log2 : -INFINITY;
-                mx = fmaxf(mx, x[k]);
+                for (int k = 0; k < kKeys; ++k) {
+                    x[k] *= scale_log2;
+                    mx = fmaxf(mx, x[k]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kKeys; ++k) {
+                    const int e = e0 + k;
+                    const int n = e - Uc;
+                    const bool vis_c = (e < ns) | (e >= e_lo);
+                    const bool vis_n =
+                        (n >= n0) & (n <= n_hi) & (((n - n0) < d_sink) | ((n - n0) >= d_lo));
+                    const bool vis = row_live & (k < valid) & (e < Uc ? vis_c : vis_n);
+                    x[k] = vis ? x[k] * scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x[k]);
+                }
             }
-            // PV(t-1) must be done before O is rescaled or P is overwritten.
-            if (t >= 1 && !warp_wait(&bars[kPvDone], (t - 1) & 1, flags)) break;
-            tc_fence_after();
             // Lazy rescale: the reference max moves only when a row's max grew
             // by more than 2^8 (also the first time it becomes finite).  The
             // rescale loop is warp-uniform; rows that keep their max use 1.
@@ -357,6 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                 m_ref = mx;
             }
             if (o_live && __any_sync(0xffffffffu, need)) {
+                // O must hold PV(t-1) before it is rescaled
+                if (!warp_wait(&bars[kPvDone + ((t - 1) & 1)], ((t - 1) >> 1) & 1, flags)) break;
+                tc_fence_after();
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t r[32];
@@ -374,7 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                 rs += x[k];
             }
             l += rs;
-            // P row as bf16 head and tail, 8 keys (16 bytes) per core-matrix row
+            // P buffer pb is free once PV(t-2) is done
+            if (t >= 2 && !warp_wait(&bars[kPvDone + pb], ((t >> 1) - 1) & 1, flags)) break;
+            uint8_t *ph = smem + C::kPOff + pb * C::kPBufBytes + poff;
+            uint8_t *pl = ph + C::kPBytes;
 #pragma unroll
             for (int j = 0; j < kKeys / 8; ++j) {
                 uint32_t hv[4], tv[4];
@@ -390,12 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&bars[kPFull]));
+            if (lane == 0) mbar_arrive(smem_addr(&bars[kPFull + pb]));
             o_live = true;
         }
         // ---------------------------------------------------- epilogue
         bool have_o = n_tiles > 0 && !flags[0];
-        if (have_o) have_o = warp_wait(&bars[kPvDone], (n_tiles - 1) & 1, flags);
+        if (have_o)
+            have_o = warp_wait(&bars[kPvDone + ((n_tiles - 1) & 1)], ((n_tiles - 1) >> 1) & 1, flags);
         have_o = __all_sync(0xffffffffu, have_o);
         tc_fence_after();
         const int h = g * G + (row_live ? rq % G : 0);
