@@ -542,7 +542,7 @@ def measure_tree(args, dev):
     return {"workload": "tree drafter: B=8, contexts log-uniform [32K, 1M], k=4, d=7 (28 nodes), "
                         "H_q=16, H_kv=2, D=256, n_sink=64, ring of n_sink+W+d*k slots",
             "timing": "CUDA events per launch, L2 flushed before each, median", "windows": res,
-            "kernel": "tree_decode_kernel<256> (mma.sync bf16)", "bf16_peak_tflops": peak_tf}
+            "kernel": "tree_tc_kernel<256> (tcgen05, TMEM accumulators)", "bf16_peak_tflops": peak_tf}
 
 
 def measure_e2e(w, args, dev):
