@@ -25,10 +25,18 @@
 //     registers.  Online softmax in base 2, max/sum across lanes with warp
 //     shuffles; the accumulator is rescaled only when a running max moves.
 //   * at the end the four warps combine through shared memory (per-head
-//     factors computed once).  Up to 16 splits of a (row, KV head) run as one
-//     thread-block cluster and merge through distributed shared memory;
-//     larger split counts write partials to the workspace, take a ticket, and
-//     the last CTA merges them in split order.  No CTA ever spins on another.
+//     factors computed once).  The splits of a (row, KV head) then merge in
+//     one of three ways:
+//       - up to 16 splits run as one thread-block cluster and merge through
+//         distributed shared memory, each CTA producing a slice of the
+//         output;
+//       - up to 8 such clusters (128 splits) merge in two levels: each
+//         cluster merges as above into a per-cluster partial of its slice,
+//         takes a ticket for that slice, and the last cluster's CTA merges
+//         the slice over the clusters in cluster order;
+//       - otherwise every split writes its partial to the workspace, takes a
+//         ticket, and the last CTA merges all splits in split order.
+//     No CTA ever spins on another.
 //   * every kernel waits on its predecessor with griddepcontrol.wait before
 //     touching global memory and is launched with programmatic stream
 //     serialization, so consecutive launches overlap only their start-up.
@@ -55,6 +63,7 @@ constexpr int kThreads = kConsumerWarps * 32;
 constexpr int kMaxGroup = 8;  // query heads per KV head handled by one CTA
 constexpr int kMaxSplits = 1024;
 constexpr int kMaxClusterMerge = 16;  // splits merged through a cluster (non-portable size)
+constexpr int kMaxClusters = 8;       // clusters merged by the second level
 constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
@@ -79,28 +88,54 @@ struct Cfg {
     static constexpr int kSmemBytes = kFlagOffset + 16;
 };
 
+// Workspace: a counter region of kMaxClusterMerge int32 per (row, KV head),
+// then the partials.  Split-order merge: lse_part [B*n_q*H_q][n_split] (base
+// 2) and o_part [B*n_q*H_q][n_split][D].  Two-level merge: o_part holds the
+// per-cluster outputs [B*n_q*H_kv][clusters][G*D] and lse_part the matching
+// per-element lse [B*n_q*H_kv][clusters][G*D/4].  Every path returns the
+// counters it used to zero.
 struct WorkspaceView {
-    int32_t *counters;  // [B*n_q*H_kv]
-    float *lse_part;    // [B*n_q*H_q*n_split], base-2 units
-    float *o_part;      // [B*n_q*H_q*n_split*D]
+    int32_t *counters;
+    float *lse_part;
+    float *o_part;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+inline size_t counter_bytes(int64_t rows_kv) { return align256((size_t)rows_kv * kMaxClusterMerge * 4); }
+
+// Bytes for the split-order merge; the two-level merge (at most n_split / 2
+// clusters, each holding rows_q * D outputs and rows_q * D / 4 lse values)
+// never needs more.
 inline size_t workspace_bytes(int64_t rows_q, int64_t rows_kv, int D, int n_split) {
     if (n_split <= 1) return 0;
-    return align256(rows_kv * 4) + align256(rows_q * n_split * 4) +
-           (size_t)rows_q * n_split * D * 4;
+    const size_t split_order =
+        counter_bytes(rows_kv) + align256((size_t)rows_q * n_split * 4) + (size_t)rows_q * n_split * D * 4;
+    const int64_t m = n_split / 2 < kMaxClusters ? n_split / 2 : kMaxClusters;
+    const size_t two_level =
+        counter_bytes(rows_kv) + align256((size_t)rows_q * m * D * 4) + (size_t)rows_q * m * D;
+    return split_order > two_level ? split_order : two_level;
 }
 
 inline WorkspaceView carve(void *ws, int64_t rows_q, int64_t rows_kv, int n_split) {
     uint8_t *p = static_cast<uint8_t *>(ws);
     WorkspaceView v;
     v.counters = reinterpret_cast<int32_t *>(p);
-    p += align256(rows_kv * 4);
+    p += counter_bytes(rows_kv);
     v.lse_part = reinterpret_cast<float *>(p);
-    p += align256(rows_q * n_split * 4);
+    p += align256((size_t)rows_q * n_split * 4);
     v.o_part = reinterpret_cast<float *>(p);
+    return v;
+}
+
+inline WorkspaceView carve_two_level(void *ws, int64_t rows_q, int64_t rows_kv, int D, int clusters) {
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    WorkspaceView v;
+    v.counters = reinterpret_cast<int32_t *>(p);
+    p += counter_bytes(rows_kv);
+    v.o_part = reinterpret_cast<float *>(p);
+    p += align256((size_t)rows_q * clusters * D * 4);
+    v.lse_part = reinterpret_cast<float *>(p);
     return v;
 }
 
@@ -110,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const __nv_bfloat16 *__restrict__ k_pool, const __nv_bfloat16 *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ table, int64_t table_stride,
     const int32_t *__restrict__ lens, float scale_log2, float *__restrict__ out,
-    float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t cluster_merge) {
+    float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t csz) {
     using C = Cfg<D>;
     constexpr int S = C::kStages;
     constexpr int R = C::kRingTiles;
@@ -119,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(smem + C::kFlagOffset);
 
     griddep_launch_dependents();
+
     griddep_wait();
 
     const int warp = threadIdx.x >> 5;
@@ -358,63 +394,148 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         cta_lse[h] = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
     }
     __syncthreads();
-    for (int e = tid; e < G * D; e += kThreads) {
-        const int h = e / D, dim = e - h * D;
-        float o_val = 0.f;
+    constexpr int D4 = D / 4;
+    for (int e = tid; e < G * D4; e += kThreads) {
+        const int h = e / D4, d4 = e - h * D4;
+        float4 o_val = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w)
-            o_val += ow[(w * kMaxGroup + h) * C::kOPitch + dim] * fac[h * kConsumerWarps + w];
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float4 v = *reinterpret_cast<const float4 *>(ow + (w * kMaxGroup + h) * C::kOPitch + 4 * d4);
+            const float f = fac[h * kConsumerWarps + w];
+            o_val.x += v.x * f;
+            o_val.y += v.y * f;
+            o_val.z += v.z * f;
+            o_val.w += v.w * f;
+        }
         const float lse2 = cta_lse[h];
-        if (n_split == 1) {
-            out[(row_q0 + h) * D + dim] = o_val;
-            if (lse && dim == 0) lse[row_q0 + h] = lse2 * kLn2;
-        } else if (cluster_merge) {
-            part_o[h * D + dim] = o_val;
-            if (dim == 0) part_lse[h] = lse2;
+        if (csz) {
+            reinterpret_cast<float4 *>(part_o + h * D)[d4] = o_val;
+            if (d4 == 0) part_lse[h] = lse2;
+        } else if (n_split == 1) {
+            reinterpret_cast<float4 *>(out + (row_q0 + h) * D)[d4] = o_val;
+            if (lse && d4 == 0) lse[row_q0 + h] = lse2 * kLn2;
         } else {
-            ws.o_part[((row_q0 + h) * n_split + split) * D + dim] = o_val;
-            if (dim == 0) ws.lse_part[(row_q0 + h) * n_split + split] = lse2;
+            reinterpret_cast<float4 *>(ws.o_part + ((row_q0 + h) * n_split + split) * D)[d4] = o_val;
+            if (d4 == 0) ws.lse_part[(row_q0 + h) * n_split + split] = lse2;
         }
     }
     if (n_split == 1) return;
 
-    if (cluster_merge) {
+    if (csz) {
         // ---------------------------------- merge through distributed smem
-        // The n_split CTAs of this (row, KV head) form one cluster; CTA `rank`
-        // merges a slice of the G x D outputs, reading every CTA's partial
-        // in split order.  The second barrier keeps each CTA's shared memory
-        // alive until all peers have read it.
+        // Each cluster of csz CTAs covers csz consecutive splits of this
+        // (row, KV head); CTA `rank` merges a slice of the G x D outputs,
+        // reading every peer's partial in split order.  Each CTA arrives on
+        // the closing barrier once its remote reads are done and waits on it
+        // just before exit, which keeps its shared memory alive until every
+        // peer has read it.
+        __syncwarp();
         cluster_sync();
         const int rank = (int)cluster_ctarank();
-        const int total = G * D;
-        const int per = (total + n_split - 1) / n_split;
-        const int lo = rank * per;
-        const int hi = lo + per < total ? lo + per : total;
+        const int n_cl = n_split / csz;  // clusters of this (row, KV head)
+        const int cl = split / csz;
+        const int64_t rk = bt * H_kv + g;
+        const int total4 = G * D4;
+        const int per4 = (total4 + csz - 1) / csz;
+        const int lo4 = rank * per4;
+        const int hi4 = lo4 + per4 < total4 ? lo4 + per4 : total4;
         const uint32_t po_addr = smem_addr(part_o), pl_addr = smem_addr(part_lse);
-        for (int e = lo + tid; e < hi; e += kThreads) {
-            const int h = e / D, dim = e - h * D;
+        for (int f = lo4 + tid; f < hi4; f += kThreads) {  // one float4 of outputs
+            const int h = f / D4;
             float ls[kMaxClusterMerge];
-            float M = -INFINITY;
+            float4 ov[kMaxClusterMerge];
+            // every remote load is issued before any is used
 #pragma unroll
             for (int s2 = 0; s2 < kMaxClusterMerge; ++s2) {
-                ls[s2] = s2 < n_split ? ld_dsmem_f32(map_to_rank(pl_addr + h * 4, s2)) : -INFINITY;
-                M = fmaxf(M, ls[s2]);
+                if (s2 < csz) {
+                    ls[s2] = ld_dsmem_f32(map_to_rank(pl_addr + h * 4, s2));
+                    ov[s2] = ld_dsmem_f32x4(map_to_rank(po_addr + f * 16, s2));
+                }
             }
-            float sum = 0.f, acc = 0.f;
+            float M = -INFINITY;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxClusterMerge; ++s2)
+                if (s2 < csz) M = fmaxf(M, ls[s2]);
+            float sum = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             if (M != -INFINITY) {
 #pragma unroll
                 for (int s2 = 0; s2 < kMaxClusterMerge; ++s2) {
-                    if (s2 < n_split && ls[s2] != -INFINITY) {
+                    if (s2 < csz && ls[s2] != -INFINITY) {
                         const float w = exp2f(ls[s2] - M);
                         sum += w;
-                        acc += w * ld_dsmem_f32(map_to_rank(po_addr + e * 4, s2));
+                        acc.x += w * ov[s2].x;
+                        acc.y += w * ov[s2].y;
+                        acc.z += w * ov[s2].z;
+                        acc.w += w * ov[s2].w;
                     }
                 }
             }
-            out[(row_q0 + h) * D + dim] = sum > 0.f ? acc / sum : 0.f;
-            if (lse && dim == 0) lse[row_q0 + h] = sum > 0.f ? (M + log2f(sum)) * kLn2 : -INFINITY;
+            const float inv = sum > 0.f ? 1.f / sum : 0.f;
+            const float4 o_cl = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            const float lse_cl = sum > 0.f ? M + log2f(sum) : -INFINITY;
+            if (n_cl == 1) {
+                reinterpret_cast<float4 *>(out + (row_q0 + h) * D)[f - h * D4] = o_cl;
+                if (lse && f == h * D4) lse[row_q0 + h] = lse_cl * kLn2;
+            } else {
+                const int64_t idx = (rk * n_cl + cl) * total4 + f;
+                reinterpret_cast<float4 *>(ws.o_part)[idx] = o_cl;
+                ws.lse_part[idx] = lse_cl;
+            }
         }
-        cluster_sync();
+        cluster_arrive();  // this CTA's reads of its peers are done
+        if (n_cl > 1) {
+            // -------------------- second level: the last cluster merges the
+            // slice over all clusters, in cluster order
+            __threadfence();
+            __syncthreads();
+            int32_t *ctr = ws.counters + rk * kMaxClusterMerge + rank;
+            if (tid == 0) flags[0] = (atomicAdd(ctr, 1) == n_cl - 1);
+            __syncthreads();
+            if (flags[0]) {
+                __threadfence();
+                const float4 *o2 = reinterpret_cast<const float4 *>(ws.o_part) + rk * n_cl * total4;
+                const float *l2 = ws.lse_part + rk * n_cl * total4;
+                for (int f = lo4 + tid; f < hi4; f += kThreads) {
+                    const int h = f / D4;
+                    float ls[kMaxClusters];
+                    float4 ov[kMaxClusters];
+#pragma unroll
+                    for (int c2 = 0; c2 < kMaxClusters; ++c2) {
+                        if (c2 < n_cl) {
+                            ls[c2] = __ldcg(l2 + (int64_t)c2 * total4 + f);
+                            ov[c2] = __ldcg(o2 + (int64_t)c2 * total4 + f);
+                        }
+                    }
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int c2 = 0; c2 < kMaxClusters; ++c2)
+                        if (c2 < n_cl) M = fmaxf(M, ls[c2]);
+                    float sum = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (M != -INFINITY) {
+#pragma unroll
+                        for (int c2 = 0; c2 < kMaxClusters; ++c2) {
+                            if (c2 < n_cl && ls[c2] != -INFINITY) {
+                                const float w = exp2f(ls[c2] - M);
+                                sum += w;
+                                acc.x += w * ov[c2].x;
+                                acc.y += w * ov[c2].y;
+                                acc.z += w * ov[c2].z;
+                                acc.w += w * ov[c2].w;
+                            }
+                        }
+                    }
+                    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+                    reinterpret_cast<float4 *>(out + (row_q0 + h) * D)[f - h * D4] =
+                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                    if (lse && f == h * D4)
+                        lse[row_q0 + h] = sum > 0.f ? (M + log2f(sum)) * kLn2 : -INFINITY;
+                }
+                if (tid == 0) *ctr = 0;  // ready for the next call
+            }
+        }
+        cluster_wait();  // peers may still read this CTA's shared memory
         return;
     }
 
@@ -459,7 +580,6 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         if (lane == 0 && lse) lse[row_q0 + h] = lse_tot * kLn2;
     }
     __syncthreads();
-    constexpr int D4 = D / 4;
     constexpr int kUnroll = 8;
     for (int e = tid; e < G * D4; e += kThreads) {
         const int h = e / D4, d4 = e - h * D4;
@@ -493,15 +613,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     if (tid == 0) ws.counters[bt * H_kv + g] = 0;  // ready for the next call
 }
 
-// Whether a cluster of `n` CTAs of this kernel can be resident on device
-// `dev` (cached per device and size).
+// How many clusters of `n` CTAs of this kernel can be resident at once on
+// device `dev` (0: none; cached per device and size).
 template <int D>
-bool cluster_merge_ok(int dev, int n) {
-    static int8_t known[64][kMaxClusterMerge + 1] = {};
-    if (n < 2 || n > kMaxClusterMerge || dev < 0 || dev >= 64) return false;
-    if (known[dev][n]) return known[dev][n] > 0;
+int cluster_capacity(int dev, int n) {
+    static int16_t known[64][kMaxClusterMerge + 1] = {};
+    if (n < 2 || n > kMaxClusterMerge || dev < 0 || dev >= 64) return 0;
+    if (known[dev][n]) return known[dev][n] > 0 ? known[dev][n] : 0;
     bool ok = cudaFuncSetAttribute(split_decode_kernel<D>,
-                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+              cudaFuncSetAttribute(split_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   Cfg<D>::kSmemBytes) == cudaSuccess;
+    int clusters = 0;
     if (ok) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)n, 1, 1);
@@ -514,13 +637,18 @@ bool cluster_merge_ok(int dev, int n) {
         attr.val.clusterDim.z = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        int clusters = 0;
         ok = cudaOccupancyMaxActiveClusters(&clusters, split_decode_kernel<D>, &cfg) == cudaSuccess &&
              clusters > 0;
+        if (!ok) clusters = 0;
     }
     cudaGetLastError();  // a refused query is not an error of this call
-    known[dev][n] = ok ? 1 : -1;
-    return ok;
+    known[dev][n] = ok ? (int16_t)(clusters < 32767 ? clusters : 32767) : -1;
+    return ok ? known[dev][n] : 0;
+}
+
+template <int D>
+bool cluster_merge_ok(int dev, int n) {
+    return cluster_capacity<D>(dev, n) > 0;
 }
 
 template <int D>
@@ -543,18 +671,33 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
             return WMTP_ECUDA;
         opted_in[dev] = 1;
     }
-    const bool use_cluster = n_split > 1 && cluster_merge_ok<D>(dev, n_split);
+    // Cluster size: all splits in one cluster, else the largest cluster that
+    // divides n_split into at most kMaxClusters clusters, else none.
+    int csz = 0;
+    if (n_split > 1) {
+        if (n_split <= kMaxClusterMerge && cluster_merge_ok<D>(dev, n_split)) {
+            csz = n_split;
+        } else {
+            for (int c = kMaxClusterMerge; c >= 2; --c) {
+                if (n_split % c == 0 && n_split / c <= kMaxClusters && cluster_merge_ok<D>(dev, c)) {
+                    csz = c;
+                    break;
+                }
+            }
+        }
+    }
     WorkspaceView ws{nullptr, nullptr, nullptr};
-    if (n_split > 1 && !use_cluster) ws = carve(workspace, rows_q, rows_kv, n_split);
+    if (n_split > 1 && csz == 0) ws = carve(workspace, rows_q, rows_kv, n_split);
+    if (csz && n_split / csz > 1) ws = carve_two_level(workspace, rows_q, rows_kv, D, n_split / csz);
     const float scale_log2 = scale * 1.4426950408889634f;
     PdlLaunch launch(dim3((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q)), dim3(kThreads),
                      C::kSmemBytes, stream);
-    if (use_cluster) launch.add_cluster((unsigned)n_split);
+    if (csz) launch.add_cluster((unsigned)csz);
     const cudaError_t err = cudaLaunchKernelEx(
         &launch.cfg, split_decode_kernel<D>, reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q,
         H_kv, H_q / H_kv, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
         reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, table, table_stride, lens,
-        scale_log2, out, lse, ws, n_split, (int32_t)(use_cluster ? 1 : 0));
+        scale_log2, out, lse, ws, n_split, (int32_t)csz);
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
@@ -655,13 +798,33 @@ wmtp_status wmtp_attn_workspace_init(void *workspace, size_t workspace_bytes, vo
 
 int32_t wmtp_attn_num_splits(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_len) {
     int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    bool sms_known = false;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+        sms_known = true;
+    cudaGetLastError();
     const int64_t rows = (int64_t)(B > 0 ? B : 1) * (n_q > 0 ? n_q : 1) * (H_kv > 0 ? H_kv : 1);
     const int64_t tiles = (max_len + kTileKeys - 1) / kTileKeys;
-    int64_t by_sms = sms / rows;                  // one CTA per SM, one wave
-    int64_t by_len = tiles / 4;                   // at least four key tiles per split
-    int64_t n = by_sms < by_len ? by_sms : by_len;
+    const int64_t by_sms = sms / rows;  // one CTA per SM, one wave
+    int64_t n;
+    if (tiles >= 4 * by_sms) {
+        // long rows: fill the SMs; the merge is small next to the copies
+        n = by_sms;
+    } else {
+        // short rows: the launch is latency-bound and the load rate of one
+        // SM is capped, so spread the row over the SMs, two key tiles per
+        // split at least.  Above one cluster, keep to whole clusters of 16
+        // (two-level merge) that are all resident at once.
+        const int64_t half = tiles / 2;
+        n = by_sms < half ? by_sms : half;
+        if (n > kMaxClusterMerge) {
+            int cap = 0;
+            if (sms_known) cap = cluster_capacity<256>(dev, kMaxClusterMerge);
+            n = n / kMaxClusterMerge * kMaxClusterMerge;
+            if (n > kMaxClusterMerge * kMaxClusters) n = kMaxClusterMerge * kMaxClusters;
+            while (n > kMaxClusterMerge && rows * (n / kMaxClusterMerge) > cap) n -= kMaxClusterMerge;
+        }
+    }
     if (n < 1) n = 1;
     if (n > kMaxSplits) n = kMaxSplits;
     return (int32_t)n;

@@ -171,13 +171,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
-// Full cluster barrier (all threads of every CTA in the cluster), with
-// release/acquire ordering of shared-memory writes across the cluster.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem_addr, uint32_t rank) {
     uint32_t r;
@@ -185,10 +178,35 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem_addr, uint32
     return r;
 }
 
+// Full cluster barrier (all threads of every CTA in the cluster), with
+// release/acquire ordering of shared-memory writes across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
     return v;
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
+// Split cluster barrier: arrive (release) now, wait (acquire) later.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // ------------------------------------------------------- tensor-core tiles

@@ -72,6 +72,19 @@ def test_workspace_size(lib):
     assert lib.wmtp_attn_workspace_bytes(-1, 1, 16, 2, 256, 2) == 0
 
 
+def test_split_heuristic_without_a_device(lib):
+    # No device here: the heuristic assumes 152 SMs and no cluster capacity,
+    # so short rows stay within one cluster of 16.
+    ns = lib.wmtp_attn_num_splits
+    assert ns(1, 1, 2, 4096) == 16           # short row: two key tiles per split, one cluster
+    assert ns(1, 1, 2, 1_048_582) == 76      # long row: one CTA per SM
+    assert ns(8, 1, 2, 4096) == 9            # 16 rows fill the SMs at 9 splits each
+    assert ns(1, 1, 2, 1088) == 8            # 17 tiles
+    assert ns(1, 1, 2, 100) == 1
+    assert ns(1, 1, 1, 200 * 64) == 16
+    assert ns(1, 1, 2, 0) == 1
+
+
 NULL = None
 P = ctypes.c_void_p(16)  # never dereferenced: every call below fails validation first
 

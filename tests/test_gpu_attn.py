@@ -50,9 +50,10 @@ def test_attn_sizes_and_splits(D, H_q, H_kv):
         q = synth.normal_bf16((B, 1, H_q, D), seed + L, DEV)
         table = torch.stack([synth.permutation(num_slots, seed + L + b, DEV) for b in range(B)])
         lens = torch.tensor([L, max(L - 7, 0), min(L + 5, num_slots)], dtype=torch.int32, device=DEV)
-        # n_split <= 16 merges through a thread-block cluster, larger counts
-        # through the workspace ticket; both paths are covered
-        for n_split in (1, 2, 3, 7, 16, 20, 37, None):
+        # n_split <= 16 merges through one thread-block cluster; 18, 24, 64
+        # and 128 in two levels (clusters of 9, 12, 16 and 16; 2 to 8
+        # clusters); 37 and 136 through the workspace ticket in split order
+        for n_split in (1, 2, 3, 7, 16, 18, 24, 37, 64, 128, 136, None):
             out, lse, ro, rl = _run_both(q, kp, vp, table, lens, 1 / math.sqrt(D), n_split)
             assert_attn_close(out, lse, ro, rl, what=f"D={D} G={H_q // H_kv} L={L} split={n_split}")
 
@@ -66,7 +67,7 @@ def test_attn_many_query_tokens_and_empty_rows():
     q = synth.normal_bf16((B, n_q, H_q, D), 23, DEV)
     table = torch.stack([synth.permutation(num_slots, 24 + b, DEV) for b in range(B)])
     lens = torch.tensor([0, 700, 1, 333], dtype=torch.int32, device=DEV)
-    for n_split in (1, 4, 11, 17):
+    for n_split in (1, 4, 11, 17, 32, 48):
         out, lse, ro, rl = _run_both(q, kp, vp, table, lens, 0.0625, n_split)
         assert_attn_close(out, lse, ro, rl, what=f"n_q=3 split={n_split}")
         assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
@@ -101,6 +102,11 @@ def test_attn_deterministic_and_split_consistent():
     d2 = wm.draft_decode_attn(q, kp, vp, table, lens, 0.0625, n_split=40)
     assert torch.equal(d1[0], d2[0]) and torch.equal(d1[1], d2[1])
     torch.testing.assert_close(a[0], d1[0], atol=2e-3, rtol=1e-2)
+    # two-level merge: the last cluster merges in cluster order
+    e1 = wm.draft_decode_attn(q, kp, vp, table, lens, 0.0625, n_split=64)
+    e2 = wm.draft_decode_attn(q, kp, vp, table, lens, 0.0625, n_split=64)
+    assert torch.equal(e1[0], e2[0]) and torch.equal(e1[1], e2[1])
+    torch.testing.assert_close(a[0], e1[0], atol=2e-3, rtol=1e-2)
 
 
 def test_attn_tiny_windowed_workload():
