@@ -8,10 +8,10 @@ draft forwards) on seeded synthetic data: K/V ~ N(0,1) with 1% of K rows x4,
 a seeded random permutation as the page table.
 
 One timed step = one decode step's draft-attention phase for both arms:
-  full arm     : full-context index build + 6 x (append_kv + attention over
-                 the whole table, 1,048,577.. keys)
-  windowed arm : sink+window index build + 6 x (append_kv + attention over
-                 64 + 4032 keys)
+  full arm     : full-context index build + 6 x (append + attention over the
+                 whole table, 1,048,577.. keys; one fused launch per step)
+  windowed arm : sink+window index build + 6 x (append + attention over
+                 64 + 4032 keys; one fused launch per step)
 The full arm is launched directly (its attention launches are each bracketed
 by CUDA events for the roofline); the windowed arm, whose kernels take a few
 microseconds, is replayed from a CUDA graph.  L2 is flushed (256 MiB write)
@@ -71,11 +71,13 @@ def bf16_peak():
         return 1900.0
 
 
-def attn_bytes(L, n_q, H_q, H_kv, D):
+def attn_bytes(L, n_q, H_q, H_kv, D, n_new=0):
     """Algorithmic bytes of one attention launch over a table row of L keys:
     K and V rows of every KV head (bf16), the int32 table, q (bf16), out and
-    lse (fp32)."""
-    return L * H_kv * D * 2 * 2 + 4 * L + n_q * H_q * D * 2 + n_q * H_q * (D + 1) * 4
+    lse (fp32); with a fused append of n_new tokens, their K/V rows are read
+    once more and written to the pool."""
+    return (L * H_kv * D * 2 * 2 + 4 * L + n_q * H_q * D * 2 + n_q * H_q * (D + 1) * 4
+            + n_new * H_kv * D * 2 * 2 * 2)
 
 
 def source_hash():
@@ -254,12 +256,12 @@ class Workload:
                                windowed=False, req_to_token=self.rtt, table=self.tab_full,
                                lens=self.len_full)
         for j in range(c["gamma"]):
-            wm.append_kv(self.kn[j], self.vn[j], self.slots[j], self.kp, self.vp)
             if events is not None:
                 events[j][0].record()
-            wm.draft_decode_attn(self.q[j], self.kp, self.vp, self.tab_full[j], self.len_full[j],
-                                 self.scale, out=self.out_full[j], lse=self.lse_full[j],
-                                 n_split=self.ns_full, workspace=self.ws_full)
+            wm.draft_decode_attn_append(self.kn[j], self.vn[j], self.slots[j],
+                                        self.q[j], self.kp, self.vp, self.tab_full[j], self.len_full[j],
+                                        self.scale, out=self.out_full[j], lse=self.lse_full[j],
+                                        n_split=self.ns_full, workspace=self.ws_full)
             if events is not None:
                 events[j][1].record()
 
@@ -270,23 +272,23 @@ class Workload:
                                windowed=True, req_to_token=self.rtt, table=self.tab_win,
                                lens=self.len_win)
         for j in range(c["gamma"]):
-            wm.append_kv(self.kn[j], self.vn[j], self.slots[j], self.kp, self.vp)
             if events is not None:
                 events[j][0].record()
-            wm.draft_decode_attn(self.q[j], self.kp, self.vp, self.tab_win[j], self.len_win[j],
-                                 self.scale, out=self.out_win[j], lse=self.lse_win[j],
-                                 n_split=self.ns_win, workspace=self.ws_win)
+            wm.draft_decode_attn_append(self.kn[j], self.vn[j], self.slots[j],
+                                        self.q[j], self.kp, self.vp, self.tab_win[j], self.len_win[j],
+                                        self.scale, out=self.out_win[j], lse=self.lse_win[j],
+                                        n_split=self.ns_win, workspace=self.ws_win)
             if events is not None:
                 events[j][1].record()
 
     def bytes_full_attn(self, j):
         c = self.cfg
-        return c["B"] * attn_bytes(c["S"] + j + 1, 1, c["H_q"], c["H_kv"], c["D"])
+        return c["B"] * attn_bytes(c["S"] + j + 1, 1, c["H_q"], c["H_kv"], c["D"], n_new=1)
 
     def bytes_win_attn(self, j):
         c = self.cfg
         L = min(c["S"] + j + 1, c["n_sink"] + c["W"])
-        return c["B"] * attn_bytes(L, 1, c["H_q"], c["H_kv"], c["D"])
+        return c["B"] * attn_bytes(L, 1, c["H_q"], c["H_kv"], c["D"], n_new=1)
 
 
 def _external_event():
@@ -383,9 +385,10 @@ def run_ours(args, dist_ctx):
         with torch.cuda.stream(cap_stream):
             with torch.cuda.graph(g2, stream=cap_stream):
                 for j in range(g):
-                    wm.draft_decode_attn(w.q[j], w.kp, w.vp, w.tab_win[j], w.len_win[j], w.scale,
-                                         out=w.out_win[j], lse=w.lse_win[j], n_split=w.ns_win,
-                                         workspace=w.ws_win)
+                    wm.draft_decode_attn_append(w.kn[j], w.vn[j], w.slots[j], w.q[j], w.kp, w.vp,
+                                                w.tab_win[j], w.len_win[j], w.scale,
+                                                out=w.out_win[j], lse=w.lse_win[j], n_split=w.ns_win,
+                                                workspace=w.ws_win)
         stream.wait_stream(cap_stream)
         for k in range(K):
             a, b = ev(), ev()
@@ -430,7 +433,7 @@ def run_ours(args, dist_ctx):
             "H_q": cfg["H_q"], "H_kv": cfg["H_kv"], "D": cfg["D"],
             "l2": "flushed before each arm (256 MiB write, outside the event brackets)",
             "parallelism": "replicas" if dist_ctx.world > 1 else "single GPU",
-            "value_is": "windowed arm: index build + 6 x (append_kv + draft attention), us per decode step",
+            "value_is": "windowed arm: index build + 6 x fused (append_kv + draft attention), us per decode step",
         },
         "arms": {
             "windowed": {
@@ -477,7 +480,7 @@ def run_ours(args, dist_ctx):
             "bytes_per_launch": int(win_bytes / g),
             "traffic": profiled_traffic("windowed_4096") if args.workload == "1m" else None,
         },
-        "gpu_launches": K * 2 * (1 + 2 * g),
+        "gpu_launches": K * 2 * (1 + g),
         "clocks": sampler.summary(),
         "timed_region_s": round(wall_max, 4),
     }

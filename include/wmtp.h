@@ -148,8 +148,10 @@ wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
  * lens[b] and n_split, so results depend on the logical key order and not
  * on the physical slots.  Partials (o, lse) are merged in split order:
  * through distributed shared memory of a thread-block cluster when
- * n_split <= 16, else through the workspace by the last CTA to finish.
- * An empty row gives out = 0, lse = -inf.
+ * n_split <= 16; in two levels (clusters of up to 16, then at most 8
+ * cluster partials per output slice through the workspace) when n_split
+ * splits into such clusters; else through the workspace by the last CTA to
+ * finish.  An empty row gives out = 0, lse = -inf.
  *
  * q        device bf16 [B][n_q][H_q][D], D in {128, 256}, H_q / H_kv <= 8.
  * table    device int32, row b at table + b * table_stride.
@@ -158,14 +160,14 @@ wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
  * lse      device fp32 [B][n_q][H_q] or NULL.
  * k_pool, v_pool 16-byte aligned; q 4-byte aligned.
  * workspace device, >= wmtp_attn_workspace_bytes(...) bytes, 256-byte
- *          aligned.  Its first bytes hold one merge counter per (request,
+ *          aligned.  Its first bytes hold 16 merge counters per (request,
  *          query token, KV head); they must be zero when a call starts.
  *          wmtp_attn_workspace_init() zeroes them, and every completed call
  *          leaves its own counters at zero, so a workspace serves any number
  *          of calls with the same B * n_q * H_kv.  Initialise again before
  *          using it for a larger B * n_q * H_kv.  Calls that share a
  *          workspace must not overlap on the GPU.  Unused when n_split == 1,
- *          and when the splits merge through a thread-block cluster (up to
+ *          and when the splits merge through one thread-block cluster (up to
  *          16 splits, where the device can hold such a cluster).
  * n_split  1 .. 1024; wmtp_attn_num_splits() gives a good value.
  * Errors: WMTP_EINVAL for null pointers, bad sizes, D not 128/256,
@@ -178,8 +180,10 @@ size_t wmtp_attn_workspace_bytes(int32_t B, int32_t n_q, int32_t H_q,
 wmtp_status wmtp_attn_workspace_init(void *workspace, size_t workspace_bytes,
                                      void *stream);
 
-/* Split count for rows of up to max_len keys on the current device: enough
- * CTAs to fill the SMs once, but no split shorter than one key tile. */
+/* Split count for rows of up to max_len keys on the current device.  Long
+ * rows (at least four 64-key tiles per SM-sized split): one CTA per SM.
+ * Short rows: two tiles per split at least, in whole clusters of 16 that
+ * the device holds at once when above 16. */
 int32_t wmtp_attn_num_splits(int32_t B, int32_t n_q, int32_t H_kv,
                              int64_t max_len);
 
@@ -192,6 +196,36 @@ wmtp_status wmtp_draft_decode_attn(const uint16_t *q, int32_t B, int32_t n_q,
                                    float *out, float *lse, void *workspace,
                                    size_t workspace_bytes, int32_t n_split,
                                    void *stream);
+
+/* wmtp_append_kv followed by wmtp_draft_decode_attn, in one launch.  A
+ * draft forward stores its own K/V in the draft KV pool (§4 Mechanism: the
+ * compact ring of n_sink + W + d slots) and attends over the kept
+ * positions, its own included; this is the usual decode order, which the
+ * pages take for granted.  Results (out, lse and the pool contents) are
+ * bit-identical to the two calls in sequence.
+ *
+ * k_new, v_new device bf16 [B][n_new][H_kv][D], 16-byte aligned: the rows
+ *              appended for request b.
+ * new_slots    device int32 [B][n_new]: their pool slots.  A slot appended
+ *              for request b must not appear in another request's table
+ *              row in the same call, and the n_new slots of one request
+ *              must differ.
+ * n_new        1 .. 4.
+ * Other arguments as wmtp_draft_decode_attn; k_pool, v_pool are written.
+ * Keys whose slot is one of request b's new slots are read from k_new /
+ * v_new; a new slot outside the pool is not written, latches
+ * WMTP_DEV_SLOT_RANGE, and its key is masked, as in the two calls. */
+wmtp_status wmtp_draft_decode_attn_append(const uint16_t *k_new,
+                                          const uint16_t *v_new,
+                                          const int32_t *new_slots, int32_t n_new,
+                                          const uint16_t *q, int32_t B, int32_t n_q,
+                                          int32_t H_q, int32_t H_kv, int32_t D,
+                                          uint16_t *k_pool, uint16_t *v_pool,
+                                          int64_t num_slots, const int32_t *table,
+                                          int64_t table_stride, const int32_t *lens,
+                                          float scale, float *out, float *lse,
+                                          void *workspace, size_t workspace_bytes,
+                                          int32_t n_split, void *stream);
 
 /* ------------------------------------------------------------------------
  * Tree-draft attention over the ring.

@@ -12,6 +12,7 @@ Calls (same names as the C ABI without the ``wmtp_`` prefix):
   ring_map             logical position -> ring slot
   append_kv            write draft K/V rows into the pool
   draft_decode_attn    split-KV flash-decode attention with LSE merge
+  draft_decode_attn_append  append_kv + draft_decode_attn in one launch
   tree_draft_attn      tree-draft attention over the ring (tree-causal mask)
 """
 from __future__ import annotations
@@ -26,7 +27,7 @@ from . import _build
 
 __all__ = [
     "WmtpError", "load", "build", "version", "device_error",
-    "build_draft_indices", "ring_map", "append_kv", "draft_decode_attn",
+    "build_draft_indices", "ring_map", "append_kv", "draft_decode_attn", "draft_decode_attn_append",
     "attn_workspace_bytes", "attn_num_splits", "AttnWorkspace", "draft_decode_attn_noalloc",
     "tree_draft_attn", "tree_workspace_bytes", "tree_num_splits",
 ]
@@ -93,6 +94,11 @@ def load():
         lib.wmtp_attn_num_splits.argtypes = [_i32, _i32, _i32, _i64]
         lib.wmtp_draft_decode_attn.restype = _i32
         lib.wmtp_draft_decode_attn.argtypes = [
+            _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, ctypes.c_float,
+            _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
+        lib.wmtp_draft_decode_attn_append.restype = _i32
+        lib.wmtp_draft_decode_attn_append.argtypes = [
+            _vp, _vp, _vp, _i32,
             _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, ctypes.c_float,
             _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
         lib.wmtp_tree_workspace_bytes.restype = ctypes.c_size_t
@@ -281,6 +287,28 @@ def draft_decode_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
     ``n_split`` defaults to ``attn_num_splits`` for ``max_len`` (default: the
     table stride).  Returns ``(out [B, n_q, H_q, D] fp32, lse [B, n_q, H_q] fp32)``.
     """
+    return _attn(None, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_len,
+                 workspace, stream)
+
+
+def draft_decode_attn_append(k_new: torch.Tensor, v_new: torch.Tensor, new_slots: torch.Tensor,
+                             q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                             table: torch.Tensor, lens: torch.Tensor, scale: float,
+                             out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                             n_split: int | None = None, max_len: int | None = None,
+                             workspace: AttnWorkspace | None = None, stream=None):
+    """``append_kv`` then ``draft_decode_attn`` in one launch
+    (``wmtp_draft_decode_attn_append``).
+
+    k_new/v_new: [B, n_new, H_kv, D] bf16 (or [B, H_kv, D] for n_new = 1);
+    new_slots: [B, n_new] (or [B]) int32 pool slots.  Other arguments and the
+    result as :func:`draft_decode_attn`; the pools are written."""
+    return _attn((k_new, v_new, new_slots), q, k_pool, v_pool, table, lens, scale, out, lse,
+                 n_split, max_len, workspace, stream)
+
+
+def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_len, workspace,
+          stream):
     _need(q, "q", torch.bfloat16)
     dev = q.device
     for t, nm in ((k_pool, "k_pool"), (v_pool, "v_pool")):
@@ -315,11 +343,27 @@ def draft_decode_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
         workspace = ws
     elif workspace.nbytes < need:
         raise ValueError(f"workspace holds {workspace.nbytes} bytes, {need} needed")
+    if append is None:
+        with torch.cuda.device(dev):
+            _check(load().wmtp_draft_decode_attn(
+                _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
+                stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf),
+                workspace.nbytes, n_split, _stream(stream)), "draft_decode_attn")
+        return out, lse
+    k_new, v_new, new_slots = append
+    _need(k_new, "k_new", torch.bfloat16, dev)
+    _need(v_new, "v_new", torch.bfloat16, dev)
+    _need(new_slots, "new_slots", torch.int32, dev)
+    n_new = new_slots.numel() // max(B, 1)
+    if (new_slots.numel() != B * n_new or k_new.numel() != B * n_new * H_kv * D
+            or v_new.shape != k_new.shape or k_new.shape[-2:] != (H_kv, D)):
+        raise ValueError("draft_decode_attn_append: k_new/v_new/new_slots shape mismatch")
     with torch.cuda.device(dev):
-        _check(load().wmtp_draft_decode_attn(
+        _check(load().wmtp_draft_decode_attn_append(
+            _ptr(k_new), _ptr(v_new), _ptr(new_slots), n_new,
             _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
             stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf),
-            workspace.nbytes, n_split, _stream(stream)), "draft_decode_attn")
+            workspace.nbytes, n_split, _stream(stream)), "draft_decode_attn_append")
     return out, lse
 
 

@@ -64,6 +64,7 @@ constexpr int kMaxGroup = 8;  // query heads per KV head handled by one CTA
 constexpr int kMaxSplits = 1024;
 constexpr int kMaxClusterMerge = 16;  // splits merged through a cluster (non-portable size)
 constexpr int kMaxClusters = 8;       // clusters merged by the second level
+constexpr int kMaxNew = 4;            // rows one request appends in a fused call (one per warp)
 constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
@@ -117,6 +118,20 @@ inline size_t workspace_bytes(int64_t rows_q, int64_t rows_kv, int D, int n_spli
     return split_order > two_level ? split_order : two_level;
 }
 
+// The step's own K/V rows, appended to the pool by the same launch:
+// k_new / v_new [B][n_new][H_kv][D] bf16, slots [B][n_new].  n_new == 0: no
+// append.  Gathers of a key whose slot is one of its request's appended
+// slots read the new row itself, so no CTA reads a pool slot that this
+// launch writes.
+struct AppendView {
+    const __nv_bfloat16 *k_new;
+    const __nv_bfloat16 *v_new;
+    const int32_t *slots;
+    __nv_bfloat16 *k_pool;
+    __nv_bfloat16 *v_pool;
+    int32_t n_new;
+};
+
 inline WorkspaceView carve(void *ws, int64_t rows_q, int64_t rows_kv, int n_split) {
     uint8_t *p = static_cast<uint8_t *>(ws);
     WorkspaceView v;
@@ -139,13 +154,13 @@ inline WorkspaceView carve_two_level(void *ws, int64_t rows_q, int64_t rows_kv, 
     return v;
 }
 
-template <int D>
+template <int D, bool kAppend>
 __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const __nv_bfloat16 *__restrict__ q, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t G,
     const __nv_bfloat16 *__restrict__ k_pool, const __nv_bfloat16 *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ table, int64_t table_stride,
     const int32_t *__restrict__ lens, float scale_log2, float *__restrict__ out,
-    float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t csz) {
+    float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t csz, AppendView ap) {
     using C = Cfg<D>;
     constexpr int S = C::kStages;
     constexpr int R = C::kRingTiles;
@@ -179,6 +194,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
             qf[kd][1] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c + 8)) : 0u;
         }
     }
+
+    // Slots this request appends in this launch (-1: none).
+    int32_t nslot[kMaxNew];
+#pragma unroll
+    for (int i = 0; i < kMaxNew; ++i)
+        nslot[i] = (kAppend && i < ap.n_new) ? __ldg(ap.slots + b * ap.n_new + i) : -1;
 
     // Chunk of this split: a multiple of the key tile, fixed by L and n_split.
     int64_t L = lens[b];
@@ -215,6 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         }
     };
     // Issue the K/V gathers of tile t (stage t % S); its slots are in the ring.
+    const uint8_t *knew = reinterpret_cast<const uint8_t *>(ap.k_new) +
+                          ((size_t)b * ap.n_new * H_kv + g) * C::kRowBytes;
+    const uint8_t *vnew = reinterpret_cast<const uint8_t *>(ap.v_new) +
+                          ((size_t)b * ap.n_new * H_kv + g) * C::kRowBytes;
     auto issue = [&](int t) {
         const int st = t % S;
         const int32_t my_slot = lane < kKeysPerWarp ? ring[(t % R) * kKeysPerWarp + lane] : 0;
@@ -222,6 +247,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         const bool in = lane < kKeysPerWarp && k < cnt;
         const bool ok = in && my_slot >= 0 && my_slot < num_slots;
         if (in && !ok) latch(WMTP_DEV_SLOT_RANGE);
+        // A key whose slot this launch appends is marked -2 - i (row i of
+        // the new rows); its vm bit stays set.
+        int32_t src_slot = my_slot;
+        if constexpr (kAppend) {
+#pragma unroll
+            for (int i = kMaxNew - 1; i >= 0; --i)
+                if (ok && my_slot == nslot[i]) src_slot = -2 - i;
+        }
         const uint32_t vm = __ballot_sync(0xffffffffu, ok) & 0xffffu;
         if (lane == 0) masks[warp * S + st] = vm;
         const uint32_t kdst = wsm_addr + st * C::kWarpStage;
@@ -233,13 +266,39 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
 #pragma unroll
         for (int r0 = 0; r0 < kKeysPerWarp; r0 += kRowsPerInst) {
             const int key = r0 + sub;
-            const int32_t slot = __shfl_sync(0xffffffffu, my_slot, key);
+            const int32_t slot = __shfl_sync(0xffffffffu, src_slot, key);
             const bool kv = (vm >> key) & 1u;
-            const size_t off = kv ? (size_t)slot * slot_bytes + col : 0;
-            cp_async_16(kdst + key * C::kPitch + col, kbase + off, kv ? 16u : 0u, policy);
-            cp_async_16(vdst + key * C::kPitch + col, vbase + off, kv ? 16u : 0u, policy);
+            const uint8_t *ksrc, *vsrc;
+            if (kAppend && slot < -1) {
+                ksrc = knew + (size_t)(-2 - slot) * slot_bytes + col;
+                vsrc = vnew + (size_t)(-2 - slot) * slot_bytes + col;
+            } else {
+                const size_t off = kv ? (size_t)slot * slot_bytes + col : 0;
+                ksrc = kbase + off;
+                vsrc = vbase + off;
+            }
+            cp_async_16(kdst + key * C::kPitch + col, ksrc, kv ? 16u : 0u, policy);
+            cp_async_16(vdst + key * C::kPitch + col, vsrc, kv ? 16u : 0u, policy);
         }
     };
+
+    // Append: the first split of each (request, KV head) writes the new rows
+    // of head g to the pool (read by later launches only).  Warp i loads row
+    // i into registers here and stores it after the main loop, so the load
+    // latency never sits on its path.
+    constexpr int kNewPerLane = (C::kRowBytes + 32 * 16 - 1) / (32 * 16);  // 16-byte pieces
+    const bool writer = kAppend && split == 0 && (bt % n_q) == 0 && warp < ap.n_new;
+    int4 new_k[kNewPerLane], new_v[kNewPerLane];
+    if (writer) {
+#pragma unroll
+        for (int u = 0; u < kNewPerLane; ++u) {
+            const int off = (u * 32 + lane) * 16;
+            if (off < C::kRowBytes) {
+                new_k[u] = *reinterpret_cast<const int4 *>(knew + (size_t)warp * slot_bytes + off);
+                new_v[u] = *reinterpret_cast<const int4 *>(vnew + (size_t)warp * slot_bytes + off);
+            }
+        }
+    }
 
     // Prologue: slots of the first 2S-1 tiles, then K/V of the first S-1.
     for (int t = 0; t < 2 * S - 1 && t < n_tiles; ++t) fetch_slots(t);
@@ -251,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         if (t < n_tiles) issue(t);
         cp_async_commit();
     }
+
 
     // -------------------------------------------------------------- compute
     float o[KD][4];
@@ -336,6 +396,27 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         __syncwarp();
     }
     cp_async_wait<0>();
+
+    if (writer) {
+        int32_t sl = nslot[0];
+#pragma unroll
+        for (int i = 1; i < kMaxNew; ++i)
+            if (warp == i) sl = nslot[i];
+        if (sl < 0 || sl >= num_slots) {
+            if (lane == 0) latch(WMTP_DEV_SLOT_RANGE);
+        } else {
+            uint8_t *kd = reinterpret_cast<uint8_t *>(ap.k_pool) + (size_t)sl * slot_bytes + (size_t)g * C::kRowBytes;
+            uint8_t *vd = reinterpret_cast<uint8_t *>(ap.v_pool) + (size_t)sl * slot_bytes + (size_t)g * C::kRowBytes;
+#pragma unroll
+            for (int u = 0; u < kNewPerLane; ++u) {
+                const int off = (u * 32 + lane) * 16;
+                if (off < C::kRowBytes) {
+                    *reinterpret_cast<int4 *>(kd + off) = new_k[u];
+                    *reinterpret_cast<int4 *>(vd + off) = new_v[u];
+                }
+            }
+        }
+    }
 
     // Row sums: add the shares of the 8 lanes that hold the same query heads.
 #pragma unroll
@@ -615,15 +696,29 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
 
 // How many clusters of `n` CTAs of this kernel can be resident at once on
 // device `dev` (0: none; cached per device and size).
+// Sets the kernel attributes (large dynamic shared memory, non-portable
+// cluster sizes) once per device for one kernel instance.
+template <int D, bool A>
+bool prepare_kernel(int dev) {
+    static int8_t done[64] = {};
+    if (dev < 0 || dev >= 64) return false;
+    if (done[dev]) return done[dev] > 0;
+    const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<D>::kSmemBytes) == cudaSuccess &&
+                    cudaFuncSetAttribute(split_decode_kernel<D, A>,
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    cudaGetLastError();
+    done[dev] = ok ? 1 : -1;
+    return ok;
+}
+
 template <int D>
 int cluster_capacity(int dev, int n) {
     static int16_t known[64][kMaxClusterMerge + 1] = {};
     if (n < 2 || n > kMaxClusterMerge || dev < 0 || dev >= 64) return 0;
     if (known[dev][n]) return known[dev][n] > 0 ? known[dev][n] : 0;
-    bool ok = cudaFuncSetAttribute(split_decode_kernel<D>,
-                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-              cudaFuncSetAttribute(split_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   Cfg<D>::kSmemBytes) == cudaSuccess;
+    bool ok = prepare_kernel<D, false>(dev);
     int clusters = 0;
     if (ok) {
         cudaLaunchConfig_t cfg = {};
@@ -637,7 +732,7 @@ int cluster_capacity(int dev, int n) {
         attr.val.clusterDim.z = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        ok = cudaOccupancyMaxActiveClusters(&clusters, split_decode_kernel<D>, &cfg) == cudaSuccess &&
+        ok = cudaOccupancyMaxActiveClusters(&clusters, split_decode_kernel<D, false>, &cfg) == cudaSuccess &&
              clusters > 0;
         if (!ok) clusters = 0;
     }
@@ -656,21 +751,17 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
                                 int32_t H_kv, const uint16_t *k_pool, const uint16_t *v_pool,
                                 int64_t num_slots, const int32_t *table, int64_t table_stride,
                                 const int32_t *lens, float scale, float *out, float *lse,
-                                void *workspace, int32_t n_split, cudaStream_t stream) {
+                                void *workspace, int32_t n_split, cudaStream_t stream,
+                                AppendView ap) {
     using C = Cfg<D>;
     const int64_t rows_q = (int64_t)B * n_q * H_q;
     const int64_t rows_kv = (int64_t)B * n_q * H_kv;
-    // Opt in to the large shared-memory carve-out once per device (outside
-    // any later stream capture of the launches).
-    static int opted_in[64] = {0};
+    // Kernel attributes are set once per device (outside any later stream
+    // capture of the launches).
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WMTP_ECUDA;
-    if (!opted_in[dev]) {
-        if (cudaFuncSetAttribute(split_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmemBytes) != cudaSuccess)
-            return WMTP_ECUDA;
-        opted_in[dev] = 1;
-    }
+    const bool append = ap.n_new > 0;
+    if (!(append ? prepare_kernel<D, true>(dev) : prepare_kernel<D, false>(dev))) return WMTP_ECUDA;
     // Cluster size: all splits in one cluster, else the largest cluster that
     // divides n_split into at most kMaxClusters clusters, else none.
     int csz = 0;
@@ -694,10 +785,10 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
                      C::kSmemBytes, stream);
     if (csz) launch.add_cluster((unsigned)csz);
     const cudaError_t err = cudaLaunchKernelEx(
-        &launch.cfg, split_decode_kernel<D>, reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q,
-        H_kv, H_q / H_kv, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
-        reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, table, table_stride, lens,
-        scale_log2, out, lse, ws, n_split, (int32_t)csz);
+        &launch.cfg, append ? split_decode_kernel<D, true> : split_decode_kernel<D, false>,
+        reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q, H_kv, H_q / H_kv,
+        reinterpret_cast<const __nv_bfloat16 *>(k_pool), reinterpret_cast<const __nv_bfloat16 *>(v_pool),
+        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, ap);
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
@@ -753,17 +844,15 @@ wmtp_status launch_split_decode_noalloc(const uint16_t *q, int32_t B, int32_t n_
         if (cudaMemsetAsync(ws.counters, 0, (size_t)rows_kv * 4, stream) != cudaSuccess)
             return WMTP_ECUDA;
     }
-    if (cudaFuncSetAttribute(split_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
-        return WMTP_ECUDA;
+    if (!prepare_kernel<D, false>(dev)) return WMTP_ECUDA;
     const float scale_log2 = scale * 1.4426950408889634f;
     PdlLaunch launch(dim3((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q)), dim3(kThreads),
                      C::kSmemBytes, stream);
     const cudaError_t err = cudaLaunchKernelEx(
-        &launch.cfg, split_decode_kernel<D>, reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q,
+        &launch.cfg, split_decode_kernel<D, false>, reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q,
         H_kv, H_q / H_kv, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
         reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, table, table_stride, lens,
-        scale_log2, out, lse, ws, n_split, (int32_t)0);
+        scale_log2, out, lse, ws, n_split, (int32_t)0, AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0});
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
@@ -830,23 +919,32 @@ int32_t wmtp_attn_num_splits(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_l
     return (int32_t)n;
 }
 
-wmtp_status wmtp_draft_decode_attn(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
-                                   int32_t H_kv, int32_t D, const uint16_t *k_pool,
-                                   const uint16_t *v_pool, int64_t num_slots,
-                                   const int32_t *table, int64_t table_stride,
-                                   const int32_t *lens, float scale, float *out, float *lse,
-                                   void *workspace, size_t workspace_bytes_, int32_t n_split,
-                                   void *stream) {
+}  // extern "C"
+
+namespace wmtp {
+namespace {
+
+wmtp_status draft_decode_attn_checked(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
+                                      int32_t H_kv, int32_t D, const uint16_t *k_pool,
+                                      const uint16_t *v_pool, int64_t num_slots,
+                                      const int32_t *table, int64_t table_stride,
+                                      const int32_t *lens, float scale, float *out, float *lse,
+                                      void *workspace, size_t workspace_bytes_, int32_t n_split,
+                                      void *stream, AppendView ap) {
     if (B < 0 || n_q < 0 || H_q < 1 || H_kv < 1 || (H_q % H_kv) != 0) return WMTP_EINVAL;
     if (H_q / H_kv > kMaxGroup) return WMTP_EINVAL;
     if (D != 128 && D != 256) return WMTP_EINVAL;
     if (n_split < 1 || n_split > kMaxSplits || table_stride < 1 || num_slots < 0)
         return WMTP_EINVAL;
     if ((int64_t)B * n_q > 65535 || H_kv > 65535) return WMTP_EINVAL;
+    if (ap.n_new < 0 || ap.n_new > kMaxNew) return WMTP_EINVAL;
     if (B == 0 || n_q == 0) return WMTP_OK;
     if (!q || !k_pool || !v_pool || !table || !lens || !out) return WMTP_EINVAL;
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(q) & 3u))
+        return WMTP_EINVAL;
+    if (ap.n_new > 0 && (!ap.k_new || !ap.v_new || !ap.slots || !aligned16(ap.k_new) ||
+                         !aligned16(ap.v_new)))
         return WMTP_EINVAL;
     if (n_split > 1) {
         if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return WMTP_EINVAL;
@@ -856,9 +954,46 @@ wmtp_status wmtp_draft_decode_attn(const uint16_t *q, int32_t B, int32_t n_q, in
     cudaStream_t s = as_stream(stream);
     if (D == 256)
         return launch_split_decode<256>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
-                                        table_stride, lens, scale, out, lse, workspace, n_split, s);
+                                        table_stride, lens, scale, out, lse, workspace, n_split, s, ap);
     return launch_split_decode<128>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
-                                    table_stride, lens, scale, out, lse, workspace, n_split, s);
+                                    table_stride, lens, scale, out, lse, workspace, n_split, s, ap);
+}
+
+}  // namespace
+}  // namespace wmtp
+
+extern "C" {
+
+wmtp_status wmtp_draft_decode_attn(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
+                                   int32_t H_kv, int32_t D, const uint16_t *k_pool,
+                                   const uint16_t *v_pool, int64_t num_slots,
+                                   const int32_t *table, int64_t table_stride,
+                                   const int32_t *lens, float scale, float *out, float *lse,
+                                   void *workspace, size_t workspace_bytes_, int32_t n_split,
+                                   void *stream) {
+    return draft_decode_attn_checked(q, B, n_q, H_q, H_kv, D, k_pool, v_pool, num_slots, table,
+                                     table_stride, lens, scale, out, lse, workspace,
+                                     workspace_bytes_, n_split, stream,
+                                     AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0});
+}
+
+wmtp_status wmtp_draft_decode_attn_append(const uint16_t *k_new, const uint16_t *v_new,
+                                          const int32_t *new_slots, int32_t n_new,
+                                          const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
+                                          int32_t H_kv, int32_t D, uint16_t *k_pool,
+                                          uint16_t *v_pool, int64_t num_slots,
+                                          const int32_t *table, int64_t table_stride,
+                                          const int32_t *lens, float scale, float *out,
+                                          float *lse, void *workspace, size_t workspace_bytes_,
+                                          int32_t n_split, void *stream) {
+    if (n_new < 1) return WMTP_EINVAL;
+    const AppendView ap{reinterpret_cast<const __nv_bfloat16 *>(k_new),
+                        reinterpret_cast<const __nv_bfloat16 *>(v_new), new_slots,
+                        reinterpret_cast<__nv_bfloat16 *>(k_pool),
+                        reinterpret_cast<__nv_bfloat16 *>(v_pool), n_new};
+    return draft_decode_attn_checked(q, B, n_q, H_q, H_kv, D, k_pool, v_pool, num_slots, table,
+                                     table_stride, lens, scale, out, lse, workspace,
+                                     workspace_bytes_, n_split, stream, ap);
 }
 
 wmtp_status wmtp_draft_decode_attn_noalloc(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,

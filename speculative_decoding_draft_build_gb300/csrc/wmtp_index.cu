@@ -160,9 +160,10 @@ wmtp_status wmtp_build_draft_indices(const int32_t *seq_lens, int32_t B, int32_t
     if (!seq_lens || !table || !lens) return WMTP_EINVAL;
     if (!req_to_token && !ring_base) return WMTP_EINVAL;
     if (req_to_token && rtt_stride < 1) return WMTP_EINVAL;
+    // One entry per thread (each is one dependent global load), up to 8192
+    // CTAs per row.
     constexpr int kThreads = 256;
-    constexpr int64_t kPerCta = kThreads * 4;
-    int64_t gx = (stride + kPerCta - 1) / kPerCta;
+    int64_t gx = (stride + kThreads - 1) / kThreads;
     if (gx > 8192) gx = 8192;
     PdlLaunch L(dim3((unsigned)gx, (unsigned)(gamma * B)), dim3(kThreads), 0, as_stream(stream));
     return cudaLaunchKernelEx(&L.cfg, build_indices_kernel, seq_lens, B, n_sink, window, depth,
