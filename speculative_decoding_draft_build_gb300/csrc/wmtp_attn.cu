@@ -202,19 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         nslot[i] = (kAppend && i < ap.n_new) ? __ldg(ap.slots + b * ap.n_new + i) : -1;
 
     // Chunk of this split: a multiple of the key tile, fixed by L and n_split.
-    int64_t L = lens[b];
-    if (L < 0 || L > table_stride) {
-        if (threadIdx.x == 0 && split == 0 && g == 0) latch(WMTP_DEV_LEN_RANGE);
-        L = L < 0 ? 0 : table_stride;
-    }
-    int64_t chunk = (L + n_split - 1) / n_split;
-    chunk = (chunk + kTileKeys - 1) / kTileKeys * kTileKeys;
-    const int64_t start = (int64_t)split * chunk;
-    const int64_t cnt = L - start < 0 ? 0 : (L - start < chunk ? L - start : chunk);
-    const int n_tiles = (int)((cnt + kTileKeys - 1) / kTileKeys);
-
-    // ------------------------------------------------ per-warp copy pipeline
-    const int32_t *__restrict__ trow = table + b * table_stride + start;
+    // The slot fetch starts for the chunk of a full row (L = table_stride)
+    // while the length is still loading, and is redone only if the real
+    // chunk differs.
+    const int32_t L_in = lens[b];
+    auto chunk_of = [&](int64_t len) {
+        const int64_t ch = (len + n_split - 1) / n_split;
+        return (ch + kTileKeys - 1) / kTileKeys * kTileKeys;
+    };
     const uint64_t policy = l2_policy_evict_first();
     const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * C::kRowBytes;
     const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * C::kRowBytes;
@@ -226,15 +221,40 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     // rows, so issuing a tile's gathers never waits on a global load.
     const int32_t *ring = reinterpret_cast<const int32_t *>(smem + C::kRingOffset) + warp * R * kKeysPerWarp;
     const uint32_t ring_addr = smem_addr(ring);
-    auto fetch_slots = [&](int t) {
+    auto fetch_slots_from = [&](int t, const int32_t *row, int64_t n) {
         if (lane < kKeysPerWarp) {
             const int64_t k = (int64_t)t * kTileKeys + warp * kKeysPerWarp + lane;
-            const bool in = k < cnt;
+            const bool in = k < n;
             cp_async_4(ring_addr + ((t % R) * kKeysPerWarp + lane) * 4,
-                       in ? static_cast<const void *>(trow + k) : static_cast<const void *>(table),
+                       in ? static_cast<const void *>(row + k) : static_cast<const void *>(table),
                        in ? 4u : 0u);
         }
     };
+    const int64_t chunk_g = chunk_of(table_stride);
+    const int64_t start_g = (int64_t)split * chunk_g;
+    const int64_t cnt_g = table_stride - start_g < 0 ? 0 : (table_stride - start_g < chunk_g ? table_stride - start_g : chunk_g);
+    const int n_tiles_g = (int)((cnt_g + kTileKeys - 1) / kTileKeys);
+    for (int t = 0; t < 2 * S - 1 && t < n_tiles_g; ++t) fetch_slots_from(t, table + b * table_stride + start_g, cnt_g);
+    cp_async_commit();
+
+    int64_t L = L_in;
+    if (L < 0 || L > table_stride) {
+        if (threadIdx.x == 0 && split == 0 && g == 0) latch(WMTP_DEV_LEN_RANGE);
+        L = L < 0 ? 0 : table_stride;
+    }
+    const int64_t chunk = chunk_of(L);
+    const int64_t start = (int64_t)split * chunk;
+    const int64_t cnt = L - start < 0 ? 0 : (L - start < chunk ? L - start : chunk);
+    const int n_tiles = (int)((cnt + kTileKeys - 1) / kTileKeys);
+    const int32_t *__restrict__ trow = table + b * table_stride + start;
+    auto fetch_slots = [&](int t) { fetch_slots_from(t, trow, cnt); };
+    if (chunk != chunk_g) {  // a shorter row: fetch its own chunk
+        cp_async_wait<0>();
+        __syncwarp();
+        for (int t = 0; t < 2 * S - 1 && t < n_tiles; ++t) fetch_slots(t);
+        cp_async_commit();
+    }
+
     // Issue the K/V gathers of tile t (stage t % S); its slots are in the ring.
     const uint8_t *knew = reinterpret_cast<const uint8_t *>(ap.k_new) +
                           ((size_t)b * ap.n_new * H_kv + g) * C::kRowBytes;
@@ -300,9 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         }
     }
 
-    // Prologue: slots of the first 2S-1 tiles, then K/V of the first S-1.
-    for (int t = 0; t < 2 * S - 1 && t < n_tiles; ++t) fetch_slots(t);
-    cp_async_commit();
+    // Prologue: slots of the first 2S-1 tiles (fetched above), then K/V of
+    // the first S-1.
     cp_async_wait<0>();
     __syncwarp();
 #pragma unroll
