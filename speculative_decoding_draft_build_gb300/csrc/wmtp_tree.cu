@@ -60,6 +60,7 @@ constexpr int kLoadThreads = kLoadWarps * 32;
 constexpr int kMmaWarp = kSoftWarps + kLoadWarps;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr int kMaxSplits = 64;
+constexpr int kMaxClusterSplits = 8;  // key chunks merged through one (portable) cluster
 constexpr float kLazyRescale = 8.f;  // log2 of the growth tolerated before rescaling O
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -94,6 +95,8 @@ struct Cfg {
     static constexpr int kTmemCols = (kOCol + D <= 256) ? 256 : 512;
     static_assert(kRows * kMaxSplits * 4 <= kKvStages * kStageBytes, "merge weights must fit");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kRows * D * 4 <= kKvStages * kStageBytes, "cluster-merge partial must fit the K/V stages");
+    static_assert(kRows * 4 <= 2 * kPBufBytes, "cluster-merge lse must fit the P buffers");
 };
 
 struct TreeWs {
@@ -148,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     const __nv_bfloat16 *__restrict__ k_pool, const __nv_bfloat16 *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ ring_base,
     int32_t n_sink, int32_t window, int32_t depth, int32_t tree_k, float scale_log2,
-    float *__restrict__ out, float *__restrict__ lse, TreeWs ws, int32_t n_split, int32_t n_rb) {
+    float *__restrict__ out, float *__restrict__ lse, TreeWs ws, int32_t n_split, int32_t n_rb,
+    int32_t cluster_merge) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
@@ -431,7 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         const float inv = (have_o && l > 0.f) ? 1.f / l : 0.f;
         const float lse2 = (have_o && l > 0.f) ? m_ref + log2f(l) : -INFINITY;
         float *dst = nullptr;
-        if (row_live) {
+        // Cluster merge: this CTA's normalised partial O goes to its own
+        // shared memory (the K/V stages, idle now), row-major with the
+        // float4 index of row i XOR-swizzled by i % 8; its lse to the P area.
+        float *po = reinterpret_cast<float *>(smem + C::kKvOff);
+        if (cluster_merge) {
+            reinterpret_cast<float *>(smem + C::kPOff)[i] = (row_live && !flags[0]) ? lse2 : -INFINITY;
+        } else if (row_live) {
             if (n_split == 1) {
                 const int64_t orow = (b * n_nodes + node) * H_q + h;
                 dst = out + orow * D;
@@ -446,7 +456,18 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t r[32];
             if (have_o) tc_ld32(lane_base + C::kOCol + c0, r);  // warp-uniform
-            if (row_live) {
+            if (cluster_merge) {
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    float4 v;
+                    v.x = have_o ? __uint_as_float(r[k]) * inv : 0.f;
+                    v.y = have_o ? __uint_as_float(r[k + 1]) * inv : 0.f;
+                    v.z = have_o ? __uint_as_float(r[k + 2]) * inv : 0.f;
+                    v.w = have_o ? __uint_as_float(r[k + 3]) * inv : 0.f;
+                    const int d4 = (c0 + k) / 4;
+                    reinterpret_cast<float4 *>(po + i * D)[d4 ^ (i & 7)] = v;
+                }
+            } else if (row_live) {
 #pragma unroll
                 for (int k = 0; k < 32; k += 4) {
                     float4 v;
@@ -469,6 +490,73 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     }
     if (n_split == 1) return;
 
+    const int row0 = rb * kRows;
+    const int n_rows = R - row0 < kRows ? R - row0 : kRows;
+    constexpr int D4 = D / 4;
+    if (cluster_merge) {
+        // ------------------------------- merge through distributed smem
+        // The n_split CTAs of this (request, KV head, row block) form one
+        // cluster; CTA `rank` merges a slice of the rows, reading every
+        // peer's partial in split order.  The closing barrier keeps each
+        // CTA's shared memory alive until its peers have read it.
+        __syncwarp();
+        cluster_sync();
+        const int rank = (int)cluster_ctarank();
+        const int per = (n_rows + n_split - 1) / n_split;
+        const int r_lo = rank * per;
+        const int r_hi = r_lo + per < n_rows ? r_lo + per : n_rows;
+        const uint32_t po_addr = smem_addr(smem + C::kKvOff);
+        const uint32_t pl_addr = smem_addr(smem + C::kPOff);
+        float *wts = reinterpret_cast<float *>(smem + C::kQOff);  // [per][n_split] merge weights
+        for (int i = r_lo + tid; i < r_hi; i += kThreads) {
+            float ls[kMaxClusterSplits];
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+                ls[s2] = s2 < n_split ? ld_dsmem_f32(map_to_rank(pl_addr + i * 4, s2)) : -INFINITY;
+            float M = -INFINITY;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) M = fmaxf(M, ls[s2]);
+            float sum = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+                    sum += ls[s2] == -INFINITY ? 0.f : exp2f(ls[s2] - M);
+            }
+            const float lt = sum > 0.f ? M + log2f(sum) : -INFINITY;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+                if (s2 < n_split) wts[(i - r_lo) * n_split + s2] = (sum > 0.f && ls[s2] != -INFINITY) ? exp2f(ls[s2] - lt) : 0.f;
+            const int rq = row0 + i;
+            if (lse) lse[(b * n_nodes + rq / G) * H_q + g * G + rq % G] = lt * kLn2;
+        }
+        __syncthreads();
+        for (int e = tid; e < (r_hi - r_lo) * D4; e += kThreads) {
+            const int i = r_lo + e / D4, d4 = e - (e / D4) * D4;
+            const float *w = wts + (i - r_lo) * n_split;
+            const uint32_t off = (uint32_t)(i * D4 + (d4 ^ (i & 7))) * 16;
+            float4 v[kMaxClusterSplits];
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+                if (s2 < n_split) v[s2] = ld_dsmem_f32x4(map_to_rank(po_addr + off, s2));
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+                if (s2 < n_split) {
+                    acc.x += w[s2] * v[s2].x;
+                    acc.y += w[s2] * v[s2].y;
+                    acc.z += w[s2] * v[s2].z;
+                    acc.w += w[s2] * v[s2].w;
+                }
+            }
+            const int rq = row0 + i;
+            reinterpret_cast<float4 *>(out + ((b * n_nodes + rq / G) * H_q + g * G + rq % G) * D)[d4] = acc;
+        }
+        __syncwarp();
+        cluster_arrive();
+        cluster_wait();
+        return;
+    }
+
     // ------------------------------------------ ticket; the last CTA merges
     __threadfence();
     __syncthreads();
@@ -480,8 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     __syncthreads();
     if (!flags[1]) return;
     __threadfence();
-    const int row0 = rb * kRows;
-    const int n_rows = R - row0 < kRows ? R - row0 : kRows;
     float *wts = reinterpret_cast<float *>(smem + C::kKvOff);  // [rows][n_split]
     const int64_t prow0 = (b * H_kv + g) * R + row0;
     for (int e = tid; e < n_rows * n_split; e += kThreads) wts[e] = __ldcg(ws.lse_part + prow0 * n_split + e);
@@ -500,7 +586,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         if (lse) lse[(b * n_nodes + rq / G) * H_q + g * G + rq % G] = lt * kLn2;
     }
     __syncthreads();
-    constexpr int D4 = D / 4;
     for (int e = tid; e < n_rows * D4; e += kThreads) {
         const int i = e / D4, d4 = e - i * D4;
         const float *w = wts + i * n_split;
@@ -517,6 +602,32 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         reinterpret_cast<float4 *>(out + ((b * n_nodes + rq / G) * H_q + g * G + rq % G) * D)[d4] = acc;
     }
     if (tid == 0) ws.counters[cidx] = 0;
+}
+
+// Whether clusters of n CTAs of the tree kernel can be resident on device
+// dev (cached per device and size).
+template <int D>
+bool tree_cluster_ok(int dev, int n) {
+    static int8_t known[64][kMaxClusterSplits + 1] = {};
+    if (n < 2 || n > kMaxClusterSplits || dev < 0 || dev >= 64) return false;
+    if (known[dev][n]) return known[dev][n] > 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)n;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    const bool ok = cudaOccupancyMaxActiveClusters(&clusters, tree_tc_kernel<D>, &cfg) == cudaSuccess &&
+                    clusters > 0;
+    cudaGetLastError();  // a refused query is not an error of this call
+    known[dev][n] = ok ? 1 : -1;
+    return ok;
 }
 
 template <int D>
@@ -539,8 +650,9 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
             return WMTP_ECUDA;
         opted_in[dev] = 1;
     }
+    const bool use_cluster = n_split > 1 && tree_cluster_ok<D>(dev, n_split);
     TreeWs ws{nullptr, nullptr, nullptr};
-    if (n_split > 1) {
+    if (n_split > 1 && !use_cluster) {
         uint8_t *p = static_cast<uint8_t *>(workspace);
         ws.counters = reinterpret_cast<int32_t *>(p);
         p += align256((size_t)B * H_kv * n_rb * 4);
@@ -550,11 +662,13 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
     }
     PdlLaunch launch(dim3((unsigned)n_split, (unsigned)(H_kv * n_rb), (unsigned)B), dim3(kThreads),
                      C::kSmemBytes, stream);
+    if (use_cluster) launch.add_cluster((unsigned)n_split);
     const cudaError_t err = cudaLaunchKernelEx(
         &launch.cfg, tree_tc_kernel<D>, reinterpret_cast<const __nv_bfloat16 *>(q), H_q, H_kv, G,
         n_nodes, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
         reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, seq_lens, ring_base, n_sink,
-        window, depth, tree_k, scale * 1.4426950408889634f, out, lse, ws, n_split, n_rb);
+        window, depth, tree_k, scale * 1.4426950408889634f, out, lse, ws, n_split, n_rb,
+        (int32_t)(use_cluster ? 1 : 0));
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
