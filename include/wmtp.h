@@ -249,7 +249,9 @@ wmtp_status wmtp_draft_decode_attn_append(const uint16_t *k_new,
  * workspace >= wmtp_tree_workspace_bytes(...), 256-byte aligned; its merge
  *           counters must be zero at the first call (wmtp_attn_workspace_init
  *           zeroes a whole workspace) and every completed call leaves them
- *           zero.  Unused when n_split == 1.
+ *           zero.  Unused when n_split == 1, and when the key chunks merge
+ *           through a thread-block cluster (n_split <= 8, where the device
+ *           holds such clusters).
  * n_split   1 .. 64 key chunks per request; wmtp_tree_num_splits() gives one.
  * Errors: WMTP_EINVAL for null or misaligned pointers, bad sizes, D not
  * 128/256, H_q % H_kv != 0, W < 1, d < 1, k < 1; WMTP_ECAPACITY for a small
