@@ -509,7 +509,7 @@ def measure_tree(args, dev):
     peak_tf = bf16_peak()
     res = {}
     reps = max(5, min(args.steps, 30))
-    for W in (1024, 2048, 4096, 8192):
+    for W in (args.tree_w or (1024, 2048, 4096, 8192)):
         R = n_sink + W + d * k
         rb = torch.tensor(synth.ring_bases(B, R, B + 2, 5000 + W), dtype=torch.int32, device=dev)
         kp = synth.normal_bf16(((B + 2) * R, H_kv, D), 5001 + W, dev)
@@ -702,6 +702,10 @@ def main(argv=None):
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="1m")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-tree", action="store_true", help="skip the tree-drafter measurement")
+    p.add_argument("--tree-only", action="store_true",
+                   help="run only the tree-drafter measurement (a profiling driver; prints the tree object)")
+    p.add_argument("--tree-w", type=int, action="append",
+                   help="window(s) for the tree measurement (default 1024, 2048, 4096, 8192)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -711,6 +715,13 @@ def main(argv=None):
             if dist_ctx.rank != 0:
                 return 0
             res = run_reference(args, dist_ctx)
+        elif args.tree_only:
+            import speculative_decoding_draft_build_gb300 as wm
+            wm.build()
+            wm.load()
+            dev = torch.device("cuda", dist_ctx.local)
+            torch.cuda.set_device(dev)
+            res = {"tree": measure_tree(args, dev)}
         else:
             res = run_ours(args, dist_ctx)
         if dist_ctx.rank == 0:
