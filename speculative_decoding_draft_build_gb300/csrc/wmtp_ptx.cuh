@@ -133,6 +133,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// 3-D tiled TMA load (cp.async.bulk.tensor) of the box at coordinates
+// (x, y, z) of tensor map `map` (a __grid_constant__ kernel parameter) into
+// this CTA's shared memory at dst, completing its bytes on mbarrier bar.
+// x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 // 16-byte global->shared copy through L2 only (cp.async.cg); src_bytes = 0
 // writes zeros without reading global memory.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes,

@@ -27,6 +27,18 @@ __device__ __forceinline__ uint64_t tc_smem_desc(uint32_t smem_addr, uint32_t lb
     return d;
 }
 
+// Descriptor of an operand in the 128-byte-swizzled canonical layout
+// (swizzle mode 2 in bits 61-63): 8-row atoms of 128-byte rows, 1024-byte
+// aligned, whose 16-byte chunks are XORed with the row within the atom (the
+// layout a 128-byte-swizzle TMA box writes).  K-major: SBO = stride between
+// 8-row atoms, steps along K inside an atom advance the start address by
+// 32 bytes per 16 elements; MN-major: LBO = stride between 64-element blocks
+// along M/N, SBO = stride between 8-row atoms along K.  Checked on the device
+// against exact integer products before use.
+__device__ __forceinline__ uint64_t tc_smem_desc_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+    return tc_smem_desc(smem_addr, lbo, sbo) | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B, fp32 D.
 // b_mn_major: B stored N-contiguous (transposed).
 __host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N, int b_mn_major) {

@@ -23,16 +23,20 @@
 //              accumulator is rescaled in tensor memory only when the max
 //              grows by more than 2^8), writes P as bf16 head + tail into
 //              shared memory, and at the end reads its row of O.
-//   warps 4-5  gather: slots from the ring rule (no table), 16-byte cp.async
-//              of each key's K and V rows into the no-swizzle core-matrix
-//              layouts the MMA reads (K K-major, V MN-major), two stages.
-//   warp 6     one thread issues the MMAs: S(t) = Q K(t)^T (M=128, N=64,
+//   warp 4     gather: slots from the ring rule (no table); 32-key tiles
+//              of consecutive ring slots arrive as TMA boxes (64 dims x 1
+//              head x 32 or 8 slots, 128-byte swizzle), other keys through
+//              16-byte cp.async into the same swizzled layout; four stages.
+//   warp 5     one thread issues the MMAs: S(t) = Q K(t)^T (M=128, N=32,
 //              K=D) into one of two S buffers, then O += P_hi V + P_lo V
-//              (M=128, N=D, K=64); completion is signalled through mbarriers
-//              with tcgen05.commit.
-// Key chunks are split over CTAs; the last CTA of a (request, KV head, row
-// block) merges the partials from the workspace in split order.  Every wait
-// has a time limit; tensor memory is always released.
+//              (M=128, N=D, K=32); completion is signalled through mbarriers
+//              with tcgen05.commit.  Q and P are no-swizzle K-major; K is
+//              K-major and V MN-major, both 128-byte swizzled.
+// Key chunks are split over CTAs; up to 8 chunks of a (request, KV head,
+// row block) run as one cluster and merge through distributed shared memory,
+// more through the workspace (the last CTA merges in split order).  Every
+// wait has a time limit; tensor memory is always released.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -55,7 +59,7 @@ constexpr int kRows = 128;  // query rows per CTA (MMA M)
 constexpr int kKeys = 32;   // keys per tile (N of QK^T, K of PV)
 constexpr int kKvStages = 4;
 constexpr int kSoftWarps = 4;
-constexpr int kLoadWarps = 2;
+constexpr int kLoadWarps = 1;
 constexpr int kLoadThreads = kLoadWarps * 32;
 constexpr int kMmaWarp = kSoftWarps + kLoadWarps;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
@@ -90,7 +94,9 @@ struct Cfg {
     static constexpr int kKvOff = kQBytes;
     static constexpr int kPOff = kKvOff + kKvStages * kStageBytes;
     static constexpr int kBarOff = kPOff + 2 * kPBufBytes;
-    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16;
+    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
+    static constexpr int kDimBlocks = D / 64;                 // 128-byte swizzle atoms per K/V row
+    static constexpr int kBlockBytes = kKeys * 128;           // one 64-dim block of a tile
     static constexpr int kOCol = 2 * kKeys;                  // O after the two S buffers
     static constexpr int kTmemCols = (kOCol + D <= 256) ? 256 : 512;
     static_assert(kRows * kMaxSplits * 4 <= kKvStages * kStageBytes, "merge weights must fit");
@@ -152,9 +158,12 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     int64_t num_slots, const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ ring_base,
     int32_t n_sink, int32_t window, int32_t depth, int32_t tree_k, float scale_log2,
     float *__restrict__ out, float *__restrict__ lse, TreeWs ws, int32_t n_split, int32_t n_rb,
-    int32_t cluster_merge) {
+    int32_t cluster_merge, const __grid_constant__ CUtensorMap tm_k32, const __grid_constant__ CUtensorMap tm_v32,
+    const __grid_constant__ CUtensorMap tm_k8, const __grid_constant__ CUtensorMap tm_v8) {
     using C = Cfg<D>;
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 128-byte-swizzled K/V tiles need 1024-byte aligned atoms
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);  // [0] abort [1] ticket
@@ -184,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
 
     if (tid == 0) {
         for (int i = 0; i < kKvStages; ++i) {
-            mbar_init(smem_addr(&bars[kKvFull + i]), kLoadThreads);
+            mbar_init(smem_addr(&bars[kKvFull + i]), kLoadThreads + 1);  // + the TMA byte count
             mbar_init(smem_addr(&bars[kKvEmpty + i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -222,50 +231,94 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
 
     if (warp >= kSoftWarps && warp < kMmaWarp) {
         // ----------------------------------------------------------- gather
-        // Each loader warp owns 16 keys of every 32-key tile; every loader
-        // thread arrives on the stage's barrier when its copies land, so up
-        // to four tiles are in flight.
-        const int lw = warp - kSoftWarps;
+        // One warp: lane k holds the slot of key k of the tile.  A tile whose
+        // 32 keys sit in consecutive pool slots comes in as one TMA box per
+        // 64-dim block of K and of V; otherwise each such 8-key group does,
+        // and the remaining keys (ring wrap, segment edges, the tail, bad
+        // slots) are copied or zero-filled with cp.async.  Both land in the
+        // 128-byte-swizzled K-major layout the MMAs read; the stage barrier
+        // counts the 32 cp.async arrivals and one byte-count arrival for the
+        // TMA boxes.
         const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * D * 2;
         const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * D * 2;
         const size_t slot_bytes = (size_t)H_kv * D * 2;
-        constexpr int kKeysPerWarp = kKeys / kLoadWarps;                  // 16
-        constexpr int kLanesPerRow = C::kChunks < 32 ? C::kChunks : 32;   // 16 (D=128) or 32
-        constexpr int kRowsPerInst = 32 / kLanesPerRow;
-        const int sub = lane / kLanesPerRow, col = lane % kLanesPerRow;
         for (int t = 0; t < n_tiles; ++t) {
             const int st = t % kKvStages;
             if (t >= kKvStages &&
                 !mbar_wait(&bars[kKvEmpty + st], ((t / kKvStages) - 1) & 1, flags))
                 break;
             if (flags[0]) break;
-            // lanes 0-15 hold the slots of this warp's 16 keys
-            const int key = lw * kKeysPerWarp + (lane & (kKeysPerWarp - 1));
-            const int64_t kk = (int64_t)t * kKeys + key;
+            const int64_t kk = (int64_t)t * kKeys + lane;
             int64_t slot = 0;
             bool ok = false;
-            if (lane < kKeysPerWarp && kk < cnt) {
+            if (kk < cnt) {
                 const int2 inf = key_info(geo, start + kk, depth);
                 const int br = inf.y < 0 ? 0 : (inf.y >> 8);
                 slot = ring_slot(base, inf.x, br, n_sink, window, depth, tree_k);
                 ok = slot >= 0 && slot < num_slots;
                 if (!ok) latch(WMTP_DEV_SLOT_RANGE);
             }
+            // contiguity: key k continues key k-1's slot
+            const int64_t prev = __shfl_up_sync(0xffffffffu, slot, 1);
+            const bool cont = ok && (lane == 0 || slot == prev + 1);
+            const uint32_t contm = __ballot_sync(0xffffffffu, cont);
             const uint32_t okm = __ballot_sync(0xffffffffu, ok);
+            const int64_t slot0 = __shfl_sync(0xffffffffu, slot, 0);
+            uint32_t tma_groups = 0;  // bit gi: group gi by box-8 TMA
+            bool whole = okm == 0xffffffffu && (contm | 1u) == 0xffffffffu;
+            if (!whole) {
+#pragma unroll
+                for (int gi = 0; gi < kKeys / 8; ++gi) {
+                    const uint32_t gm = 0xffu << (gi * 8);
+                    // all 8 valid, and keys 1..7 of the group continue the run
+                    if ((okm & gm) == gm && (contm & (gm & ~(1u << (gi * 8)))) == (gm & ~(1u << (gi * 8))))
+                        tma_groups |= 1u << gi;
+                }
+            }
             const uint32_t kt = sbase + C::kKvOff + st * C::kStageBytes;
             const uint32_t vt = kt + C::kTileBytes;
+            const uint32_t bar = smem_addr(&bars[kKvFull + st]);
+            if (lane == 0) {
+                const uint32_t bytes = whole ? 2u * C::kTileBytes : (uint32_t)__popc(tma_groups) * 2u * 8u * (uint32_t)(D * 2);
+                mbar_arrive_expect_tx(bar, bytes);
+                if (whole) {
 #pragma unroll
-            for (int r0 = 0; r0 < kKeysPerWarp; r0 += kRowsPerInst) {
-                const int kr = r0 + sub;
-                const int tk = lw * kKeysPerWarp + kr;  // key within the tile
-                const int64_t sl = __shfl_sync(0xffffffffu, slot, kr);
-                const bool kok = (okm >> kr) & 1u;
-                const size_t off = kok ? (size_t)sl * slot_bytes + col * 16 : 0;
-                const uint32_t dst = (tk >> 3) * C::kRowSbo + col * 128 + (tk & 7) * 16;
-                cp_async_16(kt + dst, kbase + off, kok ? 16u : 0u, keep);
-                cp_async_16(vt + dst, vbase + off, kok ? 16u : 0u, keep);
+                    for (int db = 0; db < C::kDimBlocks; ++db) {
+                        tma_load_3d(kt + db * C::kBlockBytes, &tm_k32, db * 64, g, (int32_t)slot0, bar);
+                        tma_load_3d(vt + db * C::kBlockBytes, &tm_v32, db * 64, g, (int32_t)slot0, bar);
+                    }
+                }
             }
-            cp_async_mbar_arrive(smem_addr(&bars[kKvFull + st]));
+            if (!whole) {
+#pragma unroll
+                for (int gi = 0; gi < kKeys / 8; ++gi) {
+                    const int64_t gs = __shfl_sync(0xffffffffu, slot, gi * 8);
+                    if ((tma_groups >> gi) & 1u) {
+                        if (lane == 0) {
+#pragma unroll
+                            for (int db = 0; db < C::kDimBlocks; ++db) {
+                                tma_load_3d(kt + db * C::kBlockBytes + gi * 1024, &tm_k8, db * 64, g, (int32_t)gs, bar);
+                                tma_load_3d(vt + db * C::kBlockBytes + gi * 1024, &tm_v8, db * 64, g, (int32_t)gs, bar);
+                            }
+                        }
+                    } else {
+                        // 8 keys x D/8 16-byte chunks over 32 lanes
+#pragma unroll 4
+                        for (int idx = lane; idx < 8 * (D / 8); idx += 32) {
+                            const int kr = gi * 8 + (idx >> (D == 256 ? 5 : 4));
+                            const int c = idx & (D / 8 - 1);
+                            const int64_t sl = __shfl_sync(0xffffffffu, slot, kr);  // uniform index per 32 idx
+                            const bool kok = (okm >> kr) & 1u;
+                            const size_t off = kok ? (size_t)sl * slot_bytes + c * 16 : 0;
+                            const int db = c >> 3, cb = c & 7;
+                            const uint32_t dst = db * C::kBlockBytes + kr * 128 + ((cb ^ (kr & 7)) << 4);
+                            cp_async_16(kt + dst, kbase + off, kok ? 16u : 0u, keep);
+                            cp_async_16(vt + dst, vbase + off, kok ? 16u : 0u, keep);
+                        }
+                    }
+                }
+            }
+            cp_async_mbar_arrive(bar);
         }
         cp_async_wait<0>();
     } else if (warp == kMmaWarp) {
@@ -284,7 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     tc_mma_bf16(tmem + sb * kKeys, tc_smem_desc(q_s + kk * 256, 128, C::kRowSbo),
-                                tc_smem_desc(kt + kk * 256, 128, C::kRowSbo), idesc_qk, kk > 0);
+                                tc_smem_desc_sw128(kt + (kk / 4) * C::kBlockBytes + (kk % 4) * 32, 16, 1024),
+                                idesc_qk, kk > 0);
                 tc_commit(smem_addr(&bars[kSFull + sb]));
                 return true;
             };
@@ -298,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                 const uint32_t p_hi = sbase + C::kPOff + pb * C::kPBufBytes, p_lo = p_hi + C::kPBytes;
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    const uint64_t vd = tc_smem_desc(vt + 2 * kk * C::kRowSbo, C::kRowSbo, 128);
+                    const uint64_t vd = tc_smem_desc_sw128(vt + kk * 16 * 128, C::kBlockBytes, 1024);
                     tc_mma_bf16(tmem + C::kOCol, tc_smem_desc(p_hi + kk * 256, 128, C::kPSbo), vd,
                                 idesc_pv, (t > 0 || kk > 0));
                     tc_mma_bf16(tmem + C::kOCol, tc_smem_desc(p_lo + kk * 256, 128, C::kPSbo), vd,
@@ -606,6 +660,40 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
 
 // Whether clusters of n CTAs of the tree kernel can be resident on device
 // dev (cached per device and size).
+// cuTensorMapEncodeTiled from the driver, looked up once.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+    }
+    return fn;
+}
+
+// 3-D map of a [num_slots][H_kv][D] bf16 pool: boxes of 64 dims x 1 head x
+// `rows` consecutive slots, 128-byte swizzle.
+bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t num_slots, int H_kv, int D, int rows) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn || num_slots < 1) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H_kv, (cuuint64_t)num_slots};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H_kv * D * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 bool tree_cluster_ok(int dev, int n) {
     static int8_t known[64][kMaxClusterSplits + 1] = {};
@@ -660,6 +748,12 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
         p += align256((size_t)B * H_kv * R * n_split * 4);
         ws.o_part = reinterpret_cast<float *>(p);
     }
+    CUtensorMap tm_k32, tm_v32, tm_k8, tm_v8;
+    if (!pool_tensor_map(&tm_k32, k_pool, num_slots, H_kv, D, kKeys) ||
+        !pool_tensor_map(&tm_v32, v_pool, num_slots, H_kv, D, kKeys) ||
+        !pool_tensor_map(&tm_k8, k_pool, num_slots, H_kv, D, 8) ||
+        !pool_tensor_map(&tm_v8, v_pool, num_slots, H_kv, D, 8))
+        return WMTP_ECUDA;
     PdlLaunch launch(dim3((unsigned)n_split, (unsigned)(H_kv * n_rb), (unsigned)B), dim3(kThreads),
                      C::kSmemBytes, stream);
     if (use_cluster) launch.add_cluster((unsigned)n_split);
@@ -668,7 +762,7 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
         n_nodes, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
         reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, seq_lens, ring_base, n_sink,
         window, depth, tree_k, scale * 1.4426950408889634f, out, lse, ws, n_split, n_rb,
-        (int32_t)(use_cluster ? 1 : 0));
+        (int32_t)(use_cluster ? 1 : 0), tm_k32, tm_v32, tm_k8, tm_v8);
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
