@@ -18,7 +18,8 @@
 // One CTA = 128 query rows (the MMA's M) x one key chunk of one request and
 // KV head.  Warp roles:
 //   warps 0-3  softmax: thread i owns query row i = tensor-memory lane i.  It
-//              reads its row of S = Q K^T from tensor memory, applies the
+//              first writes its row of Q into tensor memory (the A operand of
+//              QK), then per tile reads its row of S = Q K^T, applies the
 //              tree-causal mask, keeps a running reference max (the O
 //              accumulator is rescaled in tensor memory only when the max
 //              grows by more than 2^8), writes P as bf16 head + tail into
@@ -26,12 +27,13 @@
 //   warp 4     gather: slots from the ring rule (no table); 32-key tiles
 //              of consecutive ring slots arrive as TMA boxes (64 dims x 1
 //              head x 32 or 8 slots, 128-byte swizzle), other keys through
-//              16-byte cp.async into the same swizzled layout; four stages.
+//              16-byte cp.async into the same swizzled layout; six stages.
 //   warp 5     one thread issues the MMAs: S(t) = Q K(t)^T (M=128, N=32,
 //              K=D) into one of two S buffers, then O += P_hi V + P_lo V
 //              (M=128, N=D, K=32); completion is signalled through mbarriers
-//              with tcgen05.commit.  Q and P are no-swizzle K-major; K is
-//              K-major and V MN-major, both 128-byte swizzled.
+//              with tcgen05.commit.  Q is read from tensor memory, P from
+//              no-swizzle K-major shared memory; K is K-major and V
+//              MN-major, both 128-byte swizzled.
 // Key chunks are split over CTAs; up to 8 chunks of a (request, KV head,
 // row block) run as one cluster and merge through distributed shared memory,
 // more through the workspace (the last CTA merges in split order).  Every
@@ -57,7 +59,7 @@ __device__ __forceinline__ void latch(int32_t code) { atomicCAS(&g_tree_tc_error
 
 constexpr int kRows = 128;  // query rows per CTA (MMA M)
 constexpr int kKeys = 32;   // keys per tile (N of QK^T, K of PV)
-constexpr int kKvStages = 4;
+constexpr int kKvStages = 6;
 constexpr int kSoftWarps = 4;
 constexpr int kLoadWarps = 1;
 constexpr int kLoadThreads = kLoadWarps * 32;
@@ -77,32 +79,35 @@ enum {
     kSEmpty = kSFull + 2,
     kPFull = kSEmpty + 2,
     kPvDone = kPFull + 2,
-    kNumBars = kPvDone + 2
+    kQFull = kPvDone + 2,
+    kNumBars = kQFull + 1
 };
 
 template <int D>
 struct Cfg {
     static constexpr int kChunks = D / 8;                    // 16-byte chunks per row
     static constexpr int kRowSbo = kChunks * 128;            // 8-row group stride (Q, K, V)
-    static constexpr int kQBytes = kRows / 8 * kRowSbo;
+
     static constexpr int kTileBytes = kKeys / 8 * kRowSbo;   // K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kPSbo = kKeys / 8 * 128;            // P: 8-row group stride
     static constexpr int kPBytes = kRows / 8 * kPSbo;        // one of P_hi / P_lo
     static constexpr int kPBufBytes = 2 * kPBytes;           // P_hi then P_lo
-    static constexpr int kQOff = 0;
-    static constexpr int kKvOff = kQBytes;
+    static constexpr int kKvOff = 0;
     static constexpr int kPOff = kKvOff + kKvStages * kStageBytes;
     static constexpr int kBarOff = kPOff + 2 * kPBufBytes;
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
     static constexpr int kDimBlocks = D / 64;                 // 128-byte swizzle atoms per K/V row
     static constexpr int kBlockBytes = kKeys * 128;           // one 64-dim block of a tile
     static constexpr int kOCol = 2 * kKeys;                  // O after the two S buffers
-    static constexpr int kTmemCols = (kOCol + D <= 256) ? 256 : 512;
+    static constexpr int kQCol = kOCol + D;                  // Q (A operand of QK): two bf16 per column
+    static constexpr int kTmemCols = (kQCol + D / 2 <= 256) ? 256 : 512;
+    static_assert(kQCol + D / 2 <= 512, "tensor memory budget");
     static_assert(kRows * kMaxSplits * 4 <= kKvStages * kStageBytes, "merge weights must fit");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kRows * D * 4 <= kKvStages * kStageBytes, "cluster-merge partial must fit the K/V stages");
-    static_assert(kRows * 4 <= 2 * kPBufBytes, "cluster-merge lse must fit the P buffers");
+    static_assert(kRows * 4 + kRows * kMaxClusterSplits * 4 <= 2 * kPBufBytes,
+                  "cluster-merge lse and weights must fit the P buffers");
 };
 
 struct TreeWs {
@@ -202,28 +207,15 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             mbar_init(smem_addr(&bars[kPFull + i]), kSoftWarps);
             mbar_init(smem_addr(&bars[kPvDone + i]), 1);
         }
+        mbar_init(smem_addr(&bars[kQFull]), kSoftWarps);
         flags[0] = 0;
         flags[1] = 0;
         fence_mbar_init();
     }
     if (warp == 0) tc_alloc(smem_addr(tmem_slot), C::kTmemCols);
 
-    // Q rows of this block -> shared memory (K-major core-matrix layout).
     const uint32_t sbase = smem_addr(smem);
     const uint64_t keep = l2_policy_evict_last();
-    for (int idx = tid; idx < kRows * C::kChunks; idx += kThreads) {
-        const int i = idx / C::kChunks, j = idx - i * C::kChunks;
-        const int rq = rb * kRows + i;
-        const bool live = rq < R;
-        const int t = live ? rq / G : 0;
-        const int h = g * G + (live ? rq % G : 0);
-        const __nv_bfloat16 *src = q + ((b * n_nodes + t) * H_q + h) * (int64_t)D + j * 8;
-        cp_async_16(sbase + C::kQOff + (i >> 3) * C::kRowSbo + j * 128 + (i & 7) * 16, src,
-                    live ? 16u : 0u, keep);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -326,9 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         if (lane == 0) {
             constexpr uint32_t idesc_qk = tc_idesc_bf16(kRows, kKeys, 0);
             constexpr uint32_t idesc_pv = tc_idesc_bf16(kRows, D, 1);
-            const uint32_t q_s = sbase + C::kQOff;
             auto issue_qk = [&](int t) -> bool {
                 const int st = t % kKvStages, sb = t & 1;
+                if (t == 0 && !mbar_wait(&bars[kQFull], 0, flags)) return false;
                 if (!mbar_wait(&bars[kKvFull + st], (t / kKvStages) & 1, flags)) return false;
                 if (t >= 2 && !mbar_wait(&bars[kSEmpty + sb], ((t >> 1) - 1) & 1, flags)) return false;
                 fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
@@ -336,9 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                 const uint32_t kt = sbase + C::kKvOff + st * C::kStageBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    tc_mma_bf16(tmem + sb * kKeys, tc_smem_desc(q_s + kk * 256, 128, C::kRowSbo),
-                                tc_smem_desc_sw128(kt + (kk / 4) * C::kBlockBytes + (kk % 4) * 32, 16, 1024),
-                                idesc_qk, kk > 0);
+                    tc_mma_bf16_ta(tmem + sb * kKeys, tmem + C::kQCol + kk * 8,
+                                   tc_smem_desc_sw128(kt + (kk / 4) * C::kBlockBytes + (kk % 4) * 32, 16, 1024),
+                                   idesc_qk, kk > 0);
                 tc_commit(smem_addr(&bars[kSFull + sb]));
                 return true;
             };
@@ -364,6 +356,31 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         }
     } else {
         // --------------------------------------------------------- softmax
+        // Q row `tid` of this block -> tensor-memory lane tid (A operand of
+        // QK), while the gather warp already fetches the first tiles.
+        {
+            const int rq = rb * kRows + tid;
+            const bool live = rq < R;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(
+                q + ((b * n_nodes + (live ? rq / G : 0)) * H_q + g * G + (live ? rq % G : 0)) * (int64_t)D);
+            const uint32_t qlane = tmem + ((uint32_t)(warp * 32) << 16) + C::kQCol;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D / 2; c0 += 32) {
+                uint32_t r[32];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const uint4 v = live ? __ldg(reinterpret_cast<const uint4 *>(src + c0 + j)) : make_uint4(0, 0, 0, 0);
+                    r[j] = v.x;
+                    r[j + 1] = v.y;
+                    r[j + 2] = v.z;
+                    r[j + 3] = v.w;
+                }
+                tc_st32(qlane + c0, r);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bars[kQFull]));
+        }
         const int i = tid;  // row = tensor-memory lane
         const int rq = rb * kRows + i;
         const bool row_live = rq < R;
@@ -561,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         const int r_hi = r_lo + per < n_rows ? r_lo + per : n_rows;
         const uint32_t po_addr = smem_addr(smem + C::kKvOff);
         const uint32_t pl_addr = smem_addr(smem + C::kPOff);
-        float *wts = reinterpret_cast<float *>(smem + C::kQOff);  // [per][n_split] merge weights
+        float *wts = reinterpret_cast<float *>(smem + C::kPOff + kRows * 4);  // [per][n_split] merge weights
         for (int i = r_lo + tid; i < r_hi; i += kThreads) {
             float ls[kMaxClusterSplits];
 #pragma unroll
