@@ -99,6 +99,32 @@ wmtp_status wmtp_build_draft_indices(const int32_t *seq_lens, int32_t B,
                                      int64_t stride, int32_t *lens,
                                      void *stream);
 
+/* Index table of a draft-extend pass (the draft forward over the n new
+ * tokens a request accepted, at positions S..S+n-1, in one launch; see
+ * wmtp_draft_extend_attn).  Row b is the union of the key sets of its n
+ * tokens under the keep rule above: token t sees kv_len = S + t + 1, so the
+ * union is the keep rule at kv_len = S + n with window W + n - 1 --
+ * positions [0, n_sink) then [S + 1 - W, S + n) when S + 1 > n_sink + W
+ * (windowed mode), else [0, S + n) -- mapped to slots as above.  A request
+ * with n = 0 gets an empty row.
+ *
+ * seq_lens   device int32 [B]: committed length S before the new tokens.
+ * n_new      device int32 [B]: new tokens per request (>= 0; a negative
+ *            count is treated as 0 and latches WMTP_DEV_ARG_RANGE).
+ * table      device int32 [B][stride]; lens device int32 [B].
+ * Other arguments and errors as wmtp_build_draft_indices (gamma = 1). */
+wmtp_status wmtp_build_extend_indices(const int32_t *seq_lens,
+                                      const int32_t *n_new, int32_t B,
+                                      int32_t n_sink, int32_t window,
+                                      int32_t depth, int32_t tree_k,
+                                      int32_t windowed,
+                                      const int32_t *req_to_token,
+                                      const int32_t *req_pool_idx,
+                                      int64_t rtt_stride,
+                                      const int32_t *ring_base, int32_t *table,
+                                      int64_t stride, int32_t *lens,
+                                      void *stream);
+
 /* ------------------------------------------------------------------------
  * Ring slot mapper.
  * "Windowed-MTP", App. A: slot = ring_base(r) + logical position, with a
@@ -226,6 +252,34 @@ wmtp_status wmtp_draft_decode_attn_append(const uint16_t *k_new,
                                           float scale, float *out, float *lse,
                                           void *workspace, size_t workspace_bytes,
                                           int32_t n_split, void *stream);
+
+/* Draft-extend attention: the draft forward over the n = n_new[b] tokens a
+ * request accepted (positions S..S+n-1, K/V already appended), in one
+ * launch.  Row t < n of request b is the attention of its query heads over
+ * exactly the keys draft step t sees under the keep rule (kv_len = S + t + 1,
+ * §4 Mechanism / App. A): the union table of wmtp_build_extend_indices
+ * restricted to positions below S + t + 1 and, when windowed and S + t + 1 >
+ * n_sink + W, to sinks and positions from S + t + 1 - W.  Rows t >= n give
+ * out = 0, lse = -inf.  Keys outside a row's set are not read.
+ *
+ * q          device bf16 [B][n_q][H_q][D]; n_q >= max n_new.
+ * table,lens the union table and lengths of wmtp_build_extend_indices built
+ *            with the same seq_lens, n_new, n_sink, W and windowed flag.
+ * seq_lens   device int32 [B] (S); n_new device int32 [B].
+ * Other arguments, the split plan, workspace and errors as
+ * wmtp_draft_decode_attn; additionally WMTP_EINVAL for null seq_lens or
+ * n_new, n_sink < 0 or W < 1. */
+wmtp_status wmtp_draft_extend_attn(const uint16_t *q, int32_t B, int32_t n_q,
+                                   int32_t H_q, int32_t H_kv, int32_t D,
+                                   const uint16_t *k_pool,
+                                   const uint16_t *v_pool, int64_t num_slots,
+                                   const int32_t *table, int64_t table_stride,
+                                   const int32_t *lens, const int32_t *seq_lens,
+                                   const int32_t *n_new, int32_t n_sink,
+                                   int32_t window, int32_t windowed, float scale,
+                                   float *out, float *lse, void *workspace,
+                                   size_t workspace_bytes, int32_t n_split,
+                                   void *stream);
 
 /* ------------------------------------------------------------------------
  * Tree-draft attention over the ring.

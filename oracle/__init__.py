@@ -14,7 +14,9 @@ from .oracle import (  # noqa: F401
     append_kv,
     build,
     build_draft_indices,
+    build_extend_indices,
     draft_decode_attn,
+    draft_extend_attn,
     keep,
     num_threads,
     ring_map,

@@ -256,3 +256,79 @@ def acceptance_length(hist):
     al = _load().orc_acceptance_length(_ptr(h, ctypes.c_double), gamma,
                                        _ptr(alpha, ctypes.c_double))
     return alpha, float(al)
+
+
+# ------------------------------------------------------------ draft extend
+# A draft-extend pass is the draft forward over the n tokens a request
+# accepted, at positions S..S+n-1, in one call.  Token t is exactly draft
+# step t of build_draft_indices (kv_len = S + t + 1, §4 Mechanism; App. A
+# keep rule), so both functions below compose the pinned functions above
+# and add no arithmetic of their own.
+
+def build_extend_indices(seq_lens, n_new, n_sink, window, depth, tree_k=1,
+                         windowed=True, req_to_token=None, req_pool_idx=None,
+                         ring_base=None, stride=None):
+    """Union, in ascending position order, of the keep sets of steps
+    0..n_new[b]-1 of each request, mapped to slots like build_draft_indices.
+
+    Returns ``(table[B, stride] int32, lens[B] int32)``; entries past lens
+    are -1."""
+    sl = _as(seq_lens, np.int32)
+    nn = _as(n_new, np.int32)
+    B = sl.shape[0]
+    rtt = _as(req_to_token, np.int32)
+    rpi = _as(req_pool_idx, np.int32)
+    rb = _as(ring_base, np.int32)
+    if rtt is not None and rpi is None:
+        rpi = np.arange(B, dtype=np.int32)
+    rows = []
+    for b in range(B):
+        pos = set()
+        for t in range(max(int(nn[b]), 0)):
+            pos.update(int(p) for p in keep(int(sl[b]) + t + 1, n_sink, window, windowed))
+        pos = np.array(sorted(pos), dtype=np.int64)
+        if rtt is not None:
+            slots = rtt[int(rpi[b])][pos] if pos.size else np.zeros(0, np.int32)
+        else:
+            slots = ring_map(np.array([rb[b]], np.int32), pos.astype(np.int32),
+                             np.zeros(pos.size, np.int32), n_sink, window, depth, tree_k)
+        rows.append(np.asarray(slots, dtype=np.int32))
+    if stride is None:
+        stride = max([r.size for r in rows] + [1])
+    table = np.full((B, stride), -1, dtype=np.int32)
+    lens = np.zeros(B, dtype=np.int32)
+    for b, r in enumerate(rows):
+        n = min(r.size, stride)
+        table[b, :n] = r[:n]
+        lens[b] = r.size
+    return table, lens
+
+
+def draft_extend_attn(q, k_pool, v_pool, seq_lens, n_new, n_sink, window,
+                      scale, windowed=True, req_to_token=None, req_pool_idx=None,
+                      ring_base=None, depth=1, tree_k=1):
+    """Row t < n_new[b] of request b: draft_decode_attn over the table of
+    draft step t (build_draft_indices); rows t >= n_new[b]: out 0, lse -inf.
+
+    q: [B, n_q, H_q, D] bf16 bits.  Returns ``(out float64, lse float64)``."""
+    q = _as(q, np.uint16)
+    sl = _as(seq_lens, np.int32)
+    nn = _as(n_new, np.int32)
+    B, n_q, H_q, D = q.shape
+    out = np.zeros((B, n_q, H_q, D), dtype=np.float64)
+    lse = np.full((B, n_q, H_q), -np.inf, dtype=np.float64)
+    if B == 0 or n_q == 0:
+        return out, lse
+    gamma = max(int(min(nn.max(), n_q)), 0)
+    if gamma == 0:
+        return out, lse
+    tables, lens = build_draft_indices(sl, gamma, n_sink, window, depth, tree_k,
+                                       windowed, req_to_token, req_pool_idx,
+                                       ring_base)
+    for b in range(B):
+        for t in range(min(max(int(nn[b]), 0), n_q)):
+            o, l = draft_decode_attn(q[b:b + 1, t:t + 1], k_pool, v_pool,
+                                     tables[t][b:b + 1], lens[t][b:b + 1], scale)
+            out[b, t] = o[0, 0]
+            lse[b, t] = l[0, 0]
+    return out, lse

@@ -13,6 +13,8 @@ Calls (same names as the C ABI without the ``wmtp_`` prefix):
   append_kv            write draft K/V rows into the pool
   draft_decode_attn    split-KV flash-decode attention with LSE merge
   draft_decode_attn_append  append_kv + draft_decode_attn in one launch
+  build_extend_indices / draft_extend_attn  the draft forward over a request's
+                       accepted tokens in one launch (each token its own keys)
   tree_draft_attn      tree-draft attention over the ring (tree-causal mask)
 """
 from __future__ import annotations
@@ -27,7 +29,8 @@ from . import _build
 
 __all__ = [
     "WmtpError", "load", "build", "version", "device_error",
-    "build_draft_indices", "ring_map", "append_kv", "draft_decode_attn", "draft_decode_attn_append",
+    "build_draft_indices", "build_extend_indices", "ring_map", "append_kv", "draft_decode_attn",
+    "draft_decode_attn_append", "draft_extend_attn",
     "attn_workspace_bytes", "attn_num_splits", "AttnWorkspace", "draft_decode_attn_noalloc",
     "tree_draft_attn", "tree_workspace_bytes", "tree_num_splits",
 ]
@@ -82,6 +85,13 @@ def load():
         lib.wmtp_build_draft_indices.restype = _i32
         lib.wmtp_build_draft_indices.argtypes = [
             _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp]
+        lib.wmtp_build_extend_indices.restype = _i32
+        lib.wmtp_build_extend_indices.argtypes = [
+            _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp]
+        lib.wmtp_draft_extend_attn.restype = _i32
+        lib.wmtp_draft_extend_attn.argtypes = [
+            _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32,
+            _i32, ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
         lib.wmtp_ring_map.restype = _i32
         lib.wmtp_ring_map.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]
         lib.wmtp_append_kv.restype = _i32
@@ -202,6 +212,53 @@ def build_draft_indices(seq_lens: torch.Tensor, gamma: int, n_sink: int, window:
     return table, lens
 
 
+def build_extend_indices(seq_lens: torch.Tensor, n_new: torch.Tensor, n_sink: int, window: int,
+                         depth: int, tree_k: int = 1, windowed: bool = True,
+                         req_to_token: torch.Tensor | None = None,
+                         req_pool_idx: torch.Tensor | None = None,
+                         ring_base: torch.Tensor | None = None, stride: int | None = None,
+                         table: torch.Tensor | None = None, lens: torch.Tensor | None = None,
+                         stream=None):
+    """Union index table of a draft-extend pass (``wmtp_build_extend_indices``).
+
+    Returns ``(table[B, stride] int32, lens[B] int32)``.  When ``stride`` is
+    omitted it is ``n_sink + window + max_new - 1`` with ``max_new`` =
+    ``n_new.max()`` (windowed), or ``req_to_token.shape[1]`` (full, paged).
+    """
+    _need(seq_lens, "seq_lens", torch.int32)
+    dev = seq_lens.device
+    _need(n_new, "n_new", torch.int32, dev)
+    B = seq_lens.shape[0]
+    if req_to_token is not None:
+        _need(req_to_token, "req_to_token", torch.int32, dev)
+        if req_pool_idx is not None:
+            _need(req_pool_idx, "req_pool_idx", torch.int32, dev)
+    if ring_base is not None:
+        _need(ring_base, "ring_base", torch.int32, dev)
+    if stride is None:
+        if table is not None:
+            stride = table.shape[-1]
+        elif windowed:
+            stride = n_sink + window + max(int(n_new.max().item()) if B else 1, 1) - 1
+        elif req_to_token is not None:
+            stride = req_to_token.shape[1]
+        else:
+            raise ValueError("stride is required for a full-context ring table")
+    if table is None:
+        table = torch.empty((B, stride), dtype=torch.int32, device=dev)
+    if lens is None:
+        lens = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(table, "table", torch.int32, dev)
+    _need(lens, "lens", torch.int32, dev)
+    rtt_stride = req_to_token.shape[1] if req_to_token is not None else 0
+    with torch.cuda.device(dev):
+        _check(load().wmtp_build_extend_indices(
+            _ptr(seq_lens), _ptr(n_new), B, n_sink, window, depth, tree_k, int(bool(windowed)),
+            _ptr(req_to_token), _ptr(req_pool_idx), rtt_stride, _ptr(ring_base), _ptr(table),
+            stride, _ptr(lens), _stream(stream)), "build_extend_indices")
+    return table, lens
+
+
 # ---------------------------------------------------------------- a2
 def ring_map(ring_base: torch.Tensor, pos: torch.Tensor, req_of: torch.Tensor, n_sink: int,
              window: int, depth: int, tree_k: int = 1, branch: torch.Tensor | None = None,
@@ -307,6 +364,24 @@ def draft_decode_attn_append(k_new: torch.Tensor, v_new: torch.Tensor, new_slots
                  n_split, max_len, workspace, stream)
 
 
+def draft_extend_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                      table: torch.Tensor, lens: torch.Tensor, seq_lens: torch.Tensor,
+                      n_new: torch.Tensor, n_sink: int, window: int, scale: float,
+                      windowed: bool = True, out: torch.Tensor | None = None,
+                      lse: torch.Tensor | None = None, n_split: int | None = None,
+                      max_len: int | None = None, workspace: AttnWorkspace | None = None,
+                      stream=None):
+    """Draft-extend attention over a union table (``wmtp_draft_extend_attn``):
+    row t of request b attends the keys draft step t sees; rows t >= n_new[b]
+    give zeros and lse = -inf.  q: [B, n_q, H_q, D] bf16; table/lens from
+    :func:`build_extend_indices`.  Returns ``(out, lse)`` as
+    :func:`draft_decode_attn`."""
+    _need(seq_lens, "seq_lens", torch.int32, q.device)
+    _need(n_new, "n_new", torch.int32, q.device)
+    return _attn(("extend", seq_lens, n_new, n_sink, window, windowed), q, k_pool, v_pool, table,
+                 lens, scale, out, lse, n_split, max_len, workspace, stream)
+
+
 def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_len, workspace,
           stream):
     _need(q, "q", torch.bfloat16)
@@ -349,6 +424,15 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
                 _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
                 stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf),
                 workspace.nbytes, n_split, _stream(stream)), "draft_decode_attn")
+        return out, lse
+    if append[0] == "extend":
+        _, seq_lens, n_new, n_sink, window, windowed = append
+        with torch.cuda.device(dev):
+            _check(load().wmtp_draft_extend_attn(
+                _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
+                stride, _ptr(lens), _ptr(seq_lens), _ptr(n_new), n_sink, window, int(bool(windowed)),
+                float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf), workspace.nbytes, n_split,
+                _stream(stream)), "draft_extend_attn")
         return out, lse
     k_new, v_new, new_slots = append
     _need(k_new, "k_new", torch.bfloat16, dev)

@@ -131,6 +131,18 @@ struct AppendView {
     __nv_bfloat16 *v_pool;
     int32_t n_new;
 };
+// Draft-extend pass: the n_q rows of request b are its new tokens at
+// positions S..S+n-1 (n = n_new[b]; rows t >= n are empty), all reading the
+// union table of wmtp_build_extend_indices; token t sees only the keys of
+// its own keep set (positions below S + t + 1, and, when windowed, sinks or
+// positions from S + t + 1 - W).  seq_lens == nullptr: not an extend pass.
+struct ExtendView {
+    const int32_t *seq_lens;
+    const int32_t *n_new;
+    int32_t n_sink;
+    int32_t window;
+    int32_t windowed;
+};
 
 inline WorkspaceView carve(void *ws, int64_t rows_q, int64_t rows_kv, int n_split) {
     uint8_t *p = static_cast<uint8_t *>(ws);
@@ -154,13 +166,14 @@ inline WorkspaceView carve_two_level(void *ws, int64_t rows_q, int64_t rows_kv, 
     return v;
 }
 
-template <int D, bool kAppend>
+template <int D, bool kAppend, bool kExtend>
 __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const __nv_bfloat16 *__restrict__ q, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t G,
     const __nv_bfloat16 *__restrict__ k_pool, const __nv_bfloat16 *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ table, int64_t table_stride,
     const int32_t *__restrict__ lens, float scale_log2, float *__restrict__ out,
-    float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t csz, AppendView ap) {
+    float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t csz, AppendView ap,
+    ExtendView ev) {
     using C = Cfg<D>;
     constexpr int S = C::kStages;
     constexpr int R = C::kRingTiles;
@@ -242,6 +255,24 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         if (threadIdx.x == 0 && split == 0 && g == 0) latch(WMTP_DEV_LEN_RANGE);
         L = L < 0 ? 0 : table_stride;
     }
+    // Extend pass: position of union entry e is e below n_sink (or when the
+    // union is not windowed), else lo_u + e - n_sink; this row's token sees
+    // positions below kv_t and, if windowed, only sinks or from lo_t.
+    int64_t x_lo_u = 0, x_kv_t = 0, x_lo_t = 0;
+    bool x_win_u = false, x_win_t = false;
+    if constexpr (kExtend) {
+        const int t = (int)(bt % n_q);
+        int32_t nn = ev.n_new[b];
+        nn = nn < 0 ? 0 : nn;
+        const int64_t S = ev.seq_lens[b];
+        if (t >= nn) L = 0;
+        const int64_t kv_u = S + nn, w_u = (int64_t)ev.window + (nn > 0 ? nn - 1 : 0);
+        x_win_u = ev.windowed && kv_u > (int64_t)ev.n_sink + w_u;
+        x_lo_u = kv_u - w_u;
+        x_kv_t = S + t + 1;
+        x_win_t = ev.windowed && x_kv_t > (int64_t)ev.n_sink + ev.window;
+        x_lo_t = x_kv_t - ev.window;
+    }
     const int64_t chunk = chunk_of(L);
     const int64_t start = (int64_t)split * chunk;
     const int64_t cnt = L - start < 0 ? 0 : (L - start < chunk ? L - start : chunk);
@@ -265,8 +296,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         const int32_t my_slot = lane < kKeysPerWarp ? ring[(t % R) * kKeysPerWarp + lane] : 0;
         const int64_t k = (int64_t)t * kTileKeys + warp * kKeysPerWarp + (lane & 15);
         const bool in = lane < kKeysPerWarp && k < cnt;
-        const bool ok = in && my_slot >= 0 && my_slot < num_slots;
+        bool ok = in && my_slot >= 0 && my_slot < num_slots;
         if (in && !ok) latch(WMTP_DEV_SLOT_RANGE);
+        if constexpr (kExtend) {
+            const int64_t e = start + k;
+            const int64_t pos = (x_win_u && e >= ev.n_sink) ? x_lo_u + (e - ev.n_sink) : e;
+            ok = ok && pos < x_kv_t && (!x_win_t || pos < ev.n_sink || pos >= x_lo_t);
+        }
         // A key whose slot this launch appends is marked -2 - i (row i of
         // the new rows); its vm bit stays set.
         int32_t src_slot = my_slot;
@@ -717,15 +753,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
 // device `dev` (0: none; cached per device and size).
 // Sets the kernel attributes (large dynamic shared memory, non-portable
 // cluster sizes) once per device for one kernel instance.
-template <int D, bool A>
+template <int D, bool A, bool X>
 bool prepare_kernel(int dev) {
     static int8_t done[64] = {};
     if (dev < 0 || dev >= 64) return false;
     if (done[dev]) return done[dev] > 0;
-    const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A>,
+    const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A, X>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<D>::kSmemBytes) == cudaSuccess &&
-                    cudaFuncSetAttribute(split_decode_kernel<D, A>,
+                    cudaFuncSetAttribute(split_decode_kernel<D, A, X>,
                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
     cudaGetLastError();
     done[dev] = ok ? 1 : -1;
@@ -737,7 +773,7 @@ int cluster_capacity(int dev, int n) {
     static int16_t known[64][kMaxClusterMerge + 1] = {};
     if (n < 2 || n > kMaxClusterMerge || dev < 0 || dev >= 64) return 0;
     if (known[dev][n]) return known[dev][n] > 0 ? known[dev][n] : 0;
-    bool ok = prepare_kernel<D, false>(dev);
+    bool ok = prepare_kernel<D, false, false>(dev);
     int clusters = 0;
     if (ok) {
         cudaLaunchConfig_t cfg = {};
@@ -751,7 +787,7 @@ int cluster_capacity(int dev, int n) {
         attr.val.clusterDim.z = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        ok = cudaOccupancyMaxActiveClusters(&clusters, split_decode_kernel<D, false>, &cfg) == cudaSuccess &&
+        ok = cudaOccupancyMaxActiveClusters(&clusters, split_decode_kernel<D, false, false>, &cfg) == cudaSuccess &&
              clusters > 0;
         if (!ok) clusters = 0;
     }
@@ -771,7 +807,7 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
                                 int64_t num_slots, const int32_t *table, int64_t table_stride,
                                 const int32_t *lens, float scale, float *out, float *lse,
                                 void *workspace, int32_t n_split, cudaStream_t stream,
-                                AppendView ap) {
+                                AppendView ap, ExtendView ev) {
     using C = Cfg<D>;
     const int64_t rows_q = (int64_t)B * n_q * H_q;
     const int64_t rows_kv = (int64_t)B * n_q * H_kv;
@@ -780,7 +816,10 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WMTP_ECUDA;
     const bool append = ap.n_new > 0;
-    if (!(append ? prepare_kernel<D, true>(dev) : prepare_kernel<D, false>(dev))) return WMTP_ECUDA;
+    const bool extend = ev.seq_lens != nullptr;
+    if (!(append ? prepare_kernel<D, true, false>(dev)
+                 : (extend ? prepare_kernel<D, false, true>(dev) : prepare_kernel<D, false, false>(dev))))
+        return WMTP_ECUDA;
     // Cluster size: all splits in one cluster, else the largest cluster that
     // divides n_split into at most kMaxClusters clusters, else none.
     int csz = 0;
@@ -804,10 +843,12 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
                      C::kSmemBytes, stream);
     if (csz) launch.add_cluster((unsigned)csz);
     const cudaError_t err = cudaLaunchKernelEx(
-        &launch.cfg, append ? split_decode_kernel<D, true> : split_decode_kernel<D, false>,
+        &launch.cfg,
+        append ? split_decode_kernel<D, true, false>
+               : (extend ? split_decode_kernel<D, false, true> : split_decode_kernel<D, false, false>),
         reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q, H_kv, H_q / H_kv,
         reinterpret_cast<const __nv_bfloat16 *>(k_pool), reinterpret_cast<const __nv_bfloat16 *>(v_pool),
-        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, ap);
+        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, ap, ev);
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
@@ -863,15 +904,16 @@ wmtp_status launch_split_decode_noalloc(const uint16_t *q, int32_t B, int32_t n_
         if (cudaMemsetAsync(ws.counters, 0, (size_t)rows_kv * 4, stream) != cudaSuccess)
             return WMTP_ECUDA;
     }
-    if (!prepare_kernel<D, false>(dev)) return WMTP_ECUDA;
+    if (!prepare_kernel<D, false, false>(dev)) return WMTP_ECUDA;
     const float scale_log2 = scale * 1.4426950408889634f;
     PdlLaunch launch(dim3((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q)), dim3(kThreads),
                      C::kSmemBytes, stream);
     const cudaError_t err = cudaLaunchKernelEx(
-        &launch.cfg, split_decode_kernel<D, false>, reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q,
+        &launch.cfg, split_decode_kernel<D, false, false>, reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q,
         H_kv, H_q / H_kv, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
         reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, table, table_stride, lens,
-        scale_log2, out, lse, ws, n_split, (int32_t)0, AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0});
+        scale_log2, out, lse, ws, n_split, (int32_t)0, AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0},
+        ExtendView{nullptr, nullptr, 0, 0, 0});
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
@@ -949,7 +991,8 @@ wmtp_status draft_decode_attn_checked(const uint16_t *q, int32_t B, int32_t n_q,
                                       const int32_t *table, int64_t table_stride,
                                       const int32_t *lens, float scale, float *out, float *lse,
                                       void *workspace, size_t workspace_bytes_, int32_t n_split,
-                                      void *stream, AppendView ap) {
+                                      void *stream, AppendView ap,
+                                      ExtendView ev = ExtendView{nullptr, nullptr, 0, 0, 0}) {
     if (B < 0 || n_q < 0 || H_q < 1 || H_kv < 1 || (H_q % H_kv) != 0) return WMTP_EINVAL;
     if (H_q / H_kv > kMaxGroup) return WMTP_EINVAL;
     if (D != 128 && D != 256) return WMTP_EINVAL;
@@ -973,9 +1016,9 @@ wmtp_status draft_decode_attn_checked(const uint16_t *q, int32_t B, int32_t n_q,
     cudaStream_t s = as_stream(stream);
     if (D == 256)
         return launch_split_decode<256>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
-                                        table_stride, lens, scale, out, lse, workspace, n_split, s, ap);
+                                        table_stride, lens, scale, out, lse, workspace, n_split, s, ap, ev);
     return launch_split_decode<128>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
-                                    table_stride, lens, scale, out, lse, workspace, n_split, s, ap);
+                                    table_stride, lens, scale, out, lse, workspace, n_split, s, ap, ev);
 }
 
 }  // namespace
@@ -1013,6 +1056,23 @@ wmtp_status wmtp_draft_decode_attn_append(const uint16_t *k_new, const uint16_t 
     return draft_decode_attn_checked(q, B, n_q, H_q, H_kv, D, k_pool, v_pool, num_slots, table,
                                      table_stride, lens, scale, out, lse, workspace,
                                      workspace_bytes_, n_split, stream, ap);
+}
+
+wmtp_status wmtp_draft_extend_attn(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
+                                   int32_t H_kv, int32_t D, const uint16_t *k_pool,
+                                   const uint16_t *v_pool, int64_t num_slots,
+                                   const int32_t *table, int64_t table_stride,
+                                   const int32_t *lens, const int32_t *seq_lens,
+                                   const int32_t *n_new, int32_t n_sink, int32_t window,
+                                   int32_t windowed, float scale, float *out, float *lse,
+                                   void *workspace, size_t workspace_bytes_, int32_t n_split,
+                                   void *stream) {
+    if (!seq_lens || !n_new || n_sink < 0 || window < 1) return WMTP_EINVAL;
+    return draft_decode_attn_checked(q, B, n_q, H_q, H_kv, D, k_pool, v_pool, num_slots, table,
+                                     table_stride, lens, scale, out, lse, workspace,
+                                     workspace_bytes_, n_split, stream,
+                                     AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0},
+                                     ExtendView{seq_lens, n_new, n_sink, window, windowed ? 1 : 0});
 }
 
 wmtp_status wmtp_draft_decode_attn_noalloc(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,

@@ -31,21 +31,33 @@ __global__ void __launch_bounds__(256) build_indices_kernel(
     int32_t depth, int32_t tree_k, int32_t windowed,
     const int32_t *__restrict__ req_to_token, const int32_t *__restrict__ req_pool_idx,
     int64_t rtt_stride, const int32_t *__restrict__ ring_base, int32_t *__restrict__ table,
-    int64_t stride, int32_t *__restrict__ lens) {
+    int64_t stride, int32_t *__restrict__ lens, const int32_t *__restrict__ n_new) {
     griddep_launch_dependents();
     griddep_wait();
     const int32_t row = blockIdx.y;
     const int32_t j = row / B;
     const int32_t b = row - j * B;
-    const int64_t kv_len = (int64_t)seq_lens[b] + j + 1;
-    const bool win = windowed && kv_len > (int64_t)n_sink + window;
-    const int64_t n = kv_len <= 0 ? 0 : (win ? (int64_t)n_sink + window : kv_len);
+    int64_t kv_len = (int64_t)seq_lens[b] + j + 1;
+    int64_t keep_w = window;  // window of the keep rule (the ring keeps `window`)
+    if (n_new) {
+        // extend: the union of the key sets of the n new tokens at positions
+        // S..S+n-1 = the keep rule at kv_len S + n with window W + n - 1
+        int32_t nn = n_new[b];
+        if (nn < 0) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) latch(WMTP_DEV_ARG_RANGE);
+            nn = 0;
+        }
+        kv_len = nn == 0 ? 0 : (int64_t)seq_lens[b] + nn;
+        keep_w = (int64_t)window + (nn > 0 ? nn - 1 : 0);
+    }
+    const bool win = windowed && kv_len > (int64_t)n_sink + keep_w;
+    const int64_t n = kv_len <= 0 ? 0 : (win ? (int64_t)n_sink + keep_w : kv_len);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         lens[row] = (int32_t)n;
         if (n > stride) latch(WMTP_DEV_TABLE_OVERFLOW);
     }
     const int64_t n_write = n < stride ? n : stride;
-    const int64_t shift = win ? kv_len - window - n_sink : 0;
+    const int64_t shift = win ? kv_len - keep_w - n_sink : 0;
     int32_t *__restrict__ out = table + (int64_t)row * stride;
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
     if (req_to_token) {
@@ -168,7 +180,31 @@ wmtp_status wmtp_build_draft_indices(const int32_t *seq_lens, int32_t B, int32_t
     PdlLaunch L(dim3((unsigned)gx, (unsigned)(gamma * B)), dim3(kThreads), 0, as_stream(stream));
     return cudaLaunchKernelEx(&L.cfg, build_indices_kernel, seq_lens, B, n_sink, window, depth,
                               tree_k, windowed, req_to_token, req_pool_idx, rtt_stride, ring_base,
-                              table, stride, lens) == cudaSuccess
+                              table, stride, lens, static_cast<const int32_t *>(nullptr)) == cudaSuccess
+               ? WMTP_OK
+               : WMTP_ECUDA;
+}
+
+wmtp_status wmtp_build_extend_indices(const int32_t *seq_lens, const int32_t *n_new, int32_t B,
+                                      int32_t n_sink, int32_t window, int32_t depth,
+                                      int32_t tree_k, int32_t windowed,
+                                      const int32_t *req_to_token,
+                                      const int32_t *req_pool_idx, int64_t rtt_stride,
+                                      const int32_t *ring_base, int32_t *table,
+                                      int64_t stride, int32_t *lens, void *stream) {
+    if (B < 0 || n_sink < 0 || window < 1 || depth < 1 || tree_k < 1 || stride < 1 || B > 65535)
+        return WMTP_EINVAL;
+    if (B == 0) return WMTP_OK;
+    if (!seq_lens || !n_new || !table || !lens) return WMTP_EINVAL;
+    if (!req_to_token && !ring_base) return WMTP_EINVAL;
+    if (req_to_token && rtt_stride < 1) return WMTP_EINVAL;
+    constexpr int kThreads = 256;
+    int64_t gx = (stride + kThreads - 1) / kThreads;
+    if (gx > 8192) gx = 8192;
+    PdlLaunch L(dim3((unsigned)gx, (unsigned)B), dim3(kThreads), 0, as_stream(stream));
+    return cudaLaunchKernelEx(&L.cfg, build_indices_kernel, seq_lens, B, n_sink, window, depth,
+                              tree_k, windowed, req_to_token, req_pool_idx, rtt_stride, ring_base,
+                              table, stride, lens, n_new) == cudaSuccess
                ? WMTP_OK
                : WMTP_ECUDA;
 }

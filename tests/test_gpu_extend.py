@@ -1,0 +1,103 @@
+"""GPU parity of the draft-extend pass (union index table + extend attention)
+against the oracle: the table bit-exact, each token's attention within
+2e-3 abs + 1e-2 rel of the fp64 attention over its own draft-step table."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_draft_build_gb300 as wm
+from speculative_decoding_draft_build_gb300 import synth
+from wmtp_testutil import assert_attn_close, bits, host_i32
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    wm.build()
+    wm.load()
+    wm.device_error(clear=True)
+    yield
+    assert wm.device_error(clear=True) == 0
+
+
+def _case(S_list, n_list, n_sink, W, D, H_q, H_kv, windowed, ring, seed, n_q=None, splits=(None,)):
+    B = len(S_list)
+    n_q = n_q or max(max(n_list), 1)
+    scale = 1 / math.sqrt(D)
+    d = 7
+    seq = torch.tensor(S_list, dtype=torch.int32, device=DEV)
+    nn = torch.tensor(n_list, dtype=torch.int32, device=DEV)
+    if ring:
+        R = n_sink + W + d
+        rb_list = synth.ring_bases(B, R, B + 1, seed)
+        rb = torch.tensor(rb_list, dtype=torch.int32, device=DEV)
+        num_slots = (B + 1) * R
+        kw = dict(ring_base=rb)
+        okw = dict(ring_base=np.array(rb_list, np.int32))
+    else:
+        ctx = max(S + n for S, n in zip(S_list, n_list)) + 1
+        num_slots = B * ctx
+        rtt = synth.permutation(num_slots, seed, DEV).view(B, ctx)
+        kw = dict(req_to_token=rtt)
+        okw = dict(req_to_token=host_i32(rtt))
+    kp = synth.normal_bf16((num_slots, H_kv, D), seed + 1, DEV)
+    vp = synth.normal_bf16((num_slots, H_kv, D), seed + 2, DEV)
+    q = synth.normal_bf16((B, n_q, H_q, D), seed + 3, DEV)
+    stride = None if windowed else (None if not ring else max(S + n for S, n in zip(S_list, n_list)) + 1)
+    tab, ln = wm.build_extend_indices(seq, nn, n_sink, W, d, windowed=windowed, stride=stride, **kw)
+    otab, oln = oracle.build_extend_indices(np.array(S_list, np.int32), np.array(n_list, np.int32),
+                                            n_sink, W, d, windowed=windowed, **okw)
+    assert np.array_equal(host_i32(ln), oln)
+    for b in range(B):
+        assert np.array_equal(host_i32(tab[b, :ln[b]]), otab[b, :oln[b]]), f"table row {b}"
+    ro, rl = oracle.draft_extend_attn(bits(q), bits(kp), bits(vp), np.array(S_list, np.int32),
+                                      np.array(n_list, np.int32), n_sink, W, scale, windowed=windowed,
+                                      depth=d, **okw)
+    for n_split in splits:
+        out, lse = wm.draft_extend_attn(q, kp, vp, tab, ln, seq, nn, n_sink, W, scale, windowed=windowed,
+                                        n_split=n_split)
+        assert_attn_close(out, lse, ro, rl, what=f"extend S={S_list} n={n_list} split={n_split}")
+        for b, n in enumerate(n_list):
+            assert torch.all(out[b, n:] == 0) and torch.all(torch.isneginf(lse[b, n:]))
+
+
+@pytest.mark.parametrize("ring", [False, True])
+@pytest.mark.parametrize("windowed", [True, False])
+def test_extend_ragged_batch(ring, windowed):
+    # n_sink=64, W=1024: requests inside the sinks, below / across / above the
+    # window threshold, and long; ragged counts incl. 0 and 7
+    S_list = [10, 1080, 1087, 1090, 5000, 40_000]
+    n_list = [3, 7, 2, 0, 5, 1]
+    if not windowed and ring:
+        S_list = [10, 300, 900]   # a full-context ring table only holds a short context
+        n_list = [3, 7, 1]
+    _case(S_list, n_list, 64, 1024, 128, 8, 2, windowed, ring, 300 + 10 * ring + windowed,
+          splits=(1, 3, 16, 32, 37, None))
+
+
+@pytest.mark.parametrize("D,H_q,H_kv", [(256, 16, 2), (128, 4, 1)])
+def test_extend_shapes_and_small_windows(D, H_q, H_kv):
+    _case([0, 4, 9, 25, 300], [7, 5, 7, 4, 6], 4, 9, D, H_q, H_kv, True, False, 400 + D,
+          n_q=8, splits=(1, 2, 7, None))
+
+
+def test_extend_one_token_equals_decode_step():
+    D, H_q, H_kv, n_sink, W = 256, 16, 2, 64, 4032
+    S = 50_000
+    seq = torch.tensor([S], dtype=torch.int32, device=DEV)
+    nn = torch.tensor([1], dtype=torch.int32, device=DEV)
+    rtt = synth.permutation(S + 8, 501, DEV).view(1, -1)
+    kp = synth.normal_bf16((S + 8, H_kv, D), 502, DEV)
+    vp = synth.normal_bf16((S + 8, H_kv, D), 503, DEV)
+    q = synth.normal_bf16((1, 1, H_q, D), 504, DEV)
+    tab, ln = wm.build_extend_indices(seq, nn, n_sink, W, 7, req_to_token=rtt)
+    dt, dl = wm.build_draft_indices(seq, 1, n_sink, W, 7, req_to_token=rtt)
+    assert torch.equal(tab[0, :ln[0]], dt[0, 0, :dl[0, 0]])
+    a = wm.draft_extend_attn(q, kp, vp, tab, ln, seq, nn, n_sink, W, 1 / 16, n_split=16)
+    b = wm.draft_decode_attn(q, kp, vp, dt[0], dl[0], 1 / 16, n_split=16)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
