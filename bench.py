@@ -488,9 +488,61 @@ def run_ours(args, dist_ctx):
     result["e2e"] = measure_e2e(w, args, dev)
     if args.workload == "1m" and not args.no_tree:
         result["tree"] = measure_tree(args, dev)
+    if args.workload == "1m" and not args.no_extend:
+        result["extend"] = measure_extend(w, args, dev)
     if dist_ctx.rank == 0 and dist_ctx.world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args)
     return result
+
+
+def measure_extend(w, args, dev):
+    """Draft-extend pass on the million-token workload: the draft forward over
+    n_new = 5 accepted tokens (positions S..S+4) in one launch, windowed and
+    full-context.  Event-timed with L2 flushed before each launch; algorithmic
+    bytes count each token's own key set (K and V of every KV head), the union
+    table, q, out and lse."""
+    import speculative_decoding_draft_build_gb300 as wm
+    c = w.cfg
+    B, S, H_q, H_kv, D = c["B"], c["S"], c["H_q"], c["H_kv"], c["D"]
+    n = 5
+    seq = torch.full((B,), S, dtype=torch.int32, device=dev)
+    nn = torch.full((B,), n, dtype=torch.int32, device=dev)
+    q = w.q[:n].permute(1, 0, 2, 3, 4).reshape(B, n, H_q, D).contiguous()
+    out = torch.empty((B, n, H_q, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, n, H_q), dtype=torch.float32, device=dev)
+    peak, _ = hbm_peak()
+    reps = max(5, min(args.steps, 30))
+    res = {"n_new": n, "B": B, "S": S,
+           "timing": "CUDA events per launch, L2 flushed before each, median"}
+    for windowed in (True, False):
+        tab, ln = wm.build_extend_indices(seq, nn, c["n_sink"], c["W"], c["gamma"] + 1,
+                                          windowed=windowed, req_to_token=w.rtt)
+        ns = wm.attn_num_splits(B, n, H_kv, tab.shape[-1], dev)
+        ws = wm.AttnWorkspace(wm.attn_workspace_bytes(B, n, H_q, H_kv, D, ns), dev)
+
+        def call():
+            wm.draft_extend_attn(q, w.kp, w.vp, tab, ln, seq, nn, c["n_sink"], c["W"], w.scale,
+                                 windowed=windowed, out=out, lse=lse, n_split=ns, workspace=ws)
+        for _ in range(3):
+            call()
+        ts = []
+        for _ in range(reps):
+            w.flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            call()
+            b.record()
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b) * 1e-3)
+        t = statistics.median(ts)
+        keys = sum(min(S + j + 1, c["n_sink"] + c["W"]) if windowed else S + j + 1 for j in range(n))
+        L = int(ln.max().item())
+        nbytes = B * (keys * H_kv * D * 2 * 2 + 4 * L + n * H_q * (D * 2 + (D + 1) * 4))
+        res["windowed" if windowed else "full"] = {
+            "us_per_pass": round(t * 1e6, 2), "kv_gbs": round(nbytes / t / 1e9, 1),
+            "frac_of_hbm": round(nbytes / t / 1e9 / peak, 4), "n_split": ns,
+            "union_keys": L, "bytes_per_pass": int(nbytes)}
+    return res
 
 
 def measure_tree(args, dev):
@@ -702,6 +754,7 @@ def main(argv=None):
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="1m")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-tree", action="store_true", help="skip the tree-drafter measurement")
+    p.add_argument("--no-extend", action="store_true", help="skip the draft-extend measurement")
     p.add_argument("--tree-only", action="store_true",
                    help="run only the tree-drafter measurement (a profiling driver; prints the tree object)")
     p.add_argument("--tree-w", type=int, action="append",
