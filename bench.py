@@ -486,6 +486,7 @@ def run_ours(args, dist_ctx):
     }
 
     result["e2e"] = measure_e2e(w, args, dev)
+    result["mass_diagnostics"] = measure_mass(w, dev)
     if args.workload == "1m" and not args.no_tree:
         result["tree"] = measure_tree(args, dev)
     if args.workload == "1m" and not args.no_extend:
@@ -493,6 +494,30 @@ def run_ours(args, dist_ctx):
     if dist_ctx.rank == 0 and dist_ctx.world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args)
     return result
+
+
+def measure_mass(w, dev):
+    """Attention-mass diagnostics (in-window mass, win_perturb, tail out-frac;
+    App. C, Table 12) of the step's six draft queries, from the full-context
+    and windowed attention outputs the two arms just computed: one launch over
+    all query rows, event-timed (median of 20)."""
+    import speculative_decoding_draft_build_gb300 as wm
+    args = (w.out_full, w.lse_full, w.out_win, w.lse_win)
+    for _ in range(3):
+        res = wm.attn_mass_diagnostics(*args)
+    ts = []
+    for _ in range(20):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        res = wm.attn_mass_diagnostics(*args)
+        b.record()
+        torch.cuda.synchronize(dev)
+        ts.append(a.elapsed_time(b) * 1e3)
+    in_win, perturb, tail = (r.double().mean().item() for r in res)
+    return {"us_per_launch": round(statistics.median(ts), 2), "rows": int(w.lse_full.numel()),
+            "mean_in_win": round(in_win, 6), "mean_win_perturb": round(perturb, 6),
+            "mean_tail_out_frac": round(tail, 6),
+            "note": "synthetic N(0,1) keys and values; the pages measure these on model activations"}
 
 
 def measure_extend(w, args, dev):

@@ -281,6 +281,30 @@ wmtp_status wmtp_draft_extend_attn(const uint16_t *q, int32_t B, int32_t n_q,
                                    size_t workspace_bytes, int32_t n_split,
                                    void *stream);
 
+/* Attention-mass diagnostics of the windowed draft ("Windowed-MTP", §5 "A
+ * partition-function view"; App. C, Table 12), per query row, from the
+ * full-context and the windowed attention of the same query (o and lse of
+ * wmtp_draft_decode_attn over the full and the sink + window table):
+ *   in_win[r]        = Z_w / Z = exp(lse_win - lse_full): softmax mass inside
+ *                      the kept set (1 - Z_far / Z);
+ *   win_perturb[r]   = ||o_full - o_win|| / ||o_full||;
+ *   tail_out_frac[r] = ||o_full - in_win * o_win|| / ||o_full||, the share
+ *                      of ||o|| from far keys (o_full = in_win * o_win +
+ *                      sum over far keys of p_k v_k).
+ * An empty kept set gives in_win = 0; ||o_full|| = 0 gives 0 ratios.
+ *
+ * o_full, o_win  device fp32 [rows][D]; lse_full, lse_win device fp32 [rows]
+ *                (natural log, as wmtp_draft_decode_attn writes them).
+ * in_win, win_perturb, tail_out_frac  device fp32 [rows]; any may be NULL,
+ *                not all three.
+ * Errors: WMTP_EINVAL for rows < 0, D < 1 or null inputs. */
+wmtp_status wmtp_attn_mass_diagnostics(const float *o_full,
+                                       const float *lse_full,
+                                       const float *o_win, const float *lse_win,
+                                       int64_t rows, int32_t D, float *in_win,
+                                       float *win_perturb,
+                                       float *tail_out_frac, void *stream);
+
 /* ------------------------------------------------------------------------
  * Tree-draft attention over the ring.
  * "Windowed-MTP" §7 "Compatibility with tree speculation": windowing changes

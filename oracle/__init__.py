@@ -12,6 +12,7 @@ from .oracle import (  # noqa: F401
     ORC_OK,
     acceptance_length,
     append_kv,
+    attn_mass,
     build,
     build_draft_indices,
     build_extend_indices,

@@ -332,3 +332,48 @@ def draft_extend_attn(q, k_pool, v_pool, seq_lens, n_new, n_sink, window,
             out[b, t] = o[0, 0]
             lse[b, t] = l[0, 0]
     return out, lse
+
+
+# ------------------------------------------------- attention-mass diagnostics
+def attn_mass(q, k_pool, v_pool, table_full, len_full, table_win, len_win, scale):
+    """App. C, Table 12 quantities for every query row, straight from their
+    definitions in fp64: logits z over the full table row, the kept set =
+    the slots of the windowed row; in_win = sum_kept e^z / sum_all e^z,
+    win_perturb = ||o_full - o_win|| / ||o_full|| with o_win the softmax
+    read-out over the kept keys alone, tail_out_frac = ||sum_far p v|| /
+    ||o_full|| with p the full softmax.  Plain numpy (test sizes).
+
+    q: [B, n_q, H_q, D] bf16 bits; tables [B, stride].  Returns three float64
+    arrays [B, n_q, H_q]."""
+    q = _as(q, np.uint16)
+    kp = _as(k_pool, np.uint16)
+    vp = _as(v_pool, np.uint16)
+    tf, lf = _as(table_full, np.int32), _as(len_full, np.int32)
+    tw, lw = _as(table_win, np.int32), _as(len_win, np.int32)
+    B, n_q, H_q, D = q.shape
+    H_kv = kp.shape[1]
+    G = H_q // H_kv
+
+    def f64(u):
+        return (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+    res = np.zeros((3, B, n_q, H_q), dtype=np.float64)
+    for b in range(B):
+        slots = tf[b, :lf[b]]
+        kept = np.isin(slots, tw[b, :lw[b]])
+        for h in range(H_q):
+            g = h // G
+            K = f64(kp[slots, g])
+            V = f64(vp[slots, g])
+            for t in range(n_q):
+                z = scale * (K @ f64(q[b, t, h]))
+                e = np.exp(z - z.max()) if z.size else z
+                Z, Zw = e.sum(), e[kept].sum()
+                o_full = (e[:, None] * V).sum(0) / Z if Z > 0 else np.zeros(D)
+                o_win = (e[kept][:, None] * V[kept]).sum(0) / Zw if Zw > 0 else np.zeros(D)
+                o_far = (e[~kept][:, None] * V[~kept]).sum(0) / Z if Z > 0 else np.zeros(D)
+                nf = np.linalg.norm(o_full)
+                res[0, b, t, h] = Zw / Z if Z > 0 else 0.0
+                res[1, b, t, h] = np.linalg.norm(o_full - o_win) / nf if nf > 0 else 0.0
+                res[2, b, t, h] = np.linalg.norm(o_far) / nf if nf > 0 else 0.0
+    return res[0], res[1], res[2]

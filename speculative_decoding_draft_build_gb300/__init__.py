@@ -15,6 +15,7 @@ Calls (same names as the C ABI without the ``wmtp_`` prefix):
   draft_decode_attn_append  append_kv + draft_decode_attn in one launch
   build_extend_indices / draft_extend_attn  the draft forward over a request's
                        accepted tokens in one launch (each token its own keys)
+  attn_mass_diagnostics  in-window mass, win_perturb, tail out-frac per query
   tree_draft_attn      tree-draft attention over the ring (tree-causal mask)
 """
 from __future__ import annotations
@@ -30,7 +31,7 @@ from . import _build
 __all__ = [
     "WmtpError", "load", "build", "version", "device_error",
     "build_draft_indices", "build_extend_indices", "ring_map", "append_kv", "draft_decode_attn",
-    "draft_decode_attn_append", "draft_extend_attn",
+    "draft_decode_attn_append", "draft_extend_attn", "attn_mass_diagnostics",
     "attn_workspace_bytes", "attn_num_splits", "AttnWorkspace", "draft_decode_attn_noalloc",
     "tree_draft_attn", "tree_workspace_bytes", "tree_num_splits",
 ]
@@ -92,6 +93,8 @@ def load():
         lib.wmtp_draft_extend_attn.argtypes = [
             _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32,
             _i32, ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
+        lib.wmtp_attn_mass_diagnostics.restype = _i32
+        lib.wmtp_attn_mass_diagnostics.argtypes = [_vp, _vp, _vp, _vp, _i64, _i32, _vp, _vp, _vp, _vp]
         lib.wmtp_ring_map.restype = _i32
         lib.wmtp_ring_map.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]
         lib.wmtp_append_kv.restype = _i32
@@ -449,6 +452,26 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
             stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf),
             workspace.nbytes, n_split, _stream(stream)), "draft_decode_attn_append")
     return out, lse
+
+
+def attn_mass_diagnostics(o_full: torch.Tensor, lse_full: torch.Tensor, o_win: torch.Tensor,
+                          lse_win: torch.Tensor, stream=None):
+    """Per query row: (in_win, win_perturb, tail_out_frac) from the full and
+    windowed attention of the same queries (``wmtp_attn_mass_diagnostics``).
+    o_*: [..., D] fp32; lse_*: [...] fp32.  Returns three fp32 tensors shaped
+    like lse_full."""
+    for t, nm in ((o_full, "o_full"), (lse_full, "lse_full"), (o_win, "o_win"), (lse_win, "lse_win")):
+        _need(t, nm, torch.float32, o_full.device)
+    D = o_full.shape[-1]
+    rows = lse_full.numel()
+    if o_full.numel() != rows * D or o_win.numel() != rows * D or lse_win.numel() != rows:
+        raise ValueError("attn_mass_diagnostics: shape mismatch")
+    res = [torch.empty_like(lse_full) for _ in range(3)]
+    with torch.cuda.device(o_full.device):
+        _check(load().wmtp_attn_mass_diagnostics(
+            _ptr(o_full), _ptr(lse_full), _ptr(o_win), _ptr(lse_win), rows, D, _ptr(res[0]),
+            _ptr(res[1]), _ptr(res[2]), _stream(stream)), "attn_mass_diagnostics")
+    return tuple(res)
 
 
 def draft_decode_attn_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
