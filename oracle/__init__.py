@@ -12,12 +12,17 @@ from .oracle import (  # noqa: F401
     ORC_OK,
     acceptance_length,
     append_kv,
+    append_kv_fp8,
     attn_mass,
     build,
     build_draft_indices,
     build_extend_indices,
     draft_decode_attn,
+    draft_decode_attn_fp8,
     draft_extend_attn,
+    e4m3_table,
+    e4m3_to_f64,
+    f32_to_e4m3,
     keep,
     num_threads,
     ring_map,

@@ -29,6 +29,8 @@ _i32p = ctypes.POINTER(ctypes.c_int32)
 _i64p = ctypes.POINTER(ctypes.c_int64)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _f64p = ctypes.POINTER(ctypes.c_double)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 _i64 = ctypes.c_int64
 
 
@@ -81,6 +83,18 @@ def _load():
             _u16p, _i64, _i64, _i64, _i64, _u16p, _u16p, _i64, _i32p, _i32p,
             _i64, _i64, _i64, _i64, ctypes.c_double, _i64p, _i64, _f64p,
             _f64p, ctypes.c_int]
+        lib.orc_e4m3_to_f64.restype = ctypes.c_double
+        lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.orc_f32_to_e4m3.restype = ctypes.c_uint8
+        lib.orc_f32_to_e4m3.argtypes = [ctypes.c_float]
+        lib.orc_append_kv_fp8.restype = ctypes.c_int
+        lib.orc_append_kv_fp8.argtypes = [_u16p, _u16p, _i32p, _i64, _i64, _i64,
+                                          _f32p, _f32p, _u8p, _u8p, _i64]
+        lib.orc_draft_decode_attn_fp8.restype = ctypes.c_int
+        lib.orc_draft_decode_attn_fp8.argtypes = [
+            _u16p, _i64, _i64, _i64, _i64, _i64, _u8p, _u8p, _f32p, _f32p, _i64,
+            _i32p, _i64, _i32p, ctypes.c_double, _i64p, _i64, _f64p, _f64p, _f64p,
+            _i64, ctypes.c_int]
         lib.orc_acceptance_length.restype = ctypes.c_double
         lib.orc_acceptance_length.argtypes = [_f64p, _i64, _f64p]
         _lib = lib
@@ -377,3 +391,73 @@ def attn_mass(q, k_pool, v_pool, table_full, len_full, table_win, len_win, scale
                 res[1, b, t, h] = np.linalg.norm(o_full - o_win) / nf if nf > 0 else 0.0
                 res[2, b, t, h] = np.linalg.norm(o_far) / nf if nf > 0 else 0.0
     return res[0], res[1], res[2]
+
+
+# --- fp8 (E4M3) KV with per-KV-head scales ([WMTP] §6, "Robustness to
+# KV-cache quantization"; reading R13) ---
+
+def e4m3_to_f64(code: int) -> float:
+    """Value of one OCP FP8 E4M3 code (bias 7, subnormals m * 2^-9, no inf)."""
+    return float(_load().orc_e4m3_to_f64(int(code) & 0xFF))
+
+
+def f32_to_e4m3(x: float) -> int:
+    """Nearest E4M3 code to the fp32 value x, ties to even, saturating at 448."""
+    return int(_load().orc_f32_to_e4m3(float(np.float32(x))))
+
+
+def e4m3_table() -> np.ndarray:
+    """float64[256]: the value of every code (NaN for 0x7F and 0xFF)."""
+    return np.array([e4m3_to_f64(c) for c in range(256)], dtype=np.float64)
+
+
+def append_kv_fp8(k_new, v_new, slots, k_scale, v_scale, k_pool, v_pool) -> None:
+    """Quantise each new token's bf16 K/V rows to E4M3 codes,
+    code = E4M3(fp32(x) * fp32(1 / scale[h])), into pool slot ``slots[i]``
+    (uint8 pools [num_slots, H_kv, D], in place)."""
+    kn = _as(k_new, np.uint16)
+    vn = _as(v_new, np.uint16)
+    sl = _as(slots, np.int32)
+    ks = _as(k_scale, np.float32)
+    vs = _as(v_scale, np.float32)
+    assert k_pool.dtype == np.uint8 and k_pool.flags["C_CONTIGUOUS"]
+    assert v_pool.dtype == np.uint8 and v_pool.flags["C_CONTIGUOUS"]
+    n, H_kv, D = kn.shape
+    assert ks.shape == (H_kv,) and vs.shape == (H_kv,)
+    _check(_load().orc_append_kv_fp8(_ptr(kn, ctypes.c_uint16), _ptr(vn, ctypes.c_uint16),
+                                     _ptr(sl, ctypes.c_int32), n, H_kv, D,
+                                     _ptr(ks, ctypes.c_float), _ptr(vs, ctypes.c_float),
+                                     _ptr(k_pool, ctypes.c_uint8),
+                                     _ptr(v_pool, ctypes.c_uint8), k_pool.shape[0]),
+           "append_kv_fp8")
+
+
+def draft_decode_attn_fp8(q, k_pool, v_pool, k_scale, v_scale, table, lens, scale,
+                          rows=None, nthreads=None):
+    """fp64 softmax attention over E4M3 pools: key i of KV head g is
+    code * k_scale[g], its value code * v_scale[g]; otherwise as
+    ``draft_decode_attn``."""
+    q = _as(q, np.uint16)
+    kp = _as(k_pool, np.uint8)
+    vp = _as(v_pool, np.uint8)
+    ks = _as(k_scale, np.float32)
+    vs = _as(v_scale, np.float32)
+    tb = _as(table, np.int32)
+    ln = _as(lens, np.int32)
+    B, n_q, H_q, D = q.shape
+    num_slots, H_kv, _ = kp.shape
+    rws = _as(rows, np.int64)
+    nthreads = nthreads or num_threads()
+    out = np.full((B, n_q, H_q, D), np.nan, dtype=np.float64)
+    lse = np.full((B, n_q, H_q), np.nan, dtype=np.float64)
+    scratch_len = max(int(ln.max()) if ln.size else 0, 1)
+    scratch = np.empty(scratch_len * nthreads, dtype=np.float64)
+    _check(_load().orc_draft_decode_attn_fp8(
+        _ptr(q, ctypes.c_uint16), B, n_q, H_q, H_kv, D, _ptr(kp, ctypes.c_uint8),
+        _ptr(vp, ctypes.c_uint8), _ptr(ks, ctypes.c_float), _ptr(vs, ctypes.c_float),
+        num_slots, _ptr(tb, ctypes.c_int32), tb.shape[-1], _ptr(ln, ctypes.c_int32),
+        float(scale), _ptr(rws, ctypes.c_int64), 0 if rws is None else rws.shape[0],
+        _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double),
+        _ptr(scratch, ctypes.c_double), scratch_len, nthreads),
+        "draft_decode_attn_fp8")
+    return out, lse

@@ -368,3 +368,145 @@ double orc_acceptance_length(const double *H, int64_t gamma, double *alpha) {
     }
     return al;
 }
+
+/* ------------------------------------------------------------------------ */
+/* fp8 KV.  [WMTP] §6, "Robustness to KV-cache quantization": windowing
+ * composes with an fp8 KV cache (the saving scales with bytes per entry), and
+ * the pages' own fp8-KV path has no fused attention kernel; the checkpoints
+ * ship per-layer fp8 KV scales.  Reading R13: K and V rows are stored
+ * as OCP FP8 E4M3 codes with one fp32 scale per KV head; the stored value is
+ * code_value * scale, and a new row is quantised as
+ *   code = E4M3_RNE_satfinite( (float)x * (1.0f / scale) )
+ * in fp32 arithmetic (the integer decision in the same precision as the
+ * kernel).  E4M3: sign bit 7, exponent bits 6..3 with bias 7, mantissa bits
+ * 2..0; exponent 0 encodes subnormals m * 2^-9; S.1111.111 is NaN (no
+ * infinities); the largest finite magnitude is 1.75 * 2^8 = 448. */
+double orc_e4m3_to_f64(uint8_t c) {
+    int sign = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 code to x, ties to the even code; finite magnitudes beyond
+ * 448 (and infinities) saturate to 448; NaN gives 0x7F.  Plain search over
+ * the 127 non-negative finite codes, compared in fp64 (exact). */
+uint8_t orc_f32_to_e4m3(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    int best = 0;
+    double best_d = a;  /* distance to code 0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        double d = fabs(orc_e4m3_to_f64((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* Quantising append: each new token's K and V rows (bf16) become E4M3 codes
+ * with the per-KV-head scales (reading R13), written to pool slot slots[i]. */
+int orc_append_kv_fp8(const uint16_t *k_new, const uint16_t *v_new,
+                      const int32_t *slots, int64_t n, int64_t H_kv, int64_t D,
+                      const float *k_scale, const float *v_scale,
+                      uint8_t *k_pool, uint8_t *v_pool, int64_t num_slots) {
+    for (int64_t i = 0; i < n; ++i) {
+        if (slots[i] < 0 || slots[i] >= num_slots) return ORC_EBOUNDS;
+        for (int64_t g = 0; g < H_kv; ++g) {
+            float ik = 1.0f / k_scale[g], iv = 1.0f / v_scale[g];
+            for (int64_t d = 0; d < D; ++d) {
+                int64_t e = g * D + d;
+                float kx = (float)bf16_to_f64(k_new[i * H_kv * D + e]);
+                float vx = (float)bf16_to_f64(v_new[i * H_kv * D + e]);
+                float ky = kx * ik, vy = vx * iv;
+                k_pool[(int64_t)slots[i] * H_kv * D + e] = orc_f32_to_e4m3(ky);
+                v_pool[(int64_t)slots[i] * H_kv * D + e] = orc_f32_to_e4m3(vy);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* attend_one over an fp8 pool: k_i = code * k_scale, v_i = code * v_scale
+ * (fp64), otherwise the same definition. */
+static int attend_one_fp8(const uint16_t *q, const uint8_t *k_pool,
+                          const uint8_t *v_pool, int64_t num_slots, int64_t H_kv,
+                          int64_t g, int64_t D, const int32_t *slots, int64_t L,
+                          double scale, double k_scale, double v_scale,
+                          double *s_buf, double *out, double *lse) {
+    for (int64_t d = 0; d < D; ++d) out[d] = 0.0;
+    if (L == 0) {
+        *lse = -INFINITY;
+        return ORC_OK;
+    }
+    double m = -INFINITY;
+    for (int64_t i = 0; i < L; ++i) {
+        int64_t slot = slots[i];
+        if (slot < 0 || slot >= num_slots) return ORC_EBOUNDS;
+        const uint8_t *k = k_pool + (slot * H_kv + g) * D;
+        double dot = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+            dot += bf16_to_f64(q[d]) * (orc_e4m3_to_f64(k[d]) * k_scale);
+        s_buf[i] = scale * dot;
+        if (s_buf[i] > m) m = s_buf[i];
+    }
+    double z = 0.0;
+    for (int64_t i = 0; i < L; ++i) {
+        double w = exp(s_buf[i] - m);
+        const uint8_t *v = v_pool + ((int64_t)slots[i] * H_kv + g) * D;
+        for (int64_t d = 0; d < D; ++d) out[d] += w * (orc_e4m3_to_f64(v[d]) * v_scale);
+        z += w;
+    }
+    for (int64_t d = 0; d < D; ++d) out[d] /= z;
+    *lse = m + log(z);
+    return ORC_OK;
+}
+
+/* orc_draft_decode_attn over fp8 pools with per-KV-head scales. */
+int orc_draft_decode_attn_fp8(const uint16_t *q, int64_t B, int64_t n_q,
+                              int64_t H_q, int64_t H_kv, int64_t D,
+                              const uint8_t *k_pool, const uint8_t *v_pool,
+                              const float *k_scale, const float *v_scale,
+                              int64_t num_slots, const int32_t *table,
+                              int64_t stride, const int32_t *lens, double scale,
+                              const int64_t *rows, int64_t n_rows, double *out,
+                              double *lse, double *s_scratch, int64_t scratch_len,
+                              int nthreads) {
+    if (H_kv < 1 || H_q % H_kv != 0 || D < 1) return ORC_EINVAL;
+    int64_t G = H_q / H_kv;
+    int64_t total = rows ? n_rows : B * n_q * H_q;
+    int status = ORC_OK;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1)
+#endif
+    for (int64_t r = 0; r < total; ++r) {
+        int tid = 0;
+#ifdef _OPENMP
+        tid = omp_get_thread_num();
+#endif
+        int64_t row = rows ? rows[r] : r;
+        int64_t h = row % H_q;
+        int64_t bt = row / H_q;
+        int64_t b = bt / n_q;
+        int64_t L = lens[b];
+        if (L > scratch_len || L > stride) {
+            status = ORC_ECAPACITY;
+            continue;
+        }
+        int64_t g = h / G;
+        int st = attend_one_fp8(q + row * D, k_pool, v_pool, num_slots, H_kv, g, D,
+                                table + b * stride, L, scale, (double)k_scale[g],
+                                (double)v_scale[g],
+                                s_scratch + (int64_t)tid * scratch_len,
+                                out + row * D, lse + row);
+        if (st != ORC_OK) status = st;
+    }
+    return status;
+}
