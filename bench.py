@@ -491,6 +491,8 @@ def run_ours(args, dist_ctx):
         result["tree"] = measure_tree(args, dev)
     if args.workload == "1m" and not args.no_extend:
         result["extend"] = measure_extend(w, args, dev)
+    if args.workload == "1m" and not args.no_fp8:
+        result["fp8"] = measure_fp8(w, args, dev)
     if dist_ctx.rank == 0 and dist_ctx.world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args)
     return result
@@ -567,6 +569,68 @@ def measure_extend(w, args, dev):
             "us_per_pass": round(t * 1e6, 2), "kv_gbs": round(nbytes / t / 1e9, 1),
             "frac_of_hbm": round(nbytes / t / 1e9 / peak, 4), "n_split": ns,
             "union_keys": L, "bytes_per_pass": int(nbytes)}
+    return res
+
+
+def measure_fp8(w, args, dev):
+    """fp8 (E4M3) KV on the million-token workload ([WMTP] §6, "Robustness to
+    KV-cache quantization"): the bf16 pools quantised once with per-KV-head
+    scales (amax / 448), then for each of the 6 draft steps the quantising
+    append of the step's K/V and the attention, full-context and windowed.
+    Each launch event-timed with L2 flushed before it; algorithmic bytes are
+    one byte per K/V element plus the table, q, out and lse."""
+    import speculative_decoding_draft_build_gb300 as wm
+    c = w.cfg
+    B, S, H_q, H_kv, D, g = c["B"], c["S"], c["H_q"], c["H_kv"], c["D"], c["gamma"]
+    n_slots = w.kp.shape[0]
+    ks = (w.kp.abs().amax(dim=(0, 2)).float() / 448).contiguous()
+    vs = (w.vp.abs().amax(dim=(0, 2)).float() / 448).contiguous()
+    kp8 = torch.empty((n_slots, H_kv, D), dtype=torch.uint8, device=dev)
+    vp8 = torch.empty_like(kp8)
+    all_slots = torch.arange(n_slots, dtype=torch.int32, device=dev)
+    wm.append_kv_fp8(w.kp, w.vp, all_slots, ks, vs, kp8, vp8)
+    peak, _ = hbm_peak()
+    reps = max(3, min(args.steps, 10))
+    res = {"k_scale": [round(x, 6) for x in ks.tolist()], "v_scale": [round(x, 6) for x in vs.tolist()],
+           "timing": "CUDA events per launch, L2 flushed before each, median over steps x reps"}
+    for name, tab, ln, stride in (("full", w.tab_full, w.len_full, w.full_stride),
+                                  ("windowed", w.tab_win, w.len_win, w.win_stride)):
+        ns = wm.attn_num_splits(B, 1, H_kv, stride, dev)
+        ws = wm.AttnWorkspace(wm.attn_workspace_bytes(B, 1, H_q, H_kv, D, ns), dev)
+        out = torch.empty((B, 1, H_q, D), dtype=torch.float32, device=dev)
+        lse = torch.empty((B, 1, H_q), dtype=torch.float32, device=dev)
+
+        def attn(j):
+            wm.draft_decode_attn_fp8(w.q[j], kp8, vp8, ks, vs, tab[j], ln[j], w.scale, out=out, lse=lse,
+                                     n_split=ns, workspace=ws)
+
+        def append(j):
+            wm.append_kv_fp8(w.kn[j], w.vn[j], w.slots[j], ks, vs, kp8, vp8)
+        for j in range(g):
+            append(j)
+            attn(j)
+        t_attn, t_app, gbs = [], [], []
+        for _ in range(reps):
+            for j in range(g):
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                w.flush.zero_()
+                ev[0].record()
+                append(j)
+                ev[1].record()
+                attn(j)
+                ev[2].record()
+                torch.cuda.synchronize(dev)
+                ta = ev[1].elapsed_time(ev[2]) * 1e-3
+                L = min(S + j + 1, c["n_sink"] + c["W"]) if name == "windowed" else S + j + 1
+                nbytes = B * (L * H_kv * D * 2 + 4 * L + H_q * D * 2 + H_q * (D + 1) * 4)
+                t_attn.append(ta)
+                t_app.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+                gbs.append(nbytes / ta / 1e9)
+        res[name] = {"attn_us_per_launch": round(statistics.median(t_attn) * 1e6, 2),
+                     "append_us_per_launch": round(statistics.median(t_app) * 1e6, 2),
+                     "kv_gbs": round(statistics.median(gbs), 1),
+                     "frac_of_hbm": round(statistics.median(gbs) / peak, 4), "n_split": ns}
+    del kp8, vp8
     return res
 
 
@@ -780,6 +844,7 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-tree", action="store_true", help="skip the tree-drafter measurement")
     p.add_argument("--no-extend", action="store_true", help="skip the draft-extend measurement")
+    p.add_argument("--no-fp8", action="store_true", help="skip the fp8-KV measurement")
     p.add_argument("--tree-only", action="store_true",
                    help="run only the tree-drafter measurement (a profiling driver; prints the tree object)")
     p.add_argument("--tree-w", type=int, action="append",

@@ -384,6 +384,50 @@ wmtp_status wmtp_draft_decode_attn_noalloc(
     const int32_t *lens, float scale, float *out, float *lse, int32_t n_split,
     void *stream);
 
+/* ------------------------------------------------------------------------
+ * fp8 KV ("Windowed-MTP", §6 "Robustness to KV-cache quantization": the
+ * window bounds the number of KV entries read, so its saving composes with a
+ * lower-precision cache, whose bytes per entry it does not change; the
+ * pages' own fp8-KV path has no fused attention kernel).  The pools hold
+ * OCP FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 fraction bits;
+ * largest finite 448; no infinities) in the layout [num_slots][H_kv][D],
+ * one byte per element, and each KV head g has one fp32 scale for K and one
+ * for V: element = code * scale[g].  Codes 0x7F / 0xFF (NaN) are never
+ * written by wmtp_append_kv_fp8; the attention reads them as NaN. */
+
+/* Quantising append: for token i < n, KV head g and element e,
+ *   k_pool[slots[i]][g][e] = E4M3_rn_satfinite(k_new[i][g][e] * (1 / k_scale[g]))
+ * (likewise v), the reciprocal and the product each rounded once in fp32,
+ * round to nearest even, finite values beyond +-448 saturating.
+ *
+ * k_new, v_new device bf16 [n][H_kv][D], 16-byte aligned; D % 16 == 0.
+ * k_scale, v_scale device fp32 [H_kv], positive and finite.
+ * k_pool, v_pool   device uint8 [num_slots][H_kv][D], 16-byte aligned.
+ * A slot outside [0, num_slots) is not written and latches
+ * WMTP_DEV_SLOT_RANGE. */
+wmtp_status wmtp_append_kv_fp8(const uint16_t *k_new, const uint16_t *v_new,
+                               const int32_t *slots, int32_t n, int32_t H_kv,
+                               int32_t D, const float *k_scale,
+                               const float *v_scale, uint8_t *k_pool,
+                               uint8_t *v_pool, int64_t num_slots,
+                               void *stream);
+
+/* wmtp_draft_decode_attn over E4M3 pools:
+ *   s_i = scale * <q[b,t,h,:], k_scale[g] * Kcode[table[b,i], g, :]>
+ *   out = sum_i softmax(s)_i * v_scale[g] * Vcode[table[b,i], g, :]
+ * Same arguments, workspace, split plan, merges and checks as
+ * wmtp_draft_decode_attn (wmtp_attn_workspace_bytes sizes the workspace),
+ * with uint8 pools and the per-KV-head scales k_scale, v_scale (device fp32
+ * [H_kv]).  The codes are widened exactly to fp16 on chip and q is rounded
+ * to fp16 (exact for |q| >= 2^-14), products accumulate in fp32. */
+wmtp_status wmtp_draft_decode_attn_fp8(
+    const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q, int32_t H_kv,
+    int32_t D, const uint8_t *k_pool, const uint8_t *v_pool,
+    const float *k_scale, const float *v_scale, int64_t num_slots,
+    const int32_t *table, int64_t table_stride, const int32_t *lens,
+    float scale, float *out, float *lse, void *workspace,
+    size_t workspace_bytes, int32_t n_split, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

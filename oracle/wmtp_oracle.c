@@ -398,10 +398,16 @@ uint8_t orc_f32_to_e4m3(float x) {
     uint8_t sign = signbit(x) ? 0x80 : 0;
     double a = fabs((double)x);
     if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    static double value[0x7F];
+    static int have_values = 0;
+    if (!have_values) {
+        for (int c = 0; c < 0x7F; ++c) value[c] = orc_e4m3_to_f64((uint8_t)c);
+        have_values = 1;
+    }
     int best = 0;
     double best_d = a;  /* distance to code 0 */
     for (int c = 1; c <= 0x7E; ++c) {
-        double d = fabs(orc_e4m3_to_f64((uint8_t)c) - a);
+        double d = fabs(value[c] - a);
         if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
             best = c;
             best_d = d;

@@ -16,6 +16,8 @@ Calls (same names as the C ABI without the ``wmtp_`` prefix):
   build_extend_indices / draft_extend_attn  the draft forward over a request's
                        accepted tokens in one launch (each token its own keys)
   attn_mass_diagnostics  in-window mass, win_perturb, tail out-frac per query
+  append_kv_fp8 / draft_decode_attn_fp8  the same over E4M3 KV pools with
+                       per-KV-head scales
   tree_draft_attn      tree-draft attention over the ring (tree-causal mask)
 """
 from __future__ import annotations
@@ -34,6 +36,7 @@ __all__ = [
     "draft_decode_attn_append", "draft_extend_attn", "attn_mass_diagnostics",
     "attn_workspace_bytes", "attn_num_splits", "AttnWorkspace", "draft_decode_attn_noalloc",
     "tree_draft_attn", "tree_workspace_bytes", "tree_num_splits",
+    "append_kv_fp8", "draft_decode_attn_fp8",
 ]
 
 WMTP_OK = 0
@@ -121,6 +124,13 @@ def load():
         lib.wmtp_tree_draft_attn.restype = _i32
         lib.wmtp_tree_draft_attn.argtypes = [
             _vp, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32,
+            ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
+        lib.wmtp_append_kv_fp8.restype = _i32
+        lib.wmtp_append_kv_fp8.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64,
+                                           _vp]
+        lib.wmtp_draft_decode_attn_fp8.restype = _i32
+        lib.wmtp_draft_decode_attn_fp8.argtypes = [
+            _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _i64, _vp,
             ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
         lib.wmtp_draft_decode_attn_noalloc.restype = _i32
         lib.wmtp_draft_decode_attn_noalloc.argtypes = [
@@ -301,6 +311,31 @@ def append_kv(k_new: torch.Tensor, v_new: torch.Tensor, slots: torch.Tensor,
                "append_kv")
 
 
+def append_kv_fp8(k_new: torch.Tensor, v_new: torch.Tensor, slots: torch.Tensor,
+                  k_scale: torch.Tensor, v_scale: torch.Tensor, k_pool: torch.Tensor,
+                  v_pool: torch.Tensor, stream=None) -> None:
+    """Quantise each new token's bf16 K/V rows to E4M3 codes with the per-KV-head
+    scales and write them to pool slot ``slots[i]`` (``wmtp_append_kv_fp8``).
+    k_new/v_new: [n, H_kv, D] bf16; k_scale/v_scale: [H_kv] fp32; pools:
+    [num_slots, H_kv, D] uint8."""
+    _need(k_pool, "k_pool", torch.uint8)
+    dev = k_pool.device
+    _need(v_pool, "v_pool", torch.uint8, dev)
+    for t, nm in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, nm, torch.bfloat16, dev)
+    for t, nm in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, nm, torch.float32, dev)
+    _need(slots, "slots", torch.int32, dev)
+    n, H_kv, D = k_new.shape
+    if (v_new.shape != k_new.shape or k_pool.shape[1:] != (H_kv, D) or v_pool.shape != k_pool.shape
+            or k_scale.numel() != H_kv or v_scale.numel() != H_kv or slots.numel() != n):
+        raise ValueError("append_kv_fp8: shape mismatch")
+    with torch.cuda.device(dev):
+        _check(load().wmtp_append_kv_fp8(_ptr(k_new), _ptr(v_new), _ptr(slots), n, H_kv, D,
+                                         _ptr(k_scale), _ptr(v_scale), _ptr(k_pool), _ptr(v_pool),
+                                         k_pool.shape[0], _stream(stream)), "append_kv_fp8")
+
+
 # ---------------------------------------------------------------- a3 + a4
 def attn_workspace_bytes(B: int, n_q: int, H_q: int, H_kv: int, D: int, n_split: int) -> int:
     return int(load().wmtp_attn_workspace_bytes(B, n_q, H_q, H_kv, D, n_split))
@@ -385,12 +420,30 @@ def draft_extend_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
                  lens, scale, out, lse, n_split, max_len, workspace, stream)
 
 
+def draft_decode_attn_fp8(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                          k_scale: torch.Tensor, v_scale: torch.Tensor, table: torch.Tensor,
+                          lens: torch.Tensor, scale: float, out: torch.Tensor | None = None,
+                          lse: torch.Tensor | None = None, n_split: int | None = None,
+                          max_len: int | None = None, workspace: AttnWorkspace | None = None,
+                          stream=None):
+    """:func:`draft_decode_attn` over E4M3 pools (``wmtp_draft_decode_attn_fp8``):
+    k_pool/v_pool [num_slots, H_kv, D] uint8 codes, element = code *
+    k_scale[g] (or v_scale[g]), k_scale/v_scale [H_kv] fp32."""
+    for t, nm in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, nm, torch.float32, q.device)
+    if k_scale.numel() != k_pool.shape[1] or v_scale.numel() != k_pool.shape[1]:
+        raise ValueError("draft_decode_attn_fp8: one scale per KV head expected")
+    return _attn(("fp8", k_scale, v_scale), q, k_pool, v_pool, table, lens, scale, out, lse,
+                 n_split, max_len, workspace, stream)
+
+
 def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_len, workspace,
           stream):
     _need(q, "q", torch.bfloat16)
     dev = q.device
+    pool_dtype = torch.uint8 if (append is not None and append[0] == "fp8") else torch.bfloat16
     for t, nm in ((k_pool, "k_pool"), (v_pool, "v_pool")):
-        _need(t, nm, torch.bfloat16, dev)
+        _need(t, nm, pool_dtype, dev)
     _need(table, "table", torch.int32, dev)
     _need(lens, "lens", torch.int32, dev)
     B, n_q, H_q, D = q.shape
@@ -427,6 +480,15 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
                 _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
                 stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf),
                 workspace.nbytes, n_split, _stream(stream)), "draft_decode_attn")
+        return out, lse
+    if append[0] == "fp8":
+        _, k_scale, v_scale = append
+        with torch.cuda.device(dev):
+            _check(load().wmtp_draft_decode_attn_fp8(
+                _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+                _ptr(v_scale), num_slots, _ptr(table), stride, _ptr(lens), float(scale), _ptr(out),
+                _ptr(lse), _ptr(workspace.buf), workspace.nbytes, n_split, _stream(stream)),
+                "draft_decode_attn_fp8")
         return out, lse
     if append[0] == "extend":
         _, seq_lens, n_new, n_sink, window, windowed = append

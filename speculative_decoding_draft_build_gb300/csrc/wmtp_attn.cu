@@ -67,11 +67,12 @@ constexpr int kMaxClusters = 8;       // clusters merged by the second level
 constexpr int kMaxNew = 4;            // rows one request appends in a fused call (one per warp)
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int D>
+template <int D, bool kFp8 = false>
 struct Cfg {
-    static constexpr int kRowBytes = D * 2;        // one K (or V) row of one head
-    static constexpr int kPitch = kRowBytes + 16;  // padded: conflict-free ldmatrix
-    static constexpr int kStages = 3;
+    static constexpr int kRowBytes = D * (kFp8 ? 1 : 2);  // one K (or V) row of one head
+    static constexpr int kPitch = kRowBytes + 16;         // padded: conflict-free ldmatrix
+    // fp8 rows are half as long: more stages keep the same bytes in flight
+    static constexpr int kStages = kFp8 ? 5 : 3;
     static constexpr int kWarpTile = kKeysPerWarp * kPitch;     // 16 rows of K (or V)
     static constexpr int kWarpStage = 2 * kWarpTile;            // K rows then V rows
     static constexpr int kWarpBytes = kStages * kWarpStage;     // one warp's pipeline
@@ -143,6 +144,17 @@ struct ExtendView {
     int32_t window;
     int32_t windowed;
 };
+// fp8 KV: the pools hold E4M3 codes; key/value element = code * scale of
+// its KV head (k_scale / v_scale [H_kv] fp32).  k_scale folds into the
+// softmax scale, v_scale into the output.  k_scale == nullptr: bf16 pools.
+struct Fp8View {
+    const float *k_scale;
+    const float *v_scale;
+};
+// The fp8 path feeds P to the tensor cores in fp16, scaled by 2^15 so that
+// weights down to 2^-29 keep full fp16 precision (P <= 1 after the running
+// max); the scale is divided out with the output normalisation.
+constexpr float kPScaleF16 = 32768.f;
 
 inline WorkspaceView carve(void *ws, int64_t rows_q, int64_t rows_kv, int n_split) {
     uint8_t *p = static_cast<uint8_t *>(ws);
@@ -166,15 +178,16 @@ inline WorkspaceView carve_two_level(void *ws, int64_t rows_q, int64_t rows_kv, 
     return v;
 }
 
-template <int D, bool kAppend, bool kExtend>
+template <int D, bool kAppend, bool kExtend, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const __nv_bfloat16 *__restrict__ q, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t G,
-    const __nv_bfloat16 *__restrict__ k_pool, const __nv_bfloat16 *__restrict__ v_pool,
+    const void *__restrict__ k_pool, const void *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ table, int64_t table_stride,
     const int32_t *__restrict__ lens, float scale_log2, float *__restrict__ out,
     float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t csz, AppendView ap,
-    ExtendView ev) {
-    using C = Cfg<D>;
+    ExtendView ev, Fp8View fv) {
+    static_assert(!(kFp8 && (kAppend || kExtend)), "the fp8 path appends with its own kernel");
+    using C = Cfg<D, kFp8>;
     constexpr int S = C::kStages;
     constexpr int R = C::kRingTiles;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -196,16 +209,31 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     constexpr int KD = D / 16;
 
     // Query fragments (B operand of QK^T), loaded first so that their latency
-    // overlaps the table fetch.
+    // overlaps the table fetch.  fp8 path: fp16 fragments, with the head
+    // dimension in the order the E4M3 key fragments come in (k index 2c+e of
+    // step kd is dimension 16kd + 4c + e, k index 2c+8+e is 16kd + 4c+2+e).
     uint32_t qf[KD][2];
     {
         const bool live = r < G;
         const __nv_bfloat16 *qrow = q + (bt * H_q + (int64_t)g * G + (live ? r : 0)) * D;
 #pragma unroll
         for (int kd = 0; kd < KD; ++kd) {
-            qf[kd][0] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c)) : 0u;
-            qf[kd][1] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c + 8)) : 0u;
+            if constexpr (kFp8) {
+                const uint32_t *q2 = reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 4 * c);
+                const uint32_t w0 = live ? __ldg(q2) : 0u, w1 = live ? __ldg(q2 + 1) : 0u;
+                qf[kd][0] = pack_f16x2(bf16_lo_to_f32(w0), bf16_hi_to_f32(w0));
+                qf[kd][1] = pack_f16x2(bf16_lo_to_f32(w1), bf16_hi_to_f32(w1));
+            } else {
+                qf[kd][0] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c)) : 0u;
+                qf[kd][1] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c + 8)) : 0u;
+            }
         }
+    }
+    float sl2 = scale_log2;  // softmax scale in base 2 (times k_scale for fp8 keys)
+    float out_scale = 1.f;   // v_scale / P scale for fp8 values
+    if constexpr (kFp8) {
+        sl2 *= __ldg(fv.k_scale + g);
+        out_scale = __ldg(fv.v_scale + g) * (1.f / kPScaleF16);
     }
 
     // Slots this request appends in this launch (-1: none).
@@ -390,24 +418,42 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         const uint32_t wm = masks[warp * S + st];
         if (wm) {
             const uint32_t kaddr = wsm_addr + st * C::kWarpStage + k_off;
-            const uint32_t vaddr = wsm_addr + st * C::kWarpStage + C::kWarpTile + v_off;
+            const uint32_t vaddr = wsm_addr + st * C::kWarpStage + C::kWarpTile + (kFp8 ? k_off : v_off);
             // Four independent accumulation chains over the head dimension.
             float sacc[4][4] = {};
+            if constexpr (kFp8) {
+                // One ldmatrix brings 32 dimensions of 16 keys: register j
+                // holds 4 codes (dimensions 4c..4c+3 of a 16-byte half) of
+                // key r (j = 0, 2) or r + 8 (j = 1, 3), widened to two fp16
+                // pairs for two k16 MMAs.
 #pragma unroll
-            for (int kd = 0; kd < KD; ++kd) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(kaddr + kd * 32, a0, a1, a2, a3);
-                mma_bf16_16816(sacc[kd & 3], a0, a1, a2, a3, qf[kd][0], qf[kd][1]);
+                for (int kc = 0; kc < D / 32; ++kc) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kaddr + kc * 32, a0, a1, a2, a3);
+                    mma_f16_16816(sacc[(2 * kc) & 3], e4m3x2_to_f16x2(a0), e4m3x2_to_f16x2(a1),
+                                  e4m3x2_to_f16x2(a0 >> 16), e4m3x2_to_f16x2(a1 >> 16),
+                                  qf[2 * kc][0], qf[2 * kc][1]);
+                    mma_f16_16816(sacc[(2 * kc + 1) & 3], e4m3x2_to_f16x2(a2), e4m3x2_to_f16x2(a3),
+                                  e4m3x2_to_f16x2(a2 >> 16), e4m3x2_to_f16x2(a3 >> 16),
+                                  qf[2 * kc + 1][0], qf[2 * kc + 1][1]);
+                }
+            } else {
+#pragma unroll
+                for (int kd = 0; kd < KD; ++kd) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kaddr + kd * 32, a0, a1, a2, a3);
+                    mma_bf16_16816(sacc[kd & 3], a0, a1, a2, a3, qf[kd][0], qf[kd][1]);
+                }
             }
             float sc[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) sc[i] = (sacc[0][i] + sacc[1][i]) + (sacc[2][i] + sacc[3][i]);
             // sc[0]: key r, head 2c; sc[1]: key r, head 2c+1; sc[2], sc[3]: key r+8.
             const bool ok_lo = (wm >> r) & 1u, ok_hi = (wm >> (r + 8)) & 1u;
-            const float x0 = ok_lo ? sc[0] * scale_log2 : -INFINITY;
-            const float x1 = ok_lo ? sc[1] * scale_log2 : -INFINITY;
-            const float x2 = ok_hi ? sc[2] * scale_log2 : -INFINITY;
-            const float x3 = ok_hi ? sc[3] * scale_log2 : -INFINITY;
+            const float x0 = ok_lo ? sc[0] * sl2 : -INFINITY;
+            const float x1 = ok_lo ? sc[1] * sl2 : -INFINITY;
+            const float x2 = ok_hi ? sc[2] * sl2 : -INFINITY;
+            const float x3 = ok_hi ? sc[3] * sl2 : -INFINITY;
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
             for (int sh = 4; sh < 32; sh <<= 1) {
@@ -431,21 +477,47 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
                     o[dt][3] *= al1;
                 }
             }
-            // P^T as the B operand: keys 2c,2c+1 (and +8) for query head r.
-            // P is split into a bf16 head and a bf16 tail (p = hi + lo to about
-            // 16 significant bits) so that rounding the weights to bf16 does
-            // not cost accuracy; both halves share the same V fragment.
-            const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-            const uint32_t t01 = pack_bf16x2(p0 - bf16_lo_to_f32(h01), p1 - bf16_hi_to_f32(h01));
-            const uint32_t t23 = pack_bf16x2(p2 - bf16_lo_to_f32(h23), p3 - bf16_hi_to_f32(h23));
-            const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
-            const uint32_t pl0 = movmatrix_trans(t01), pl1 = movmatrix_trans(t23);
+            if constexpr (kFp8) {
+                // P^T in fp16 (11 significant bits, scaled by 2^15) as the B
+                // operand.  V^T comes from plain ldmatrix rows of codes: the
+                // fp16 pairs of key r hold dimensions (4c, 4c+1) and
+                // (4c+2, 4c+3), and movmatrix turns each 8x8 block into the
+                // A fragment with M row r standing for dimension
+                // 4(r/2) + r%2 (rows r) and that + 2 (rows r + 8) of its
+                // 16-dimension group.
+                const uint32_t ph0 = movmatrix_trans(pack_f16x2(p0 * kPScaleF16, p1 * kPScaleF16));
+                const uint32_t ph1 = movmatrix_trans(pack_f16x2(p2 * kPScaleF16, p3 * kPScaleF16));
 #pragma unroll
-            for (int dt = 0; dt < KD; ++dt) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_trans(vaddr + dt * 32, a0, a1, a2, a3);
-                mma_bf16_16816(o[dt], a0, a1, a2, a3, ph0, ph1);
-                mma_bf16_16816(o[dt], a0, a1, a2, a3, pl0, pl1);
+                for (int kc = 0; kc < D / 32; ++kc) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(vaddr + kc * 32, a0, a1, a2, a3);
+                    mma_f16_16816(o[2 * kc], movmatrix_trans(e4m3x2_to_f16x2(a0)),
+                                  movmatrix_trans(e4m3x2_to_f16x2(a0 >> 16)),
+                                  movmatrix_trans(e4m3x2_to_f16x2(a1)),
+                                  movmatrix_trans(e4m3x2_to_f16x2(a1 >> 16)), ph0, ph1);
+                    mma_f16_16816(o[2 * kc + 1], movmatrix_trans(e4m3x2_to_f16x2(a2)),
+                                  movmatrix_trans(e4m3x2_to_f16x2(a2 >> 16)),
+                                  movmatrix_trans(e4m3x2_to_f16x2(a3)),
+                                  movmatrix_trans(e4m3x2_to_f16x2(a3 >> 16)), ph0, ph1);
+                }
+            } else {
+                // P^T as the B operand: keys 2c,2c+1 (and +8) for query head
+                // r.  P is split into a bf16 head and a bf16 tail (p = hi + lo
+                // to about 16 significant bits) so that rounding the weights
+                // to bf16 does not cost accuracy; both halves share the same V
+                // fragment.
+                const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+                const uint32_t t01 = pack_bf16x2(p0 - bf16_lo_to_f32(h01), p1 - bf16_hi_to_f32(h01));
+                const uint32_t t23 = pack_bf16x2(p2 - bf16_lo_to_f32(h23), p3 - bf16_hi_to_f32(h23));
+                const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
+                const uint32_t pl0 = movmatrix_trans(t01), pl1 = movmatrix_trans(t23);
+#pragma unroll
+                for (int dt = 0; dt < KD; ++dt) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_trans(vaddr + dt * 32, a0, a1, a2, a3);
+                    mma_bf16_16816(o[dt], a0, a1, a2, a3, ph0, ph1);
+                    mma_bf16_16816(o[dt], a0, a1, a2, a3, pl0, pl1);
+                }
             }
         }
         __syncwarp();
@@ -491,12 +563,16 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     {
         float *o_lo = ow + (warp * kMaxGroup + 2 * c) * C::kOPitch;
         float *o_hi = o_lo + C::kOPitch;
+        // accumulator rows r and r + 8 of group dt: dimensions 16dt + r and
+        // 16dt + r + 8 (bf16), or 16dt + 4(r/2) + r%2 and that + 2 (fp8)
+        const int d_a = kFp8 ? 4 * (r >> 1) + (r & 1) : r;
+        const int d_b = kFp8 ? d_a + 2 : r + 8;
 #pragma unroll
         for (int dt = 0; dt < KD; ++dt) {
-            o_lo[dt * 16 + r] = o[dt][0];
-            o_hi[dt * 16 + r] = o[dt][1];
-            o_lo[dt * 16 + r + 8] = o[dt][2];
-            o_hi[dt * 16 + r + 8] = o[dt][3];
+            o_lo[dt * 16 + d_a] = o[dt][0];
+            o_hi[dt * 16 + d_a] = o[dt][1];
+            o_lo[dt * 16 + d_b] = o[dt][2];
+            o_hi[dt * 16 + d_b] = o[dt][3];
         }
         if (r == 0) {
             mw[warp * kMaxGroup + 2 * c] = m0;
@@ -524,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
             f[w] = M == -INFINITY ? 0.f : exp2f(mw[w * kMaxGroup + h] - M);
             Ls += lw[w * kMaxGroup + h] * f[w];
         }
-        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        const float inv = Ls > 0.f ? out_scale / Ls : 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) fac[h * kConsumerWarps + w] = f[w] * inv;
         cta_lse[h] = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
@@ -753,33 +829,33 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
 // device `dev` (0: none; cached per device and size).
 // Sets the kernel attributes (large dynamic shared memory, non-portable
 // cluster sizes) once per device for one kernel instance.
-template <int D, bool A, bool X>
+template <int D, bool A, bool X, bool F = false>
 bool prepare_kernel(int dev) {
     static int8_t done[64] = {};
     if (dev < 0 || dev >= 64) return false;
     if (done[dev]) return done[dev] > 0;
-    const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A, X>,
+    const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A, X, F>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<D>::kSmemBytes) == cudaSuccess &&
-                    cudaFuncSetAttribute(split_decode_kernel<D, A, X>,
+                                         Cfg<D, F>::kSmemBytes) == cudaSuccess &&
+                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F>,
                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
     cudaGetLastError();
     done[dev] = ok ? 1 : -1;
     return ok;
 }
 
-template <int D>
+template <int D, bool F = false>
 int cluster_capacity(int dev, int n) {
     static int16_t known[64][kMaxClusterMerge + 1] = {};
     if (n < 2 || n > kMaxClusterMerge || dev < 0 || dev >= 64) return 0;
     if (known[dev][n]) return known[dev][n] > 0 ? known[dev][n] : 0;
-    bool ok = prepare_kernel<D, false, false>(dev);
+    bool ok = prepare_kernel<D, false, false, F>(dev);
     int clusters = 0;
     if (ok) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)n, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+        cfg.dynamicSmemBytes = Cfg<D, F>::kSmemBytes;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
         attr.val.clusterDim.x = (unsigned)n;
@@ -787,7 +863,7 @@ int cluster_capacity(int dev, int n) {
         attr.val.clusterDim.z = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        ok = cudaOccupancyMaxActiveClusters(&clusters, split_decode_kernel<D, false, false>, &cfg) == cudaSuccess &&
+        ok = cudaOccupancyMaxActiveClusters(&clusters, split_decode_kernel<D, false, false, F>, &cfg) == cudaSuccess &&
              clusters > 0;
         if (!ok) clusters = 0;
     }
@@ -796,19 +872,19 @@ int cluster_capacity(int dev, int n) {
     return ok ? known[dev][n] : 0;
 }
 
-template <int D>
+template <int D, bool F = false>
 bool cluster_merge_ok(int dev, int n) {
-    return cluster_capacity<D>(dev, n) > 0;
+    return cluster_capacity<D, F>(dev, n) > 0;
 }
 
-template <int D>
+template <int D, bool F>
 wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
-                                int32_t H_kv, const uint16_t *k_pool, const uint16_t *v_pool,
+                                int32_t H_kv, const void *k_pool, const void *v_pool,
                                 int64_t num_slots, const int32_t *table, int64_t table_stride,
                                 const int32_t *lens, float scale, float *out, float *lse,
                                 void *workspace, int32_t n_split, cudaStream_t stream,
-                                AppendView ap, ExtendView ev) {
-    using C = Cfg<D>;
+                                AppendView ap, ExtendView ev, Fp8View fv) {
+    using C = Cfg<D, F>;
     const int64_t rows_q = (int64_t)B * n_q * H_q;
     const int64_t rows_kv = (int64_t)B * n_q * H_kv;
     // Kernel attributes are set once per device (outside any later stream
@@ -817,18 +893,19 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WMTP_ECUDA;
     const bool append = ap.n_new > 0;
     const bool extend = ev.seq_lens != nullptr;
-    if (!(append ? prepare_kernel<D, true, false>(dev)
-                 : (extend ? prepare_kernel<D, false, true>(dev) : prepare_kernel<D, false, false>(dev))))
+    if (F ? !prepare_kernel<D, false, false, true>(dev)
+          : !(append ? prepare_kernel<D, true, false>(dev)
+                     : (extend ? prepare_kernel<D, false, true>(dev) : prepare_kernel<D, false, false>(dev))))
         return WMTP_ECUDA;
     // Cluster size: all splits in one cluster, else the largest cluster that
     // divides n_split into at most kMaxClusters clusters, else none.
     int csz = 0;
     if (n_split > 1) {
-        if (n_split <= kMaxClusterMerge && cluster_merge_ok<D>(dev, n_split)) {
+        if (n_split <= kMaxClusterMerge && cluster_merge_ok<D, F>(dev, n_split)) {
             csz = n_split;
         } else {
             for (int c = kMaxClusterMerge; c >= 2; --c) {
-                if (n_split % c == 0 && n_split / c <= kMaxClusters && cluster_merge_ok<D>(dev, c)) {
+                if (n_split % c == 0 && n_split / c <= kMaxClusters && cluster_merge_ok<D, F>(dev, c)) {
                     csz = c;
                     break;
                 }
@@ -844,11 +921,12 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     if (csz) launch.add_cluster((unsigned)csz);
     const cudaError_t err = cudaLaunchKernelEx(
         &launch.cfg,
-        append ? split_decode_kernel<D, true, false>
-               : (extend ? split_decode_kernel<D, false, true> : split_decode_kernel<D, false, false>),
-        reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q, H_kv, H_q / H_kv,
-        reinterpret_cast<const __nv_bfloat16 *>(k_pool), reinterpret_cast<const __nv_bfloat16 *>(v_pool),
-        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, ap, ev);
+        F ? split_decode_kernel<D, false, false, true>
+          : (append ? split_decode_kernel<D, true, false, false>
+                    : (extend ? split_decode_kernel<D, false, true, false>
+                              : split_decode_kernel<D, false, false, false>)),
+        reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q, H_kv, H_q / H_kv, k_pool, v_pool,
+        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, ap, ev, fv);
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
@@ -909,11 +987,11 @@ wmtp_status launch_split_decode_noalloc(const uint16_t *q, int32_t B, int32_t n_
     PdlLaunch launch(dim3((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q)), dim3(kThreads),
                      C::kSmemBytes, stream);
     const cudaError_t err = cudaLaunchKernelEx(
-        &launch.cfg, split_decode_kernel<D, false, false>, reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q,
-        H_kv, H_q / H_kv, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
-        reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, table, table_stride, lens,
-        scale_log2, out, lse, ws, n_split, (int32_t)0, AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0},
-        ExtendView{nullptr, nullptr, 0, 0, 0});
+        &launch.cfg, split_decode_kernel<D, false, false, false>, reinterpret_cast<const __nv_bfloat16 *>(q), n_q,
+        H_q, H_kv, H_q / H_kv, static_cast<const void *>(k_pool), static_cast<const void *>(v_pool), num_slots,
+        table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)0,
+        AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0}, ExtendView{nullptr, nullptr, 0, 0, 0},
+        Fp8View{nullptr, nullptr});
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
@@ -986,13 +1064,14 @@ namespace wmtp {
 namespace {
 
 wmtp_status draft_decode_attn_checked(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
-                                      int32_t H_kv, int32_t D, const uint16_t *k_pool,
-                                      const uint16_t *v_pool, int64_t num_slots,
+                                      int32_t H_kv, int32_t D, const void *k_pool,
+                                      const void *v_pool, int64_t num_slots,
                                       const int32_t *table, int64_t table_stride,
                                       const int32_t *lens, float scale, float *out, float *lse,
                                       void *workspace, size_t workspace_bytes_, int32_t n_split,
                                       void *stream, AppendView ap,
-                                      ExtendView ev = ExtendView{nullptr, nullptr, 0, 0, 0}) {
+                                      ExtendView ev = ExtendView{nullptr, nullptr, 0, 0, 0},
+                                      Fp8View fv = Fp8View{nullptr, nullptr}) {
     if (B < 0 || n_q < 0 || H_q < 1 || H_kv < 1 || (H_q % H_kv) != 0) return WMTP_EINVAL;
     if (H_q / H_kv > kMaxGroup) return WMTP_EINVAL;
     if (D != 128 && D != 256) return WMTP_EINVAL;
@@ -1014,11 +1093,23 @@ wmtp_status draft_decode_attn_checked(const uint16_t *q, int32_t B, int32_t n_q,
             return WMTP_ECAPACITY;
     }
     cudaStream_t s = as_stream(stream);
+    if (fv.k_scale) {
+        if (!fv.v_scale) return WMTP_EINVAL;
+        if (D == 256)
+            return launch_split_decode<256, true>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
+                                                  table_stride, lens, scale, out, lse, workspace, n_split, s,
+                                                  ap, ev, fv);
+        return launch_split_decode<128, true>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
+                                              table_stride, lens, scale, out, lse, workspace, n_split, s, ap,
+                                              ev, fv);
+    }
     if (D == 256)
-        return launch_split_decode<256>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
-                                        table_stride, lens, scale, out, lse, workspace, n_split, s, ap, ev);
-    return launch_split_decode<128>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
-                                    table_stride, lens, scale, out, lse, workspace, n_split, s, ap, ev);
+        return launch_split_decode<256, false>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
+                                               table_stride, lens, scale, out, lse, workspace, n_split, s, ap,
+                                               ev, fv);
+    return launch_split_decode<128, false>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
+                                           table_stride, lens, scale, out, lse, workspace, n_split, s, ap, ev,
+                                           fv);
 }
 
 }  // namespace
@@ -1105,6 +1196,26 @@ wmtp_status wmtp_draft_decode_attn_noalloc(const uint16_t *q, int32_t B, int32_t
                                                 table, table_stride, lens, scale, out, lse, n_split, s);
     return launch_split_decode_noalloc<128>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
                                             table_stride, lens, scale, out, lse, n_split, s);
+}
+
+}  // extern "C"
+
+extern "C" {
+
+wmtp_status wmtp_draft_decode_attn_fp8(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
+                                       int32_t H_kv, int32_t D, const uint8_t *k_pool,
+                                       const uint8_t *v_pool, const float *k_scale,
+                                       const float *v_scale, int64_t num_slots,
+                                       const int32_t *table, int64_t table_stride,
+                                       const int32_t *lens, float scale, float *out, float *lse,
+                                       void *workspace, size_t workspace_bytes_, int32_t n_split,
+                                       void *stream) {
+    if (B > 0 && n_q > 0 && (!k_scale || !v_scale)) return WMTP_EINVAL;
+    return draft_decode_attn_checked(q, B, n_q, H_q, H_kv, D, k_pool, v_pool, num_slots, table,
+                                     table_stride, lens, scale, out, lse, workspace,
+                                     workspace_bytes_, n_split, stream,
+                                     AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0},
+                                     ExtendView{nullptr, nullptr, 0, 0, 0}, Fp8View{k_scale, v_scale});
 }
 
 }  // extern "C"

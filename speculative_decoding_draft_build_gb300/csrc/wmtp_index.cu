@@ -118,6 +118,40 @@ __global__ void __launch_bounds__(256) append_kv_kernel(
     v_pool[slot * chunks_per_token + e] = v_new[idx];
 }
 
+// fp8 KV append: one thread per 8 elements of one token's K rows and V rows
+// (16 bytes of bf16 in, 8 bytes of E4M3 codes out).  Element x of KV head h
+// becomes E4M3_rn_satfinite(x * (1 / scale[h])), the reciprocal and the
+// product each rounded once in fp32.
+__global__ void __launch_bounds__(256) append_kv_fp8_kernel(
+    const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+    const int32_t *__restrict__ slots, int64_t total, int32_t chunks_per_token, int32_t chunks_per_head,
+    const float *__restrict__ k_scale, const float *__restrict__ v_scale, uint2 *__restrict__ k_pool,
+    uint2 *__restrict__ v_pool, int64_t num_slots) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const int64_t i = idx / chunks_per_token;
+    const int64_t e = idx - i * chunks_per_token;
+    const int64_t slot = slots[i];
+    if (slot < 0 || slot >= num_slots) {
+        latch(WMTP_DEV_SLOT_RANGE);
+        return;
+    }
+    const int h = (int)(e / chunks_per_head);
+    const float ik = __frcp_rn(k_scale[h]), iv = __frcp_rn(v_scale[h]);
+    auto quant = [](uint4 x, float inv) {
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t c[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            c[u] = f32x2_to_e4m3x2(__fmul_rn(bf16_lo_to_f32(w[u]), inv), __fmul_rn(bf16_hi_to_f32(w[u]), inv));
+        return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    };
+    k_pool[slot * chunks_per_token + e] = quant(k_new[idx], ik);
+    v_pool[slot * chunks_per_token + e] = quant(v_new[idx], iv);
+}
+
 }  // namespace
 
 cudaError_t read_index_error(int32_t *code, bool clear) {
@@ -241,6 +275,32 @@ wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
     return cudaLaunchKernelEx(&L.cfg, append_kv_kernel, reinterpret_cast<const uint4 *>(k_new),
                               reinterpret_cast<const uint4 *>(v_new), slots, total, chunks,
                               reinterpret_cast<uint4 *>(k_pool), reinterpret_cast<uint4 *>(v_pool),
+                              num_slots) == cudaSuccess
+               ? WMTP_OK
+               : WMTP_ECUDA;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+wmtp_status wmtp_append_kv_fp8(const uint16_t *k_new, const uint16_t *v_new,
+                               const int32_t *slots, int32_t n, int32_t H_kv, int32_t D,
+                               const float *k_scale, const float *v_scale, uint8_t *k_pool,
+                               uint8_t *v_pool, int64_t num_slots, void *stream) {
+    if (n < 0 || H_kv < 1 || D < 1 || (D % 16) != 0 || num_slots < 0) return WMTP_EINVAL;
+    if (n == 0) return WMTP_OK;
+    if (!k_new || !v_new || !slots || !k_scale || !v_scale || !k_pool || !v_pool) return WMTP_EINVAL;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+        return WMTP_EINVAL;
+    const int32_t chunks = H_kv * D / 8;
+    const int64_t total = (int64_t)n * chunks;
+    constexpr int kThreads = 256;
+    const int64_t blocks = (total + kThreads - 1) / kThreads;
+    PdlLaunch L(dim3((unsigned)blocks), dim3(kThreads), 0, as_stream(stream));
+    return cudaLaunchKernelEx(&L.cfg, append_kv_fp8_kernel, reinterpret_cast<const uint4 *>(k_new),
+                              reinterpret_cast<const uint4 *>(v_new), slots, total, chunks, D / 8, k_scale,
+                              v_scale, reinterpret_cast<uint2 *>(k_pool), reinterpret_cast<uint2 *>(v_pool),
                               num_slots) == cudaSuccess
                ? WMTP_OK
                : WMTP_ECUDA;

@@ -65,3 +65,13 @@ def ring_bases(B: int, ring_size: int, n_regions: int, seed: int) -> list[int]:
     g = generator(seed, "cpu")
     regions = torch.randperm(n_regions, generator=g)[:B]
     return [int(r) * ring_size for r in regions]
+
+
+def e4m3_codes(shape, seed: int, device, lo: int = 0x20, hi: int = 0x68) -> torch.Tensor:
+    """Random E4M3 codes (uint8): a random sign and a magnitude code drawn
+    uniformly from [lo, hi) -- values log-uniform over (hi - lo) / 8 octaves,
+    2^-3 .. 2^6 by default; never a NaN code while hi <= 0x7F."""
+    g = generator(seed, device)
+    mag = torch.randint(lo, hi, shape, generator=g, device=device, dtype=torch.int32)
+    sign = torch.randint(0, 2, shape, generator=g, device=device, dtype=torch.int32) * 0x80
+    return (mag | sign).to(torch.uint8)
