@@ -25,6 +25,8 @@ from .oracle import (  # noqa: F401
     f32_to_e4m3,
     keep,
     num_threads,
+    prefill_keep_positions,
+    ring_fill,
     ring_map,
     ring_slot,
     tree_draft_attn,

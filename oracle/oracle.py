@@ -461,3 +461,28 @@ def draft_decode_attn_fp8(q, k_pool, v_pool, k_scale, v_scale, table, lens, scal
         _ptr(scratch, ctypes.c_double), scratch_len, nthreads),
         "draft_decode_attn_fp8")
     return out, lse
+
+
+# --- pruned draft prefill ([WMTP] §7 "Prefill sparsification and TTFT";
+# reading R14: the draft KV kept after a prompt of S positions is keep(S)) ---
+
+def prefill_keep_positions(seq_lens, n_sink, window):
+    """Per request, the prompt positions whose draft KV the windowed draft
+    reads after the prompt: keep(S) (App. A keep rule at kv length S)."""
+    return [keep(int(S), n_sink, window, True) for S in np.asarray(seq_lens).reshape(-1)]
+
+
+def ring_fill(k_rows, v_rows, seq_lens, ring_base, n_sink, window, depth, k_pool, v_pool, tree_k=1):
+    """Write row i of request b (its draft K/V at the i-th kept position, rows
+    [B, stride, H_kv, D] bf16 bits) to that position's ring slot (in place):
+    the keep rule, the ring rule and append_kv, composed."""
+    kr = _as(k_rows, np.uint16)
+    vr = _as(v_rows, np.uint16)
+    rb = _as(ring_base, np.int32)
+    for b, pos in enumerate(prefill_keep_positions(seq_lens, n_sink, window)):
+        n = min(len(pos), kr.shape[1])
+        if n == 0:
+            continue
+        slots = ring_map(rb, pos[:n].astype(np.int32), np.full(n, b, np.int32), n_sink, window, depth,
+                         tree_k)
+        append_kv(kr[b, :n], vr[b, :n], slots, k_pool, v_pool)
