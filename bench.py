@@ -491,8 +491,10 @@ def run_ours(args, dist_ctx):
         result["tree"] = measure_tree(args, dev)
     if args.workload == "1m" and not args.no_extend:
         result["extend"] = measure_extend(w, args, dev)
-    if args.workload == "1m" and not args.no_fp8:
+    if not args.no_fp8:
         result["fp8"] = measure_fp8(w, args, dev)
+    if not args.no_ring:
+        result["ring"] = measure_ring(w, args, dev)
     if dist_ctx.rank == 0 and dist_ctx.world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args)
     return result
@@ -595,7 +597,7 @@ def measure_fp8(w, args, dev):
            "timing": "CUDA events per launch, L2 flushed before each, median over steps x reps"}
     for name, tab, ln, stride in (("full", w.tab_full, w.len_full, w.full_stride),
                                   ("windowed", w.tab_win, w.len_win, w.win_stride)):
-        ns = wm.attn_num_splits(B, 1, H_kv, stride, dev)
+        ns = wm.attn_num_splits(B, 1, H_kv, stride, dev, fp8=True)
         ws = wm.AttnWorkspace(wm.attn_workspace_bytes(B, 1, H_q, H_kv, D, ns), dev)
         out = torch.empty((B, 1, H_q, D), dtype=torch.float32, device=dev)
         lse = torch.empty((B, 1, H_q), dtype=torch.float32, device=dev)
@@ -630,8 +632,97 @@ def measure_fp8(w, args, dev):
                      "append_us_per_launch": round(statistics.median(t_app) * 1e6, 2),
                      "kv_gbs": round(statistics.median(gbs), 1),
                      "frac_of_hbm": round(statistics.median(gbs) / peak, 4), "n_split": ns}
+    full_bytes = B * (S + 1) * H_kv * D * 2 + 4 * B * (S + 1) + B * H_q * (D * 2 + (D + 1) * 4)
+    res["roofline"] = {
+        "kernel": "split_decode_kernel<256, fp8> (full-context draft attention over E4M3 pools)",
+        "bound": "hbm", "achieved": res["full"]["kv_gbs"], "peak": peak, "unit": "GB/s",
+        "frac": res["full"]["frac_of_hbm"], "bytes_per_launch": int(full_bytes),
+        "traffic": profiled_traffic("fp8_full_1m") if args.workload == "1m" else None}
     del kp8, vp8
     return res
+
+
+def measure_ring(w, args, dev):
+    """Ring path without tables ([WMTP] App. A ring; §7 "Prefill
+    sparsification and TTFT") on the million-token workload:
+      prefill: the draft KV build of the prompt pruned to keep(S) (one ring
+               fill of n_sink + W rows) against the unpruned build (all S + 6
+               rows appended to a full-length pool), event-timed, L2 flushed;
+      step:    6 implicit-table ring draft steps (fused append + attention,
+               slots from the ring rule in the kernel, no index build)
+               replayed from a CUDA graph, L2 flushed before each replay."""
+    import speculative_decoding_draft_build_gb300 as wm
+    c = w.cfg
+    B, S, H_q, H_kv, D, g = c["B"], c["S"], c["H_q"], c["H_kv"], c["D"], c["gamma"]
+    n_sink, W, d = c["n_sink"], c["W"], c["gamma"] + 1
+    R = n_sink + W + d
+    ring_base = (torch.arange(B, dtype=torch.int32, device=dev) * R).contiguous()
+    ring_k = torch.zeros((B * R, H_kv, D), dtype=torch.bfloat16, device=dev)
+    ring_v = torch.zeros_like(ring_k)
+    pos, cnt = wm.prefill_keep_positions(w.seq, n_sink, W)
+    live = torch.arange(pos.shape[1], device=dev).view(1, -1) < cnt.view(-1, 1).long()
+    pos = torch.where(live, pos, torch.zeros_like(pos))
+    rows = torch.gather(w.rtt, 1, pos.long()).long()  # pool rows of the kept prompt positions
+    rows_k = w.kp[rows].contiguous()
+    rows_v = w.vp[rows].contiguous()
+    full_k = torch.empty_like(w.kp)
+    full_v = torch.empty_like(w.vp)
+    all_slots = torch.arange(w.kp.shape[0], dtype=torch.int32, device=dev)
+    reps = max(3, min(args.steps, 10))
+
+    def timed(fn):
+        fn()
+        ts = []
+        for _ in range(reps):
+            w.flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+    t_pruned = timed(lambda: wm.ring_fill(rows_k, rows_v, w.seq, ring_base, n_sink, W, d, ring_k, ring_v))
+    t_full = timed(lambda: wm.append_kv(w.kp, w.vp, all_slots, full_k, full_v))
+    del full_k, full_v
+    ns = wm.attn_num_splits(B, 1, H_kv, n_sink + W, dev)
+    ws = wm.AttnWorkspace(wm.attn_workspace_bytes(B, 1, H_q, H_kv, D, ns), dev)
+    out = torch.empty((g, B, 1, H_q, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((g, B, 1, H_q), dtype=torch.float32, device=dev)
+
+    def step():
+        for j in range(g):
+            wm.draft_decode_attn_ring(w.q[j], ring_k, ring_v, w.seq, ring_base, j, n_sink, W, d, w.scale,
+                                      k_new=w.kn[j], v_new=w.vn[j], out=out[j], lse=lse[j], n_split=ns,
+                                      workspace=ws)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    cap = torch.cuda.Stream(dev)
+    cur = torch.cuda.current_stream(dev)
+    cap.wait_stream(cur)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(gr, stream=cap):
+            step()
+    cur.wait_stream(cap)
+    for _ in range(3):
+        gr.replay()
+    torch.cuda.synchronize(dev)
+    t_step = timed(gr.replay)
+    peak, _ = hbm_peak()
+    step_bytes = sum(B * attn_bytes(min(S + j + 1, n_sink + W), 1, H_q, H_kv, D, n_new=1) - B * 4 *
+                     min(S + j + 1, n_sink + W) for j in range(g))
+    return {"ring_slots_per_request": R, "n_split": ns,
+            "prefill_kv_build": {"pruned_us": round(t_pruned, 2), "unpruned_us": round(t_full, 2),
+                                 "rows_pruned": int(B * min(S, n_sink + W)), "rows_unpruned": int(w.kp.shape[0]),
+                                 "note": "the draft's prompt KV build only; the draft prompt pass itself "
+                                         "(projections over the kept positions) needs the model"},
+            "step": {"us_per_step": round(t_step, 3), "us_per_launch": round(t_step / g, 3),
+                     "launches": g, "kv_gbs": round(step_bytes / (t_step * 1e-6) / 1e9, 1),
+                     "frac_of_hbm": round(step_bytes / (t_step * 1e-6) / 1e9 / peak, 4),
+                     "launch": "cuda graph, no index build, no table"},
+            "timing": "CUDA events, L2 flushed before each, median"}
 
 
 def measure_tree(args, dev):
@@ -845,6 +936,7 @@ def main(argv=None):
     p.add_argument("--no-tree", action="store_true", help="skip the tree-drafter measurement")
     p.add_argument("--no-extend", action="store_true", help="skip the draft-extend measurement")
     p.add_argument("--no-fp8", action="store_true", help="skip the fp8-KV measurement")
+    p.add_argument("--no-ring", action="store_true", help="skip the table-free ring measurement")
     p.add_argument("--tree-only", action="store_true",
                    help="run only the tree-drafter measurement (a profiling driver; prints the tree object)")
     p.add_argument("--tree-w", type=int, action="append",

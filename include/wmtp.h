@@ -385,6 +385,63 @@ wmtp_status wmtp_draft_decode_attn_noalloc(
     void *stream);
 
 /* ------------------------------------------------------------------------
+ * Ring path without tables.
+ *
+ * Pruned draft prefill ("Windowed-MTP", §7 "Prefill sparsification and
+ * TTFT"): after a prompt of S positions the windowed draft reads only its KV
+ * of keep(S) = [0, n_sink) u [S - W, S) (all S positions when
+ * S <= n_sink + W), so the draft's prompt pass and KV build are needed for
+ * those positions only.
+ *
+ * wmtp_prefill_keep_positions: positions[b][i], i < counts[b] =
+ * min(S_b, n_sink + W), in keep order (sinks, then the window).
+ *   seq_lens device int32 [B] (prompt lengths); positions device int32
+ *   [B][stride]; counts device int32 [B].  A list longer than stride is cut
+ *   at stride and latches WMTP_DEV_TABLE_OVERFLOW; a negative length latches
+ *   WMTP_DEV_LEN_RANGE and gives an empty list. */
+wmtp_status wmtp_prefill_keep_positions(const int32_t *seq_lens, int32_t B,
+                                        int32_t n_sink, int32_t window,
+                                        int32_t *positions, int64_t stride,
+                                        int32_t *counts, void *stream);
+
+/* wmtp_ring_fill: writes row i of request b -- its draft K and V at kept
+ * position p_i of keep(S_b), in the order of wmtp_prefill_keep_positions --
+ * to ring slot ring_slot(ring_base[b], p_i) (the ring rule of
+ * wmtp_ring_map, branch 0), for i < min(S_b, n_sink + W, stride).
+ *   k_rows, v_rows device bf16 [B][stride][H_kv][D], 16-byte aligned;
+ *   seq_lens, ring_base device int32 [B]; k_pool, v_pool as
+ *   wmtp_append_kv.  A slot outside the pool is skipped and latches
+ *   WMTP_DEV_SLOT_RANGE. */
+wmtp_status wmtp_ring_fill(const uint16_t *k_rows, const uint16_t *v_rows,
+                           const int32_t *seq_lens, int32_t B, int64_t stride,
+                           int32_t H_kv, int32_t D, const int32_t *ring_base,
+                           int32_t n_sink, int32_t window, int32_t depth,
+                           int32_t tree_k, uint16_t *k_pool, uint16_t *v_pool,
+                           int64_t num_slots, void *stream);
+
+/* Implicit-table ring decode step: wmtp_build_draft_indices (ring layout,
+ * windowed) + wmtp_draft_decode_attn_append for draft step `step`, in one
+ * launch and with no table in memory.  Request b (committed length
+ * S = seq_lens[b]) attends keep(S + step + 1); entry e of that list is
+ * mapped to its ring slot in the kernel, in the same logical order as the
+ * table, so results are bit-identical to the table path with the same
+ * n_split.  When k_new / v_new (device bf16 [B][H_kv][D]) are given, the
+ * step's own row is written to the slot of position S + step first (as
+ * wmtp_draft_decode_attn_append with n_new = 1); both NULL: no append.
+ * n_q = 1; other arguments as wmtp_draft_decode_attn; the workspace is
+ * sized by wmtp_attn_workspace_bytes(B, 1, H_q, H_kv, D, n_split) and
+ * wmtp_attn_num_splits(B, 1, H_kv, n_sink + W) is the usual split count.
+ * Errors: WMTP_EINVAL for n_sink < 0, W < 1, depth < 1, tree_k < 1,
+ * step < 0, or only one of k_new / v_new. */
+wmtp_status wmtp_draft_decode_attn_ring(
+    const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q, int32_t B,
+    int32_t H_q, int32_t H_kv, int32_t D, uint16_t *k_pool, uint16_t *v_pool,
+    int64_t num_slots, const int32_t *seq_lens, const int32_t *ring_base,
+    int32_t step, int32_t n_sink, int32_t window, int32_t depth,
+    int32_t tree_k, float scale, float *out, float *lse, void *workspace,
+    size_t workspace_bytes, int32_t n_split, void *stream);
+
+/* ------------------------------------------------------------------------
  * fp8 KV ("Windowed-MTP", §6 "Robustness to KV-cache quantization": the
  * window bounds the number of KV entries read, so its saving composes with a
  * lower-precision cache, whose bytes per entry it does not change; the
@@ -420,6 +477,12 @@ wmtp_status wmtp_append_kv_fp8(const uint16_t *k_new, const uint16_t *v_new,
  * with uint8 pools and the per-KV-head scales k_scale, v_scale (device fp32
  * [H_kv]).  The codes are widened exactly to fp16 on chip and q is rounded
  * to fp16 (exact for |q| >= 2^-14), products accumulate in fp32. */
+/* Split count wmtp_draft_decode_attn_fp8 uses when the caller has no
+ * preference: as wmtp_attn_num_splits, for the fp8 instance, which holds two
+ * CTAs per SM (its tiles take half the shared memory). */
+int32_t wmtp_attn_num_splits_fp8(int32_t B, int32_t n_q, int32_t H_kv,
+                                 int64_t max_len);
+
 wmtp_status wmtp_draft_decode_attn_fp8(
     const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q, int32_t H_kv,
     int32_t D, const uint8_t *k_pool, const uint8_t *v_pool,

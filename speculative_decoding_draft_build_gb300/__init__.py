@@ -18,6 +18,10 @@ Calls (same names as the C ABI without the ``wmtp_`` prefix):
   attn_mass_diagnostics  in-window mass, win_perturb, tail out-frac per query
   append_kv_fp8 / draft_decode_attn_fp8  the same over E4M3 KV pools with
                        per-KV-head scales
+  prefill_keep_positions / ring_fill  pruned draft prefill: the kept prompt
+                       positions and their KV written into the ring
+  draft_decode_attn_ring  a draft step over the ring with no table (slots
+                       from the ring rule in the kernel), append fused
   tree_draft_attn      tree-draft attention over the ring (tree-causal mask)
 """
 from __future__ import annotations
@@ -36,7 +40,8 @@ __all__ = [
     "draft_decode_attn_append", "draft_extend_attn", "attn_mass_diagnostics",
     "attn_workspace_bytes", "attn_num_splits", "AttnWorkspace", "draft_decode_attn_noalloc",
     "tree_draft_attn", "tree_workspace_bytes", "tree_num_splits",
-    "append_kv_fp8", "draft_decode_attn_fp8",
+    "append_kv_fp8", "draft_decode_attn_fp8", "prefill_keep_positions", "ring_fill",
+    "draft_decode_attn_ring",
 ]
 
 WMTP_OK = 0
@@ -128,9 +133,20 @@ def load():
         lib.wmtp_append_kv_fp8.restype = _i32
         lib.wmtp_append_kv_fp8.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64,
                                            _vp]
+        lib.wmtp_attn_num_splits_fp8.restype = _i32
+        lib.wmtp_attn_num_splits_fp8.argtypes = [_i32, _i32, _i32, _i64]
         lib.wmtp_draft_decode_attn_fp8.restype = _i32
         lib.wmtp_draft_decode_attn_fp8.argtypes = [
             _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _i64, _vp,
+            ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
+        lib.wmtp_prefill_keep_positions.restype = _i32
+        lib.wmtp_prefill_keep_positions.argtypes = [_vp, _i32, _i32, _i32, _vp, _i64, _vp, _vp]
+        lib.wmtp_ring_fill.restype = _i32
+        lib.wmtp_ring_fill.argtypes = [_vp, _vp, _vp, _i32, _i64, _i32, _i32, _vp, _i32, _i32, _i32, _i32,
+                                       _vp, _vp, _i64, _vp]
+        lib.wmtp_draft_decode_attn_ring.restype = _i32
+        lib.wmtp_draft_decode_attn_ring.argtypes = [
+            _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
             ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
         lib.wmtp_draft_decode_attn_noalloc.restype = _i32
         lib.wmtp_draft_decode_attn_noalloc.argtypes = [
@@ -341,10 +357,11 @@ def attn_workspace_bytes(B: int, n_q: int, H_q: int, H_kv: int, D: int, n_split:
     return int(load().wmtp_attn_workspace_bytes(B, n_q, H_q, H_kv, D, n_split))
 
 
-def attn_num_splits(B: int, n_q: int, H_kv: int, max_len: int, device=None) -> int:
+def attn_num_splits(B: int, n_q: int, H_kv: int, max_len: int, device=None, fp8: bool = False) -> int:
     dev = device if device is not None else torch.cuda.current_device()
+    fn = load().wmtp_attn_num_splits_fp8 if fp8 else load().wmtp_attn_num_splits
     with torch.cuda.device(dev):
-        return int(load().wmtp_attn_num_splits(B, n_q, H_kv, int(max_len)))
+        return int(fn(B, n_q, H_kv, int(max_len)))
 
 
 class AttnWorkspace:
@@ -460,7 +477,8 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
     _need(out, "out", torch.float32, dev)
     _need(lse, "lse", torch.float32, dev)
     if n_split is None:
-        n_split = attn_num_splits(B, n_q, H_kv, max_len if max_len is not None else stride, dev)
+        n_split = attn_num_splits(B, n_q, H_kv, max_len if max_len is not None else stride, dev,
+                                  fp8=pool_dtype == torch.uint8)
     need = attn_workspace_bytes(B, n_q, H_q, H_kv, D, n_split)
     if workspace is None:
         # one zero-initialised workspace per (device, stream, layout): the merge
@@ -621,4 +639,104 @@ def tree_draft_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
             _ptr(q), B, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(seq_lens),
             _ptr(ring_base), n_sink, window, depth, tree_k, float(scale), _ptr(out), _ptr(lse),
             _ptr(workspace.buf), workspace.nbytes, n_split, _stream(stream)), "tree_draft_attn")
+    return out, lse
+
+
+# ---------------------------------------------------------------- ring path without tables
+def prefill_keep_positions(seq_lens: torch.Tensor, n_sink: int, window: int, stride: int | None = None,
+                           positions: torch.Tensor | None = None, counts: torch.Tensor | None = None,
+                           stream=None):
+    """Prompt positions whose draft KV the windowed draft needs after the
+    prompt (``wmtp_prefill_keep_positions``).  Returns ``(positions[B, stride],
+    counts[B])`` int32; ``stride`` defaults to ``n_sink + window``."""
+    _need(seq_lens, "seq_lens", torch.int32)
+    dev = seq_lens.device
+    B = seq_lens.numel()
+    stride = stride if stride is not None else n_sink + window
+    if positions is None:
+        positions = torch.empty((B, stride), dtype=torch.int32, device=dev)
+    if counts is None:
+        counts = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(positions, "positions", torch.int32, dev)
+    _need(counts, "counts", torch.int32, dev)
+    with torch.cuda.device(dev):
+        _check(load().wmtp_prefill_keep_positions(_ptr(seq_lens), B, n_sink, window, _ptr(positions),
+                                                  positions.shape[-1], _ptr(counts), _stream(stream)),
+               "prefill_keep_positions")
+    return positions, counts
+
+
+def ring_fill(k_rows: torch.Tensor, v_rows: torch.Tensor, seq_lens: torch.Tensor, ring_base: torch.Tensor,
+              n_sink: int, window: int, depth: int, k_pool: torch.Tensor, v_pool: torch.Tensor,
+              tree_k: int = 1, stream=None) -> None:
+    """Write each request's draft K/V of its kept prompt positions (rows in
+    keep order, ``[B, stride, H_kv, D]`` bf16) into its ring (``wmtp_ring_fill``)."""
+    _need(k_pool, "k_pool", torch.bfloat16)
+    dev = k_pool.device
+    for t, nm in ((v_pool, "v_pool"), (k_rows, "k_rows"), (v_rows, "v_rows")):
+        _need(t, nm, torch.bfloat16, dev)
+    _need(seq_lens, "seq_lens", torch.int32, dev)
+    _need(ring_base, "ring_base", torch.int32, dev)
+    B, stride, H_kv, D = k_rows.shape
+    if v_rows.shape != k_rows.shape or k_pool.shape[1:] != (H_kv, D) or v_pool.shape != k_pool.shape:
+        raise ValueError("ring_fill: shape mismatch")
+    with torch.cuda.device(dev):
+        _check(load().wmtp_ring_fill(_ptr(k_rows), _ptr(v_rows), _ptr(seq_lens), B, stride, H_kv, D,
+                                     _ptr(ring_base), n_sink, window, depth, tree_k, _ptr(k_pool),
+                                     _ptr(v_pool), k_pool.shape[0], _stream(stream)), "ring_fill")
+
+
+def draft_decode_attn_ring(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           seq_lens: torch.Tensor, ring_base: torch.Tensor, step: int, n_sink: int,
+                           window: int, depth: int, scale: float, k_new: torch.Tensor | None = None,
+                           v_new: torch.Tensor | None = None, tree_k: int = 1,
+                           out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                           n_split: int | None = None, workspace: AttnWorkspace | None = None,
+                           stream=None):
+    """Draft step ``step`` over the ring with no table (``wmtp_draft_decode_attn_ring``):
+    q [B, 1, H_q, D] (or [B, H_q, D]) bf16; k_new/v_new [B, H_kv, D] bf16 appended at
+    position S + step first (optional).  Returns ``(out [B, 1, H_q, D], lse [B, 1, H_q])``."""
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    for t, nm in ((k_pool, "k_pool"), (v_pool, "v_pool")):
+        _need(t, nm, torch.bfloat16, dev)
+    _need(seq_lens, "seq_lens", torch.int32, dev)
+    _need(ring_base, "ring_base", torch.int32, dev)
+    B = seq_lens.numel()
+    D = q.shape[-1]
+    H_q = q.numel() // (B * D) if B else 0
+    num_slots, H_kv, Dk = k_pool.shape
+    if Dk != D or v_pool.shape != k_pool.shape:
+        raise ValueError("draft_decode_attn_ring: pool shape mismatch")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("draft_decode_attn_ring: give both k_new and v_new, or neither")
+    if k_new is not None:
+        _need(k_new, "k_new", torch.bfloat16, dev)
+        _need(v_new, "v_new", torch.bfloat16, dev)
+        if k_new.numel() != B * H_kv * D or v_new.shape != k_new.shape:
+            raise ValueError("draft_decode_attn_ring: k_new/v_new shape mismatch")
+    if out is None:
+        out = torch.empty((B, 1, H_q, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, 1, H_q), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev)
+    _need(lse, "lse", torch.float32, dev)
+    if n_split is None:
+        n_split = attn_num_splits(B, 1, H_kv, n_sink + window, dev)
+    need = attn_workspace_bytes(B, 1, H_q, H_kv, D, n_split)
+    if workspace is None:
+        sid = torch.cuda.current_stream(dev).cuda_stream if stream is None else stream.cuda_stream
+        key = (dev, sid, B * H_kv, H_q, D, n_split)
+        workspace = _ws_cache.get(key)
+        if workspace is None:
+            workspace = AttnWorkspace(need, dev, stream)
+            _ws_cache[key] = workspace
+    elif workspace.nbytes < need:
+        raise ValueError(f"workspace holds {workspace.nbytes} bytes, {need} needed")
+    with torch.cuda.device(dev):
+        _check(load().wmtp_draft_decode_attn_ring(
+            _ptr(k_new), _ptr(v_new), _ptr(q), B, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots,
+            _ptr(seq_lens), _ptr(ring_base), int(step), n_sink, window, depth, tree_k, float(scale),
+            _ptr(out), _ptr(lse), _ptr(workspace.buf), workspace.nbytes, n_split, _stream(stream)),
+            "draft_decode_attn_ring")
     return out, lse

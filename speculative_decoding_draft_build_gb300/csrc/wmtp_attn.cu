@@ -71,8 +71,7 @@ template <int D, bool kFp8 = false>
 struct Cfg {
     static constexpr int kRowBytes = D * (kFp8 ? 1 : 2);  // one K (or V) row of one head
     static constexpr int kPitch = kRowBytes + 16;         // padded: conflict-free ldmatrix
-    // fp8 rows are half as long: more stages keep the same bytes in flight
-    static constexpr int kStages = kFp8 ? 5 : 3;
+    static constexpr int kStages = 3;
     static constexpr int kWarpTile = kKeysPerWarp * kPitch;     // 16 rows of K (or V)
     static constexpr int kWarpStage = 2 * kWarpTile;            // K rows then V rows
     static constexpr int kWarpBytes = kStages * kWarpStage;     // one warp's pipeline
@@ -155,6 +154,21 @@ struct Fp8View {
 // weights down to 2^-29 keep full fp16 precision (P <= 1 after the running
 // max); the scale is divided out with the output normalisation.
 constexpr float kPScaleF16 = 32768.f;
+// Implicit-table ring attention: no table is read.  Draft step `step` of
+// request b (committed length S = seq_lens[b]) sees kv_len = S + step + 1
+// positions; the kept entries (sinks, then the W most recent when kv_len >
+// n_sink + W) are mapped to ring slots in the kernel by the ring rule of
+// ring_base[b].  With the fused append, the new row is position S + step.
+// seq_lens == nullptr: not a ring launch.
+struct RingView {
+    const int32_t *seq_lens;
+    const int32_t *ring_base;
+    int32_t n_sink;
+    int32_t window;
+    int32_t depth;
+    int32_t tree_k;
+    int32_t step;
+};
 
 inline WorkspaceView carve(void *ws, int64_t rows_q, int64_t rows_kv, int n_split) {
     uint8_t *p = static_cast<uint8_t *>(ws);
@@ -178,15 +192,19 @@ inline WorkspaceView carve_two_level(void *ws, int64_t rows_q, int64_t rows_kv, 
     return v;
 }
 
-template <int D, bool kAppend, bool kExtend, bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
+// fp8 tiles take half the shared memory: two CTAs share an SM (two warps per
+// scheduler hide each other's dependency latency; the bytes in flight per SM
+// equal the bf16 instance's).
+template <int D, bool kAppend, bool kExtend, bool kFp8, bool kRing = false>
+__global__ void __launch_bounds__(kThreads, kFp8 ? 2 : 1) split_decode_kernel(
     const __nv_bfloat16 *__restrict__ q, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t G,
     const void *__restrict__ k_pool, const void *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ table, int64_t table_stride,
     const int32_t *__restrict__ lens, float scale_log2, float *__restrict__ out,
     float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t csz, AppendView ap,
-    ExtendView ev, Fp8View fv) {
+    ExtendView ev, Fp8View fv, RingView rv) {
     static_assert(!(kFp8 && (kAppend || kExtend)), "the fp8 path appends with its own kernel");
+    static_assert(!(kRing && (kExtend || kFp8)), "ring launches are bf16 decode steps");
     using C = Cfg<D, kFp8>;
     constexpr int S = C::kStages;
     constexpr int R = C::kRingTiles;
@@ -207,6 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const int r = lane >> 2;  // MMA group: key row (QK) / output dim row (PV)
     const int c = lane & 3;   // thread in group: query-head pair 2c, 2c+1
     constexpr int KD = D / 16;
+    // Ring launch: the request's length and ring base, loaded before q so
+    // that both loads are in flight together.
+    int32_t r_S = 0, r_base32 = 0;
+    if constexpr (kRing) {
+        r_S = __ldg(rv.seq_lens + b);
+        r_base32 = __ldg(rv.ring_base + b);
+    }
 
     // Query fragments (B operand of QK^T), loaded first so that their latency
     // overlaps the table fetch.  fp8 path: fp16 fragments, with the head
@@ -236,17 +261,39 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         out_scale = __ldg(fv.v_scale + g) * (1.f / kPScaleF16);
     }
 
+    // Ring launch: this step's kv length, its keep rule and the ring.
+    int64_t r_kv = 0, r_lo = 0, r_base = 0;
+    bool r_win = false;
+    if constexpr (kRing) {
+        if (r_S < 0 && threadIdx.x == 0 && split == 0 && g == 0) latch(WMTP_DEV_LEN_RANGE);
+        r_kv = r_S < 0 ? 0 : (int64_t)r_S + rv.step + 1;
+        r_win = r_kv > (int64_t)rv.n_sink + rv.window;
+        r_lo = r_kv - rv.window;
+        r_base = r_base32;
+    }
+    const uint32_t r_mod = kRing ? (uint32_t)(rv.window + rv.depth * rv.tree_k) : 1u;
+    // ring rule on branch 0 in 32-bit arithmetic (positions, ring sizes and
+    // slots are below 2^31: checked on the host)
+    auto ring_slot32 = [&](int64_t pos) -> int32_t {
+        return pos < rv.n_sink ? (int32_t)(r_base + pos)
+                               : (int32_t)r_base + rv.n_sink + (int32_t)((uint32_t)(pos - rv.n_sink) % r_mod);
+    };
     // Slots this request appends in this launch (-1: none).
     int32_t nslot[kMaxNew];
 #pragma unroll
-    for (int i = 0; i < kMaxNew; ++i)
-        nslot[i] = (kAppend && i < ap.n_new) ? __ldg(ap.slots + b * ap.n_new + i) : -1;
+    for (int i = 0; i < kMaxNew; ++i) {
+        if constexpr (kRing)
+            nslot[i] = (kAppend && i == 0 && r_kv > 0) ? ring_slot32(r_kv - 1) : -1;
+        else
+            nslot[i] = (kAppend && i < ap.n_new) ? __ldg(ap.slots + b * ap.n_new + i) : -1;
+    }
 
     // Chunk of this split: a multiple of the key tile, fixed by L and n_split.
     // The slot fetch starts for the chunk of a full row (L = table_stride)
     // while the length is still loading, and is redone only if the real
     // chunk differs.
-    const int32_t L_in = lens[b];
+    const int32_t L_in = kRing ? (int32_t)(r_kv <= 0 ? 0 : (r_win ? (int64_t)rv.n_sink + rv.window : r_kv))
+                               : lens[b];
     auto chunk_of = [&](int64_t len) {
         const int64_t ch = (len + n_split - 1) / n_split;
         return (ch + kTileKeys - 1) / kTileKeys * kTileKeys;
@@ -263,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const int32_t *ring = reinterpret_cast<const int32_t *>(smem + C::kRingOffset) + warp * R * kKeysPerWarp;
     const uint32_t ring_addr = smem_addr(ring);
     auto fetch_slots_from = [&](int t, const int32_t *row, int64_t n) {
-        if (lane < kKeysPerWarp) {
+        if (!kRing && lane < kKeysPerWarp) {
             const int64_t k = (int64_t)t * kTileKeys + warp * kKeysPerWarp + lane;
             const bool in = k < n;
             cp_async_4(ring_addr + ((t % R) * kKeysPerWarp + lane) * 4,
@@ -321,8 +368,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
                           ((size_t)b * ap.n_new * H_kv + g) * C::kRowBytes;
     auto issue = [&](int t) {
         const int st = t % S;
-        const int32_t my_slot = lane < kKeysPerWarp ? ring[(t % R) * kKeysPerWarp + lane] : 0;
         const int64_t k = (int64_t)t * kTileKeys + warp * kKeysPerWarp + (lane & 15);
+        int32_t my_slot = 0;
+        if constexpr (kRing) {
+            const int64_t e = start + k;
+            const int64_t pos = (r_win && e >= rv.n_sink) ? r_lo + (e - rv.n_sink) : e;
+            if (lane < kKeysPerWarp && k < cnt) my_slot = ring_slot32(pos);
+        } else {
+            my_slot = lane < kKeysPerWarp ? ring[(t % R) * kKeysPerWarp + lane] : 0;
+        }
         const bool in = lane < kKeysPerWarp && k < cnt;
         bool ok = in && my_slot >= 0 && my_slot < num_slots;
         if (in && !ok) latch(WMTP_DEV_SLOT_RANGE);
@@ -829,16 +883,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
 // device `dev` (0: none; cached per device and size).
 // Sets the kernel attributes (large dynamic shared memory, non-portable
 // cluster sizes) once per device for one kernel instance.
-template <int D, bool A, bool X, bool F = false>
+template <int D, bool A, bool X, bool F = false, bool RG = false>
 bool prepare_kernel(int dev) {
     static int8_t done[64] = {};
     if (dev < 0 || dev >= 64) return false;
     if (done[dev]) return done[dev] > 0;
-    const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A, X, F>,
+    const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<D, F>::kSmemBytes) == cudaSuccess &&
-                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F>,
-                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG>,
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG>,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
     cudaGetLastError();
     done[dev] = ok ? 1 : -1;
     return ok;
@@ -883,7 +939,7 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
                                 int64_t num_slots, const int32_t *table, int64_t table_stride,
                                 const int32_t *lens, float scale, float *out, float *lse,
                                 void *workspace, int32_t n_split, cudaStream_t stream,
-                                AppendView ap, ExtendView ev, Fp8View fv) {
+                                AppendView ap, ExtendView ev, Fp8View fv, RingView rv) {
     using C = Cfg<D, F>;
     const int64_t rows_q = (int64_t)B * n_q * H_q;
     const int64_t rows_kv = (int64_t)B * n_q * H_kv;
@@ -893,10 +949,17 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WMTP_ECUDA;
     const bool append = ap.n_new > 0;
     const bool extend = ev.seq_lens != nullptr;
-    if (F ? !prepare_kernel<D, false, false, true>(dev)
-          : !(append ? prepare_kernel<D, true, false>(dev)
-                     : (extend ? prepare_kernel<D, false, true>(dev) : prepare_kernel<D, false, false>(dev))))
-        return WMTP_ECUDA;
+    const bool ring = rv.seq_lens != nullptr;
+    bool prepared;
+    if (F)
+        prepared = prepare_kernel<D, false, false, true>(dev);
+    else if (ring)
+        prepared = append ? prepare_kernel<D, true, false, false, true>(dev)
+                          : prepare_kernel<D, false, false, false, true>(dev);
+    else
+        prepared = append ? prepare_kernel<D, true, false>(dev)
+                          : (extend ? prepare_kernel<D, false, true>(dev) : prepare_kernel<D, false, false>(dev));
+    if (!prepared) return WMTP_ECUDA;
     // Cluster size: all splits in one cluster, else the largest cluster that
     // divides n_split into at most kMaxClusters clusters, else none.
     int csz = 0;
@@ -921,12 +984,14 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     if (csz) launch.add_cluster((unsigned)csz);
     const cudaError_t err = cudaLaunchKernelEx(
         &launch.cfg,
-        F ? split_decode_kernel<D, false, false, true>
-          : (append ? split_decode_kernel<D, true, false, false>
-                    : (extend ? split_decode_kernel<D, false, true, false>
-                              : split_decode_kernel<D, false, false, false>)),
+        F      ? split_decode_kernel<D, false, false, true>
+        : ring ? (append ? split_decode_kernel<D, true, false, false, true>
+                         : split_decode_kernel<D, false, false, false, true>)
+               : (append ? split_decode_kernel<D, true, false, false>
+                         : (extend ? split_decode_kernel<D, false, true, false>
+                                   : split_decode_kernel<D, false, false, false>)),
         reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q, H_kv, H_q / H_kv, k_pool, v_pool,
-        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, ap, ev, fv);
+        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, ap, ev, fv, rv);
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
@@ -991,7 +1056,7 @@ wmtp_status launch_split_decode_noalloc(const uint16_t *q, int32_t B, int32_t n_
         H_q, H_kv, H_q / H_kv, static_cast<const void *>(k_pool), static_cast<const void *>(v_pool), num_slots,
         table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)0,
         AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0}, ExtendView{nullptr, nullptr, 0, 0, 0},
-        Fp8View{nullptr, nullptr});
+        Fp8View{nullptr, nullptr}, RingView{nullptr, nullptr, 0, 0, 0, 0, 0});
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
@@ -1024,7 +1089,15 @@ wmtp_status wmtp_attn_workspace_init(void *workspace, size_t workspace_bytes, vo
                : WMTP_ECUDA;
 }
 
-int32_t wmtp_attn_num_splits(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_len) {
+}  // extern "C"
+
+namespace wmtp {
+namespace {
+
+// Split count of a row set: `per_sm` resident CTAs per SM of the instance,
+// cluster capacity from the same instance.
+template <bool F>
+int32_t num_splits_for(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_len, int per_sm) {
     int dev = 0, sms = 152;
     bool sms_known = false;
     if (cudaGetDevice(&dev) == cudaSuccess &&
@@ -1033,7 +1106,7 @@ int32_t wmtp_attn_num_splits(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_l
     cudaGetLastError();
     const int64_t rows = (int64_t)(B > 0 ? B : 1) * (n_q > 0 ? n_q : 1) * (H_kv > 0 ? H_kv : 1);
     const int64_t tiles = (max_len + kTileKeys - 1) / kTileKeys;
-    const int64_t by_sms = sms / rows;  // one CTA per SM, one wave
+    const int64_t by_sms = (int64_t)sms * per_sm / rows;  // every resident CTA slot, one wave
     int64_t n;
     if (tiles >= 4 * by_sms) {
         // long rows: fill the SMs; the merge is small next to the copies
@@ -1047,7 +1120,7 @@ int32_t wmtp_attn_num_splits(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_l
         n = by_sms < half ? by_sms : half;
         if (n > kMaxClusterMerge) {
             int cap = 0;
-            if (sms_known) cap = cluster_capacity<256>(dev, kMaxClusterMerge);
+            if (sms_known) cap = cluster_capacity<256, F>(dev, kMaxClusterMerge);
             n = n / kMaxClusterMerge * kMaxClusterMerge;
             if (n > kMaxClusterMerge * kMaxClusters) n = kMaxClusterMerge * kMaxClusters;
             while (n > kMaxClusterMerge && rows * (n / kMaxClusterMerge) > cap) n -= kMaxClusterMerge;
@@ -1056,6 +1129,19 @@ int32_t wmtp_attn_num_splits(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_l
     if (n < 1) n = 1;
     if (n > kMaxSplits) n = kMaxSplits;
     return (int32_t)n;
+}
+
+}  // namespace
+}  // namespace wmtp
+
+extern "C" {
+
+int32_t wmtp_attn_num_splits(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_len) {
+    return num_splits_for<false>(B, n_q, H_kv, max_len, 1);
+}
+
+int32_t wmtp_attn_num_splits_fp8(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_len) {
+    return num_splits_for<true>(B, n_q, H_kv, max_len, 2);
 }
 
 }  // extern "C"
@@ -1071,7 +1157,8 @@ wmtp_status draft_decode_attn_checked(const uint16_t *q, int32_t B, int32_t n_q,
                                       void *workspace, size_t workspace_bytes_, int32_t n_split,
                                       void *stream, AppendView ap,
                                       ExtendView ev = ExtendView{nullptr, nullptr, 0, 0, 0},
-                                      Fp8View fv = Fp8View{nullptr, nullptr}) {
+                                      Fp8View fv = Fp8View{nullptr, nullptr},
+                                      RingView rv = RingView{nullptr, nullptr, 0, 0, 0, 0, 0}) {
     if (B < 0 || n_q < 0 || H_q < 1 || H_kv < 1 || (H_q % H_kv) != 0) return WMTP_EINVAL;
     if (H_q / H_kv > kMaxGroup) return WMTP_EINVAL;
     if (D != 128 && D != 256) return WMTP_EINVAL;
@@ -1080,11 +1167,13 @@ wmtp_status draft_decode_attn_checked(const uint16_t *q, int32_t B, int32_t n_q,
     if ((int64_t)B * n_q > 65535 || H_kv > 65535) return WMTP_EINVAL;
     if (ap.n_new < 0 || ap.n_new > kMaxNew) return WMTP_EINVAL;
     if (B == 0 || n_q == 0) return WMTP_OK;
-    if (!q || !k_pool || !v_pool || !table || !lens || !out) return WMTP_EINVAL;
+    if (!q || !k_pool || !v_pool || !out) return WMTP_EINVAL;
+    if (!rv.seq_lens && (!table || !lens)) return WMTP_EINVAL;
+    if (rv.seq_lens && !rv.ring_base) return WMTP_EINVAL;
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(q) & 3u))
         return WMTP_EINVAL;
-    if (ap.n_new > 0 && (!ap.k_new || !ap.v_new || !ap.slots || !aligned16(ap.k_new) ||
+    if (ap.n_new > 0 && (!ap.k_new || !ap.v_new || (!ap.slots && !rv.seq_lens) || !aligned16(ap.k_new) ||
                          !aligned16(ap.v_new)))
         return WMTP_EINVAL;
     if (n_split > 1) {
@@ -1098,18 +1187,18 @@ wmtp_status draft_decode_attn_checked(const uint16_t *q, int32_t B, int32_t n_q,
         if (D == 256)
             return launch_split_decode<256, true>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
                                                   table_stride, lens, scale, out, lse, workspace, n_split, s,
-                                                  ap, ev, fv);
+                                                  ap, ev, fv, rv);
         return launch_split_decode<128, true>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
                                               table_stride, lens, scale, out, lse, workspace, n_split, s, ap,
-                                              ev, fv);
+                                              ev, fv, rv);
     }
     if (D == 256)
         return launch_split_decode<256, false>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
                                                table_stride, lens, scale, out, lse, workspace, n_split, s, ap,
-                                               ev, fv);
+                                               ev, fv, rv);
     return launch_split_decode<128, false>(q, B, n_q, H_q, H_kv, k_pool, v_pool, num_slots, table,
                                            table_stride, lens, scale, out, lse, workspace, n_split, s, ap, ev,
-                                           fv);
+                                           fv, rv);
 }
 
 }  // namespace
@@ -1216,6 +1305,36 @@ wmtp_status wmtp_draft_decode_attn_fp8(const uint16_t *q, int32_t B, int32_t n_q
                                      workspace_bytes_, n_split, stream,
                                      AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0},
                                      ExtendView{nullptr, nullptr, 0, 0, 0}, Fp8View{k_scale, v_scale});
+}
+
+}  // extern "C"
+
+extern "C" {
+
+wmtp_status wmtp_draft_decode_attn_ring(const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q,
+                                        int32_t B, int32_t H_q, int32_t H_kv, int32_t D, uint16_t *k_pool,
+                                        uint16_t *v_pool, int64_t num_slots, const int32_t *seq_lens,
+                                        const int32_t *ring_base, int32_t step, int32_t n_sink,
+                                        int32_t window, int32_t depth, int32_t tree_k, float scale,
+                                        float *out, float *lse, void *workspace, size_t workspace_bytes_,
+                                        int32_t n_split, void *stream) {
+    if (n_sink < 0 || window < 1 || depth < 1 || tree_k < 1 || step < 0) return WMTP_EINVAL;
+    // ring slots and positions stay below 2^31 (the kernel maps them in
+    // 32-bit arithmetic)
+    if ((int64_t)n_sink + window + (int64_t)depth * tree_k > (int64_t)1 << 30 || num_slots > INT32_MAX)
+        return WMTP_EINVAL;
+    if ((k_new == nullptr) != (v_new == nullptr)) return WMTP_EINVAL;
+    if (B > 0 && (!seq_lens || !ring_base)) return WMTP_EINVAL;
+    const AppendView ap = k_new ? AppendView{reinterpret_cast<const __nv_bfloat16 *>(k_new),
+                                             reinterpret_cast<const __nv_bfloat16 *>(v_new), nullptr,
+                                             reinterpret_cast<__nv_bfloat16 *>(k_pool),
+                                             reinterpret_cast<__nv_bfloat16 *>(v_pool), 1}
+                                : AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0};
+    return draft_decode_attn_checked(q, B, 1, H_q, H_kv, D, k_pool, v_pool, num_slots, nullptr,
+                                     (int64_t)n_sink + window, nullptr, scale, out, lse, workspace,
+                                     workspace_bytes_, n_split, stream, ap, ExtendView{nullptr, nullptr, 0, 0, 0},
+                                     Fp8View{nullptr, nullptr},
+                                     RingView{seq_lens, ring_base, n_sink, window, depth, tree_k, step});
 }
 
 }  // extern "C"

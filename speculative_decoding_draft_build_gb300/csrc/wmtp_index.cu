@@ -152,6 +152,72 @@ __global__ void __launch_bounds__(256) append_kv_fp8_kernel(
     v_pool[slot * chunks_per_token + e] = quant(v_new[idx], iv);
 }
 
+// Pruned draft prefill ("Windowed-MTP", §7 "Prefill sparsification and
+// TTFT"): after a prompt of S positions the windowed draft needs only its KV
+// of keep(S) = [0, n_sink) u [S - W, S) (all S positions when S <= n_sink + W).
+// Entry i of request b's kept list is position i (sinks, or a short prompt)
+// or S - W + (i - n_sink).
+__device__ __forceinline__ int64_t kept_position(int64_t S, int64_t i, int32_t n_sink, int32_t window) {
+    const bool win = S > (int64_t)n_sink + window;
+    return (win && i >= n_sink) ? S - window + (i - n_sink) : i;
+}
+
+__device__ __forceinline__ int64_t kept_count(int64_t S, int32_t n_sink, int32_t window) {
+    if (S <= 0) return 0;
+    return S > (int64_t)n_sink + window ? (int64_t)n_sink + window : S;
+}
+
+// One grid row per request; writes the kept prompt positions and their count.
+__global__ void __launch_bounds__(256) keep_positions_kernel(const int32_t *__restrict__ seq_lens,
+                                                             int32_t n_sink, int32_t window,
+                                                             int32_t *__restrict__ positions, int64_t stride,
+                                                             int32_t *__restrict__ counts) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int32_t b = blockIdx.y;
+    const int64_t S = seq_lens[b];
+    const int64_t n = kept_count(S, n_sink, window);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (S < 0) latch(WMTP_DEV_LEN_RANGE);
+        if (n > stride) latch(WMTP_DEV_TABLE_OVERFLOW);
+        counts[b] = (int32_t)(n < stride ? n : stride);
+    }
+    const int64_t n_write = n < stride ? n : stride;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_write;
+         i += (int64_t)gridDim.x * blockDim.x)
+        positions[(int64_t)b * stride + i] = (int32_t)kept_position(S, i, n_sink, window);
+}
+
+// Ring fill from the pruned prefill: row i of request b (its draft K and V at
+// kept position i, bf16 [B][stride][H_kv][D]) goes to the ring slot of that
+// position.  One thread per 16-byte chunk; grid row = request.
+__global__ void __launch_bounds__(256) ring_fill_kernel(
+    const uint4 *__restrict__ k_rows, const uint4 *__restrict__ v_rows, const int32_t *__restrict__ seq_lens,
+    const int32_t *__restrict__ ring_base, int32_t n_sink, int32_t window, int32_t depth, int32_t tree_k,
+    int64_t stride, int32_t chunks_per_row, uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool,
+    int64_t num_slots) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int32_t b = blockIdx.y;
+    const int64_t S = seq_lens[b];
+    int64_t n = kept_count(S, n_sink, window);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && n > stride) latch(WMTP_DEV_TABLE_OVERFLOW);
+    if (n > stride) n = stride;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n * chunks_per_row) return;
+    const int64_t i = idx / chunks_per_row;
+    const int64_t e = idx - i * chunks_per_row;
+    const int64_t slot =
+        ring_slot(ring_base[b], kept_position(S, i, n_sink, window), 0, n_sink, window, depth, tree_k);
+    if (slot < 0 || slot >= num_slots) {
+        latch(WMTP_DEV_SLOT_RANGE);
+        return;
+    }
+    const int64_t src = ((int64_t)b * stride + i) * chunks_per_row + e;
+    k_pool[slot * chunks_per_row + e] = k_rows[src];
+    v_pool[slot * chunks_per_row + e] = v_rows[src];
+}
+
 }  // namespace
 
 cudaError_t read_index_error(int32_t *code, bool clear) {
@@ -302,6 +368,50 @@ wmtp_status wmtp_append_kv_fp8(const uint16_t *k_new, const uint16_t *v_new,
                               reinterpret_cast<const uint4 *>(v_new), slots, total, chunks, D / 8, k_scale,
                               v_scale, reinterpret_cast<uint2 *>(k_pool), reinterpret_cast<uint2 *>(v_pool),
                               num_slots) == cudaSuccess
+               ? WMTP_OK
+               : WMTP_ECUDA;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+wmtp_status wmtp_prefill_keep_positions(const int32_t *seq_lens, int32_t B, int32_t n_sink,
+                                        int32_t window, int32_t *positions, int64_t stride,
+                                        int32_t *counts, void *stream) {
+    if (B < 0 || n_sink < 0 || window < 1 || stride < 1 || B > 65535) return WMTP_EINVAL;
+    if (B == 0) return WMTP_OK;
+    if (!seq_lens || !positions || !counts) return WMTP_EINVAL;
+    constexpr int kThreads = 256;
+    const int64_t need = (int64_t)n_sink + window < stride ? (int64_t)n_sink + window : stride;
+    int64_t gx = (need + kThreads - 1) / kThreads;
+    if (gx < 1) gx = 1;
+    PdlLaunch L(dim3((unsigned)gx, (unsigned)B), dim3(kThreads), 0, as_stream(stream));
+    return cudaLaunchKernelEx(&L.cfg, keep_positions_kernel, seq_lens, n_sink, window, positions, stride,
+                              counts) == cudaSuccess
+               ? WMTP_OK
+               : WMTP_ECUDA;
+}
+
+wmtp_status wmtp_ring_fill(const uint16_t *k_rows, const uint16_t *v_rows, const int32_t *seq_lens,
+                           int32_t B, int64_t stride, int32_t H_kv, int32_t D, const int32_t *ring_base,
+                           int32_t n_sink, int32_t window, int32_t depth, int32_t tree_k, uint16_t *k_pool,
+                           uint16_t *v_pool, int64_t num_slots, void *stream) {
+    if (B < 0 || B > 65535 || stride < 1 || H_kv < 1 || D < 1 || (D % 8) != 0 || n_sink < 0 || window < 1 ||
+        depth < 1 || tree_k < 1 || num_slots < 0)
+        return WMTP_EINVAL;
+    if (B == 0) return WMTP_OK;
+    if (!k_rows || !v_rows || !seq_lens || !ring_base || !k_pool || !v_pool) return WMTP_EINVAL;
+    if (!aligned16(k_rows) || !aligned16(v_rows) || !aligned16(k_pool) || !aligned16(v_pool)) return WMTP_EINVAL;
+    const int32_t chunks = H_kv * D / 8;
+    const int64_t rows = (int64_t)n_sink + window < stride ? (int64_t)n_sink + window : stride;
+    constexpr int kThreads = 256;
+    const int64_t gx = (rows * chunks + kThreads - 1) / kThreads;
+    PdlLaunch L(dim3((unsigned)gx, (unsigned)B), dim3(kThreads), 0, as_stream(stream));
+    return cudaLaunchKernelEx(&L.cfg, ring_fill_kernel, reinterpret_cast<const uint4 *>(k_rows),
+                              reinterpret_cast<const uint4 *>(v_rows), seq_lens, ring_base, n_sink, window, depth,
+                              tree_k, stride, chunks, reinterpret_cast<uint4 *>(k_pool),
+                              reinterpret_cast<uint4 *>(v_pool), num_slots) == cudaSuccess
                ? WMTP_OK
                : WMTP_ECUDA;
 }
