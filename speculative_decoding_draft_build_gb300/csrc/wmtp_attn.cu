@@ -278,15 +278,13 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 2 : 1) split_decode_kernel(
         return pos < rv.n_sink ? (int32_t)(r_base + pos)
                                : (int32_t)r_base + rv.n_sink + (int32_t)((uint32_t)(pos - rv.n_sink) % r_mod);
     };
-    // Slots this request appends in this launch (-1: none).
+    // Slots this request appends in this launch (-1: none).  A ring launch
+    // needs none before the loop: its new row is always the last kept entry
+    // (position S + step), and the writer maps it after the loop.
     int32_t nslot[kMaxNew];
 #pragma unroll
-    for (int i = 0; i < kMaxNew; ++i) {
-        if constexpr (kRing)
-            nslot[i] = (kAppend && i == 0 && r_kv > 0) ? ring_slot32(r_kv - 1) : -1;
-        else
-            nslot[i] = (kAppend && i < ap.n_new) ? __ldg(ap.slots + b * ap.n_new + i) : -1;
-    }
+    for (int i = 0; i < kMaxNew; ++i)
+        nslot[i] = (!kRing && kAppend && i < ap.n_new) ? __ldg(ap.slots + b * ap.n_new + i) : -1;
 
     // Chunk of this split: a multiple of the key tile, fixed by L and n_split.
     // The slot fetch starts for the chunk of a full row (L = table_stride)
@@ -388,7 +386,9 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 2 : 1) split_decode_kernel(
         // A key whose slot this launch appends is marked -2 - i (row i of
         // the new rows); its vm bit stays set.
         int32_t src_slot = my_slot;
-        if constexpr (kAppend) {
+        if constexpr (kAppend && kRing) {
+            if (ok && start + k == L - 1) src_slot = -2;
+        } else if constexpr (kAppend) {
 #pragma unroll
             for (int i = kMaxNew - 1; i >= 0; --i)
                 if (ok && my_slot == nslot[i]) src_slot = -2 - i;
@@ -583,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 2 : 1) split_decode_kernel(
 #pragma unroll
         for (int i = 1; i < kMaxNew; ++i)
             if (warp == i) sl = nslot[i];
+        if constexpr (kRing) sl = r_kv > 0 ? ring_slot32(r_kv - 1) : -1;
         if (sl < 0 || sl >= num_slots) {
             if (lane == 0) latch(WMTP_DEV_SLOT_RANGE);
         } else {
