@@ -528,8 +528,10 @@ def measure_extend(w, args, dev):
     """Draft-extend pass on the million-token workload: the draft forward over
     n_new = 5 accepted tokens (positions S..S+4) in one launch, windowed and
     full-context.  Event-timed with L2 flushed before each launch; algorithmic
-    bytes count each token's own key set (K and V of every KV head), the union
-    table, q, out and lse."""
+    bytes are the pass's unique bytes: K and V of every key of the union table
+    once (every KV head), the table, q, out and lse.  `token_reads_gbs` counts
+    instead each token's own key set, as this kernel reads it (the tokens of
+    a request share most of their keys)."""
     import speculative_decoding_draft_build_gb300 as wm
     c = w.cfg
     B, S, H_q, H_kv, D = c["B"], c["S"], c["H_q"], c["H_kv"], c["D"]
@@ -566,11 +568,14 @@ def measure_extend(w, args, dev):
         t = statistics.median(ts)
         keys = sum(min(S + j + 1, c["n_sink"] + c["W"]) if windowed else S + j + 1 for j in range(n))
         L = int(ln.max().item())
-        nbytes = B * (keys * H_kv * D * 2 * 2 + 4 * L + n * H_q * (D * 2 + (D + 1) * 4))
+        rest = 4 * L + n * H_q * (D * 2 + (D + 1) * 4)
+        nbytes = B * (L * H_kv * D * 2 * 2 + rest)
+        token_bytes = B * (keys * H_kv * D * 2 * 2 + rest)
         res["windowed" if windowed else "full"] = {
             "us_per_pass": round(t * 1e6, 2), "kv_gbs": round(nbytes / t / 1e9, 1),
             "frac_of_hbm": round(nbytes / t / 1e9 / peak, 4), "n_split": ns,
-            "union_keys": L, "bytes_per_pass": int(nbytes)}
+            "union_keys": L, "bytes_per_pass": int(nbytes),
+            "token_reads_gbs": round(token_bytes / t / 1e9, 1)}
     return res
 
 

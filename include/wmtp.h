@@ -177,7 +177,9 @@ wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
  * n_split <= 16; in two levels (clusters of up to 16, then at most 8
  * cluster partials per output slice through the workspace) when n_split
  * splits into such clusters; else through the workspace by the last CTA to
- * finish.  An empty row gives out = 0, lse = -inf.
+ * finish.  A cluster merge is used only when the device holds all of the
+ * launch's clusters at once (cudaOccupancyMaxActiveClusters).  An empty row
+ * gives out = 0, lse = -inf.
  *
  * q        device bf16 [B][n_q][H_q][D], D in {128, 256}, H_q / H_kv <= 8.
  * table    device int32, row b at table + b * table_stride.

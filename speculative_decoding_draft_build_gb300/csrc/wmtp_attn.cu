@@ -929,11 +929,6 @@ int cluster_capacity(int dev, int n) {
     return ok ? known[dev][n] : 0;
 }
 
-template <int D, bool F = false>
-bool cluster_merge_ok(int dev, int n) {
-    return cluster_capacity<D, F>(dev, n) > 0;
-}
-
 template <int D, bool F>
 wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
                                 int32_t H_kv, const void *k_pool, const void *v_pool,
@@ -962,14 +957,21 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
                           : (extend ? prepare_kernel<D, false, true>(dev) : prepare_kernel<D, false, false>(dev));
     if (!prepared) return WMTP_ECUDA;
     // Cluster size: all splits in one cluster, else the largest cluster that
-    // divides n_split into at most kMaxClusters clusters, else none.
+    // divides n_split into at most kMaxClusters clusters, provided the device
+    // holds every cluster of the launch at once (clusters that wait for a
+    // second wave cost more than any merge saves); else no cluster: the
+    // workspace merge, which needs no co-residency.
     int csz = 0;
     if (n_split > 1) {
-        if (n_split <= kMaxClusterMerge && cluster_merge_ok<D, F>(dev, n_split)) {
+        auto fits = [&](int c) {
+            const int cap = cluster_capacity<D, F>(dev, c);
+            return cap > 0 && rows_kv * (n_split / c) <= cap;
+        };
+        if (n_split <= kMaxClusterMerge && fits(n_split)) {
             csz = n_split;
         } else {
             for (int c = kMaxClusterMerge; c >= 2; --c) {
-                if (n_split % c == 0 && n_split / c <= kMaxClusters && cluster_merge_ok<D, F>(dev, c)) {
+                if (n_split % c == 0 && n_split / c <= kMaxClusters && fits(c)) {
                     csz = c;
                     break;
                 }
@@ -1129,6 +1131,12 @@ int32_t num_splits_for(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_len, in
     }
     if (n < 1) n = 1;
     if (n > kMaxSplits) n = kMaxSplits;
+    // Up to one cluster: drop splits the whole-tile chunks leave empty (the
+    // chunk of n splits covers ceil(tiles / n) tiles).
+    if (n <= kMaxClusterMerge && tiles > 0) {
+        const int64_t per = (tiles + n - 1) / n;
+        n = (tiles + per - 1) / per;
+    }
     return (int32_t)n;
 }
 

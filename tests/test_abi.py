@@ -78,8 +78,8 @@ def test_split_heuristic_without_a_device(lib):
     ns = lib.wmtp_attn_num_splits
     assert ns(1, 1, 2, 4096) == 16           # short row: two key tiles per split, one cluster
     assert ns(1, 1, 2, 1_048_582) == 76      # long row: one CTA per SM
-    assert ns(8, 1, 2, 4096) == 9            # 16 rows fill the SMs at 9 splits each
-    assert ns(1, 1, 2, 1088) == 8            # 17 tiles
+    assert ns(8, 1, 2, 4096) == 8            # 16 rows fill the SMs at 9 splits; 8 cover the 64 tiles
+    assert ns(1, 1, 2, 1088) == 6            # 17 tiles: 8 splits of 3 tiles leave 2 empty
     assert ns(1, 1, 2, 100) == 1
     assert ns(1, 1, 1, 200 * 64) == 16
     assert ns(1, 1, 2, 0) == 1
