@@ -548,7 +548,7 @@ def measure_extend(w, args, dev):
     for windowed in (True, False):
         tab, ln = wm.build_extend_indices(seq, nn, c["n_sink"], c["W"], c["gamma"] + 1,
                                           windowed=windowed, req_to_token=w.rtt)
-        ns = wm.attn_num_splits(B, n, H_kv, tab.shape[-1], dev)
+        ns = wm.extend_num_splits(B, n, H_kv, tab.shape[-1], dev)
         ws = wm.AttnWorkspace(wm.attn_workspace_bytes(B, n, H_q, H_kv, D, ns), dev)
 
         def call():

@@ -270,7 +270,13 @@ wmtp_status wmtp_draft_decode_attn_append(const uint16_t *k_new,
  * seq_lens   device int32 [B] (S); n_new device int32 [B].
  * Other arguments, the split plan, workspace and errors as
  * wmtp_draft_decode_attn; additionally WMTP_EINVAL for null seq_lens or
- * n_new, n_sink < 0 or W < 1. */
+ * n_new, n_sink < 0 or W < 1.
+ * With 2 <= n_q <= 8, n_split <= 128 and table_stride >= 1024 * n_split
+ * (long rows) one launch reads each union key once for all of a request's
+ * tokens (a CTA per split of the union row and KV head, one warp per token)
+ * and merges the splits through the workspace; otherwise every (request,
+ * token) row is its own set of CTAs, as wmtp_draft_decode_attn.
+ * wmtp_extend_num_splits gives the usual split count of either launch. */
 wmtp_status wmtp_draft_extend_attn(const uint16_t *q, int32_t B, int32_t n_q,
                                    int32_t H_q, int32_t H_kv, int32_t D,
                                    const uint16_t *k_pool,
@@ -282,6 +288,13 @@ wmtp_status wmtp_draft_extend_attn(const uint16_t *q, int32_t B, int32_t n_q,
                                    float *out, float *lse, void *workspace,
                                    size_t workspace_bytes, int32_t n_split,
                                    void *stream);
+
+/* Split count for wmtp_draft_extend_attn when the caller has no preference:
+ * n = min(wmtp_attn_num_splits(B, 1, H_kv, max_len), 128) when
+ * 2 <= n_q <= 8 and max_len >= 1024 * n (the one-read launch), else
+ * wmtp_attn_num_splits(B, n_q, H_kv, max_len). */
+int32_t wmtp_extend_num_splits(int32_t B, int32_t n_q, int32_t H_kv,
+                               int64_t max_len);
 
 /* Attention-mass diagnostics of the windowed draft ("Windowed-MTP", §5 "A
  * partition-function view"; App. C, Table 12), per query row, from the
@@ -480,8 +493,8 @@ wmtp_status wmtp_append_kv_fp8(const uint16_t *k_new, const uint16_t *v_new,
  * [H_kv]).  The codes are widened exactly to fp16 on chip and q is rounded
  * to fp16 (exact for |q| >= 2^-14), products accumulate in fp32. */
 /* Split count wmtp_draft_decode_attn_fp8 uses when the caller has no
- * preference: as wmtp_attn_num_splits, for the fp8 instance, which holds two
- * CTAs per SM (its tiles take half the shared memory). */
+ * preference: as wmtp_attn_num_splits, with the cluster capacity of the fp8
+ * instance (one CTA per SM, a deeper copy pipeline). */
 int32_t wmtp_attn_num_splits_fp8(int32_t B, int32_t n_q, int32_t H_kv,
                                  int64_t max_len);
 

@@ -38,7 +38,7 @@ __all__ = [
     "WmtpError", "load", "build", "version", "device_error",
     "build_draft_indices", "build_extend_indices", "ring_map", "append_kv", "draft_decode_attn",
     "draft_decode_attn_append", "draft_extend_attn", "attn_mass_diagnostics",
-    "attn_workspace_bytes", "attn_num_splits", "AttnWorkspace", "draft_decode_attn_noalloc",
+    "attn_workspace_bytes", "attn_num_splits", "extend_num_splits", "AttnWorkspace", "draft_decode_attn_noalloc",
     "tree_draft_attn", "tree_workspace_bytes", "tree_num_splits",
     "append_kv_fp8", "draft_decode_attn_fp8", "prefill_keep_positions", "ring_fill",
     "draft_decode_attn_ring",
@@ -133,6 +133,8 @@ def load():
         lib.wmtp_append_kv_fp8.restype = _i32
         lib.wmtp_append_kv_fp8.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64,
                                            _vp]
+        lib.wmtp_extend_num_splits.restype = _i32
+        lib.wmtp_extend_num_splits.argtypes = [_i32, _i32, _i32, _i64]
         lib.wmtp_attn_num_splits_fp8.restype = _i32
         lib.wmtp_attn_num_splits_fp8.argtypes = [_i32, _i32, _i32, _i64]
         lib.wmtp_draft_decode_attn_fp8.restype = _i32
@@ -364,6 +366,13 @@ def attn_num_splits(B: int, n_q: int, H_kv: int, max_len: int, device=None, fp8:
         return int(fn(B, n_q, H_kv, int(max_len)))
 
 
+def extend_num_splits(B: int, n_q: int, H_kv: int, max_len: int, device=None) -> int:
+    """Usual split count of :func:`draft_extend_attn` (``wmtp_extend_num_splits``)."""
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        return int(load().wmtp_extend_num_splits(B, n_q, H_kv, int(max_len)))
+
+
 class AttnWorkspace:
     """Device scratch for the split-KV partials, zeroed once at creation.
 
@@ -477,8 +486,12 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
     _need(out, "out", torch.float32, dev)
     _need(lse, "lse", torch.float32, dev)
     if n_split is None:
-        n_split = attn_num_splits(B, n_q, H_kv, max_len if max_len is not None else stride, dev,
-                                  fp8=pool_dtype == torch.uint8)
+        ml = max_len if max_len is not None else stride
+        if append is not None and append[0] == "extend":
+            with torch.cuda.device(dev):
+                n_split = int(load().wmtp_extend_num_splits(B, n_q, H_kv, int(ml)))
+        else:
+            n_split = attn_num_splits(B, n_q, H_kv, ml, dev, fp8=pool_dtype == torch.uint8)
     need = attn_workspace_bytes(B, n_q, H_q, H_kv, D, n_split)
     if workspace is None:
         # one zero-initialised workspace per (device, stream, layout): the merge

@@ -67,11 +67,16 @@ constexpr int kMaxClusters = 8;       // clusters merged by the second level
 constexpr int kMaxNew = 4;            // rows one request appends in a fused call (one per warp)
 constexpr float kLn2 = 0.69314718055994530942f;
 
+#ifndef WMTP_FP8_STAGES
+#define WMTP_FP8_STAGES 5
+#endif
+
 template <int D, bool kFp8 = false>
 struct Cfg {
     static constexpr int kRowBytes = D * (kFp8 ? 1 : 2);  // one K (or V) row of one head
     static constexpr int kPitch = kRowBytes + 16;         // padded: conflict-free ldmatrix
-    static constexpr int kStages = 3;
+    // fp8 rows are half as long: more stages keep as many bytes in flight
+    static constexpr int kStages = kFp8 ? WMTP_FP8_STAGES : 3;
     static constexpr int kWarpTile = kKeysPerWarp * kPitch;     // 16 rows of K (or V)
     static constexpr int kWarpStage = 2 * kWarpTile;            // K rows then V rows
     static constexpr int kWarpBytes = kStages * kWarpStage;     // one warp's pipeline
@@ -192,11 +197,8 @@ inline WorkspaceView carve_two_level(void *ws, int64_t rows_q, int64_t rows_kv, 
     return v;
 }
 
-// fp8 tiles take half the shared memory: two CTAs share an SM (two warps per
-// scheduler hide each other's dependency latency; the bytes in flight per SM
-// equal the bf16 instance's).
 template <int D, bool kAppend, bool kExtend, bool kFp8, bool kRing = false>
-__global__ void __launch_bounds__(kThreads, kFp8 ? 2 : 1) split_decode_kernel(
+__global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const __nv_bfloat16 *__restrict__ q, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t G,
     const void *__restrict__ k_pool, const void *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ table, int64_t table_stride,
@@ -1150,7 +1152,7 @@ int32_t wmtp_attn_num_splits(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_l
 }
 
 int32_t wmtp_attn_num_splits_fp8(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_len) {
-    return num_splits_for<true>(B, n_q, H_kv, max_len, 2);
+    return num_splits_for<true>(B, n_q, H_kv, max_len, 1);
 }
 
 }  // extern "C"
@@ -1191,6 +1193,17 @@ wmtp_status draft_decode_attn_checked(const uint16_t *q, int32_t B, int32_t n_q,
             return WMTP_ECAPACITY;
     }
     cudaStream_t s = as_stream(stream);
+    if (ev.seq_lens && !fv.k_scale && !rv.seq_lens && n_q >= 2 && n_q <= kMaxExtendTokens &&
+        n_split <= kMaxExtendSplits && table_stride >= (int64_t)kExtendMinKeysPerSplit * n_split) {
+        // several new tokens per request: one K/V read serves them all
+        WorkspaceView w{nullptr, nullptr, nullptr};
+        if (n_split > 1) w = carve(workspace, (int64_t)B * n_q * H_q, (int64_t)B * n_q * H_kv, n_split);
+        return extend_multi_launch(static_cast<const uint16_t *>(q), B, n_q, H_q, H_kv, D,
+                                   static_cast<const uint16_t *>(k_pool), static_cast<const uint16_t *>(v_pool),
+                                   num_slots, table, table_stride, lens, ev.seq_lens, ev.n_new, ev.n_sink,
+                                   ev.window, ev.windowed, scale, out, lse, w.counters, w.lse_part, w.o_part,
+                                   n_split, s);
+    }
     if (fv.k_scale) {
         if (!fv.v_scale) return WMTP_EINVAL;
         if (D == 256)

@@ -249,11 +249,12 @@ const char *wmtp_status_string(int32_t status) {
 wmtp_status wmtp_get_device_error(int32_t *code, int32_t clear) {
     if (!code) return WMTP_EINVAL;
     if (cudaDeviceSynchronize() != cudaSuccess) return WMTP_ECUDA;
-    int32_t a = 0, b = 0, t = 0;
+    int32_t a = 0, b = 0, t = 0, x = 0;
     if (read_index_error(&a, clear != 0) != cudaSuccess) return WMTP_ECUDA;
     if (read_attn_error(&b, clear != 0) != cudaSuccess) return WMTP_ECUDA;
     if (read_tree_tc_error(&t, clear != 0) != cudaSuccess) return WMTP_ECUDA;
-    *code = a ? a : (b ? b : t);
+    if (read_extend_error(&x, clear != 0) != cudaSuccess) return WMTP_ECUDA;
+    *code = a ? a : (b ? b : (t ? t : x));
     return WMTP_OK;
 }
 

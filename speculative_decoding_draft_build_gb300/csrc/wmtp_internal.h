@@ -21,6 +21,23 @@ wmtp_status tree_tc_launch(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
                            int32_t window, int32_t depth, int32_t tree_k, float scale, float *out,
                            float *lse, void *workspace, int32_t n_split, cudaStream_t stream);
 
+// Draft extend with one K/V read per request (wmtp_extend.cu): up to
+// kMaxExtendTokens tokens per request, up to kMaxExtendSplits splits; the
+// partials use the split-order workspace layout of the decode attention.
+constexpr int kMaxExtendTokens = 8;
+constexpr int kMaxExtendSplits = 128;
+// Rows (table strides) of at least this many keys per split take the
+// one-read launch; shorter rows, where a CTA sees a few tiles and latency
+// dominates, are faster as one set of CTAs per token (L2 serves the rereads).
+constexpr int kExtendMinKeysPerSplit = 1024;
+cudaError_t read_extend_error(int32_t *code, bool clear);
+wmtp_status extend_multi_launch(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t D,
+                                const uint16_t *k_pool, const uint16_t *v_pool, int64_t num_slots,
+                                const int32_t *table, int64_t table_stride, const int32_t *lens,
+                                const int32_t *seq_lens, const int32_t *n_new, int32_t n_sink, int32_t window,
+                                int32_t windowed, float scale, float *out, float *lse, int32_t *counters,
+                                float *lse_part, float *o_part, int32_t n_split, cudaStream_t stream);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }

@@ -83,11 +83,11 @@ def test_split_heuristic_without_a_device(lib):
     assert ns(1, 1, 2, 100) == 1
     assert ns(1, 1, 1, 200 * 64) == 16
     assert ns(1, 1, 2, 0) == 1
-    # the fp8 instance holds two CTAs per SM
+    # the fp8 instance: one CTA per SM as well
     ns8 = lib.wmtp_attn_num_splits_fp8
-    assert ns8(1, 1, 2, 1_048_582) == 152
+    assert ns8(1, 1, 2, 1_048_582) == 76
     assert ns8(1, 1, 2, 4096) == 16
-    assert ns8(8, 1, 2, 4096) == 16
+    assert ns8(8, 1, 2, 4096) == 8
     assert ns8(1, 1, 2, 100) == 1
 
 

@@ -101,3 +101,15 @@ def test_extend_one_token_equals_decode_step():
     a = wm.draft_extend_attn(q, kp, vp, tab, ln, seq, nn, n_sink, W, 1 / 16, n_split=16)
     b = wm.draft_decode_attn(q, kp, vp, dt[0], dl[0], 1 / 16, n_split=16)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("windowed", [True, False])
+def test_extend_split_counts_and_fallback(windowed):
+    # one-read-per-request launch (rows of >= 1024 keys per split) at 1..8
+    # splits; 16+ splits of these rows, 129 splits and n_q = 9 take the
+    # per-token launch; all within tolerance of the oracle
+    _case([3000, 9000], [5, 2], 64, 1024, 256, 16, 2, windowed, False, 620 + windowed, n_q=6,
+          splits=(1, 3, 8, 16, 40, 128, 129))
+    _case([70_000, 200_000], [7, 3], 64, 4032, 256, 16, 2, windowed, False, 640 + windowed, n_q=8,
+          splits=(None, 100, 128))
+    _case([2000], [9], 64, 512, 128, 8, 2, windowed, True, 630 + windowed, n_q=9, splits=(None, 3))
