@@ -140,16 +140,8 @@ __global__ void __launch_bounds__(256) append_kv_fp8_kernel(
     }
     const int h = (int)(e / chunks_per_head);
     const float ik = __frcp_rn(k_scale[h]), iv = __frcp_rn(v_scale[h]);
-    auto quant = [](uint4 x, float inv) {
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        uint32_t c[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            c[u] = f32x2_to_e4m3x2(__fmul_rn(bf16_lo_to_f32(w[u]), inv), __fmul_rn(bf16_hi_to_f32(w[u]), inv));
-        return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-    };
-    k_pool[slot * chunks_per_token + e] = quant(k_new[idx], ik);
-    v_pool[slot * chunks_per_token + e] = quant(v_new[idx], iv);
+    k_pool[slot * chunks_per_token + e] = quant_e4m3x8(k_new[idx], ik);
+    v_pool[slot * chunks_per_token + e] = quant_e4m3x8(v_new[idx], iv);
 }
 
 // Pruned draft prefill ("Windowed-MTP", §7 "Prefill sparsification and

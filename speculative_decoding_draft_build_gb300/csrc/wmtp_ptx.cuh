@@ -276,6 +276,19 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
     return y;
 }
 
+// Eight bf16 values (a packed 16-byte chunk, element 0 in the low half of
+// .x) times `inv`, each product rounded once in fp32, to eight E4M3 codes
+// (element 0 in the low byte of .x).
+__device__ __forceinline__ uint2 quant_e4m3x8(uint4 x, float inv) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        c[u] = f32x2_to_e4m3x2(__fmul_rn(__uint_as_float(w[u] << 16), inv),
+                               __fmul_rn(__uint_as_float(w[u] & 0xffff0000u), inv));
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     uint32_t y;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(y) : "f"(hi), "f"(lo));
