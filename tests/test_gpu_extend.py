@@ -113,3 +113,10 @@ def test_extend_split_counts_and_fallback(windowed):
     _case([70_000, 200_000], [7, 3], 64, 4032, 256, 16, 2, windowed, False, 640 + windowed, n_q=8,
           splits=(None, 100, 128))
     _case([2000], [9], 64, 512, 128, 8, 2, windowed, True, 630 + windowed, n_q=9, splits=(None, 3))
+
+
+@pytest.mark.parametrize("n_q,n_list", [(3, [3, 1, 2]), (8, [8, 5, 0])])
+def test_extend_one_read_head_dim_128(n_q, n_list):
+    # long rows take the one-read launch at D = 128 as well (G = 4 heads)
+    _case([20_000, 45_000, 9_000], n_list, 64, 1024, 128, 8, 2, False, False, 660 + n_q, n_q=n_q,
+          splits=(None, 2, 9))
