@@ -26,6 +26,7 @@ Calls (same names as the C ABI without the ``wmtp_`` prefix):
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -171,6 +172,15 @@ def _ptr(t: torch.Tensor | None):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _on(dev):
+    """Make `dev` the current CUDA device for a library call (the library
+    keeps per-device state); a no-op when it already is."""
+    idx = dev.index if isinstance(dev, torch.device) else int(dev)
+    if idx is None or idx == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(idx)
+
+
 def _stream(stream) -> ctypes.c_void_p:
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
@@ -235,7 +245,7 @@ def build_draft_indices(seq_lens: torch.Tensor, gamma: int, n_sink: int, window:
     _need(table, "table", torch.int32, dev)
     _need(lens, "lens", torch.int32, dev)
     rtt_stride = req_to_token.shape[1] if req_to_token is not None else 0
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(load().wmtp_build_draft_indices(
             _ptr(seq_lens), B, gamma, n_sink, window, depth, tree_k, int(bool(windowed)),
             _ptr(req_to_token), _ptr(req_pool_idx), rtt_stride, _ptr(ring_base), _ptr(table),
@@ -282,7 +292,7 @@ def build_extend_indices(seq_lens: torch.Tensor, n_new: torch.Tensor, n_sink: in
     _need(table, "table", torch.int32, dev)
     _need(lens, "lens", torch.int32, dev)
     rtt_stride = req_to_token.shape[1] if req_to_token is not None else 0
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(load().wmtp_build_extend_indices(
             _ptr(seq_lens), _ptr(n_new), B, n_sink, window, depth, tree_k, int(bool(windowed)),
             _ptr(req_to_token), _ptr(req_pool_idx), rtt_stride, _ptr(ring_base), _ptr(table),
@@ -305,7 +315,7 @@ def ring_map(ring_base: torch.Tensor, pos: torch.Tensor, req_of: torch.Tensor, n
     if slots is None:
         slots = torch.empty(n, dtype=torch.int32, device=dev)
     _need(slots, "slots", torch.int32, dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(load().wmtp_ring_map(_ptr(ring_base), _ptr(pos), _ptr(branch), _ptr(req_of), n,
                                     n_sink, window, depth, tree_k, _ptr(slots), _stream(stream)),
                "ring_map")
@@ -323,7 +333,7 @@ def append_kv(k_new: torch.Tensor, v_new: torch.Tensor, slots: torch.Tensor,
     n, H_kv, D = k_new.shape
     if v_new.shape != k_new.shape or k_pool.shape[1:] != (H_kv, D) or v_pool.shape != k_pool.shape:
         raise ValueError("append_kv: shape mismatch")
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(load().wmtp_append_kv(_ptr(k_new), _ptr(v_new), _ptr(slots), n, H_kv, D,
                                      _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _stream(stream)),
                "append_kv")
@@ -348,7 +358,7 @@ def append_kv_fp8(k_new: torch.Tensor, v_new: torch.Tensor, slots: torch.Tensor,
     if (v_new.shape != k_new.shape or k_pool.shape[1:] != (H_kv, D) or v_pool.shape != k_pool.shape
             or k_scale.numel() != H_kv or v_scale.numel() != H_kv or slots.numel() != n):
         raise ValueError("append_kv_fp8: shape mismatch")
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(load().wmtp_append_kv_fp8(_ptr(k_new), _ptr(v_new), _ptr(slots), n, H_kv, D,
                                          _ptr(k_scale), _ptr(v_scale), _ptr(k_pool), _ptr(v_pool),
                                          k_pool.shape[0], _stream(stream)), "append_kv_fp8")
@@ -362,14 +372,14 @@ def attn_workspace_bytes(B: int, n_q: int, H_q: int, H_kv: int, D: int, n_split:
 def attn_num_splits(B: int, n_q: int, H_kv: int, max_len: int, device=None, fp8: bool = False) -> int:
     dev = device if device is not None else torch.cuda.current_device()
     fn = load().wmtp_attn_num_splits_fp8 if fp8 else load().wmtp_attn_num_splits
-    with torch.cuda.device(dev):
+    with _on(dev):
         return int(fn(B, n_q, H_kv, int(max_len)))
 
 
 def extend_num_splits(B: int, n_q: int, H_kv: int, max_len: int, device=None) -> int:
     """Usual split count of :func:`draft_extend_attn` (``wmtp_extend_num_splits``)."""
     dev = device if device is not None else torch.cuda.current_device()
-    with torch.cuda.device(dev):
+    with _on(dev):
         return int(load().wmtp_extend_num_splits(B, n_q, H_kv, int(max_len)))
 
 
@@ -383,7 +393,7 @@ class AttnWorkspace:
     def __init__(self, nbytes: int, device, stream=None):
         self.nbytes = int(nbytes)
         self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device)
-        with torch.cuda.device(self.buf.device):
+        with _on(self.buf.device):
             _check(load().wmtp_attn_workspace_init(_ptr(self.buf), self.nbytes, _stream(stream)),
                    "attn_workspace_init")
 
@@ -488,7 +498,7 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
     if n_split is None:
         ml = max_len if max_len is not None else stride
         if append is not None and append[0] == "extend":
-            with torch.cuda.device(dev):
+            with _on(dev):
                 n_split = int(load().wmtp_extend_num_splits(B, n_q, H_kv, int(ml)))
         else:
             n_split = attn_num_splits(B, n_q, H_kv, ml, dev, fp8=pool_dtype == torch.uint8)
@@ -506,7 +516,7 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
     elif workspace.nbytes < need:
         raise ValueError(f"workspace holds {workspace.nbytes} bytes, {need} needed")
     if append is None:
-        with torch.cuda.device(dev):
+        with _on(dev):
             _check(load().wmtp_draft_decode_attn(
                 _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
                 stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf),
@@ -514,7 +524,7 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
         return out, lse
     if append[0] == "fp8":
         _, k_scale, v_scale = append
-        with torch.cuda.device(dev):
+        with _on(dev):
             _check(load().wmtp_draft_decode_attn_fp8(
                 _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
                 _ptr(v_scale), num_slots, _ptr(table), stride, _ptr(lens), float(scale), _ptr(out),
@@ -523,7 +533,7 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
         return out, lse
     if append[0] == "extend":
         _, seq_lens, n_new, n_sink, window, windowed = append
-        with torch.cuda.device(dev):
+        with _on(dev):
             _check(load().wmtp_draft_extend_attn(
                 _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
                 stride, _ptr(lens), _ptr(seq_lens), _ptr(n_new), n_sink, window, int(bool(windowed)),
@@ -538,7 +548,7 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
     if (new_slots.numel() != B * n_new or k_new.numel() != B * n_new * H_kv * D
             or v_new.shape != k_new.shape or k_new.shape[-2:] != (H_kv, D)):
         raise ValueError("draft_decode_attn_append: k_new/v_new/new_slots shape mismatch")
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(load().wmtp_draft_decode_attn_append(
             _ptr(k_new), _ptr(v_new), _ptr(new_slots), n_new,
             _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
@@ -560,7 +570,7 @@ def attn_mass_diagnostics(o_full: torch.Tensor, lse_full: torch.Tensor, o_win: t
     if o_full.numel() != rows * D or o_win.numel() != rows * D or lse_win.numel() != rows:
         raise ValueError("attn_mass_diagnostics: shape mismatch")
     res = [torch.empty_like(lse_full) for _ in range(3)]
-    with torch.cuda.device(o_full.device):
+    with _on(o_full.device):
         _check(load().wmtp_attn_mass_diagnostics(
             _ptr(o_full), _ptr(lse_full), _ptr(o_win), _ptr(lse_win), rows, D, _ptr(res[0]),
             _ptr(res[1]), _ptr(res[2]), _stream(stream)), "attn_mass_diagnostics")
@@ -586,7 +596,7 @@ def draft_decode_attn_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: tor
     _need(lse, "lse", torch.float32, dev)
     B, n_q, H_q, D = q.shape
     num_slots, H_kv, _ = k_pool.shape
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(load().wmtp_draft_decode_attn_noalloc(
             _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
             table.shape[-1], _ptr(lens), float(scale), _ptr(out), _ptr(lse), n_split,
@@ -602,7 +612,7 @@ def tree_workspace_bytes(B: int, H_q: int, H_kv: int, D: int, depth: int, tree_k
 def tree_num_splits(B: int, H_q: int, H_kv: int, depth: int, tree_k: int, n_sink: int,
                     window: int, device=None) -> int:
     dev = device if device is not None else torch.cuda.current_device()
-    with torch.cuda.device(dev):
+    with _on(dev):
         return int(load().wmtp_tree_num_splits(B, H_q, H_kv, depth, tree_k, n_sink, window))
 
 
@@ -647,7 +657,7 @@ def tree_draft_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
         workspace = ws
     elif workspace.nbytes < need:
         raise ValueError(f"workspace holds {workspace.nbytes} bytes, {need} needed")
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(load().wmtp_tree_draft_attn(
             _ptr(q), B, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(seq_lens),
             _ptr(ring_base), n_sink, window, depth, tree_k, float(scale), _ptr(out), _ptr(lse),
@@ -672,7 +682,7 @@ def prefill_keep_positions(seq_lens: torch.Tensor, n_sink: int, window: int, str
         counts = torch.empty((B,), dtype=torch.int32, device=dev)
     _need(positions, "positions", torch.int32, dev)
     _need(counts, "counts", torch.int32, dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(load().wmtp_prefill_keep_positions(_ptr(seq_lens), B, n_sink, window, _ptr(positions),
                                                   positions.shape[-1], _ptr(counts), _stream(stream)),
                "prefill_keep_positions")
@@ -693,7 +703,7 @@ def ring_fill(k_rows: torch.Tensor, v_rows: torch.Tensor, seq_lens: torch.Tensor
     B, stride, H_kv, D = k_rows.shape
     if v_rows.shape != k_rows.shape or k_pool.shape[1:] != (H_kv, D) or v_pool.shape != k_pool.shape:
         raise ValueError("ring_fill: shape mismatch")
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(load().wmtp_ring_fill(_ptr(k_rows), _ptr(v_rows), _ptr(seq_lens), B, stride, H_kv, D,
                                      _ptr(ring_base), n_sink, window, depth, tree_k, _ptr(k_pool),
                                      _ptr(v_pool), k_pool.shape[0], _stream(stream)), "ring_fill")
@@ -746,7 +756,7 @@ def draft_decode_attn_ring(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
             _ws_cache[key] = workspace
     elif workspace.nbytes < need:
         raise ValueError(f"workspace holds {workspace.nbytes} bytes, {need} needed")
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check(load().wmtp_draft_decode_attn_ring(
             _ptr(k_new), _ptr(v_new), _ptr(q), B, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots,
             _ptr(seq_lens), _ptr(ring_base), int(step), n_sink, window, depth, tree_k, float(scale),
