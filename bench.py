@@ -291,6 +291,13 @@ class Workload:
         return c["B"] * attn_bytes(L, 1, c["H_q"], c["H_kv"], c["D"], n_new=1)
 
 
+def hold_gpu(us: float = 150.0):
+    """Queue a spin kernel so the GPU is still busy when a timed call is
+    enqueued: its start event then stamps the kernel, not the host time the
+    Python binding spends preparing the launch (tens of microseconds)."""
+    torch.cuda._sleep(int(us * 2100))  # cycles at about 2.1 GHz
+
+
 def _external_event():
     try:
         return torch.cuda.Event(enable_timing=True, external=True)
@@ -362,7 +369,9 @@ def run_ours(args, dist_ctx):
     full_ms = [a.elapsed_time(b) for a, b in e_full]
     win_ms = [a.elapsed_time(b) for a, b in e_win]
     attn_full_ms = [[e_attn[k][j][0].elapsed_time(e_attn[k][j][1]) for j in range(g)] for k in range(K)]
-    full_attn_mean_ms = statistics.mean(x for row in attn_full_ms for x in row)
+    # median over the launches: the first launch of a step can start after a
+    # host-side gap (its Python call is prepared while the index build runs)
+    full_attn_mean_ms = statistics.median(x for row in attn_full_ms for x in row)
 
     # windowed attention per launch, on the same graph with inner events
     win_attn_ms = []
@@ -512,6 +521,7 @@ def measure_mass(w, dev):
     ts = []
     for _ in range(20):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_gpu()
         a.record()
         res = wm.attn_mass_diagnostics(*args)
         b.record()
@@ -559,6 +569,7 @@ def measure_extend(w, args, dev):
         ts = []
         for _ in range(reps):
             w.flush.zero_()
+            hold_gpu()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             call()
@@ -619,15 +630,19 @@ def measure_fp8(w, args, dev):
         t_attn, t_app, gbs = [], [], []
         for _ in range(reps):
             for j in range(g):
-                ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
                 w.flush.zero_()
+                hold_gpu()
                 ev[0].record()
                 append(j)
                 ev[1].record()
-                attn(j)
+                w.flush.zero_()
+                hold_gpu()
                 ev[2].record()
+                attn(j)
+                ev[3].record()
                 torch.cuda.synchronize(dev)
-                ta = ev[1].elapsed_time(ev[2]) * 1e-3
+                ta = ev[2].elapsed_time(ev[3]) * 1e-3
                 L = min(S + j + 1, c["n_sink"] + c["W"]) if name == "windowed" else S + j + 1
                 nbytes = B * (L * H_kv * D * 2 + 4 * L + H_q * D * 2 + H_q * (D + 1) * 4)
                 t_attn.append(ta)
@@ -680,6 +695,7 @@ def measure_ring(w, args, dev):
         ts = []
         for _ in range(reps):
             w.flush.zero_()
+            hold_gpu()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -762,6 +778,7 @@ def measure_tree(args, dev):
         ts = []
         for _ in range(reps):
             flush.zero_()
+            hold_gpu()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             wm.tree_draft_attn(q, kp, vp, seq, rb, n_sink, W, d, k, 1 / 16, out=out, lse=lse,
