@@ -882,7 +882,7 @@ def _oracle_inputs(w):
                 rtt=w.rtt.cpu().numpy(), slots=w.slots.cpu().numpy(), seq=w.seq.cpu().numpy())
 
 
-def oracle_windowed_step(o, w, host):
+def oracle_windowed_step(o, w, host, nthreads=None):
     """One windowed decode step in the oracle: tables, then per draft step the
     append and the attention of every query head."""
     c = w.cfg
@@ -891,7 +891,8 @@ def oracle_windowed_step(o, w, host):
                                         req_to_token=host["rtt"], stride=c["n_sink"] + c["W"])
     for j in range(g):
         o.append_kv(host["kn"][j], host["vn"][j], host["slots"][j], host["kp"], host["vp"])
-        o.draft_decode_attn(host["q"][j], host["kp"], host["vp"], table[j], lens[j], w.scale)
+        o.draft_decode_attn(host["q"][j], host["kp"], host["vp"], table[j], lens[j], w.scale,
+                            nthreads=nthreads)
 
 
 def cpu_baseline(w, args):
@@ -908,6 +909,9 @@ def cpu_baseline(w, args):
         oracle_windowed_step(o, w, host)
         ts.append(time.perf_counter() - t)
     win_us = statistics.median(ts) * 1e6
+    t = time.perf_counter()
+    oracle_windowed_step(o, w, host, nthreads=1)
+    win_1t_us = (time.perf_counter() - t) * 1e6
     # full arm: one draft forward over the whole table, all query heads
     c = w.cfg
     g = c["gamma"]
@@ -922,7 +926,8 @@ def cpu_baseline(w, args):
             "sample": f"windowed decode step (gamma={g}, all {c['H_q']} heads) x{len(ts)}, median; "
                       f"full arm estimated from one full-context forward ({c['S'] + 1} keys, all heads) "
                       f"x{g} + one table build",
-            "full_us_per_step_est": round((t_fwd * g + t_build * g) * 1e6, 1)}
+            "full_us_per_step_est": round((t_fwd * g + t_build * g) * 1e6, 1),
+            "single_thread_us": round(win_1t_us, 1)}
 
 
 def run_reference(args, dist_ctx):
