@@ -23,9 +23,16 @@ __device__ int32_t g_index_error = 0;
 
 __device__ __forceinline__ void latch(int32_t code) { atomicCAS(&g_index_error, 0, code); }
 
+// Table entries per thread of the index builder: long rows take many per
+// thread (loads in flight), short rows one (more CTAs, less latency).
+constexpr int kIndexPerThreadLong = 8;
+constexpr int64_t kIndexLongRow = 65536;
+
 // One grid row (blockIdx.y) per (draft step j, request b); the x dimension
-// strides over the row's entries.  Entry e of a windowed row is position e
-// for the sinks and e + (kv_len - W - n_sink) for the window.
+// strides over the row's entries, kIndexPerThread per thread.  Entry e of a
+// windowed row is position e for the sinks and e + (kv_len - W - n_sink) for
+// the window.
+template <int kIndexPerThread>
 __global__ void __launch_bounds__(256) build_indices_kernel(
     const int32_t *__restrict__ seq_lens, int32_t B, int32_t n_sink, int32_t window,
     int32_t depth, int32_t tree_k, int32_t windowed,
@@ -59,23 +66,43 @@ __global__ void __launch_bounds__(256) build_indices_kernel(
     const int64_t n_write = n < stride ? n : stride;
     const int64_t shift = win ? kv_len - keep_w - n_sink : 0;
     int32_t *__restrict__ out = table + (int64_t)row * stride;
-    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    // Each thread takes kIndexPerThread entries a block apart: coalesced
+    // accesses, and that many independent loads in flight per thread.
+    const int64_t span = (int64_t)blockDim.x * kIndexPerThread;
+    const int64_t step = (int64_t)gridDim.x * span;
     if (req_to_token) {
         const int32_t pool_row = req_pool_idx ? req_pool_idx[b] : b;
         const int32_t *__restrict__ src = req_to_token + (int64_t)pool_row * rtt_stride;
-        for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n_write; e += step) {
-            const int64_t p = (win && e >= n_sink) ? e + shift : e;
-            if (p >= rtt_stride) {
-                latch(WMTP_DEV_ARG_RANGE);
-                continue;
+        for (int64_t e0 = (int64_t)blockIdx.x * span + threadIdx.x; e0 < n_write; e0 += step) {
+            int32_t v[kIndexPerThread];
+#pragma unroll
+            for (int u = 0; u < kIndexPerThread; ++u) {
+                const int64_t e = e0 + (int64_t)u * blockDim.x;
+                const int64_t p = (win && e >= n_sink) ? e + shift : e;
+                v[u] = (e < n_write && p < rtt_stride) ? __ldg(src + p) : 0;
             }
-            out[e] = __ldg(src + p);
+#pragma unroll
+            for (int u = 0; u < kIndexPerThread; ++u) {
+                const int64_t e = e0 + (int64_t)u * blockDim.x;
+                const int64_t p = (win && e >= n_sink) ? e + shift : e;
+                if (e >= n_write) break;
+                if (p >= rtt_stride) {
+                    latch(WMTP_DEV_ARG_RANGE);
+                    continue;
+                }
+                out[e] = v[u];
+            }
         }
     } else {
         const int64_t base = ring_base[b];
-        for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n_write; e += step) {
-            const int64_t p = (win && e >= n_sink) ? e + shift : e;
-            out[e] = (int32_t)ring_slot(base, p, 0, n_sink, window, depth, tree_k);
+        for (int64_t e0 = (int64_t)blockIdx.x * span + threadIdx.x; e0 < n_write; e0 += step) {
+#pragma unroll
+            for (int u = 0; u < kIndexPerThread; ++u) {
+                const int64_t e = e0 + (int64_t)u * blockDim.x;
+                if (e >= n_write) break;
+                const int64_t p = (win && e >= n_sink) ? e + shift : e;
+                out[e] = (int32_t)ring_slot(base, p, 0, n_sink, window, depth, tree_k);
+            }
         }
     }
 }
@@ -265,13 +292,14 @@ wmtp_status wmtp_build_draft_indices(const int32_t *seq_lens, int32_t B, int32_t
     if (!seq_lens || !table || !lens) return WMTP_EINVAL;
     if (!req_to_token && !ring_base) return WMTP_EINVAL;
     if (req_to_token && rtt_stride < 1) return WMTP_EINVAL;
-    // One entry per thread (each is one dependent global load), up to 8192
-    // CTAs per row.
+    // kIndexPerThreadLong entries per thread on long rows, up to 8192 CTAs per row.
     constexpr int kThreads = 256;
-    int64_t gx = (stride + kThreads - 1) / kThreads;
+    const bool long_rows = stride >= kIndexLongRow;
+    const int per = long_rows ? kIndexPerThreadLong : 1;
+    int64_t gx = (stride + kThreads * per - 1) / (kThreads * per);
     if (gx > 8192) gx = 8192;
     PdlLaunch L(dim3((unsigned)gx, (unsigned)(gamma * B)), dim3(kThreads), 0, as_stream(stream));
-    return cudaLaunchKernelEx(&L.cfg, build_indices_kernel, seq_lens, B, n_sink, window, depth,
+    return cudaLaunchKernelEx(&L.cfg, long_rows ? build_indices_kernel<kIndexPerThreadLong> : build_indices_kernel<1>, seq_lens, B, n_sink, window, depth,
                               tree_k, windowed, req_to_token, req_pool_idx, rtt_stride, ring_base,
                               table, stride, lens, static_cast<const int32_t *>(nullptr)) == cudaSuccess
                ? WMTP_OK
@@ -292,10 +320,12 @@ wmtp_status wmtp_build_extend_indices(const int32_t *seq_lens, const int32_t *n_
     if (!req_to_token && !ring_base) return WMTP_EINVAL;
     if (req_to_token && rtt_stride < 1) return WMTP_EINVAL;
     constexpr int kThreads = 256;
-    int64_t gx = (stride + kThreads - 1) / kThreads;
+    const bool long_rows = stride >= kIndexLongRow;
+    const int per = long_rows ? kIndexPerThreadLong : 1;
+    int64_t gx = (stride + kThreads * per - 1) / (kThreads * per);
     if (gx > 8192) gx = 8192;
     PdlLaunch L(dim3((unsigned)gx, (unsigned)B), dim3(kThreads), 0, as_stream(stream));
-    return cudaLaunchKernelEx(&L.cfg, build_indices_kernel, seq_lens, B, n_sink, window, depth,
+    return cudaLaunchKernelEx(&L.cfg, long_rows ? build_indices_kernel<kIndexPerThreadLong> : build_indices_kernel<1>, seq_lens, B, n_sink, window, depth,
                               tree_k, windowed, req_to_token, req_pool_idx, rtt_stride, ring_base,
                               table, stride, lens, n_new) == cudaSuccess
                ? WMTP_OK
