@@ -364,16 +364,22 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             const uint32_t *src = reinterpret_cast<const uint32_t *>(
                 q + ((b * n_nodes + (live ? rq / G : 0)) * H_q + g * G + (live ? rq % G : 0)) * (int64_t)D);
             const uint32_t qlane = tmem + ((uint32_t)(warp * 32) << 16) + C::kQCol;
-#pragma unroll 1
+            // the whole row in flight at once (one memory round trip), then
+            // into tensor memory 32 columns at a time
+            uint4 qv[D / 8];
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j)
+                qv[j] = live ? __ldg(reinterpret_cast<const uint4 *>(src) + j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
             for (int c0 = 0; c0 < D / 2; c0 += 32) {
                 uint32_t r[32];
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const uint4 v = live ? __ldg(reinterpret_cast<const uint4 *>(src + c0 + j)) : make_uint4(0, 0, 0, 0);
-                    r[j] = v.x;
-                    r[j + 1] = v.y;
-                    r[j + 2] = v.z;
-                    r[j + 3] = v.w;
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 v = qv[c0 / 4 + j];
+                    r[4 * j] = v.x;
+                    r[4 * j + 1] = v.y;
+                    r[4 * j + 2] = v.z;
+                    r[4 * j + 3] = v.w;
                 }
                 tc_st32(qlane + c0, r);
             }
