@@ -23,7 +23,7 @@
 //              tree-causal mask, keeps a running reference max (the O
 //              accumulator is rescaled in tensor memory only when the max
 //              grows by more than 2^8), writes P as bf16 head + tail into
-//              shared memory, and at the end reads its row of O.
+//              its tensor-memory lane, and at the end reads its row of O.
 //   warp 4     gather: slots from the ring rule (no table); 32-key tiles
 //              of consecutive ring slots arrive as TMA boxes (64 dims x 1
 //              head x 32 or 8 slots, 128-byte swizzle), other keys through
@@ -31,9 +31,9 @@
 //   warp 5     one thread issues the MMAs: S(t) = Q K(t)^T (M=128, N=32,
 //              K=D) into one of two S buffers, then O += P_hi V + P_lo V
 //              (M=128, N=D, K=32); completion is signalled through mbarriers
-//              with tcgen05.commit.  Q is read from tensor memory, P from
-//              no-swizzle K-major shared memory; K is K-major and V
-//              MN-major, both 128-byte swizzled.
+//              with tcgen05.commit.  Q and P are read from tensor memory
+//              (the A operands); K is K-major and V MN-major in shared
+//              memory, both 128-byte swizzled.
 // Key chunks are split over CTAs; up to 8 chunks of a (request, KV head,
 // row block) run as one cluster and merge through distributed shared memory,
 // more through the workspace (the last CTA merges in split order).  Every
@@ -71,7 +71,7 @@ constexpr float kLazyRescale = 8.f;  // log2 of the growth tolerated before resc
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// Barrier slots: K/V stages (4), S buffers (2), P buffers (2).
+// Barrier slots: K/V stages, S buffers (2), P buffers (2), Q.
 enum {
     kKvFull = 0,
     kKvEmpty = kKvFull + kKvStages,
@@ -90,24 +90,27 @@ struct Cfg {
 
     static constexpr int kTileBytes = kKeys / 8 * kRowSbo;   // K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kPSbo = kKeys / 8 * 128;            // P: 8-row group stride
-    static constexpr int kPBytes = kRows / 8 * kPSbo;        // one of P_hi / P_lo
-    static constexpr int kPBufBytes = 2 * kPBytes;           // P_hi then P_lo
+    // cluster merge: lse of the 128 rows, then the merge weights of this
+    // CTA's row slice (at most kRows + kMaxClusterSplits - 1 of them)
+    static constexpr int kMergeBytes = kRows * 4 + (kRows + kMaxClusterSplits) * 4;
     static constexpr int kKvOff = 0;
-    static constexpr int kPOff = kKvOff + kKvStages * kStageBytes;
-    static constexpr int kBarOff = kPOff + 2 * kPBufBytes;
-    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
+    static constexpr int kMergeOff = kKvOff + kKvStages * kStageBytes;
+    static constexpr int kBarOff = kMergeOff + kMergeBytes;
+    static constexpr int kSmemUsed = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
     static constexpr int kDimBlocks = D / 64;                 // 128-byte swizzle atoms per K/V row
     static constexpr int kBlockBytes = kKeys * 128;           // one 64-dim block of a tile
     static constexpr int kOCol = 2 * kKeys;                  // O after the two S buffers
     static constexpr int kQCol = kOCol + D;                  // Q (A operand of QK): two bf16 per column
-    static constexpr int kTmemCols = (kQCol + D / 2 <= 256) ? 256 : 512;
-    static_assert(kQCol + D / 2 <= 512, "tensor memory budget");
+    static constexpr int kPCol = kQCol + D / 2;              // P (A operand of PV): 2 buffers x (hi, lo)
+    static constexpr int kTmemCols = (kPCol + 2 * kKeys <= 256) ? 256 : 512;
+    static_assert(kPCol + 2 * kKeys <= 512, "tensor memory budget");
+    // at 512 tensor-memory columns a second CTA on the SM would only wait in
+    // tcgen05.alloc: ask for more than half the SM's shared memory
+    static constexpr int kSmemBytes =
+        (kTmemCols == 512 && kSmemUsed < 116 * 1024) ? 116 * 1024 : kSmemUsed;
     static_assert(kRows * kMaxSplits * 4 <= kKvStages * kStageBytes, "merge weights must fit");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kRows * D * 4 <= kKvStages * kStageBytes, "cluster-merge partial must fit the K/V stages");
-    static_assert(kRows * 4 + kRows * kMaxClusterSplits * 4 <= 2 * kPBufBytes,
-                  "cluster-merge lse and weights must fit the P buffers");
 };
 
 struct TreeWs {
@@ -341,14 +344,12 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                 if (!mbar_wait(&bars[kPFull + pb], (t >> 1) & 1, flags)) break;
                 tc_fence_after();
                 const uint32_t vt = sbase + C::kKvOff + (t % kKvStages) * C::kStageBytes + C::kTileBytes;
-                const uint32_t p_hi = sbase + C::kPOff + pb * C::kPBufBytes, p_lo = p_hi + C::kPBytes;
+                const uint32_t p_hi = tmem + C::kPCol + pb * kKeys, p_lo = p_hi + kKeys / 2;
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
                     const uint64_t vd = tc_smem_desc_sw128(vt + kk * 16 * 128, C::kBlockBytes, 1024);
-                    tc_mma_bf16(tmem + C::kOCol, tc_smem_desc(p_hi + kk * 256, 128, C::kPSbo), vd,
-                                idesc_pv, (t > 0 || kk > 0));
-                    tc_mma_bf16(tmem + C::kOCol, tc_smem_desc(p_lo + kk * 256, 128, C::kPSbo), vd,
-                                idesc_pv, 1);
+                    tc_mma_bf16_ta(tmem + C::kOCol, p_hi + kk * 8, vd, idesc_pv, (t > 0 || kk > 0));
+                    tc_mma_bf16_ta(tmem + C::kOCol, p_lo + kk * 8, vd, idesc_pv, 1);
                 }
                 tc_commit(smem_addr(&bars[kPvDone + pb]));
                 tc_commit(smem_addr(&bars[kKvEmpty + (t % kKvStages)]));
@@ -406,7 +407,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         float m_ref = -INFINITY, l = 0.f;
         bool o_live = false;  // O holds at least one PV product
-        const int poff = (i >> 3) * C::kPSbo + (i & 7) * 16;
         for (int t = 0; t < n_tiles; ++t) {
             const int sb = t & 1, pb = t & 1;
             if (!warp_wait(&bars[kSFull + sb], (t >> 1) & 1, flags)) break;
@@ -482,21 +482,18 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             l += rs;
             // P buffer pb is free once PV(t-2) is done
             if (t >= 2 && !warp_wait(&bars[kPvDone + pb], ((t >> 1) - 1) & 1, flags)) break;
-            uint8_t *ph = smem + C::kPOff + pb * C::kPBufBytes + poff;
-            uint8_t *pl = ph + C::kPBytes;
+            {
+                // P as bf16 head (columns 0-15) and tail (16-31) of this row's
+                // lane, two keys per column
+                uint32_t pr[32];
 #pragma unroll
-            for (int j = 0; j < kKeys / 8; ++j) {
-                uint32_t hv[4], tv[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float a = x[8 * j + 2 * u], c2 = x[8 * j + 2 * u + 1];
-                    hv[u] = pack_bf16x2(a, c2);
-                    tv[u] = pack_bf16x2(a - bf16_lo_to_f32(hv[u]), c2 - bf16_hi_to_f32(hv[u]));
+                for (int u = 0; u < kKeys / 2; ++u) {
+                    const float a = x[2 * u], c2 = x[2 * u + 1];
+                    pr[u] = pack_bf16x2(a, c2);
+                    pr[kKeys / 2 + u] = pack_bf16x2(a - bf16_lo_to_f32(pr[u]), c2 - bf16_hi_to_f32(pr[u]));
                 }
-                *reinterpret_cast<uint4 *>(ph + j * 128) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                *reinterpret_cast<uint4 *>(pl + j * 128) = make_uint4(tv[0], tv[1], tv[2], tv[3]);
+                tc_st32(lane_base + C::kPCol + pb * kKeys, pr);
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&bars[kPFull + pb]));
@@ -517,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         // float4 index of row i XOR-swizzled by i % 8; its lse to the P area.
         float *po = reinterpret_cast<float *>(smem + C::kKvOff);
         if (cluster_merge) {
-            reinterpret_cast<float *>(smem + C::kPOff)[i] = (row_live && !flags[0]) ? lse2 : -INFINITY;
+            reinterpret_cast<float *>(smem + C::kMergeOff)[i] = (row_live && !flags[0]) ? lse2 : -INFINITY;
         } else if (row_live) {
             if (n_split == 1) {
                 const int64_t orow = (b * n_nodes + node) * H_q + h;
@@ -583,8 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         const int r_lo = rank * per;
         const int r_hi = r_lo + per < n_rows ? r_lo + per : n_rows;
         const uint32_t po_addr = smem_addr(smem + C::kKvOff);
-        const uint32_t pl_addr = smem_addr(smem + C::kPOff);
-        float *wts = reinterpret_cast<float *>(smem + C::kPOff + kRows * 4);  // [per][n_split] merge weights
+        const uint32_t pl_addr = smem_addr(smem + C::kMergeOff);
+        float *wts = reinterpret_cast<float *>(smem + C::kMergeOff + kRows * 4);  // [per][n_split] merge weights
         for (int i = r_lo + tid; i < r_hi; i += kThreads) {
             float ls[kMaxClusterSplits];
 #pragma unroll
