@@ -19,18 +19,19 @@
 // KV head.  Warp roles:
 //   warps 0-3  softmax: thread i owns query row i = tensor-memory lane i.  It
 //              first writes its row of Q into tensor memory (the A operand of
-//              QK), then per tile reads its row of S = Q K^T, applies the
-//              tree-causal mask, keeps a running reference max (the O
+//              QK), then per 64-key tile reads its row of S = Q K^T, applies
+//              the tree-causal mask, keeps a running reference max (the O
 //              accumulator is rescaled in tensor memory only when the max
-//              grows by more than 2^8), writes P as bf16 head + tail into
-//              its tensor-memory lane, and at the end reads its row of O.
-//   warp 4     gather: slots from the ring rule (no table); 32-key tiles
-//              of consecutive ring slots arrive as TMA boxes (64 dims x 1
-//              head x 32 or 8 slots, 128-byte swizzle), other keys through
-//              16-byte cp.async into the same swizzled layout; six stages.
-//   warp 5     one thread issues the MMAs: S(t) = Q K(t)^T (M=128, N=32,
+//              grows by more than 2^8), writes P as bf16 head + tail over its
+//              row of S, and at the end reads its row of O.
+//   warp 4     gather: slots from the ring rule (no table); 32-key copy
+//              stages of consecutive ring slots arrive as TMA boxes (64 dims
+//              x 1 head x 32 or 8 slots, 128-byte swizzle), other keys
+//              through 16-byte cp.async into the same swizzled layout; six
+//              stages, two per MMA tile.
+//   warp 5     one thread issues the MMAs: S(t) = Q K(t)^T (M=128, N=64,
 //              K=D) into one of two S buffers, then O += P_hi V + P_lo V
-//              (M=128, N=D, K=32); completion is signalled through mbarriers
+//              (M=128, N=D, K=64); completion is signalled through mbarriers
 //              with tcgen05.commit.  Q and P are read from tensor memory
 //              (the A operands); K is K-major and V MN-major in shared
 //              memory, both 128-byte swizzled.
@@ -58,8 +59,10 @@ __device__ int32_t g_tree_tc_error = 0;
 __device__ __forceinline__ void latch(int32_t code) { atomicCAS(&g_tree_tc_error, 0, code); }
 
 constexpr int kRows = 128;  // query rows per CTA (MMA M)
-constexpr int kKeys = 32;   // keys per tile (N of QK^T, K of PV)
-constexpr int kKvStages = 6;
+constexpr int kKeys = 64;      // keys per MMA tile (N of QK^T, K of PV)
+constexpr int kCopyKeys = 32;  // keys per copy stage: two stages make one MMA tile
+constexpr int kKvStages = 6;   // copy stages (even: an MMA tile never wraps the ring)
+static_assert(kKeys == 2 * kCopyKeys && kKvStages % 2 == 0, "stage pairing");
 constexpr int kSoftWarps = 4;
 constexpr int kLoadWarps = 1;
 constexpr int kLoadThreads = kLoadWarps * 32;
@@ -71,13 +74,13 @@ constexpr float kLazyRescale = 8.f;  // log2 of the growth tolerated before resc
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// Barrier slots: K/V stages, S buffers (2), P buffers (2), Q.
+// Barrier slots: K/V copy stages, S buffers (2), P (2, written over S), PV
+// done (2, which also frees the S buffer), Q.
 enum {
     kKvFull = 0,
     kKvEmpty = kKvFull + kKvStages,
     kSFull = kKvEmpty + kKvStages,
-    kSEmpty = kSFull + 2,
-    kPFull = kSEmpty + 2,
+    kPFull = kSFull + 2,
     kPvDone = kPFull + 2,
     kQFull = kPvDone + 2,
     kNumBars = kQFull + 1
@@ -85,25 +88,30 @@ enum {
 
 template <int D>
 struct Cfg {
-    static constexpr int kChunks = D / 8;                    // 16-byte chunks per row
-    static constexpr int kRowSbo = kChunks * 128;            // 8-row group stride (Q, K, V)
-
-    static constexpr int kTileBytes = kKeys / 8 * kRowSbo;   // K (or V) tile
-    static constexpr int kStageBytes = 2 * kTileBytes;
+    // K and V each sit in shared memory as D/64 rings of 128-byte rows (one
+    // ring per 64-dim swizzle atom column, the 128-byte-swizzled K-major
+    // layout the MMAs read): copy stage st holds rows st*32 .. st*32+31 of
+    // every ring, so the two stages of an MMA tile are 64 consecutive rows,
+    // one operand with a uniform 8-row stride.
+    static constexpr int kCopyBytes = kCopyKeys * D * 2;     // K (or V) rows of one copy stage
+    static constexpr int kRingBlockBytes = kKvStages * kCopyKeys * 128;
+    static constexpr int kRegionBytes = (D / 64) * kRingBlockBytes;  // all of K (or V)
+    static constexpr int kStageBytes = 2 * kCopyBytes;
     // cluster merge: lse of the 128 rows, then the merge weights of this
     // CTA's row slice (at most kRows + kMaxClusterSplits - 1 of them)
     static constexpr int kMergeBytes = kRows * 4 + (kRows + kMaxClusterSplits) * 4;
     static constexpr int kKvOff = 0;
-    static constexpr int kMergeOff = kKvOff + kKvStages * kStageBytes;
+    static constexpr int kKOff = kKvOff;
+    static constexpr int kVOff = kKOff + kRegionBytes;
+    static constexpr int kMergeOff = kVOff + kRegionBytes;
     static constexpr int kBarOff = kMergeOff + kMergeBytes;
     static constexpr int kSmemUsed = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
     static constexpr int kDimBlocks = D / 64;                 // 128-byte swizzle atoms per K/V row
-    static constexpr int kBlockBytes = kKeys * 128;           // one 64-dim block of a tile
+    // tensor memory: S buffers (fp32, later P as bf16 head | tail), O, Q
     static constexpr int kOCol = 2 * kKeys;                  // O after the two S buffers
     static constexpr int kQCol = kOCol + D;                  // Q (A operand of QK): two bf16 per column
-    static constexpr int kPCol = kQCol + D / 2;              // P (A operand of PV): 2 buffers x (hi, lo)
-    static constexpr int kTmemCols = (kPCol + 2 * kKeys <= 256) ? 256 : 512;
-    static_assert(kPCol + 2 * kKeys <= 512, "tensor memory budget");
+    static constexpr int kTmemCols = (kQCol + D / 2 <= 256) ? 256 : 512;
+    static_assert(kQCol + D / 2 <= 512, "tensor memory budget");
     // at 512 tensor-memory columns a second CTA on the SM would only wait in
     // tcgen05.alloc: ask for more than half the SM's shared memory
     static constexpr int kSmemBytes =
@@ -144,6 +152,28 @@ __device__ __forceinline__ int2 key_info(const Geo &g, int64_t e, int depth) {
     const int br = (int)(n / depth);
     const int dep = (int)(n - (int64_t)br * depth);
     return make_int2((int)(g.S + dep), (br << 8) | dep);
+}
+
+// The same slot in 32-bit arithmetic, for requests whose positions and ring
+// slots are all below 2^31 (the caller checks): entry e of the key list is a
+// sink (below ns), a committed key of the window (below Uc, at a position
+// >= n_sink), or draft node e - Uc = branch * depth + depth index.
+struct Geo32 {
+    int32_t ns, Uc, lo0, S, base, n_sink, depth;
+    uint32_t m;  // window + depth * tree_k
+};
+
+__device__ __forceinline__ int32_t tree_slot32(const Geo32 &g, int32_t e) {
+    if (e < g.ns) return g.base + e;
+    if (e < g.Uc) return g.base + g.n_sink + (int32_t)((uint32_t)(g.lo0 + (e - g.ns) - g.n_sink) % g.m);
+    const int32_t n = e - g.Uc;
+    const int32_t br = n / g.depth;
+    const int32_t dep = n - br * g.depth;
+    const int32_t p = g.S + dep;
+    if (p < g.n_sink && br == 0) return g.base + p;
+    int32_t r = (p - g.n_sink + br * g.depth) % (int32_t)g.m;
+    if (r < 0) r += (int32_t)g.m;
+    return g.base + g.n_sink + r;
 }
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int32_t *abort) {
@@ -206,7 +236,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_addr(&bars[kSFull + i]), 1);
-            mbar_init(smem_addr(&bars[kSEmpty + i]), kSoftWarps);
             mbar_init(smem_addr(&bars[kPFull + i]), kSoftWarps);
             mbar_init(smem_addr(&bars[kPvDone + i]), 1);
         }
@@ -226,74 +255,80 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
 
     if (warp >= kSoftWarps && warp < kMmaWarp) {
         // ----------------------------------------------------------- gather
-        // One warp: lane k holds the slot of key k of the tile.  A tile whose
-        // 32 keys sit in consecutive pool slots comes in as one TMA box per
-        // 64-dim block of K and of V; otherwise each such 8-key group does,
-        // and the remaining keys (ring wrap, segment edges, the tail, bad
-        // slots) are copied or zero-filled with cp.async.  Both land in the
-        // 128-byte-swizzled K-major layout the MMAs read; the stage barrier
-        // counts the 32 cp.async arrivals and one byte-count arrival for the
-        // TMA boxes.
+        // One warp, one 32-key copy stage at a time (two per MMA tile); lane
+        // k computes the slot of key k.  A stage of 32 valid keys in
+        // consecutive pool slots comes in as one TMA box per 64-dim block of
+        // K and of V (64 dims x 1 head x 32 slots, 128-byte swizzle).
+        // Otherwise 8-key groups of consecutive slots come in as 8-slot
+        // boxes, and the remaining keys (ring wrap, segment edges, the tail,
+        // bad slots) are copied or zero-filled with cp.async into the same
+        // swizzled layout.  The stage barrier counts the 32 cp.async
+        // arrivals and one byte-count arrival for the TMA boxes.
         const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * D * 2;
         const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * D * 2;
         const size_t slot_bytes = (size_t)H_kv * D * 2;
-        for (int t = 0; t < n_tiles; ++t) {
+        const int64_t ring_m = (int64_t)window + (int64_t)depth * tree_k;
+        const bool fits32 = base >= 0 && S + (int64_t)depth * tree_k < INT32_MAX && geo.U < INT32_MAX &&
+                            base + n_sink + ring_m < INT32_MAX;
+        const Geo32 g32{(int32_t)geo.ns, (int32_t)geo.Uc, (int32_t)geo.lo0, (int32_t)S, (int32_t)base,
+                        n_sink, depth, (uint32_t)ring_m};
+        auto slot_of = [&](int64_t e) -> int64_t {
+            if (fits32) return tree_slot32(g32, (int32_t)e);
+            const int2 inf = key_info(geo, e, depth);
+            const int br = inf.y < 0 ? 0 : (inf.y >> 8);
+            return ring_slot(base, inf.x, br, n_sink, window, depth, tree_k);
+        };
+        for (int t = 0; t < 2 * n_tiles; ++t) {  // copy stages; keys past cnt are zero-filled
             const int st = t % kKvStages;
             if (t >= kKvStages &&
                 !mbar_wait(&bars[kKvEmpty + st], ((t / kKvStages) - 1) & 1, flags))
                 break;
             if (flags[0]) break;
-            const int64_t kk = (int64_t)t * kKeys + lane;
+            const uint32_t kt = sbase + C::kKOff + st * (kCopyKeys * 128);
+            const uint32_t vt = sbase + C::kVOff + st * (kCopyKeys * 128);
+            const uint32_t bar = smem_addr(&bars[kKvFull + st]);
+            const int64_t kk = (int64_t)t * kCopyKeys + lane;
             int64_t slot = 0;
             bool ok = false;
             if (kk < cnt) {
-                const int2 inf = key_info(geo, start + kk, depth);
-                const int br = inf.y < 0 ? 0 : (inf.y >> 8);
-                slot = ring_slot(base, inf.x, br, n_sink, window, depth, tree_k);
+                slot = slot_of(start + kk);
                 ok = slot >= 0 && slot < num_slots;
-                if (!ok) latch(WMTP_DEV_SLOT_RANGE);
             }
-            // contiguity: key k continues key k-1's slot
             const int64_t prev = __shfl_up_sync(0xffffffffu, slot, 1);
-            const bool cont = ok && (lane == 0 || slot == prev + 1);
-            const uint32_t contm = __ballot_sync(0xffffffffu, cont);
-            const uint32_t okm = __ballot_sync(0xffffffffu, ok);
-            const int64_t slot0 = __shfl_sync(0xffffffffu, slot, 0);
-            uint32_t tma_groups = 0;  // bit gi: group gi by box-8 TMA
-            bool whole = okm == 0xffffffffu && (contm | 1u) == 0xffffffffu;
-            if (!whole) {
-#pragma unroll
-                for (int gi = 0; gi < kKeys / 8; ++gi) {
-                    const uint32_t gm = 0xffu << (gi * 8);
-                    // all 8 valid, and keys 1..7 of the group continue the run
-                    if ((okm & gm) == gm && (contm & (gm & ~(1u << (gi * 8)))) == (gm & ~(1u << (gi * 8))))
-                        tma_groups |= 1u << gi;
-                }
-            }
-            const uint32_t kt = sbase + C::kKvOff + st * C::kStageBytes;
-            const uint32_t vt = kt + C::kTileBytes;
-            const uint32_t bar = smem_addr(&bars[kKvFull + st]);
-            if (lane == 0) {
-                const uint32_t bytes = whole ? 2u * C::kTileBytes : (uint32_t)__popc(tma_groups) * 2u * 8u * (uint32_t)(D * 2);
-                mbar_arrive_expect_tx(bar, bytes);
-                if (whole) {
+            const bool whole = __all_sync(0xffffffffu, ok && (lane == 0 || slot == prev + 1));
+            if (whole) {
+                const int64_t slot0 = __shfl_sync(0xffffffffu, slot, 0);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar, 2u * C::kCopyBytes);
 #pragma unroll
                     for (int db = 0; db < C::kDimBlocks; ++db) {
-                        tma_load_3d(kt + db * C::kBlockBytes, &tm_k32, db * 64, g, (int32_t)slot0, bar);
-                        tma_load_3d(vt + db * C::kBlockBytes, &tm_v32, db * 64, g, (int32_t)slot0, bar);
+                        tma_load_3d(kt + db * C::kRingBlockBytes, &tm_k32, db * 64, g, (int32_t)slot0, bar);
+                        tma_load_3d(vt + db * C::kRingBlockBytes, &tm_v32, db * 64, g, (int32_t)slot0, bar);
                     }
                 }
-            }
-            if (!whole) {
+            } else {
+                if (kk < cnt && !ok) latch(WMTP_DEV_SLOT_RANGE);
+                // contiguity inside 8-key groups: key k continues key k-1's slot
+                const bool cont = ok && ((lane & 7) == 0 || slot == prev + 1);
+                const uint32_t contm = __ballot_sync(0xffffffffu, cont);
+                const uint32_t okm = __ballot_sync(0xffffffffu, ok);
+                uint32_t tma_groups = 0;  // bit gi: group gi by 8-slot TMA boxes
 #pragma unroll
-                for (int gi = 0; gi < kKeys / 8; ++gi) {
-                    const int64_t gs = __shfl_sync(0xffffffffu, slot, gi * 8);
+                for (int gi = 0; gi < kCopyKeys / 8; ++gi) {
+                    const uint32_t gm = 0xffu << (gi * 8);
+                    if ((okm & gm) == gm && (contm & gm) == gm) tma_groups |= 1u << gi;
+                }
+                if (lane == 0)
+                    mbar_arrive_expect_tx(bar, (uint32_t)__popc(tma_groups) * 2u * 8u * (uint32_t)(D * 2));
+#pragma unroll
+                for (int gi = 0; gi < kCopyKeys / 8; ++gi) {
                     if ((tma_groups >> gi) & 1u) {
+                        const int64_t gs = __shfl_sync(0xffffffffu, slot, gi * 8);
                         if (lane == 0) {
 #pragma unroll
                             for (int db = 0; db < C::kDimBlocks; ++db) {
-                                tma_load_3d(kt + db * C::kBlockBytes + gi * 1024, &tm_k8, db * 64, g, (int32_t)gs, bar);
-                                tma_load_3d(vt + db * C::kBlockBytes + gi * 1024, &tm_v8, db * 64, g, (int32_t)gs, bar);
+                                tma_load_3d(kt + db * C::kRingBlockBytes + gi * 1024, &tm_k8, db * 64, g, (int32_t)gs, bar);
+                                tma_load_3d(vt + db * C::kRingBlockBytes + gi * 1024, &tm_v8, db * 64, g, (int32_t)gs, bar);
                             }
                         }
                     } else {
@@ -306,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                             const bool kok = (okm >> kr) & 1u;
                             const size_t off = kok ? (size_t)sl * slot_bytes + c * 16 : 0;
                             const int db = c >> 3, cb = c & 7;
-                            const uint32_t dst = db * C::kBlockBytes + kr * 128 + ((cb ^ (kr & 7)) << 4);
+                            const uint32_t dst = db * C::kRingBlockBytes + kr * 128 + ((cb ^ (kr & 7)) << 4);
                             cp_async_16(kt + dst, kbase + off, kok ? 16u : 0u, keep);
                             cp_async_16(vt + dst, vbase + off, kok ? 16u : 0u, keep);
                         }
@@ -321,18 +356,22 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         if (lane == 0) {
             constexpr uint32_t idesc_qk = tc_idesc_bf16(kRows, kKeys, 0);
             constexpr uint32_t idesc_pv = tc_idesc_bf16(kRows, D, 1);
+            // MMA tile t = copy stages s0, s0 + 1 (same pass over the ring)
             auto issue_qk = [&](int t) -> bool {
-                const int st = t % kKvStages, sb = t & 1;
+                const int s0 = (2 * t) % kKvStages, sb = t & 1;
+                const uint32_t ph = (uint32_t)((2 * t) / kKvStages) & 1u;
                 if (t == 0 && !mbar_wait(&bars[kQFull], 0, flags)) return false;
-                if (!mbar_wait(&bars[kKvFull + st], (t / kKvStages) & 1, flags)) return false;
-                if (t >= 2 && !mbar_wait(&bars[kSEmpty + sb], ((t >> 1) - 1) & 1, flags)) return false;
+                if (!mbar_wait(&bars[kKvFull + s0], ph, flags)) return false;
+                if (!mbar_wait(&bars[kKvFull + s0 + 1], ph, flags)) return false;
+                // S buffer sb last held P of tile t-2: its PV must be done
+                if (t >= 2 && !mbar_wait(&bars[kPvDone + sb], ((t >> 1) - 1) & 1, flags)) return false;
                 fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
                 tc_fence_after();
-                const uint32_t kt = sbase + C::kKvOff + st * C::kStageBytes;
+                const uint32_t kt = sbase + C::kKOff + s0 * (kCopyKeys * 128);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     tc_mma_bf16_ta(tmem + sb * kKeys, tmem + C::kQCol + kk * 8,
-                                   tc_smem_desc_sw128(kt + (kk / 4) * C::kBlockBytes + (kk % 4) * 32, 16, 1024),
+                                   tc_smem_desc_sw128(kt + (kk / 4) * C::kRingBlockBytes + (kk % 4) * 32, 16, 1024),
                                    idesc_qk, kk > 0);
                 tc_commit(smem_addr(&bars[kSFull + sb]));
                 return true;
@@ -343,16 +382,19 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                 const int pb = t & 1;
                 if (!mbar_wait(&bars[kPFull + pb], (t >> 1) & 1, flags)) break;
                 tc_fence_after();
-                const uint32_t vt = sbase + C::kKvOff + (t % kKvStages) * C::kStageBytes + C::kTileBytes;
-                const uint32_t p_hi = tmem + C::kPCol + pb * kKeys, p_lo = p_hi + kKeys / 2;
+                const int s0 = (2 * t) % kKvStages;
+                const uint32_t vt = sbase + C::kVOff + s0 * (kCopyKeys * 128);
+                // P was written over S buffer pb: head in its first half, tail in the second
+                const uint32_t p_hi = tmem + pb * kKeys, p_lo = p_hi + kKeys / 2;
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    const uint64_t vd = tc_smem_desc_sw128(vt + kk * 16 * 128, C::kBlockBytes, 1024);
+                    const uint64_t vd = tc_smem_desc_sw128(vt + kk * 16 * 128, C::kRingBlockBytes, 1024);
                     tc_mma_bf16_ta(tmem + C::kOCol, p_hi + kk * 8, vd, idesc_pv, (t > 0 || kk > 0));
                     tc_mma_bf16_ta(tmem + C::kOCol, p_lo + kk * 8, vd, idesc_pv, 1);
                 }
                 tc_commit(smem_addr(&bars[kPvDone + pb]));
-                tc_commit(smem_addr(&bars[kKvEmpty + (t % kKvStages)]));
+                tc_commit(smem_addr(&bars[kKvEmpty + s0]));
+                tc_commit(smem_addr(&bars[kKvEmpty + s0 + 1]));
             }
         }
     } else {
@@ -412,15 +454,13 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             if (!warp_wait(&bars[kSFull + sb], (t >> 1) & 1, flags)) break;
             tc_fence_after();
             float x[kKeys];
-            {
-                uint32_t r0[32];
-                tc_ld32(lane_base + sb * kKeys, r0);
 #pragma unroll
-                for (int k = 0; k < kKeys; ++k) x[k] = __uint_as_float(r0[k]);
+            for (int c0 = 0; c0 < kKeys; c0 += 32) {
+                uint32_t r0[32];
+                tc_ld32(lane_base + sb * kKeys + c0, r0);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) x[c0 + k] = __uint_as_float(r0[k]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&bars[kSEmpty + sb]));
             // Tree-causal mask from the key index alone, with per-row int32
             // thresholds (no loads, no division): entry e is a committed key
             // when e < Uc, else draft node n = e - Uc.  Tiles whose keys every
@@ -480,19 +520,21 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                 rs += x[k];
             }
             l += rs;
-            // P buffer pb is free once PV(t-2) is done
-            if (t >= 2 && !warp_wait(&bars[kPvDone + pb], ((t >> 1) - 1) & 1, flags)) break;
             {
-                // P as bf16 head (columns 0-15) and tail (16-31) of this row's
-                // lane, two keys per column
-                uint32_t pr[32];
+                // P over this row's S (read above): bf16 head in columns 0-31
+                // and tail in 32-63 of the buffer, two keys per column.  No
+                // MMA still reads the buffer: QK(t) was issued only after the
+                // PV of tile t-2 had finished with it.
+                uint32_t ph[kKeys / 2], pl[kKeys / 2];
 #pragma unroll
                 for (int u = 0; u < kKeys / 2; ++u) {
                     const float a = x[2 * u], c2 = x[2 * u + 1];
-                    pr[u] = pack_bf16x2(a, c2);
-                    pr[kKeys / 2 + u] = pack_bf16x2(a - bf16_lo_to_f32(pr[u]), c2 - bf16_hi_to_f32(pr[u]));
+                    ph[u] = pack_bf16x2(a, c2);
+                    pl[u] = pack_bf16x2(a - bf16_lo_to_f32(ph[u]), c2 - bf16_hi_to_f32(ph[u]));
                 }
-                tc_st32(lane_base + C::kPCol + pb * kKeys, pr);
+                static_assert(kKeys / 2 == 32, "one 32-column store per half");
+                tc_st32(lane_base + pb * kKeys, ph);
+                tc_st32(lane_base + pb * kKeys + kKeys / 2, pl);
             }
             tc_fence_before();
             __syncwarp();
@@ -769,8 +811,8 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
         ws.o_part = reinterpret_cast<float *>(p);
     }
     CUtensorMap tm_k32, tm_v32, tm_k8, tm_v8;
-    if (!pool_tensor_map(&tm_k32, k_pool, num_slots, H_kv, D, kKeys) ||
-        !pool_tensor_map(&tm_v32, v_pool, num_slots, H_kv, D, kKeys) ||
+    if (!pool_tensor_map(&tm_k32, k_pool, num_slots, H_kv, D, kCopyKeys) ||
+        !pool_tensor_map(&tm_v32, v_pool, num_slots, H_kv, D, kCopyKeys) ||
         !pool_tensor_map(&tm_k8, k_pool, num_slots, H_kv, D, 8) ||
         !pool_tensor_map(&tm_v8, v_pool, num_slots, H_kv, D, 8))
         return WMTP_ECUDA;
@@ -840,7 +882,7 @@ int32_t wmtp_tree_num_splits(int32_t B, int32_t H_q, int32_t H_kv, int32_t depth
     const int64_t per_split = (int64_t)B * H_kv * n_rb;
     const int64_t keys = (int64_t)n_sink + window + (int64_t)tree_k * depth;
     int64_t n = sms / per_split;
-    const int64_t by_len = (keys + kKeys - 1) / kKeys / 4;  // >= four tiles per split
+    const int64_t by_len = (keys + 31) / 32 / 4;  // >= 128 keys per split
     if (n > by_len) n = by_len;
     if (n < 1) n = 1;
     if (n > kMaxSplits) n = kMaxSplits;
