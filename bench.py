@@ -540,8 +540,8 @@ def measure_extend(w, args, dev):
     full-context.  Event-timed with L2 flushed before each launch; algorithmic
     bytes are the pass's unique bytes: K and V of every key of the union table
     once (every KV head), the table, q, out and lse.  `token_reads_gbs` counts
-    instead each token's own key set, as this kernel reads it (the tokens of
-    a request share most of their keys)."""
+    instead each token's own key set (the tokens of a request share most of
+    their keys).  `kernel` names the launch the library picks for the row."""
     import speculative_decoding_draft_build_gb300 as wm
     c = w.cfg
     B, S, H_q, H_kv, D = c["B"], c["S"], c["H_q"], c["H_kv"], c["D"]
@@ -582,7 +582,15 @@ def measure_extend(w, args, dev):
         rest = 4 * L + n * H_q * (D * 2 + (D + 1) * 4)
         nbytes = B * (L * H_kv * D * 2 * 2 + rest)
         token_bytes = B * (keys * H_kv * D * 2 * 2 + rest)
+        stride = tab.shape[-1]
+        if 2 <= n <= 8 and ns <= 128 and stride >= 65536:
+            kernel = f"tree_tc_kernel<{D}> (tcgen05, union table row)"
+        elif 2 <= n <= 8 and ns <= 128 and stride >= 1024 * ns:
+            kernel = f"extend_kernel<{D}> (one K/V read for all tokens)"
+        else:
+            kernel = f"split_decode_kernel<{D}, extend> (CTAs per token)"
         res["windowed" if windowed else "full"] = {
+            "kernel": kernel,
             "us_per_pass": round(t * 1e6, 2), "kv_gbs": round(nbytes / t / 1e9, 1),
             "frac_of_hbm": round(nbytes / t / 1e9 / peak, 4), "n_split": ns,
             "union_keys": L, "bytes_per_pass": int(nbytes),

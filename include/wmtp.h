@@ -271,12 +271,20 @@ wmtp_status wmtp_draft_decode_attn_append(const uint16_t *k_new,
  * Other arguments, the split plan, workspace and errors as
  * wmtp_draft_decode_attn; additionally WMTP_EINVAL for null seq_lens or
  * n_new, n_sink < 0 or W < 1.
- * With 2 <= n_q <= 8, n_split <= 128 and table_stride >= 1024 * n_split
- * (long rows) one launch reads each union key once for all of a request's
- * tokens (a CTA per split of the union row and KV head, one warp per token)
- * and merges the splits through the workspace; otherwise every (request,
- * token) row is its own set of CTAs, as wmtp_draft_decode_attn.
- * wmtp_extend_num_splits gives the usual split count of either launch. */
+ * With 2 <= n_q <= 8, n_split <= 128, table_stride >= 65536 and q 16-byte
+ * aligned, the pass runs on the 5th-generation tensor cores: a request's
+ * tokens x query heads of a KV head are one 128-row MMA block over each
+ * union key once (the tree kernel's chain case, slots from the table), the
+ * splits merging through a cluster (n_split <= 8) or the workspace.  With
+ * 2 <= n_q <= 8, n_split <= 128 and table_stride >= 1024 * n_split one
+ * launch also reads each union key once for all of a request's tokens (a
+ * CTA per split of the union row and KV head, one warp per token) and
+ * merges the splits through the workspace; otherwise every (request, token)
+ * row is its own set of CTAs, as wmtp_draft_decode_attn.  The union table
+ * must hold exactly the keep set of S + n, as wmtp_build_extend_indices
+ * writes it: on the tensor-core path a row whose length differs latches
+ * WMTP_DEV_LEN_RANGE and reads no entry past table_stride.
+ * wmtp_extend_num_splits gives the usual split count of every launch. */
 wmtp_status wmtp_draft_extend_attn(const uint16_t *q, int32_t B, int32_t n_q,
                                    int32_t H_q, int32_t H_kv, int32_t D,
                                    const uint16_t *k_pool,

@@ -1194,6 +1194,18 @@ wmtp_status draft_decode_attn_checked(const uint16_t *q, int32_t B, int32_t n_q,
     }
     cudaStream_t s = as_stream(stream);
     if (ev.seq_lens && !fv.k_scale && !rv.seq_lens && n_q >= 2 && n_q <= kMaxExtendTokens &&
+        n_split <= kTreeExtendMaxSplits && table_stride >= kTreeExtendMinKeys && aligned16(q)) {
+        // long rows: the tokens of a request are one MMA row block on the
+        // tensor cores, each union key read once
+        WorkspaceView w{nullptr, nullptr, nullptr};
+        if (n_split > 1) w = carve(workspace, (int64_t)B * n_q * H_q, (int64_t)B * n_q * H_kv, n_split);
+        return tree_extend_launch(static_cast<const uint16_t *>(q), B, n_q, H_q, H_kv, D,
+                                  static_cast<const uint16_t *>(k_pool), static_cast<const uint16_t *>(v_pool),
+                                  num_slots, table, table_stride, lens, ev.seq_lens, ev.n_new, ev.n_sink,
+                                  ev.window, ev.windowed, scale, out, lse, w.counters, w.lse_part, w.o_part,
+                                  n_split, s);
+    }
+    if (ev.seq_lens && !fv.k_scale && !rv.seq_lens && n_q >= 2 && n_q <= kMaxExtendTokens &&
         n_split <= kMaxExtendSplits && table_stride >= (int64_t)kExtendMinKeysPerSplit * n_split) {
         // several new tokens per request: one K/V read serves them all
         WorkspaceView w{nullptr, nullptr, nullptr};

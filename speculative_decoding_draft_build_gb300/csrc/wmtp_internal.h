@@ -38,6 +38,20 @@ wmtp_status extend_multi_launch(const uint16_t *q, int32_t B, int32_t n_q, int32
                                 int32_t windowed, float scale, float *out, float *lse, int32_t *counters,
                                 float *lse_part, float *o_part, int32_t n_split, cudaStream_t stream);
 
+// Draft extend on the tensor cores (wmtp_tree.cu): a chain of n_q nodes per
+// request over the union table row, for rows of at least kTreeExtendMinKeys
+// keys and up to kTreeExtendMaxSplits splits; the partials of a split-order
+// merge use the decode attention's workspace layout (counters zero at rest).
+constexpr int64_t kTreeExtendMinKeys = 65536;
+constexpr int kTreeExtendMaxSplits = 128;
+wmtp_status tree_extend_launch(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q, int32_t H_kv,
+                               int32_t D, const uint16_t *k_pool, const uint16_t *v_pool,
+                               int64_t num_slots, const int32_t *table, int64_t table_stride,
+                               const int32_t *lens, const int32_t *seq_lens, const int32_t *n_new,
+                               int32_t n_sink, int32_t window, int32_t windowed, float scale,
+                               float *out, float *lse, int32_t *ws_counters, float *ws_lse_part,
+                               float *ws_o_part, int32_t n_split, cudaStream_t stream);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }

@@ -24,17 +24,21 @@
 //              accumulator is rescaled in tensor memory only when the max
 //              grows by more than 2^8), writes P as bf16 head + tail over its
 //              row of S, and at the end reads its row of O.
-//   warp 4     gather: slots from the ring rule (no table); 32-key copy
-//              stages of consecutive ring slots arrive as TMA boxes (64 dims
+//   warps 4-7  gather: slots from the ring rule (or a table, below); 32-key
+//              copy stages of consecutive slots arrive as TMA boxes (64 dims
 //              x 1 head x 32 or 8 slots, 128-byte swizzle), other keys
-//              through 16-byte cp.async into the same swizzled layout; six
-//              stages, two per MMA tile.
-//   warp 5     one thread issues the MMAs: S(t) = Q K(t)^T (M=128, N=64,
+//              through 16-byte cp.async into the same swizzled layout, each
+//              warp one 8-key group; six stages, two per MMA tile.
+//   warp 8     one thread issues the MMAs: S(t) = Q K(t)^T (M=128, N=64,
 //              K=D) into one of two S buffers, then O += P_hi V + P_lo V
 //              (M=128, N=D, K=64); completion is signalled through mbarriers
 //              with tcgen05.commit.  Q and P are read from tensor memory
 //              (the A operands); K is K-major and V MN-major in shared
 //              memory, both 128-byte swizzled.
+// Table mode (the draft-extend pass of a chain): the key list of request b
+// is the union table row of its accepted tokens, tree_k = 1 and depth = the
+// tokens per request; token i at position S + i sees keep(S + i + 1), the
+// same key sets as node (0, i) above.
 // Key chunks are split over CTAs; up to 8 chunks of a (request, KV head,
 // row block) run as one cluster and merge through distributed shared memory,
 // more through the workspace (the last CTA merges in split order).  Every
@@ -64,11 +68,11 @@ constexpr int kCopyKeys = 32;  // keys per copy stage: two stages make one MMA t
 constexpr int kKvStages = 6;   // copy stages (even: an MMA tile never wraps the ring)
 static_assert(kKeys == 2 * kCopyKeys && kKvStages % 2 == 0, "stage pairing");
 constexpr int kSoftWarps = 4;
-constexpr int kLoadWarps = 1;
+constexpr int kLoadWarps = 4;  // gather warps: warp w copies the 8-key groups w, w + 4, ...
 constexpr int kLoadThreads = kLoadWarps * 32;
 constexpr int kMmaWarp = kSoftWarps + kLoadWarps;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
-constexpr int kMaxSplits = 64;
+constexpr int kMaxSplits = 128;
 constexpr int kMaxClusterSplits = 8;  // key chunks merged through one (portable) cluster
 constexpr float kLazyRescale = 8.f;  // log2 of the growth tolerated before rescaling O
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -125,6 +129,18 @@ struct TreeWs {
     int32_t *counters;
     float *lse_part;
     float *o_part;
+};
+
+// Slots from a table instead of the ring rule (the chain draft-extend pass,
+// tree_k = 1, depth = tokens per request): entry e of request b's key list
+// sits in slot table[b * stride + e], lens[b] (if given) must equal the
+// list's length, and the request has n_new[b] nodes (rows of later nodes are
+// empty: out = 0, lse = -inf).  table == nullptr: ring mode.
+struct TreeTable {
+    const int32_t *table;
+    int64_t stride;
+    const int32_t *lens;
+    const int32_t *n_new;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -195,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     const __nv_bfloat16 *__restrict__ k_pool, const __nv_bfloat16 *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ ring_base,
     int32_t n_sink, int32_t window, int32_t depth, int32_t tree_k, float scale_log2,
-    float *__restrict__ out, float *__restrict__ lse, TreeWs ws, int32_t n_split, int32_t n_rb,
+    float *__restrict__ out, float *__restrict__ lse, TreeWs ws, TreeTable tt, int32_t n_split, int32_t n_rb,
     int32_t cluster_merge, const __grid_constant__ CUtensorMap tm_k32, const __grid_constant__ CUtensorMap tm_v32,
     const __grid_constant__ CUtensorMap tm_k8, const __grid_constant__ CUtensorMap tm_v8) {
     using C = Cfg<D>;
@@ -221,8 +237,21 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         if (tid == 0) latch(WMTP_DEV_ARG_RANGE);
         S = 0;
     }
-    const int64_t base = ring_base[b];
-    const Geo geo = geometry(S, n_sink, window, n_nodes);
+    const int64_t base = tt.table ? 0 : ring_base[b];
+    int n_b = n_nodes;  // nodes of this request
+    if (tt.n_new) {
+        n_b = tt.n_new[b];
+        n_b = n_b < 0 ? 0 : (n_b > n_nodes ? n_nodes : n_b);
+    }
+    Geo geo = geometry(S, n_sink, window, n_b);
+    if (tt.table && n_b == 0) {
+        geo.U = geo.Uc = 0;  // no node, no row to compute: every row is 0 / -inf
+    } else if (tt.table && (geo.U > tt.stride || (tt.lens && tt.lens[b] != geo.U))) {
+        // a table that does not hold this request's key list: no read past its row
+        if (tid == 0) latch(WMTP_DEV_LEN_RANGE);
+        geo.U = geo.U < tt.stride ? geo.U : tt.stride;
+        geo.Uc = geo.Uc < geo.U ? geo.Uc : geo.U;
+    }
     int64_t chunk = (geo.U + n_split - 1) / n_split;
     chunk = (chunk + kKeys - 1) / kKeys * kKeys;
     const int64_t start = (int64_t)split * chunk;
@@ -231,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
 
     if (tid == 0) {
         for (int i = 0; i < kKvStages; ++i) {
-            mbar_init(smem_addr(&bars[kKvFull + i]), kLoadThreads + 1);  // + the TMA byte count
+            mbar_init(smem_addr(&bars[kKvFull + i]), kLoadThreads + kLoadWarps);  // + one byte-count arrival per warp
             mbar_init(smem_addr(&bars[kKvEmpty + i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -255,15 +284,17 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
 
     if (warp >= kSoftWarps && warp < kMmaWarp) {
         // ----------------------------------------------------------- gather
-        // One warp, one 32-key copy stage at a time (two per MMA tile); lane
-        // k computes the slot of key k.  A stage of 32 valid keys in
-        // consecutive pool slots comes in as one TMA box per 64-dim block of
-        // K and of V (64 dims x 1 head x 32 slots, 128-byte swizzle).
-        // Otherwise 8-key groups of consecutive slots come in as 8-slot
-        // boxes, and the remaining keys (ring wrap, segment edges, the tail,
-        // bad slots) are copied or zero-filled with cp.async into the same
-        // swizzled layout.  The stage barrier counts the 32 cp.async
-        // arrivals and one byte-count arrival for the TMA boxes.
+        // Four warps, one 32-key copy stage at a time (two per MMA tile); in
+        // every warp lane k computes the slot of key k.  A stage of 32 valid
+        // keys in consecutive pool slots comes in as one TMA box per 64-dim
+        // block of K and of V (64 dims x 1 head x 32 slots, 128-byte
+        // swizzle), issued by the first warp.  Otherwise warp w takes 8-key
+        // group w: a group of consecutive slots comes in as 8-slot boxes,
+        // other keys (ring wrap, segment edges, the tail, bad slots, a paged
+        // table) are copied or zero-filled with cp.async into the same
+        // swizzled layout.  The stage barrier counts the 128 cp.async
+        // arrivals and one byte-count arrival per warp.
+        const int lw = warp - kSoftWarps;  // gather warp index
         const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * D * 2;
         const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * D * 2;
         const size_t slot_bytes = (size_t)H_kv * D * 2;
@@ -278,6 +309,19 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             const int br = inf.y < 0 ? 0 : (inf.y >> 8);
             return ring_slot(base, inf.x, br, n_sink, window, depth, tree_k);
         };
+        // table mode: each lane's slot of the next three copy stages in
+        // registers, so that no issue waits on a table load
+        const int32_t *trow = tt.table ? tt.table + b * tt.stride + start : nullptr;
+        auto tab_load = [&](int t_) -> int32_t {
+            const int64_t k2 = (int64_t)t_ * kCopyKeys + lane;
+            return k2 < cnt ? __ldg(trow + k2) : 0;
+        };
+        int32_t pf0 = 0, pf1 = 0, pf2 = 0;
+        if (trow) {
+            pf0 = tab_load(0);
+            pf1 = tab_load(1);
+            pf2 = tab_load(2);
+        }
         for (int t = 0; t < 2 * n_tiles; ++t) {  // copy stages; keys past cnt are zero-filled
             const int st = t % kKvStages;
             if (t >= kKvStages &&
@@ -290,38 +334,47 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             const int64_t kk = (int64_t)t * kCopyKeys + lane;
             int64_t slot = 0;
             bool ok = false;
+            if (trow) {
+                slot = pf0;
+                pf0 = pf1;
+                pf1 = pf2;
+                pf2 = tab_load(t + 3);
+            }
             if (kk < cnt) {
-                slot = slot_of(start + kk);
+                if (!trow) slot = slot_of(start + kk);
                 ok = slot >= 0 && slot < num_slots;
             }
             const int64_t prev = __shfl_up_sync(0xffffffffu, slot, 1);
             const bool whole = __all_sync(0xffffffffu, ok && (lane == 0 || slot == prev + 1));
             if (whole) {
                 const int64_t slot0 = __shfl_sync(0xffffffffu, slot, 0);
-                if (lane == 0) {
+                if (lane == 0 && lw == 0) {
                     mbar_arrive_expect_tx(bar, 2u * C::kCopyBytes);
 #pragma unroll
                     for (int db = 0; db < C::kDimBlocks; ++db) {
                         tma_load_3d(kt + db * C::kRingBlockBytes, &tm_k32, db * 64, g, (int32_t)slot0, bar);
                         tma_load_3d(vt + db * C::kRingBlockBytes, &tm_v32, db * 64, g, (int32_t)slot0, bar);
                     }
+                } else if (lane == 0) {
+                    mbar_arrive(bar);
                 }
             } else {
-                if (kk < cnt && !ok) latch(WMTP_DEV_SLOT_RANGE);
+                if (lw == 0 && kk < cnt && !ok) latch(WMTP_DEV_SLOT_RANGE);
                 // contiguity inside 8-key groups: key k continues key k-1's slot
                 const bool cont = ok && ((lane & 7) == 0 || slot == prev + 1);
                 const uint32_t contm = __ballot_sync(0xffffffffu, cont);
                 const uint32_t okm = __ballot_sync(0xffffffffu, ok);
-                uint32_t tma_groups = 0;  // bit gi: group gi by 8-slot TMA boxes
+                uint32_t tma_groups = 0;  // bit gi: this warp's group gi by 8-slot TMA boxes
 #pragma unroll
                 for (int gi = 0; gi < kCopyKeys / 8; ++gi) {
                     const uint32_t gm = 0xffu << (gi * 8);
-                    if ((okm & gm) == gm && (contm & gm) == gm) tma_groups |= 1u << gi;
+                    if (gi % kLoadWarps == lw && (okm & gm) == gm && (contm & gm) == gm) tma_groups |= 1u << gi;
                 }
                 if (lane == 0)
                     mbar_arrive_expect_tx(bar, (uint32_t)__popc(tma_groups) * 2u * 8u * (uint32_t)(D * 2));
 #pragma unroll
                 for (int gi = 0; gi < kCopyKeys / 8; ++gi) {
+                    if (gi % kLoadWarps != lw) continue;
                     if ((tma_groups >> gi) & 1u) {
                         const int64_t gs = __shfl_sync(0xffffffffu, slot, gi * 8);
                         if (lane == 0) {
@@ -432,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         }
         const int i = tid;  // row = tensor-memory lane
         const int rq = rb * kRows + i;
-        const bool row_live = rq < R;
+        const bool row_valid = rq < R;            // a row of the output
+        const bool row_live = row_valid && rq / G < n_b;  // ... of a node this request has
         const int node = row_live ? rq / G : 0;
         const int rbr = node / depth, rdep = node - (node / depth) * depth;
         const int64_t kv = S + rdep + 1;
@@ -467,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             // row of the warp sees skip the mask.
             const int e0 = (int)(start + (int64_t)t * kKeys);
             const int valid = (int)(cnt - (int64_t)t * kKeys);
-            const bool lane_all = !row_live || e0 + kKeys <= ns || e0 >= e_lo;
+            const bool lane_all = !row_valid || (row_live && (e0 + kKeys <= ns || e0 >= e_lo));
             const bool fast = valid >= kKeys && e0 + kKeys <= Uc && __all_sync(0xffffffffu, lane_all);
             float mx = -INFINITY;
             if (fast) {
@@ -547,7 +601,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             have_o = warp_wait(&bars[kPvDone + ((n_tiles - 1) & 1)], ((n_tiles - 1) >> 1) & 1, flags);
         have_o = __all_sync(0xffffffffu, have_o);
         tc_fence_after();
-        const int h = g * G + (row_live ? rq % G : 0);
+        const int h = g * G + (row_valid ? rq % G : 0);
+        const int wnode = row_valid ? rq / G : 0;  // output row (a node without keys writes 0 / -inf)
         const float inv = (have_o && l > 0.f) ? 1.f / l : 0.f;
         const float lse2 = (have_o && l > 0.f) ? m_ref + log2f(l) : -INFINITY;
         float *dst = nullptr;
@@ -557,9 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         float *po = reinterpret_cast<float *>(smem + C::kKvOff);
         if (cluster_merge) {
             reinterpret_cast<float *>(smem + C::kMergeOff)[i] = (row_live && !flags[0]) ? lse2 : -INFINITY;
-        } else if (row_live) {
+        } else if (row_valid) {
             if (n_split == 1) {
-                const int64_t orow = (b * n_nodes + node) * H_q + h;
+                const int64_t orow = (b * n_nodes + wnode) * H_q + h;
                 dst = out + orow * D;
                 if (lse) lse[orow] = flags[0] ? NAN : lse2 * kLn2;
             } else {
@@ -583,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                     const int d4 = (c0 + k) / 4;
                     reinterpret_cast<float4 *>(po + i * D)[d4 ^ (i & 7)] = v;
                 }
-            } else if (row_live) {
+            } else if (row_valid) {
 #pragma unroll
                 for (int k = 0; k < 32; k += 4) {
                     float4 v;
@@ -785,7 +840,8 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
                            const uint16_t *k_pool, const uint16_t *v_pool, int64_t num_slots,
                            const int32_t *seq_lens, const int32_t *ring_base, int32_t n_sink,
                            int32_t window, int32_t depth, int32_t tree_k, float scale, float *out,
-                           float *lse, void *workspace, int32_t n_split, cudaStream_t stream) {
+                           float *lse, void *workspace, int32_t n_split, cudaStream_t stream,
+                           TreeTable tt, TreeWs ws_given) {
     using C = Cfg<D>;
     const int G = H_q / H_kv;
     const int n_nodes = tree_k * depth;
@@ -802,7 +858,9 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
     }
     const bool use_cluster = n_split > 1 && tree_cluster_ok<D>(dev, n_split);
     TreeWs ws{nullptr, nullptr, nullptr};
-    if (n_split > 1 && !use_cluster) {
+    if (n_split > 1 && !use_cluster && ws_given.counters) {
+        ws = ws_given;
+    } else if (n_split > 1 && !use_cluster) {
         uint8_t *p = static_cast<uint8_t *>(workspace);
         ws.counters = reinterpret_cast<int32_t *>(p);
         p += align256((size_t)B * H_kv * n_rb * 4);
@@ -823,7 +881,7 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
         &launch.cfg, tree_tc_kernel<D>, reinterpret_cast<const __nv_bfloat16 *>(q), H_q, H_kv, G,
         n_nodes, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
         reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, seq_lens, ring_base, n_sink,
-        window, depth, tree_k, scale * 1.4426950408889634f, out, lse, ws, n_split, n_rb,
+        window, depth, tree_k, scale * 1.4426950408889634f, out, lse, ws, tt, n_split, n_rb,
         (int32_t)(use_cluster ? 1 : 0), tm_k32, tm_v32, tm_k8, tm_v8);
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
@@ -849,13 +907,34 @@ wmtp_status tree_tc_launch(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
                            const int32_t *seq_lens, const int32_t *ring_base, int32_t n_sink,
                            int32_t window, int32_t depth, int32_t tree_k, float scale, float *out,
                            float *lse, void *workspace, int32_t n_split, cudaStream_t stream) {
+    const TreeTable tt{nullptr, 0, nullptr, nullptr};
+    const TreeWs none{nullptr, nullptr, nullptr};
     if (D == 256)
         return launch_tree_tc<256>(q, B, H_q, H_kv, k_pool, v_pool, num_slots, seq_lens, ring_base,
                                    n_sink, window, depth, tree_k, scale, out, lse, workspace,
-                                   n_split, stream);
+                                   n_split, stream, tt, none);
     return launch_tree_tc<128>(q, B, H_q, H_kv, k_pool, v_pool, num_slots, seq_lens, ring_base,
                                n_sink, window, depth, tree_k, scale, out, lse, workspace, n_split,
-                               stream);
+                               stream, tt, none);
+}
+
+wmtp_status tree_extend_launch(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q, int32_t H_kv,
+                               int32_t D, const uint16_t *k_pool, const uint16_t *v_pool,
+                               int64_t num_slots, const int32_t *table, int64_t table_stride,
+                               const int32_t *lens, const int32_t *seq_lens, const int32_t *n_new,
+                               int32_t n_sink, int32_t window, int32_t windowed, float scale,
+                               float *out, float *lse, int32_t *ws_counters, float *ws_lse_part,
+                               float *ws_o_part, int32_t n_split, cudaStream_t stream) {
+    // A chain of n_q nodes whose key list is the union table row; without
+    // windowing, a window no kv length reaches.
+    const int32_t w = windowed ? window : INT32_MAX / 4;
+    const TreeTable tt{table, table_stride, lens, n_new};
+    const TreeWs ws{ws_counters, ws_lse_part, ws_o_part};
+    if (D == 256)
+        return launch_tree_tc<256>(q, B, H_q, H_kv, k_pool, v_pool, num_slots, seq_lens, nullptr, n_sink,
+                                   w, n_q, 1, scale, out, lse, nullptr, n_split, stream, tt, ws);
+    return launch_tree_tc<128>(q, B, H_q, H_kv, k_pool, v_pool, num_slots, seq_lens, nullptr, n_sink, w,
+                               n_q, 1, scale, out, lse, nullptr, n_split, stream, tt, ws);
 }
 
 }  // namespace wmtp

@@ -120,3 +120,14 @@ def test_extend_one_read_head_dim_128(n_q, n_list):
     # long rows take the one-read launch at D = 128 as well (G = 4 heads)
     _case([20_000, 45_000, 9_000], n_list, 64, 1024, 128, 8, 2, False, False, 660 + n_q, n_q=n_q,
           splits=(None, 2, 9))
+
+
+@pytest.mark.parametrize("windowed,D,H_q,H_kv", [(False, 128, 8, 2), (True, 256, 16, 2)])
+def test_extend_tensor_core_path_long_rows(windowed, D, H_q, H_kv):
+    # union rows of >= 65536 keys take the tensor-core launch (a request's
+    # tokens as one MMA row block over each union key once): one split,
+    # cluster merges, workspace merges, a request without new tokens, the
+    # ragged tail; the windowed union holds n_sink + W + n - 1 keys
+    W = 65_536 if windowed else 1024
+    _case([70_001, 150_000, 99_999], [5, 0, 2], 64, W, D, H_q, H_kv, windowed, False, 680 + windowed,
+          n_q=5, splits=(None, 1, 4, 8, 100))
