@@ -51,7 +51,7 @@ typedef int32_t wmtp_status;
 #define WMTP_DEV_OK 0
 #define WMTP_DEV_SLOT_RANGE 1    /* a slot index outside [0, num_slots) */
 #define WMTP_DEV_TABLE_OVERFLOW 2 /* a table row needs more than `stride` entries */
-#define WMTP_DEV_LEN_RANGE 3     /* a lens[] entry is negative or above the row stride */
+#define WMTP_DEV_LEN_RANGE 3     /* a lens[] entry is negative, above the row stride, or not the length of its key list */
 #define WMTP_DEV_WAIT_TIMEOUT 4  /* a pipeline wait ran out of time; results invalid */
 #define WMTP_DEV_ARG_RANGE 5     /* a device-side position, branch or length is out of range */
 

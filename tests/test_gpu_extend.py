@@ -131,3 +131,24 @@ def test_extend_tensor_core_path_long_rows(windowed, D, H_q, H_kv):
     W = 65_536 if windowed else 1024
     _case([70_001, 150_000, 99_999], [5, 0, 2], 64, W, D, H_q, H_kv, windowed, False, 680 + windowed,
           n_q=5, splits=(None, 1, 4, 8, 100))
+
+
+def test_extend_tensor_core_path_wrong_union_length_is_latched():
+    # a union length that is not the keep set of S + n is latched
+    # (WMTP_DEV_LEN_RANGE) on the tensor-core path; the launch reads no entry
+    # past the table row and the outputs stay finite
+    S, n, n_sink, W, H_q, H_kv, D = 80_000, 3, 64, 1024, 8, 2, 128
+    seq = torch.tensor([S], dtype=torch.int32, device=DEV)
+    nn = torch.tensor([n], dtype=torch.int32, device=DEV)
+    rtt = synth.permutation(S + 8, 690, DEV).view(1, -1)
+    kp = synth.normal_bf16((S + 8, H_kv, D), 691, DEV)
+    vp = synth.normal_bf16((S + 8, H_kv, D), 692, DEV)
+    q = synth.normal_bf16((1, n, H_q, D), 693, DEV)
+    tab, ln = wm.build_extend_indices(seq, nn, n_sink, W, 7, windowed=False, req_to_token=rtt)
+    assert tab.shape[-1] >= 65_536 and int(ln[0]) == S + n
+    wm.device_error(clear=True)
+    out, lse = wm.draft_extend_attn(q, kp, vp, tab, ln - 1, seq, nn, n_sink, W, 0.1, windowed=False,
+                                    n_split=16)
+    torch.cuda.synchronize()
+    assert wm.device_error(clear=True) == 3  # WMTP_DEV_LEN_RANGE
+    assert torch.all(torch.isfinite(out))
