@@ -276,7 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     if (warp == 0) tc_alloc(smem_addr(tmem_slot), C::kTmemCols);
 
     const uint32_t sbase = smem_addr(smem);
-    const uint64_t keep = l2_policy_evict_last();
+    // ring mode: the row-block CTAs of a request read the same keys, keep
+    // them in L2; table mode streams a long union row once
+    const uint64_t keep = tt.table ? l2_policy_evict_first() : l2_policy_evict_last();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
