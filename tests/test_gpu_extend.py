@@ -152,3 +152,12 @@ def test_extend_tensor_core_path_wrong_union_length_is_latched():
     torch.cuda.synchronize()
     assert wm.device_error(clear=True) == 3  # WMTP_DEV_LEN_RANGE
     assert torch.all(torch.isfinite(out))
+
+
+def test_extend_tensor_core_path_ring_layout():
+    # a windowed union of n_sink + W + n - 1 >= 65536 keys over per-request
+    # rings: the union row's slots run consecutively, so the tensor-core
+    # launch brings them in as TMA boxes (runs of 32 and 8 slots, the ring
+    # wrap and the sink seam by cp.async)
+    _case([70_001, 150_000, 99_999], [5, 0, 2], 64, 65_536, 256, 16, 2, True, True, 700,
+          n_q=5, splits=(None, 1, 8, 100))
