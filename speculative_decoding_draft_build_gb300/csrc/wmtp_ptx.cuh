@@ -71,31 +71,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// As mbar_try_wait, but the thread may sleep up to `hint_ns` inside the
-// instruction (it wakes as soon as the phase completes) instead of spinning.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait that sleeps in the barrier between checks.
-__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint32_t bar, uint32_t parity,
-                                                        uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 10000u)) return true;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
-}
-
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` nanoseconds and returns false; never spins without a bound.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
@@ -120,17 +95,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
-}
-
-// One contiguous global->shared copy on the TMA engine, completing `bytes`
-// transactions on mbarrier `bar`.  dst/src 16-byte aligned, bytes % 16 == 0.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                         uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-        : "memory");
 }
 
 // 3-D tiled TMA load (cp.async.bulk.tensor) of the box at coordinates
