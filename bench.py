@@ -210,6 +210,20 @@ class Dist:
 
 
 # ------------------------------------------------------------------ workload
+def packed(dev, parts):
+    """One device byte buffer holding tensors of the given (dtype, shape) at
+    256-byte aligned offsets, and the tensors as views into it (so that a set
+    of inputs or outputs moves between host and device in one copy)."""
+    offs, off = [], 0
+    for dt, shape in parts:
+        nbytes = math.prod(shape) * torch.empty((), dtype=dt).element_size()
+        offs.append((off, nbytes))
+        off += (nbytes + 255) // 256 * 256
+    buf = torch.empty(off, dtype=torch.uint8, device=dev)
+    views = [buf[o:o + n].view(dt).view(shape) for (o, n), (dt, shape) in zip(offs, parts)]
+    return buf, views
+
+
 class Workload:
     """Inputs resident on the device; tables, outputs and workspaces preallocated."""
 
@@ -226,11 +240,17 @@ class Workload:
         if cfg["outlier_frac"] > 0:
             synth.scale_random_rows_(self.kp, cfg["outlier_frac"], 4.0, seed + 1)
         self.vp = synth.normal_bf16((pool, H_kv, D), seed + 2, dev)
-        self.kn = synth.normal_bf16((g, B, H_kv, D), seed + 3, dev)
-        self.vn = synth.normal_bf16((g, B, H_kv, D), seed + 4, dev)
-        self.q = synth.normal_bf16((g, B, 1, H_q, D), seed + 5, dev)
+        # the step's inputs from the host (new K/V, queries, lengths) in one
+        # buffer, its windowed outputs in another: one copy each way per step
+        # in the end-to-end leg
+        bf = torch.bfloat16
+        self.io_in, (self.kn, self.vn, self.q, self.seq) = packed(
+            dev, [(bf, (g, B, H_kv, D)), (bf, (g, B, H_kv, D)), (bf, (g, B, 1, H_q, D)), (torch.int32, (B,))])
+        self.kn.copy_(synth.normal_bf16((g, B, H_kv, D), seed + 3, dev))
+        self.vn.copy_(synth.normal_bf16((g, B, H_kv, D), seed + 4, dev))
+        self.q.copy_(synth.normal_bf16((g, B, 1, H_q, D), seed + 5, dev))
+        self.seq.fill_(S)
         self.rtt = synth.permutation(pool, seed + 6, dev).view(B, S + g)
-        self.seq = torch.full((B,), S, dtype=torch.int32, device=dev)
         self.slots = torch.stack([self.rtt[:, S + j] for j in range(g)]).contiguous()  # [g, B]
         self.full_stride = S + g
         self.win_stride = cfg["n_sink"] + cfg["W"]
@@ -240,8 +260,8 @@ class Workload:
         self.len_win = torch.empty((g, B), dtype=torch.int32, device=dev)
         self.out_full = torch.empty((g, B, 1, H_q, D), dtype=torch.float32, device=dev)
         self.lse_full = torch.empty((g, B, 1, H_q), dtype=torch.float32, device=dev)
-        self.out_win = torch.empty_like(self.out_full)
-        self.lse_win = torch.empty_like(self.lse_full)
+        self.io_out, (self.out_win, self.lse_win) = packed(
+            dev, [(torch.float32, (g, B, 1, H_q, D)), (torch.float32, (g, B, 1, H_q))])
         self.ns_full = wm.attn_num_splits(B, 1, H_kv, S + g, dev)
         self.ns_win = wm.attn_num_splits(B, 1, H_kv, self.win_stride, dev)
         self.ws_full = wm.AttnWorkspace(wm.attn_workspace_bytes(B, 1, H_q, H_kv, D, self.ns_full), dev)
@@ -812,32 +832,22 @@ def measure_tree(args, dev):
 
 def measure_e2e(w, args, dev):
     """Windowed arm through the Python binding with host buffers: every step
-    copies its inputs (q, new K/V, seq_lens) from pinned host memory, runs
-    the arm, and reads the outputs back; timed on the host around a stream
-    synchronisation.  `value`: the whole step (copies in, index build, six
-    fused launches, copies out) captured once in a CUDA graph and replayed
-    per step, as a serving loop runs it; `eager_us`: the same step with
-    direct calls from Python."""
-    c = w.cfg
-    g = c["gamma"]
-    q_h = w.q.cpu().pin_memory()
-    kn_h = w.kn.cpu().pin_memory()
-    vn_h = w.vn.cpu().pin_memory()
-    seq_h = w.seq.cpu().pin_memory()
-    out_h = torch.empty(w.out_win.shape, dtype=torch.float32).pin_memory()
-    lse_h = torch.empty(w.lse_win.shape, dtype=torch.float32).pin_memory()
+    copies its inputs (q, new K/V, seq_lens; one packed buffer) from pinned
+    host memory, runs the arm, and reads the outputs (out, lse; one packed
+    buffer) back; timed on the host around a stream synchronisation.
+    `value`: the whole step (copy in, index build, six fused launches, copy
+    out) captured once in a CUDA graph and replayed per step, as a serving
+    loop runs it; `eager_us`: the same step with direct calls from Python."""
+    in_h = w.io_in.cpu().pin_memory()
+    out_h = torch.empty(w.io_out.shape, dtype=torch.uint8).pin_memory()
     stream = torch.cuda.current_stream(dev)
-    h2d = q_h.numel() * 2 + kn_h.numel() * 2 + vn_h.numel() * 2 + seq_h.numel() * 4
-    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    h2d = in_h.numel()
+    d2h = out_h.numel()
 
     def step():
-        w.q.copy_(q_h, non_blocking=True)
-        w.kn.copy_(kn_h, non_blocking=True)
-        w.vn.copy_(vn_h, non_blocking=True)
-        w.seq.copy_(seq_h, non_blocking=True)
+        w.io_in.copy_(in_h, non_blocking=True)
         w.win_arm()
-        out_h.copy_(w.out_win, non_blocking=True)
-        lse_h.copy_(w.lse_win, non_blocking=True)
+        out_h.copy_(w.io_out, non_blocking=True)
         stream.synchronize()
 
     for _ in range(max(args.warmup, 1)):
@@ -855,13 +865,9 @@ def measure_e2e(w, args, dev):
     gr = torch.cuda.CUDAGraph()
     with torch.cuda.stream(cap):
         with torch.cuda.graph(gr, stream=cap):
-            w.q.copy_(q_h, non_blocking=True)
-            w.kn.copy_(kn_h, non_blocking=True)
-            w.vn.copy_(vn_h, non_blocking=True)
-            w.seq.copy_(seq_h, non_blocking=True)
+            w.io_in.copy_(in_h, non_blocking=True)
             w.win_arm()
-            out_h.copy_(w.out_win, non_blocking=True)
-            lse_h.copy_(w.lse_win, non_blocking=True)
+            out_h.copy_(w.io_out, non_blocking=True)
     stream.wait_stream(cap)
     torch.cuda.synchronize(dev)
     for _ in range(max(args.warmup, 1)):
@@ -877,7 +883,7 @@ def measure_e2e(w, args, dev):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "eager_us": round(eager * 1e6, 3),
             "how": "windowed arm with pinned host I/O, host-timed: value = one CUDA graph per step "
-                   "(copies in, index build, 6 fused launches, copies out); eager_us = direct calls"}
+                   "(packed copy in, index build, 6 fused launches, packed copy out); eager_us = direct calls"}
 
 
 # ------------------------------------------------------------------ oracle legs
