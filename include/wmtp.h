@@ -353,7 +353,7 @@ wmtp_status wmtp_attn_mass_diagnostics(const float *o_full,
  *           zero.  Unused when n_split == 1, and when the key chunks merge
  *           through a thread-block cluster (n_split <= 8, where the device
  *           holds such clusters).
- * n_split   1 .. 64 key chunks per request; wmtp_tree_num_splits() gives one.
+ * n_split   1 .. 128 key chunks per request; wmtp_tree_num_splits() gives one.
  * Errors: WMTP_EINVAL for null or misaligned pointers, bad sizes, D not
  * 128/256, H_q % H_kv != 0, W < 1, d < 1, k < 1; WMTP_ECAPACITY for a small
  * workspace; slots outside the pool latch WMTP_DEV_SLOT_RANGE. */
