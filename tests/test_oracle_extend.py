@@ -86,3 +86,28 @@ def test_extend_rows_match_brute_force_softmax():
             ref = (w[:, None] * V[slots, g]).sum(0) / w.sum()
             assert np.allclose(out[0, t, h], ref, rtol=1e-12, atol=1e-12)
             assert np.isclose(lse[0, t, h], s.max() + np.log(w.sum()), rtol=1e-12)
+
+
+def test_chain_extend_equals_tree_attention_with_one_branch():
+    # an extend of n = d tokens over the ring is the tree attention with
+    # k = 1 and depth d (node i at position S + i sees keep(S + i + 1) with
+    # the draft positions of its own, single branch): the equivalence the
+    # library's tensor-core extend path is built on
+    rng = np.random.default_rng(17)
+    H_q, H_kv, D, n_sink, W, d = 4, 2, 16, 4, 9, 5
+    R = n_sink + W + d
+    S_list = np.array([0, 3, 12, 13, 14, 50, 200], np.int32)
+    B = S_list.size
+    rb = (np.arange(B, dtype=np.int32) * R + 3).astype(np.int32)
+    num_slots = B * R + 3
+    kp = rng.integers(0, 1 << 14, size=(num_slots, H_kv, D), dtype=np.uint16) & 0x3FFF
+    vp = rng.integers(0, 1 << 14, size=(num_slots, H_kv, D), dtype=np.uint16) & 0x3FFF
+    q = rng.integers(0, 1 << 14, size=(B, d, H_q, D), dtype=np.uint16) & 0x3FFF
+    xo, xl = oracle.draft_extend_attn(q, kp, vp, S_list, np.full(B, d, np.int32), n_sink, W, 0.3,
+                                      ring_base=rb, depth=d)
+    to, tl = oracle.tree_draft_attn(q, kp, vp, S_list, rb, n_sink, W, d, 1, 0.3)
+    assert np.all(np.isfinite(xo)) and np.all(np.isfinite(to))
+    assert np.allclose(xo, to, rtol=1e-12, atol=1e-12) and np.allclose(xl, tl, rtol=1e-12, atol=1e-12)
+    # the comparison discriminates: a tree with another window gives other rows
+    so, _ = oracle.tree_draft_attn(q, kp, vp, S_list, rb, n_sink, W - 1, d, 1, 0.3)
+    assert not np.allclose(so[S_list > n_sink + W], to[S_list > n_sink + W], rtol=1e-12, atol=1e-12)
