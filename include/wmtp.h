@@ -393,7 +393,16 @@ wmtp_status wmtp_tree_draft_attn(const uint16_t *q, int32_t B, int32_t H_q,
  *     array -- returns WMTP_ECAPACITY before launching anything.
  *   - The first call on a device (with that device current) looks up the
  *     array's device address; make that first call before any stream
- *     capture.  A failed lookup returns WMTP_ECUDA.
+ *     capture.  A failed lookup returns WMTP_ECUDA.  The address is cached
+ *     per device in an atomic slot, so host threads whose first calls
+ *     overlap are safe (each looks it up and stores the same value).  A
+ *     cudaDeviceReset of the device makes the cached address stale: do not
+ *     call this entry point on that device again in the same process.
+ *   - Results: the merge path is always the workspace ("last CTA merges")
+ *     merge, so they are bit-identical to wmtp_draft_decode_attn with the
+ *     same n_split whenever that call also merges through its workspace
+ *     (no thread-block cluster fits the split plan); where it merges
+ *     through a cluster instead, the two agree within rounding.
  *   - Every call shares the one array and it keeps the last call's
  *     contents; each call first zeroes the merge counters it uses (an
  *     async memset on `stream`).  Calls that overlap on the GPU (other

@@ -473,8 +473,36 @@ def draft_decode_attn_fp8(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.T
                  n_split, max_len, workspace, stream)
 
 
+def _attn_shapes(what, q, k_pool, v_pool, table, lens, out, lse):
+    """Shape checks of an attention call, made before anything else (the
+    kernels index every buffer from these sizes, so a short buffer would be
+    read or written past its end).  q [B, n_q, H_q, D]; k_pool and v_pool
+    [num_slots, H_kv, D]; table rows of `stride` entries (at least B rows);
+    lens at least B entries; out, lse (when given) exactly [B, n_q, H_q, D]
+    and [B, n_q, H_q].  Returns (B, n_q, H_q, D, num_slots, H_kv, stride)."""
+    if q.dim() != 4 or k_pool.dim() != 3:
+        raise ValueError(f"{what}: q must be [B, n_q, H_q, D] and k_pool [num_slots, H_kv, D]")
+    B, n_q, H_q, D = q.shape
+    num_slots, H_kv, Dk = k_pool.shape
+    if Dk != D:
+        raise ValueError(f"{what}: k_pool head dim {Dk} differs from q's {D}")
+    if v_pool.shape != k_pool.shape:
+        raise ValueError(f"{what}: v_pool shape {tuple(v_pool.shape)} differs from k_pool's "
+                         f"{tuple(k_pool.shape)}")
+    stride = table.shape[-1] if table.dim() > 0 else 0
+    if stride < 1 or table.numel() < B * stride or lens.numel() < B:
+        raise ValueError(f"{what}: table/lens smaller than B rows")
+    if out is not None and tuple(out.shape) != (B, n_q, H_q, D):
+        raise ValueError(f"{what}: out shape {tuple(out.shape)}, expected {(B, n_q, H_q, D)}")
+    if lse is not None and tuple(lse.shape) != (B, n_q, H_q):
+        raise ValueError(f"{what}: lse shape {tuple(lse.shape)}, expected {(B, n_q, H_q)}")
+    return B, n_q, H_q, D, num_slots, H_kv, stride
+
+
 def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_len, workspace,
           stream):
+    B, n_q, H_q, D, num_slots, H_kv, stride = _attn_shapes("draft_decode_attn", q, k_pool, v_pool,
+                                                           table, lens, out, lse)
     _need(q, "q", torch.bfloat16)
     dev = q.device
     pool_dtype = torch.uint8 if (append is not None and append[0] == "fp8") else torch.bfloat16
@@ -482,13 +510,6 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
         _need(t, nm, pool_dtype, dev)
     _need(table, "table", torch.int32, dev)
     _need(lens, "lens", torch.int32, dev)
-    B, n_q, H_q, D = q.shape
-    num_slots, H_kv, Dk = k_pool.shape
-    if Dk != D or v_pool.shape != k_pool.shape:
-        raise ValueError("draft_decode_attn: pool shape mismatch")
-    stride = table.shape[-1]
-    if table.numel() < B * stride or lens.numel() < B:
-        raise ValueError("draft_decode_attn: table/lens smaller than B rows")
     if out is None:
         out = torch.empty((B, n_q, H_q, D), dtype=torch.float32, device=dev)
     if lse is None:
@@ -585,7 +606,13 @@ def draft_decode_attn_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: tor
     (the library uses a fixed scratch array it holds on the device).  The
     outputs must be passed in; nothing is allocated on this path.  The first
     call on a device looks up the scratch address: make it before any stream
-    capture.  Calls that overlap on the GPU share the scratch and race."""
+    capture.  Calls that overlap on the GPU share the scratch and race.
+    Shapes are checked as for :func:`draft_decode_attn`; `out` and `lse` must
+    be exactly [B, n_q, H_q, D] and [B, n_q, H_q]."""
+    if out is None or lse is None:
+        raise ValueError("draft_decode_attn_noalloc: out and lse must be passed in")
+    B, n_q, H_q, D, num_slots, H_kv, stride = _attn_shapes(
+        "draft_decode_attn_noalloc", q, k_pool, v_pool, table, lens, out, lse)
     _need(q, "q", torch.bfloat16)
     dev = q.device
     for t, nm in ((k_pool, "k_pool"), (v_pool, "v_pool")):
@@ -594,12 +621,10 @@ def draft_decode_attn_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: tor
     _need(lens, "lens", torch.int32, dev)
     _need(out, "out", torch.float32, dev)
     _need(lse, "lse", torch.float32, dev)
-    B, n_q, H_q, D = q.shape
-    num_slots, H_kv, _ = k_pool.shape
     with _on(dev):
         _check(load().wmtp_draft_decode_attn_noalloc(
             _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
-            table.shape[-1], _ptr(lens), float(scale), _ptr(out), _ptr(lse), n_split,
+            stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), int(n_split),
             _stream(stream)), "draft_decode_attn_noalloc")
     return out, lse
 

@@ -45,6 +45,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "wmtp.h"
 #include "wmtp_internal.h"
 #include "wmtp_ptx.cuh"
@@ -1011,15 +1013,21 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
 
 // Device address of the scratch array on the current device `dev`, looked up
 // once per device (host code cannot use the symbol itself as an address).
+// The cache is atomic: host threads whose first calls on a device overlap
+// each look the address up and store the same value.  A cudaDeviceReset of
+// the device makes the cached address stale (the array is re-created in the
+// next context); the header says so.
 void *noalloc_scratch(int dev) {
-    static void *addr[64] = {};
+    static std::atomic<void *> addr[64] = {};
     if (dev < 0 || dev >= 64) return nullptr;
-    if (!addr[dev]) {
+    void *cached = addr[dev].load(std::memory_order_acquire);
+    if (!cached) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = p;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+        addr[dev].store(p, std::memory_order_release);
+        cached = p;
     }
-    return addr[dev];
+    return cached;
 }
 
 // Bytes of partials (after the counter region) a call needs.
