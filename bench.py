@@ -258,8 +258,8 @@ class Workload:
         self.len_full = torch.empty((g, B), dtype=torch.int32, device=dev)
         self.tab_win = torch.empty((g, B, self.win_stride), dtype=torch.int32, device=dev)
         self.len_win = torch.empty((g, B), dtype=torch.int32, device=dev)
-        self.out_full = torch.empty((g, B, 1, H_q, D), dtype=torch.float32, device=dev)
-        self.lse_full = torch.empty((g, B, 1, H_q), dtype=torch.float32, device=dev)
+        self.io_out_full, (self.out_full, self.lse_full) = packed(
+            dev, [(torch.float32, (g, B, 1, H_q, D)), (torch.float32, (g, B, 1, H_q))])
         self.io_out, (self.out_win, self.lse_win) = packed(
             dev, [(torch.float32, (g, B, 1, H_q, D)), (torch.float32, (g, B, 1, H_q))])
         self.ns_full = wm.attn_num_splits(B, 1, H_kv, S + g, dev)
@@ -269,37 +269,51 @@ class Workload:
         self.flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize(dev)
 
-    def full_arm(self, events=None):
+    def full_arm(self, events=None, attn_only=False, n_split=None):
         import speculative_decoding_draft_build_gb300 as wm
         c = self.cfg
-        wm.build_draft_indices(self.seq, c["gamma"], c["n_sink"], c["W"], c["gamma"] + 1,
-                               windowed=False, req_to_token=self.rtt, table=self.tab_full,
-                               lens=self.len_full)
+        if not attn_only:
+            wm.build_draft_indices(self.seq, c["gamma"], c["n_sink"], c["W"], c["gamma"] + 1,
+                                   windowed=False, req_to_token=self.rtt, table=self.tab_full,
+                                   lens=self.len_full)
         for j in range(c["gamma"]):
             if events is not None:
                 events[j][0].record()
             wm.draft_decode_attn_append(self.kn[j], self.vn[j], self.slots[j],
                                         self.q[j], self.kp, self.vp, self.tab_full[j], self.len_full[j],
                                         self.scale, out=self.out_full[j], lse=self.lse_full[j],
-                                        n_split=self.ns_full, workspace=self.ws_full)
+                                        n_split=n_split or self.ns_full, workspace=self.ws_full)
             if events is not None:
                 events[j][1].record()
 
-    def win_arm(self, events=None):
+    def win_arm(self, events=None, attn_only=False, n_split=None):
         import speculative_decoding_draft_build_gb300 as wm
         c = self.cfg
-        wm.build_draft_indices(self.seq, c["gamma"], c["n_sink"], c["W"], c["gamma"] + 1,
-                               windowed=True, req_to_token=self.rtt, table=self.tab_win,
-                               lens=self.len_win)
+        if not attn_only:
+            wm.build_draft_indices(self.seq, c["gamma"], c["n_sink"], c["W"], c["gamma"] + 1,
+                                   windowed=True, req_to_token=self.rtt, table=self.tab_win,
+                                   lens=self.len_win)
+        ws = self.ws_win
+        if n_split is not None and n_split != self.ns_win:
+            ws = self.workspace_for(n_split)
         for j in range(c["gamma"]):
             if events is not None:
                 events[j][0].record()
             wm.draft_decode_attn_append(self.kn[j], self.vn[j], self.slots[j],
                                         self.q[j], self.kp, self.vp, self.tab_win[j], self.len_win[j],
                                         self.scale, out=self.out_win[j], lse=self.lse_win[j],
-                                        n_split=self.ns_win, workspace=self.ws_win)
+                                        n_split=n_split or self.ns_win, workspace=ws)
             if events is not None:
                 events[j][1].record()
+
+    def workspace_for(self, n_split):
+        import speculative_decoding_draft_build_gb300 as wm
+        c = self.cfg
+        key = ("ws", n_split)
+        if key not in self.__dict__:
+            self.__dict__[key] = wm.AttnWorkspace(
+                wm.attn_workspace_bytes(c["B"], 1, c["H_q"], c["H_kv"], c["D"], n_split), self.dev)
+        return self.__dict__[key]
 
     def bytes_full_attn(self, j):
         c = self.cfg
@@ -318,11 +332,41 @@ def hold_gpu(us: float = 150.0):
     torch.cuda._sleep(int(us * 2100))  # cycles at about 2.1 GHz
 
 
-def _external_event():
-    try:
-        return torch.cuda.Event(enable_timing=True, external=True)
-    except TypeError:
-        return None
+def graph_of(fn, dev):
+    """The launches `fn` makes, captured once in a CUDA graph (on a side
+    stream; the current stream waits for the capture)."""
+    cur = torch.cuda.current_stream(dev)
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(cur)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(gr, stream=cap):
+            fn()
+    cur.wait_stream(cap)
+    torch.cuda.synchronize(dev)
+    return gr
+
+
+def time_graph_samples(gr, flush, reps, dev, warm=3):
+    """Microseconds of `reps` replays of `gr`, each bracketed by CUDA events on
+    the current stream with L2 flushed (a 256 MiB write) just before it."""
+    for _ in range(warm):
+        gr.replay()
+    torch.cuda.synchronize(dev)
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        a.record()
+        gr.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        ts.append(a.elapsed_time(b) * 1e3)
+    return ts
+
+
+def time_graph(gr, flush, reps, dev):
+    return statistics.median(time_graph_samples(gr, flush, reps, dev))
 
 
 # ------------------------------------------------------------------ our arm
@@ -343,21 +387,8 @@ def run_ours(args, dist_ctx):
         w.win_arm()
     torch.cuda.synchronize(dev)
 
-    # windowed arm as a CUDA graph (timed loop), plus a second capture with
-    # timing events around each attention launch when this torch supports
-    # events inside a capture (used after the timed loop)
-    cap_stream = torch.cuda.Stream(dev)
-
-    def capture(events=None):
-        gr = torch.cuda.CUDAGraph()
-        cap_stream.wait_stream(stream)
-        with torch.cuda.stream(cap_stream):
-            with torch.cuda.graph(gr, stream=cap_stream):
-                w.win_arm(events)
-        stream.wait_stream(cap_stream)
-        return gr
-
-    graph = capture()
+    # windowed arm as a CUDA graph (its kernels take microseconds)
+    graph = graph_of(w.win_arm, dev)
     for _ in range(max(args.warmup, 1)):
         graph.replay()
     torch.cuda.synchronize(dev)
@@ -393,41 +424,14 @@ def run_ours(args, dist_ctx):
     # host-side gap (its Python call is prepared while the index build runs)
     full_attn_mean_ms = statistics.median(x for row in attn_full_ms for x in row)
 
-    # windowed attention per launch, on the same graph with inner events
-    win_attn_ms = []
-    win_attn_source = "cuda-graph replays with timing events around each attention node"
-    inner = [[_external_event(), _external_event()] for _ in range(g)]
-    if inner[0][0] is not None:
-        try:
-            g_ev = capture(inner)
-            for k in range(K):
-                w.flush.zero_()
-                g_ev.replay()
-                torch.cuda.synchronize(dev)
-                win_attn_ms.extend(a.elapsed_time(b) for a, b in inner)
-        except Exception:
-            win_attn_ms = []
-    if not win_attn_ms:
-        win_attn_source = "graph of the windowed attention launches alone, mean per node"
-        cap_stream.wait_stream(stream)
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap_stream):
-            with torch.cuda.graph(g2, stream=cap_stream):
-                for j in range(g):
-                    wm.draft_decode_attn_append(w.kn[j], w.vn[j], w.slots[j], w.q[j], w.kp, w.vp,
-                                                w.tab_win[j], w.len_win[j], w.scale,
-                                                out=w.out_win[j], lse=w.lse_win[j], n_split=w.ns_win,
-                                                workspace=w.ws_win)
-        stream.wait_stream(cap_stream)
-        for k in range(K):
-            a, b = ev(), ev()
-            w.flush.zero_()
-            a.record()
-            g2.replay()
-            b.record()
-            torch.cuda.synchronize(dev)
-            win_attn_ms.append(a.elapsed_time(b) / g)
-    win_attn_mean_ms = statistics.mean(win_attn_ms)
+    # windowed attention per launch: a graph of the six attention launches
+    # alone (no index build), replayed with L2 flushed before each replay;
+    # per launch = replay time / 6, so the six launches never sum to more
+    # than the step they belong to
+    win_attn_source = "graph of the six windowed attention launches alone (L2 flushed), replay time / 6"
+    g_attn = graph_of(lambda: w.win_arm(attn_only=True), dev)
+    win_attn_ms = [x / g * 1e-3 for x in time_graph_samples(g_attn, w.flush, K, dev)]
+    win_attn_mean_ms = statistics.median(win_attn_ms)
 
     full_bytes = sum(w.bytes_full_attn(j) for j in range(g))
     win_bytes = sum(w.bytes_win_attn(j) for j in range(g))
@@ -524,33 +528,250 @@ def run_ours(args, dist_ctx):
         result["fp8"] = measure_fp8(w, args, dev)
     if not args.no_ring:
         result["ring"] = measure_ring(w, args, dev)
+    if args.workload == "1m" and not args.no_configs:
+        o = None
+        if dist_ctx.rank == 0 and dist_ctx.world == 1 and not args.no_cpu_baseline:
+            import oracle as o
+            o.build()
+        result["configs"] = measure_configs(args, dev, w, result, o)
     if dist_ctx.rank == 0 and dist_ctx.world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args)
     return result
 
 
+# ------------------------------------------------------------------ the other configs
+TINY = dict(name="tiny draft step", B=1, S=8192, H_q=8, H_kv=2, D=128, n_sink=64, W=1024, gamma=1,
+            outlier_frac=0.0, seed=1000)
+
+
+def measure_arms(w, args, dev, o=None):
+    """Both arms of a workload, each replayed from a CUDA graph with L2
+    flushed before every replay: the step (index build + gamma fused append +
+    attention launches) and the gamma attention launches alone (per launch =
+    replay / gamma).  With the oracle `o`, also its host time for one step of
+    each arm (tables, appends and attention of every query head)."""
+    g = w.cfg["gamma"]
+    reps = max(5, min(args.steps, 30))
+    peak, _ = hbm_peak()
+    host = _oracle_inputs(w) if o is not None else None
+    res = {}
+    for name, arm, nbytes_fn, ns, keys in (
+            ("full", w.full_arm, w.bytes_full_attn, w.ns_full, w.cfg["S"] + 1),
+            ("windowed", w.win_arm, w.bytes_win_attn, w.ns_win,
+             min(w.cfg["S"] + 1, w.cfg["n_sink"] + w.cfg["W"]))):
+        arm()
+        torch.cuda.synchronize(dev)
+        t_step = time_graph(graph_of(arm, dev), w.flush, reps, dev)
+        t_attn = time_graph(graph_of(lambda: arm(attn_only=True), dev), w.flush, reps, dev) / g
+        nbytes = sum(nbytes_fn(j) for j in range(g)) / g
+        gbs = nbytes / (t_attn * 1e-6) / 1e9
+        res[name] = {"us_per_step": round(t_step, 3), "attn_us_per_launch": round(t_attn, 3),
+                     "keys_per_launch": keys, "kv_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
+                     "bytes_per_launch": int(nbytes), "n_split": ns}
+        if o is not None:
+            t = time.perf_counter()
+            oracle_step(o, w, host, windowed=name == "windowed")
+            res[name]["oracle_host_us_per_step"] = round((time.perf_counter() - t) * 1e6, 1)
+    if o is not None:
+        res["oracle_cores"] = o.num_threads()
+    res["timing"] = "CUDA graph replays, L2 flushed before each, median"
+    return res
+
+
+class RingBatch:
+    """Batched ring layout: B=6 requests at lengths uniform in [900K, 1M],
+    H_q=16, H_kv=2, D=256, n_sink=64, W=4032, d=7; each request's draft KV
+    lives in a ring of n_sink + W + d = 4103 slots at a seeded ring base
+    inside a pool of 2 * B rings, filled from the kept prompt positions.  The
+    same logical rows also sit un-ringed in a flat pool (every position of
+    every request, ~12 GB, a seeded permutation as the page table)."""
+
+    def __init__(self, dev, seed=1003):
+        import speculative_decoding_draft_build_gb300 as wm
+        from speculative_decoding_draft_build_gb300 import synth
+        self.dev = dev
+        B, g, n_sink, W, d = 6, 6, 64, 4032, 7
+        H_q, H_kv, D = 16, 2, 256
+        self.cfg = dict(B=B, gamma=g, n_sink=n_sink, W=W, d=d, H_q=H_q, H_kv=H_kv, D=D)
+        self.R = R = n_sink + W + d
+        self.S_list = synth.uniform_lengths(B, 900_000, 1_048_576, seed)
+        ctx = [s + g for s in self.S_list]
+        total = sum(ctx)
+        self.flat_k = synth.normal_bf16((total, H_kv, D), seed + 1, dev)
+        self.flat_v = synth.normal_bf16((total, H_kv, D), seed + 2, dev)
+        perm = synth.permutation(total, seed + 3, dev)
+        self.rtt = torch.zeros((B, max(ctx)), dtype=torch.int32, device=dev)
+        off = 0
+        for b in range(B):
+            self.rtt[b, :ctx[b]] = perm[off:off + ctx[b]]
+            off += ctx[b]
+        self.ring_base = torch.tensor(synth.ring_bases(B, R, 2 * B, seed + 4), dtype=torch.int32, device=dev)
+        self.ring_k = torch.zeros((2 * B * R, H_kv, D), dtype=torch.bfloat16, device=dev)
+        self.ring_v = torch.zeros_like(self.ring_k)
+        self.seq = torch.tensor(self.S_list, dtype=torch.int32, device=dev)
+        pos, cnt = wm.prefill_keep_positions(self.seq, n_sink, W)
+        live = torch.arange(pos.shape[1], device=dev).view(1, -1) < cnt.view(-1, 1).long()
+        rows = torch.gather(self.rtt, 1, torch.where(live, pos, torch.zeros_like(pos)).long()).long()
+        wm.ring_fill(self.flat_k[rows].contiguous(), self.flat_v[rows].contiguous(), self.seq, self.ring_base,
+                     n_sink, W, d, self.ring_k, self.ring_v)
+        self.kn = synth.normal_bf16((g, B, H_kv, D), seed + 5, dev)
+        self.vn = synth.normal_bf16((g, B, H_kv, D), seed + 6, dev)
+        self.q = synth.normal_bf16((g, B, 1, H_q, D), seed + 7, dev)
+        req = torch.arange(B, dtype=torch.int32, device=dev)
+        self.slots_ring = torch.stack([wm.ring_map(self.ring_base, (self.seq + j).to(torch.int32), req,
+                                                   n_sink, W, d) for j in range(g)]).contiguous()
+        self.slots_flat = torch.stack([self.rtt[req.long(), (self.seq + j).long()] for j in range(g)]).contiguous()
+        self.stride = n_sink + W
+        self.tab_ring = torch.empty((g, B, self.stride), dtype=torch.int32, device=dev)
+        self.tab_flat = torch.empty_like(self.tab_ring)
+        self.len_ring = torch.empty((g, B), dtype=torch.int32, device=dev)
+        self.len_flat = torch.empty_like(self.len_ring)
+        self.ns = wm.attn_num_splits(B, 1, H_kv, self.stride, dev)
+        self.ws = wm.AttnWorkspace(wm.attn_workspace_bytes(B, 1, H_q, H_kv, D, self.ns), dev)
+        self.out_ring = torch.empty((g, B, 1, H_q, D), dtype=torch.float32, device=dev)
+        self.lse_ring = torch.empty((g, B, 1, H_q), dtype=torch.float32, device=dev)
+        self.out_flat = torch.empty_like(self.out_ring)
+        self.lse_flat = torch.empty_like(self.lse_ring)
+        self.flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        self.scale = 1.0 / math.sqrt(D)
+        torch.cuda.synchronize(dev)
+
+    def arm(self, ring=True, attn_only=False):
+        import speculative_decoding_draft_build_gb300 as wm
+        c = self.cfg
+        kp, vp = (self.ring_k, self.ring_v) if ring else (self.flat_k, self.flat_v)
+        tab, ln = (self.tab_ring, self.len_ring) if ring else (self.tab_flat, self.len_flat)
+        slots = self.slots_ring if ring else self.slots_flat
+        out, lse = (self.out_ring, self.lse_ring) if ring else (self.out_flat, self.lse_flat)
+        if not attn_only:
+            src = dict(ring_base=self.ring_base) if ring else dict(req_to_token=self.rtt)
+            wm.build_draft_indices(self.seq, c["gamma"], c["n_sink"], c["W"], c["d"], windowed=True,
+                                   table=tab, lens=ln, **src)
+        for j in range(c["gamma"]):
+            wm.draft_decode_attn_append(self.kn[j], self.vn[j], slots[j], self.q[j], kp, vp, tab[j], ln[j],
+                                        self.scale, out=out[j], lse=lse[j], n_split=self.ns, workspace=self.ws)
+
+    def bytes_per_launch(self, j):
+        c = self.cfg
+        return sum(attn_bytes(min(S + j + 1, c["n_sink"] + c["W"]), 1, c["H_q"], c["H_kv"], c["D"], n_new=1)
+                   for S in self.S_list)
+
+
+def measure_ring_batch(args, dev, o=None):
+    """The batched ring workload: gamma = 6 steps of fused append + windowed
+    attention (index build in ring layout first), replayed from a CUDA graph
+    with L2 flushed before each replay; the attention launches alone as a
+    second graph; ring outputs compared bit for bit with the same steps on the
+    un-ringed flat pool; the oracle's host time for one ring step."""
+    rb = RingBatch(dev)
+    g = rb.cfg["gamma"]
+    reps = max(5, min(args.steps, 30))
+    rb.arm(ring=True)
+    rb.arm(ring=False)
+    torch.cuda.synchronize(dev)
+    same = bool(torch.equal(rb.out_ring, rb.out_flat) and torch.equal(rb.lse_ring, rb.lse_flat))
+    t_step = time_graph(graph_of(lambda: rb.arm(ring=True), dev), rb.flush, reps, dev)
+    t_attn = time_graph(graph_of(lambda: rb.arm(ring=True, attn_only=True), dev), rb.flush, reps, dev) / g
+    nbytes = sum(rb.bytes_per_launch(j) for j in range(g)) / g
+    peak, _ = hbm_peak()
+    gbs = nbytes / (t_attn * 1e-6) / 1e9
+    res = {"workload": "B=6 requests, lengths uniform in [900K, 1M], H_q=16, H_kv=2, D=256, n_sink=64, "
+                       "W=4032, d=7, ring of 4103 slots per request at seeded ring bases, gamma=6",
+           "S": rb.S_list, "us_per_step": round(t_step, 3), "attn_us_per_launch": round(t_attn, 3),
+           "kv_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4), "bytes_per_launch": int(nbytes),
+           "n_split": rb.ns, "ring_equals_unringed_bitwise": same,
+           "timing": "CUDA graph replays, L2 flushed before each, median"}
+    if o is not None:
+        import numpy as np
+
+        def bits(t):
+            return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        c = rb.cfg
+        kp, vp = bits(rb.ring_k), bits(rb.ring_v)
+        kn, vn, q = bits(rb.kn), bits(rb.vn), bits(rb.q)
+        seq, base, slots = rb.seq.cpu().numpy(), rb.ring_base.cpu().numpy(), rb.slots_ring.cpu().numpy()
+        t = time.perf_counter()
+        table, lens = o.build_draft_indices(seq, g, c["n_sink"], c["W"], c["d"], windowed=True, ring_base=base,
+                                            stride=rb.stride)
+        for j in range(g):
+            o.append_kv(kn[j], vn[j], slots[j], kp, vp)
+            o.draft_decode_attn(q[j], kp, vp, table[j], lens[j], rb.scale)
+        res["oracle_host_us_per_step"] = round((time.perf_counter() - t) * 1e6, 1)
+        res["oracle_cores"] = o.num_threads()
+    del rb
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_configs(args, dev, w3, result, o=None):
+    """Every workload of the hot path's configuration table next to the
+    million-token headline: the tiny step (S=8192, and S=1000 inside the
+    window, where the windowed and full outputs must be bit-identical at the
+    same split count), the 131K step (full vs windowed), the batched ring, and
+    pointers to the million-token arms and the tree row measured above."""
+    res = {}
+    for key, cfg in (("1_tiny_S8192", TINY), ("1_tiny_S1000", dict(TINY, S=1000)),
+                     ("2_131k", WORKLOADS["131k"])):
+        w = Workload(cfg, dev)
+        res[key] = measure_arms(w, args, dev, o)
+        res[key]["workload"] = (f"{cfg['name']}: B={cfg['B']}, S={cfg['S']}, H_q={cfg['H_q']}, "
+                                f"H_kv={cfg['H_kv']}, D={cfg['D']}, n_sink={cfg['n_sink']}, W={cfg['W']}, "
+                                f"gamma={cfg['gamma']}, permuted page table")
+        if cfg["S"] + 1 <= cfg["n_sink"] + cfg["W"]:
+            w.full_arm()
+            w.win_arm(n_split=w.ns_full)
+            torch.cuda.synchronize(dev)
+            res[key]["windowed_equals_full_bitwise"] = bool(
+                torch.equal(w.out_win, w.out_full) and torch.equal(w.lse_win, w.lse_full))
+        del w
+        torch.cuda.empty_cache()
+    res["3_1m"] = {"see": "arms, roofline, roofline_windowed (the headline workload)",
+                   "windowed_us_per_step": result["arms"]["windowed"]["us_per_step"],
+                   "full_us_per_step": result["arms"]["full"]["us_per_step"]}
+    res["4_ring_batch"] = measure_ring_batch(args, dev, o)
+    if "tree" in result:
+        res["5_tree"] = {"see": "tree (per window W)"}
+    return res
+
+
 def measure_mass(w, dev):
     """Attention-mass diagnostics (in-window mass, win_perturb, tail out-frac;
-    App. C, Table 12) of the step's six draft queries, from the full-context
-    and windowed attention outputs the two arms just computed: one launch over
-    all query rows, event-timed (median of 20)."""
+    App. C, Table 12) of the step's six draft queries: the far-key tables of
+    the six steps, the attention over the far keys (the full-context split
+    count), then one diagnostics launch over all query rows from the windowed
+    arm's outputs and the far outputs, event-timed (median of 20).  The
+    merged output of the two parts is compared with the full arm's output."""
     import speculative_decoding_draft_build_gb300 as wm
-    args = (w.out_full, w.lse_full, w.out_win, w.lse_win)
+    c = w.cfg
+    g = c["gamma"]
+    tab_far, len_far = wm.build_far_indices(w.seq, g, c["n_sink"], c["W"], w.rtt, stride=w.full_stride)
+    o_far = torch.empty_like(w.out_win)
+    lse_far = torch.empty_like(w.lse_win)
+    for j in range(g):
+        wm.draft_decode_attn(w.q[j], w.kp, w.vp, tab_far[j], len_far[j], w.scale, out=o_far[j],
+                             lse=lse_far[j], n_split=w.ns_full, workspace=w.ws_full)
+    o_full = torch.empty_like(w.out_win)
+    lse_full = torch.empty_like(w.lse_win)
+    args = (w.out_win, w.lse_win, o_far, lse_far)
     for _ in range(3):
-        res = wm.attn_mass_diagnostics(*args)
+        res = wm.attn_mass_diagnostics(*args, o_full=o_full, lse_full=lse_full)
     ts = []
     for _ in range(20):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         hold_gpu()
         a.record()
-        res = wm.attn_mass_diagnostics(*args)
+        res = wm.attn_mass_diagnostics(*args, o_full=o_full, lse_full=lse_full)
         b.record()
         torch.cuda.synchronize(dev)
         ts.append(a.elapsed_time(b) * 1e3)
     in_win, perturb, tail = (r.double().mean().item() for r in res)
-    return {"us_per_launch": round(statistics.median(ts), 2), "rows": int(w.lse_full.numel()),
+    merged_err = (o_full - w.out_full).abs().max().item()
+    return {"us_per_launch": round(statistics.median(ts), 2), "rows": int(w.lse_win.numel()),
             "mean_in_win": round(in_win, 6), "mean_win_perturb": round(perturb, 6),
             "mean_tail_out_frac": round(tail, 6),
+            "merged_vs_full_arm_max_abs": float(f"{merged_err:.3e}"),
+            "how": "windowed attention + attention over the far-key table (wmtp_build_far_indices), "
+                   "combined per row (wmtp_attn_mass_diagnostics)",
             "note": "synthetic N(0,1) keys and values; the pages measure these on model activations"}
 
 
@@ -831,59 +1052,64 @@ def measure_tree(args, dev):
 
 
 def measure_e2e(w, args, dev):
-    """Windowed arm through the Python binding with host buffers: every step
+    """Both arms through the Python binding with host buffers: every step
     copies its inputs (q, new K/V, seq_lens; one packed buffer) from pinned
-    host memory, runs the arm, and reads the outputs (out, lse; one packed
+    host memory, runs the arm, and reads its outputs (out, lse; one packed
     buffer) back; timed on the host around a stream synchronisation.
-    `value`: the whole step (copy in, index build, six fused launches, copy
-    out) captured once in a CUDA graph and replayed per step, as a serving
-    loop runs it; `eager_us`: the same step with direct calls from Python."""
+    `value` (windowed arm) and `full.value`: the whole step (copy in, index
+    build, six fused launches, copy out) captured once in a CUDA graph and
+    replayed per step, as a serving loop runs it; `eager_us`: the windowed
+    step with direct calls from Python."""
     in_h = w.io_in.cpu().pin_memory()
-    out_h = torch.empty(w.io_out.shape, dtype=torch.uint8).pin_memory()
     stream = torch.cuda.current_stream(dev)
     h2d = in_h.numel()
-    d2h = out_h.numel()
 
-    def step():
+    def host_timed(fn, reps):
+        for _ in range(max(args.warmup, 1)):
+            fn()
+        times = []
+        for _ in range(reps):
+            t = time.perf_counter()
+            fn()
+            times.append(time.perf_counter() - t)
+        return statistics.median(times)
+
+    def graph_step(arm, io_out, out_h):
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(gr, stream=cap):
+                w.io_in.copy_(in_h, non_blocking=True)
+                arm()
+                out_h.copy_(io_out, non_blocking=True)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize(dev)
+
+        def run():
+            gr.replay()
+            stream.synchronize()
+        return run
+
+    out_h = torch.empty(w.io_out.shape, dtype=torch.uint8).pin_memory()
+
+    def eager():
         w.io_in.copy_(in_h, non_blocking=True)
         w.win_arm()
         out_h.copy_(w.io_out, non_blocking=True)
         stream.synchronize()
-
-    for _ in range(max(args.warmup, 1)):
-        step()
-    times = []
-    for _ in range(args.steps):
-        t = time.perf_counter()
-        step()
-        times.append(time.perf_counter() - t)
-    eager = statistics.median(times)
-
-    # the same step as one graph: host->device copies, arm, device->host copies
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    gr = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(gr, stream=cap):
-            w.io_in.copy_(in_h, non_blocking=True)
-            w.win_arm()
-            out_h.copy_(w.io_out, non_blocking=True)
-    stream.wait_stream(cap)
-    torch.cuda.synchronize(dev)
-    for _ in range(max(args.warmup, 1)):
-        gr.replay()
-        stream.synchronize()
-    times = []
-    for _ in range(args.steps):
-        t = time.perf_counter()
-        gr.replay()
-        stream.synchronize()
-        times.append(time.perf_counter() - t)
-    return {"value": round(statistics.median(times) * 1e6, 3), "unit": UNIT,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "eager_us": round(eager * 1e6, 3),
-            "how": "windowed arm with pinned host I/O, host-timed: value = one CUDA graph per step "
-                   "(packed copy in, index build, 6 fused launches, packed copy out); eager_us = direct calls"}
+    eager_s = host_timed(eager, args.steps)
+    win_s = host_timed(graph_step(w.win_arm, w.io_out, out_h), args.steps)
+    out_full_h = torch.empty(w.io_out_full.shape, dtype=torch.uint8).pin_memory()
+    full_s = host_timed(graph_step(w.full_arm, w.io_out_full, out_full_h), max(3, min(args.steps, 10)))
+    return {"value": round(win_s * 1e6, 3), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out_h.numel()),
+            "eager_us": round(eager_s * 1e6, 3),
+            "full": {"value": round(full_s * 1e6, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                     "d2h_bytes_per_step": int(out_full_h.numel())},
+            "how": "each arm with pinned host I/O, host-timed: one CUDA graph per step (packed copy in, "
+                   "index build, 6 fused launches, packed copy out); value = windowed arm, full.value = "
+                   "full-context arm; eager_us = windowed arm by direct calls"}
 
 
 # ------------------------------------------------------------------ oracle legs
@@ -896,13 +1122,14 @@ def _oracle_inputs(w):
                 rtt=w.rtt.cpu().numpy(), slots=w.slots.cpu().numpy(), seq=w.seq.cpu().numpy())
 
 
-def oracle_windowed_step(o, w, host, nthreads=None):
-    """One windowed decode step in the oracle: tables, then per draft step the
-    append and the attention of every query head."""
+def oracle_step(o, w, host, windowed=True, nthreads=None):
+    """One decode step of either arm in the oracle: tables, then per draft step
+    the append and the attention of every query head."""
     c = w.cfg
     g = c["gamma"]
-    table, lens = o.build_draft_indices(host["seq"], g, c["n_sink"], c["W"], g + 1, windowed=True,
-                                        req_to_token=host["rtt"], stride=c["n_sink"] + c["W"])
+    stride = c["n_sink"] + c["W"] if windowed else c["S"] + g
+    table, lens = o.build_draft_indices(host["seq"], g, c["n_sink"], c["W"], g + 1, windowed=windowed,
+                                        req_to_token=host["rtt"], stride=stride)
     for j in range(g):
         o.append_kv(host["kn"][j], host["vn"][j], host["slots"][j], host["kp"], host["vp"])
         o.draft_decode_attn(host["q"][j], host["kp"], host["vp"], table[j], lens[j], w.scale,
@@ -914,17 +1141,17 @@ def cpu_baseline(w, args):
     o.build()
     host = _oracle_inputs(w)
     t = time.perf_counter()
-    oracle_windowed_step(o, w, host)
+    oracle_step(o, w, host)
     first = time.perf_counter() - t
     reps = max(1, min(5, int(5.0 / max(first, 1e-3))))
     ts = [first]
     for _ in range(reps):
         t = time.perf_counter()
-        oracle_windowed_step(o, w, host)
+        oracle_step(o, w, host)
         ts.append(time.perf_counter() - t)
     win_us = statistics.median(ts) * 1e6
     t = time.perf_counter()
-    oracle_windowed_step(o, w, host, nthreads=1)
+    oracle_step(o, w, host, nthreads=1)
     win_1t_us = (time.perf_counter() - t) * 1e6
     # full arm: one draft forward over the whole table, all query heads
     c = w.cfg
@@ -971,12 +1198,12 @@ def run_reference(args, dist_ctx):
     w.slots = torch.stack([w.rtt[:, S + j] for j in range(g)]).contiguous()
     host = _oracle_inputs(w)
     for _ in range(args.warmup):
-        oracle_windowed_step(o, w, host)
+        oracle_step(o, w, host)
     ts = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
         t = time.perf_counter()
-        oracle_windowed_step(o, w, host)
+        oracle_step(o, w, host)
         ts.append(time.perf_counter() - t)
     wall = time.perf_counter() - t0
     val = statistics.median(ts) * 1e6
@@ -1009,6 +1236,8 @@ def main(argv=None):
     p.add_argument("--no-extend", action="store_true", help="skip the draft-extend measurement")
     p.add_argument("--no-fp8", action="store_true", help="skip the fp8-KV measurement")
     p.add_argument("--no-ring", action="store_true", help="skip the table-free ring measurement")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the tiny, 131K and batched-ring configurations")
     p.add_argument("--tree-only", action="store_true",
                    help="run only the tree-drafter measurement (a profiling driver; prints the tree object)")
     p.add_argument("--tree-w", type=int, action="append",

@@ -99,6 +99,22 @@ wmtp_status wmtp_build_draft_indices(const int32_t *seq_lens, int32_t B,
                                      int64_t stride, int32_t *lens,
                                      void *stream);
 
+/* Far-key table of the same draft steps: for draft step j of request b
+ * (kv_len = seq_lens[b] + j + 1), the positions the keep rule drops --
+ * [n_sink, kv_len - W) when kv_len > n_sink + W, none otherwise -- in
+ * ascending order, mapped to slots through req_to_token as above (paged
+ * layout only: a ring no longer holds those positions).  The far table and
+ * the windowed table of a step partition its full-context table; attention
+ * over each feeds wmtp_attn_mass_diagnostics ("Windowed-MTP", §5 "A
+ * partition-function view").  Arguments, capacity check and errors as
+ * wmtp_build_draft_indices; req_to_token must not be NULL. */
+wmtp_status wmtp_build_far_indices(const int32_t *seq_lens, int32_t B,
+                                   int32_t gamma, int32_t n_sink,
+                                   int32_t window, const int32_t *req_to_token,
+                                   const int32_t *req_pool_idx,
+                                   int64_t rtt_stride, int32_t *table,
+                                   int64_t stride, int32_t *lens, void *stream);
+
 /* Index table of a draft-extend pass (the draft forward over the n new
  * tokens a request accepted, at positions S..S+n-1, in one launch; see
  * wmtp_draft_extend_attn).  Row b is the union of the key sets of its n
@@ -305,28 +321,36 @@ int32_t wmtp_extend_num_splits(int32_t B, int32_t n_q, int32_t H_kv,
                                int64_t max_len);
 
 /* Attention-mass diagnostics of the windowed draft ("Windowed-MTP", §5 "A
- * partition-function view"; App. C, Table 12), per query row, from the
- * full-context and the windowed attention of the same query (o and lse of
- * wmtp_draft_decode_attn over the full and the sink + window table):
- *   in_win[r]        = Z_w / Z = exp(lse_win - lse_full): softmax mass inside
- *                      the kept set (1 - Z_far / Z);
- *   win_perturb[r]   = ||o_full - o_win|| / ||o_full||;
- *   tail_out_frac[r] = ||o_full - in_win * o_win|| / ||o_full||, the share
- *                      of ||o|| from far keys (o_full = in_win * o_win +
- *                      sum over far keys of p_k v_k).
- * An empty kept set gives in_win = 0; ||o_full|| = 0 gives 0 ratios.
+ * partition-function view"; App. C, Table 12), per query row.  The full key
+ * set of a draft step is the disjoint union of the kept set (sinks + window)
+ * and the far keys the keep rule drops, so Z = Z_w + Z_far.  Inputs are the
+ * attention of the same query over each part: (o_win, lse_win) over the
+ * sink + window table and (o_far, lse_far) over the far table of
+ * wmtp_build_far_indices, both as wmtp_draft_decode_attn writes them
+ * (normalised outputs, natural-log lse; an empty part has lse = -inf).
+ * With a = Z_w / Z = 1 / (1 + exp(lse_far - lse_win)) and b = Z_far / Z
+ * (from the same exponential, not 1 - a):
+ *   in_win[r]        = a: softmax mass inside the kept set;
+ *   o_full           = a o_win + b o_far (the full-context read-out);
+ *   win_perturb[r]   = ||o_full - o_win|| / ||o_full|| = b ||o_far - o_win|| / ||o_full||;
+ *   tail_out_frac[r] = ||sum over far keys of p_k v_k|| / ||o_full|| = b ||o_far|| / ||o_full||.
+ * No quantity is formed by subtracting two nearly equal outputs, so a small
+ * far share keeps its relative accuracy.  No far key gives in_win = 1 and
+ * zero ratios; no key at all gives zeros; ||o_full|| = 0 gives 0 ratios.
+ * Optionally the merged full-context attention is written: o_full[r][:] and
+ * lse_full[r] = log(e^lse_win + e^lse_far).
  *
- * o_full, o_win  device fp32 [rows][D]; lse_full, lse_win device fp32 [rows]
- *                (natural log, as wmtp_draft_decode_attn writes them).
- * in_win, win_perturb, tail_out_frac  device fp32 [rows]; any may be NULL,
- *                not all three.
- * Errors: WMTP_EINVAL for rows < 0, D < 1 or null inputs. */
-wmtp_status wmtp_attn_mass_diagnostics(const float *o_full,
-                                       const float *lse_full,
-                                       const float *o_win, const float *lse_win,
+ * o_win, o_far    device fp32 [rows][D]; lse_win, lse_far device fp32 [rows].
+ * in_win, win_perturb, tail_out_frac  device fp32 [rows]; o_full device fp32
+ *                 [rows][D]; lse_full device fp32 [rows]; any output may be
+ *                 NULL, not all five.
+ * Errors: WMTP_EINVAL for rows < 0, D < 1, null inputs or no output. */
+wmtp_status wmtp_attn_mass_diagnostics(const float *o_win, const float *lse_win,
+                                       const float *o_far, const float *lse_far,
                                        int64_t rows, int32_t D, float *in_win,
-                                       float *win_perturb,
-                                       float *tail_out_frac, void *stream);
+                                       float *win_perturb, float *tail_out_frac,
+                                       float *o_full, float *lse_full,
+                                       void *stream);
 
 /* ------------------------------------------------------------------------
  * Tree-draft attention over the ring.

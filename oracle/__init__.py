@@ -17,12 +17,14 @@ from .oracle import (  # noqa: F401
     build,
     build_draft_indices,
     build_extend_indices,
+    build_far_indices,
     draft_decode_attn,
     draft_decode_attn_fp8,
     draft_extend_attn,
     e4m3_table,
     e4m3_to_f64,
     f32_to_e4m3,
+    far_positions,
     keep,
     num_threads,
     prefill_keep_positions,

@@ -134,6 +134,38 @@ def keep(s_kv: int, n_sink: int, window: int, windowed: bool = True) -> np.ndarr
     return out
 
 
+def far_positions(s_kv: int, n_sink: int, window: int) -> np.ndarray:
+    """Positions a windowed draft step with kv length ``s_kv`` does NOT
+    attend: every position of [0, s_kv) outside :func:`keep` (§5 "A
+    partition-function view": the full key set is the kept set plus these
+    far keys), ascending.  Written as the set difference itself."""
+    kept = set(int(x) for x in keep(s_kv, n_sink, window, True))
+    return np.array([p for p in range(max(s_kv, 0)) if p not in kept], dtype=np.int64)
+
+
+def build_far_indices(seq_lens, gamma, n_sink, window, req_to_token, req_pool_idx=None,
+                      stride=None):
+    """Far-key tables: for draft step j of request b (kv length S_b + j + 1,
+    as the draft tables), the slots req_to_token[row b] of
+    :func:`far_positions`.  Returns ``(table[gamma, B, stride] int32,
+    lens[gamma, B] int32)``; entries past ``lens`` are -1."""
+    sl = _as(seq_lens, np.int64)
+    rtt = _as(req_to_token, np.int32)
+    B = sl.shape[0]
+    stride = rtt.shape[1] if stride is None else int(stride)
+    table = np.full((gamma, B, stride), -1, np.int32)
+    lens = np.zeros((gamma, B), np.int32)
+    for j in range(gamma):
+        for b in range(B):
+            row = int(req_pool_idx[b]) if req_pool_idx is not None else b
+            pos = far_positions(int(sl[b]) + j + 1, n_sink, window)
+            if len(pos) > stride:
+                raise ValueError("build_far_indices: a row needs more than stride entries")
+            lens[j, b] = len(pos)
+            table[j, b, :len(pos)] = rtt[row, pos]
+    return table, lens
+
+
 def ring_slot(ring_base: int, p: int, branch: int, n_sink: int, window: int,
               depth: int, tree_k: int = 1) -> int:
     """Ring slot of logical position ``p`` (App. A; §7 tree sizing)."""

@@ -15,7 +15,9 @@ Calls (same names as the C ABI without the ``wmtp_`` prefix):
   draft_decode_attn_append  append_kv + draft_decode_attn in one launch
   build_extend_indices / draft_extend_attn  the draft forward over a request's
                        accepted tokens in one launch (each token its own keys)
-  attn_mass_diagnostics  in-window mass, win_perturb, tail out-frac per query
+  build_far_indices    the far-key tables (positions the keep rule drops)
+  attn_mass_diagnostics  in-window mass, win_perturb, tail out-frac per query,
+                       from the windowed and the far-key attention
   append_kv_fp8 / draft_decode_attn_fp8  the same over E4M3 KV pools with
                        per-KV-head scales
   prefill_keep_positions / ring_fill  pruned draft prefill: the kept prompt
@@ -37,7 +39,7 @@ from . import _build
 
 __all__ = [
     "WmtpError", "load", "build", "version", "device_error",
-    "build_draft_indices", "build_extend_indices", "ring_map", "append_kv", "draft_decode_attn",
+    "build_draft_indices", "build_extend_indices", "build_far_indices", "ring_map", "append_kv", "draft_decode_attn",
     "draft_decode_attn_append", "draft_extend_attn", "attn_mass_diagnostics",
     "attn_workspace_bytes", "attn_num_splits", "extend_num_splits", "AttnWorkspace", "draft_decode_attn_noalloc",
     "tree_draft_attn", "tree_workspace_bytes", "tree_num_splits",
@@ -103,7 +105,11 @@ def load():
             _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32,
             _i32, ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
         lib.wmtp_attn_mass_diagnostics.restype = _i32
-        lib.wmtp_attn_mass_diagnostics.argtypes = [_vp, _vp, _vp, _vp, _i64, _i32, _vp, _vp, _vp, _vp]
+        lib.wmtp_attn_mass_diagnostics.argtypes = [_vp, _vp, _vp, _vp, _i64, _i32, _vp, _vp, _vp, _vp,
+                                                   _vp, _vp]
+        lib.wmtp_build_far_indices.restype = _i32
+        lib.wmtp_build_far_indices.argtypes = [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64,
+                                               _vp, _vp]
         lib.wmtp_ring_map.restype = _i32
         lib.wmtp_ring_map.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]
         lib.wmtp_append_kv.restype = _i32
@@ -250,6 +256,37 @@ def build_draft_indices(seq_lens: torch.Tensor, gamma: int, n_sink: int, window:
             _ptr(seq_lens), B, gamma, n_sink, window, depth, tree_k, int(bool(windowed)),
             _ptr(req_to_token), _ptr(req_pool_idx), rtt_stride, _ptr(ring_base), _ptr(table),
             stride, _ptr(lens), _stream(stream)), "build_draft_indices")
+    return table, lens
+
+
+def build_far_indices(seq_lens: torch.Tensor, gamma: int, n_sink: int, window: int,
+                      req_to_token: torch.Tensor, req_pool_idx: torch.Tensor | None = None,
+                      stride: int | None = None, table: torch.Tensor | None = None,
+                      lens: torch.Tensor | None = None, stream=None):
+    """Far-key tables (``wmtp_build_far_indices``): per draft step j, the
+    positions [n_sink, kv_len - W) the keep rule drops (none while kv_len <=
+    n_sink + W), through ``req_to_token``.  Returns ``(table[gamma, B,
+    stride], lens[gamma, B])``; ``stride`` defaults to ``req_to_token.shape[1]``."""
+    _need(seq_lens, "seq_lens", torch.int32)
+    dev = seq_lens.device
+    B = seq_lens.shape[0]
+    _need(req_to_token, "req_to_token", torch.int32, dev)
+    if req_pool_idx is not None:
+        _need(req_pool_idx, "req_pool_idx", torch.int32, dev)
+    if stride is None:
+        stride = table.shape[-1] if table is not None else req_to_token.shape[1]
+    if table is None:
+        table = torch.empty((gamma, B, stride), dtype=torch.int32, device=dev)
+    if lens is None:
+        lens = torch.empty((gamma, B), dtype=torch.int32, device=dev)
+    _need(table, "table", torch.int32, dev)
+    _need(lens, "lens", torch.int32, dev)
+    if table.numel() < gamma * B * stride or lens.numel() < gamma * B:
+        raise ValueError("build_far_indices: table/lens smaller than gamma * B rows")
+    with _on(dev):
+        _check(load().wmtp_build_far_indices(
+            _ptr(seq_lens), B, gamma, n_sink, window, _ptr(req_to_token), _ptr(req_pool_idx),
+            req_to_token.shape[1], _ptr(table), stride, _ptr(lens), _stream(stream)), "build_far_indices")
     return table, lens
 
 
@@ -578,23 +615,35 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
     return out, lse
 
 
-def attn_mass_diagnostics(o_full: torch.Tensor, lse_full: torch.Tensor, o_win: torch.Tensor,
-                          lse_win: torch.Tensor, stream=None):
-    """Per query row: (in_win, win_perturb, tail_out_frac) from the full and
-    windowed attention of the same queries (``wmtp_attn_mass_diagnostics``).
-    o_*: [..., D] fp32; lse_*: [...] fp32.  Returns three fp32 tensors shaped
-    like lse_full."""
-    for t, nm in ((o_full, "o_full"), (lse_full, "lse_full"), (o_win, "o_win"), (lse_win, "lse_win")):
-        _need(t, nm, torch.float32, o_full.device)
-    D = o_full.shape[-1]
-    rows = lse_full.numel()
-    if o_full.numel() != rows * D or o_win.numel() != rows * D or lse_win.numel() != rows:
+def attn_mass_diagnostics(o_win: torch.Tensor, lse_win: torch.Tensor, o_far: torch.Tensor,
+                          lse_far: torch.Tensor, o_full: torch.Tensor | None = None,
+                          lse_full: torch.Tensor | None = None, stream=None):
+    """Per query row: (in_win, win_perturb, tail_out_frac) from the windowed
+    attention and the attention over the far keys of the same queries
+    (``wmtp_attn_mass_diagnostics``).  o_*: [..., D] fp32; lse_*: [...] fp32.
+    Returns three fp32 tensors shaped like lse_win; when ``o_full`` /
+    ``lse_full`` are given, the merged full-context attention is written
+    there too."""
+    for t, nm in ((o_win, "o_win"), (lse_win, "lse_win"), (o_far, "o_far"), (lse_far, "lse_far")):
+        _need(t, nm, torch.float32, o_win.device)
+    D = o_win.shape[-1]
+    rows = lse_win.numel()
+    if o_win.numel() != rows * D or o_far.numel() != rows * D or lse_far.numel() != rows:
         raise ValueError("attn_mass_diagnostics: shape mismatch")
-    res = [torch.empty_like(lse_full) for _ in range(3)]
-    with _on(o_full.device):
+    if o_full is not None:
+        _need(o_full, "o_full", torch.float32, o_win.device)
+        if o_full.numel() != rows * D:
+            raise ValueError("attn_mass_diagnostics: o_full shape mismatch")
+    if lse_full is not None:
+        _need(lse_full, "lse_full", torch.float32, o_win.device)
+        if lse_full.numel() != rows:
+            raise ValueError("attn_mass_diagnostics: lse_full shape mismatch")
+    res = [torch.empty_like(lse_win) for _ in range(3)]
+    with _on(o_win.device):
         _check(load().wmtp_attn_mass_diagnostics(
-            _ptr(o_full), _ptr(lse_full), _ptr(o_win), _ptr(lse_win), rows, D, _ptr(res[0]),
-            _ptr(res[1]), _ptr(res[2]), _stream(stream)), "attn_mass_diagnostics")
+            _ptr(o_win), _ptr(lse_win), _ptr(o_far), _ptr(lse_far), rows, D, _ptr(res[0]),
+            _ptr(res[1]), _ptr(res[2]), _ptr(o_full), _ptr(lse_full), _stream(stream)),
+            "attn_mass_diagnostics")
     return tuple(res)
 
 

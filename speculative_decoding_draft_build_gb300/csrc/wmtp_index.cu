@@ -31,7 +31,9 @@ constexpr int64_t kIndexLongRow = 65536;
 // One grid row (blockIdx.y) per (draft step j, request b); the x dimension
 // strides over the row's entries, kIndexPerThread per thread.  Entry e of a
 // windowed row is position e for the sinks and e + (kv_len - W - n_sink) for
-// the window.
+// the window.  `windowed` == 2 builds the far list instead: the positions
+// the keep rule drops, [n_sink, kv_len - W) when kv_len > n_sink + W (else
+// none), entry e being position n_sink + e (paged layout only).
 template <int kIndexPerThread>
 __global__ void __launch_bounds__(256) build_indices_kernel(
     const int32_t *__restrict__ seq_lens, int32_t B, int32_t n_sink, int32_t window,
@@ -57,14 +59,19 @@ __global__ void __launch_bounds__(256) build_indices_kernel(
         kv_len = nn == 0 ? 0 : (int64_t)seq_lens[b] + nn;
         keep_w = (int64_t)window + (nn > 0 ? nn - 1 : 0);
     }
+    const bool far = windowed == 2;
     const bool win = windowed && kv_len > (int64_t)n_sink + keep_w;
-    const int64_t n = kv_len <= 0 ? 0 : (win ? (int64_t)n_sink + keep_w : kv_len);
+    const int64_t n = kv_len <= 0 ? 0
+                      : far       ? (win ? kv_len - keep_w - n_sink : 0)
+                                  : (win ? (int64_t)n_sink + keep_w : kv_len);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         lens[row] = (int32_t)n;
         if (n > stride) latch(WMTP_DEV_TABLE_OVERFLOW);
     }
     const int64_t n_write = n < stride ? n : stride;
-    const int64_t shift = win ? kv_len - keep_w - n_sink : 0;
+    // position of entry e: e + shift past the sinks (all of a far row)
+    const int64_t shift = far ? n_sink : (win ? kv_len - keep_w - n_sink : 0);
+    const int64_t first_shifted = far ? 0 : n_sink;
     int32_t *__restrict__ out = table + (int64_t)row * stride;
     // Each thread takes kIndexPerThread entries a block apart: coalesced
     // accesses, and that many independent loads in flight per thread.
@@ -78,13 +85,13 @@ __global__ void __launch_bounds__(256) build_indices_kernel(
 #pragma unroll
             for (int u = 0; u < kIndexPerThread; ++u) {
                 const int64_t e = e0 + (int64_t)u * blockDim.x;
-                const int64_t p = (win && e >= n_sink) ? e + shift : e;
+                const int64_t p = (win && e >= first_shifted) ? e + shift : e;
                 v[u] = (e < n_write && p < rtt_stride) ? __ldg(src + p) : 0;
             }
 #pragma unroll
             for (int u = 0; u < kIndexPerThread; ++u) {
                 const int64_t e = e0 + (int64_t)u * blockDim.x;
-                const int64_t p = (win && e >= n_sink) ? e + shift : e;
+                const int64_t p = (win && e >= first_shifted) ? e + shift : e;
                 if (e >= n_write) break;
                 if (p >= rtt_stride) {
                     latch(WMTP_DEV_ARG_RANGE);
@@ -100,7 +107,7 @@ __global__ void __launch_bounds__(256) build_indices_kernel(
             for (int u = 0; u < kIndexPerThread; ++u) {
                 const int64_t e = e0 + (int64_t)u * blockDim.x;
                 if (e >= n_write) break;
-                const int64_t p = (win && e >= n_sink) ? e + shift : e;
+                const int64_t p = (win && e >= first_shifted) ? e + shift : e;
                 out[e] = (int32_t)ring_slot(base, p, 0, n_sink, window, depth, tree_k);
             }
         }
@@ -292,6 +299,7 @@ wmtp_status wmtp_build_draft_indices(const int32_t *seq_lens, int32_t B, int32_t
     if (!seq_lens || !table || !lens) return WMTP_EINVAL;
     if (!req_to_token && !ring_base) return WMTP_EINVAL;
     if (req_to_token && rtt_stride < 1) return WMTP_EINVAL;
+    windowed = windowed ? 1 : 0;
     // kIndexPerThreadLong entries per thread on long rows, up to 8192 CTAs per row.
     constexpr int kThreads = 256;
     const bool long_rows = stride >= kIndexLongRow;
@@ -302,6 +310,28 @@ wmtp_status wmtp_build_draft_indices(const int32_t *seq_lens, int32_t B, int32_t
     return cudaLaunchKernelEx(&L.cfg, long_rows ? build_indices_kernel<kIndexPerThreadLong> : build_indices_kernel<1>, seq_lens, B, n_sink, window, depth,
                               tree_k, windowed, req_to_token, req_pool_idx, rtt_stride, ring_base,
                               table, stride, lens, static_cast<const int32_t *>(nullptr)) == cudaSuccess
+               ? WMTP_OK
+               : WMTP_ECUDA;
+}
+
+wmtp_status wmtp_build_far_indices(const int32_t *seq_lens, int32_t B, int32_t gamma,
+                                   int32_t n_sink, int32_t window, const int32_t *req_to_token,
+                                   const int32_t *req_pool_idx, int64_t rtt_stride, int32_t *table,
+                                   int64_t stride, int32_t *lens, void *stream) {
+    if (B < 0 || gamma < 0 || n_sink < 0 || window < 1 || stride < 1) return WMTP_EINVAL;
+    if ((int64_t)gamma * B > 65535) return WMTP_EINVAL;
+    if (B == 0 || gamma == 0) return WMTP_OK;
+    if (!seq_lens || !table || !lens || !req_to_token || rtt_stride < 1) return WMTP_EINVAL;
+    constexpr int kThreads = 256;
+    const bool long_rows = stride >= kIndexLongRow;
+    const int per = long_rows ? kIndexPerThreadLong : 1;
+    int64_t gx = (stride + kThreads * per - 1) / (kThreads * per);
+    if (gx > 8192) gx = 8192;
+    PdlLaunch L(dim3((unsigned)gx, (unsigned)(gamma * B)), dim3(kThreads), 0, as_stream(stream));
+    return cudaLaunchKernelEx(&L.cfg, long_rows ? build_indices_kernel<kIndexPerThreadLong> : build_indices_kernel<1>,
+                              seq_lens, B, n_sink, window, 1, 1, 2, req_to_token, req_pool_idx, rtt_stride,
+                              static_cast<const int32_t *>(nullptr), table, stride, lens,
+                              static_cast<const int32_t *>(nullptr)) == cudaSuccess
                ? WMTP_OK
                : WMTP_ECUDA;
 }
@@ -319,6 +349,7 @@ wmtp_status wmtp_build_extend_indices(const int32_t *seq_lens, const int32_t *n_
     if (!seq_lens || !n_new || !table || !lens) return WMTP_EINVAL;
     if (!req_to_token && !ring_base) return WMTP_EINVAL;
     if (req_to_token && rtt_stride < 1) return WMTP_EINVAL;
+    windowed = windowed ? 1 : 0;
     constexpr int kThreads = 256;
     const bool long_rows = stride >= kIndexLongRow;
     const int per = long_rows ? kIndexPerThreadLong : 1;

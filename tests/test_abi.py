@@ -126,6 +126,18 @@ def test_builder_and_ring_argument_checks(lib):
     assert b(P, 1, 1, 4, 8, 7, 1, 1, NULL, NULL, 10, NULL, P, 10, P, NULL) == wm.WMTP_EINVAL  # no layout
     assert b(P, 300, 300, 4, 8, 7, 1, 1, P, NULL, 10, NULL, P, 10, P, NULL) == wm.WMTP_EINVAL
     assert b(P, 0, 6, 4, 8, 7, 1, 1, P, NULL, 10, NULL, P, 10, P, NULL) == wm.WMTP_OK
+    f = lib.wmtp_build_far_indices
+    assert f(P, 1, 1, 64, 0, P, NULL, 10, P, 10, P, NULL) == wm.WMTP_EINVAL   # W < 1
+    assert f(P, 1, 1, -1, 8, P, NULL, 10, P, 10, P, NULL) == wm.WMTP_EINVAL  # n_sink < 0
+    assert f(P, 1, 1, 4, 8, NULL, NULL, 10, P, 10, P, NULL) == wm.WMTP_EINVAL  # paged layout only
+    assert f(P, 1, 1, 4, 8, P, NULL, 0, P, 10, P, NULL) == wm.WMTP_EINVAL     # rtt_stride < 1
+    assert f(P, 300, 300, 4, 8, P, NULL, 10, P, 10, P, NULL) == wm.WMTP_EINVAL
+    assert f(P, 0, 6, 4, 8, P, NULL, 10, P, 10, P, NULL) == wm.WMTP_OK
+    m = lib.wmtp_attn_mass_diagnostics
+    assert m(P, P, P, P, 4, 256, NULL, NULL, NULL, NULL, NULL, NULL) == wm.WMTP_EINVAL  # no output
+    assert m(P, NULL, P, P, 4, 256, P, NULL, NULL, NULL, NULL, NULL) == wm.WMTP_EINVAL  # null input
+    assert m(P, P, P, P, 4, 0, P, NULL, NULL, NULL, NULL, NULL) == wm.WMTP_EINVAL       # D < 1
+    assert m(P, P, P, P, 0, 256, P, NULL, NULL, NULL, NULL, NULL) == wm.WMTP_OK
     r = lib.wmtp_ring_map
     assert r(P, P, NULL, P, 5, 4, 8, 0, 1, P, NULL) == wm.WMTP_EINVAL  # depth < 1
     assert r(P, P, NULL, P, 5, 4, 8, 7, 0, P, NULL) == wm.WMTP_EINVAL  # tree_k < 1

@@ -134,3 +134,63 @@ def test_fused_bad_new_slot_is_latched_like_two_calls():
     assert wm.device_error(clear=True) == 1  # WMTP_DEV_SLOT_RANGE
     assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
     assert torch.equal(kp_a, kp_b) and torch.equal(vp_a, vp_b)
+
+
+def test_headline_fused_step_at_one_million_keys():
+    """The benchmark's own million-token step, in the launch configuration it
+    times: the workload object of the benchmark (B=1, S=1,048,576, H_q=16,
+    H_kv=2, D=256, 1 % of K rows x4, permuted page table), its full-context
+    arm (six fused append + attention launches over 1,048,577.. keys, the
+    split count of wmtp_attn_num_splits, its merge) and its windowed arm.
+    Checked: the full-context outputs equal, bit for bit, append_kv followed
+    by the unfused attention on a copy of the pools; sampled query heads (two
+    per step, one per KV head) and every windowed head match the fp64 oracle
+    after its own appends; the index tables match the oracle's; and after the
+    six steps both pools equal the oracle's pools bit for bit."""
+    import bench
+
+    cfg = bench.WORKLOADS["1m"]
+    w = bench.Workload(cfg, DEV)
+    g, S = cfg["gamma"], cfg["S"]
+    assert w.ns_full == wm.attn_num_splits(1, 1, cfg["H_kv"], S + g, DEV)
+    kp_h, vp_h = bits(w.kp), bits(w.vp)
+    kp2, vp2 = w.kp.clone(), w.vp.clone()
+
+    w.full_arm()
+    torch.cuda.synchronize()
+    for j in range(g):
+        wm.append_kv(w.kn[j], w.vn[j], w.slots[j], kp2, vp2)
+        o2, l2 = wm.draft_decode_attn(w.q[j], kp2, vp2, w.tab_full[j], w.len_full[j], w.scale,
+                                      n_split=w.ns_full, workspace=w.ws_full)
+        assert torch.equal(o2, w.out_full[j]) and torch.equal(l2, w.lse_full[j]), f"fused != two calls, step {j}"
+    assert torch.equal(kp2, w.kp) and torch.equal(vp2, w.vp)
+    del kp2, vp2
+
+    seq_h = host_i32(w.seq)
+    rtt_h = host_i32(w.rtt)
+    tab_f, len_f = oracle.build_draft_indices(seq_h, g, cfg["n_sink"], cfg["W"], g + 1, windowed=False,
+                                              req_to_token=rtt_h, stride=w.full_stride)
+    assert np.array_equal(host_i32(w.len_full), len_f)
+    tab_g = host_i32(w.tab_full)
+    for j in range(g):  # entries past a row's length are not written
+        assert np.array_equal(tab_g[j, 0, :len_f[j, 0]], tab_f[j, 0, :len_f[j, 0]]), f"full table, step {j}"
+    rng = np.random.default_rng(77)
+    for j in range(g):
+        oracle.append_kv(bits(w.kn[j]), bits(w.vn[j]), host_i32(w.slots[j]), kp_h, vp_h)
+        rows = np.array([rng.integers(0, 8), 8 + rng.integers(0, 8)])
+        ro, rl = oracle.draft_decode_attn(bits(w.q[j]), kp_h, vp_h, tab_f[j], len_f[j], w.scale, rows=rows)
+        assert_attn_close(w.out_full[j], w.lse_full[j], ro, rl, rows=rows, what=f"1M fused full step {j}")
+    assert np.array_equal(bits(w.kp), kp_h) and np.array_equal(bits(w.vp), vp_h), "pools differ from the oracle's"
+
+    w.win_arm()
+    torch.cuda.synchronize()
+    tab_w, len_w = oracle.build_draft_indices(seq_h, g, cfg["n_sink"], cfg["W"], g + 1, windowed=True,
+                                              req_to_token=rtt_h, stride=w.win_stride)
+    assert np.array_equal(host_i32(w.len_win), len_w)
+    tab_g = host_i32(w.tab_win)
+    for j in range(g):
+        assert np.array_equal(tab_g[j, 0, :len_w[j, 0]], tab_w[j, 0, :len_w[j, 0]]), f"windowed table, step {j}"
+    for j in range(g):
+        ro, rl = oracle.draft_decode_attn(bits(w.q[j]), kp_h, vp_h, tab_w[j], len_w[j], w.scale)
+        assert_attn_close(w.out_win[j], w.lse_win[j], ro, rl, what=f"1M fused windowed step {j}")
+    assert np.array_equal(bits(w.kp), kp_h) and np.array_equal(bits(w.vp), vp_h)

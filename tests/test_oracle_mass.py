@@ -84,3 +84,66 @@ def test_two_keys_by_hand():
     assert math.isclose(p[0, 0, 0], np.linalg.norm(o_full - np.array([0, 1])) / np.linalg.norm(o_full),
                         rel_tol=1e-12)
     assert math.isclose(t[0, 0, 0], p0 / np.linalg.norm(o_full), rel_tol=1e-12)
+
+
+# --- the far keys: the complement of the keep rule ("Windowed-MTP", §5 "A
+# partition-function view": Z = Z_w + Z_far over the kept and the dropped keys)
+
+def test_far_positions_closed_form_and_partition():
+    for n_sink, W in [(0, 1), (1, 1), (2, 3), (4, 16), (64, 100), (5, 7)]:
+        for s_kv in range(0, 200):
+            far = oracle.far_positions(s_kv, n_sink, W)
+            expect = list(range(n_sink, s_kv - W)) if s_kv > n_sink + W else []
+            assert far.tolist() == expect, (s_kv, n_sink, W)
+            kept = oracle.keep(s_kv, n_sink, W).tolist()
+            assert sorted(kept + far.tolist()) == list(range(s_kv))  # disjoint cover of [0, s_kv)
+
+
+def test_far_table_through_the_page_table():
+    rng = np.random.default_rng(5)
+    n_sink, W, gamma = 3, 10, 3
+    S_list = [0, 5, 13, 14, 40]
+    cap = max(S_list) + gamma
+    rtt = np.stack([rng.permutation(1000)[:cap] for _ in S_list]).astype(np.int32)
+    table, lens = oracle.build_far_indices(np.array(S_list, np.int32), gamma, n_sink, W, rtt)
+    for j in range(gamma):
+        for b, S in enumerate(S_list):
+            kv = S + j + 1
+            pos = np.arange(n_sink, kv - W) if kv > n_sink + W else np.arange(0)
+            assert lens[j, b] == len(pos)
+            assert np.array_equal(table[j, b, :len(pos)], rtt[b, pos])
+            assert np.all(table[j, b, len(pos):] == -1)
+
+
+def test_window_and_far_attention_merge_to_the_full_attention():
+    """The decomposition the GPU diagnostics use: with a = Z_w / Z and
+    b = Z_far / Z from the two log partition functions, a o_win + b o_far is
+    the full-context output and log(e^lse_win + e^lse_far) its lse."""
+    rng = np.random.default_rng(11)
+    n_sink, W, gamma, H_q, H_kv, D = 2, 9, 2, 4, 2, 8
+    S = 60
+    pool = S + gamma
+    kp = _bf16(rng.standard_normal((pool, H_kv, D)))
+    vp = _bf16(rng.standard_normal((pool, H_kv, D)))
+    q = _bf16(rng.standard_normal((1, 1, H_q, D)))
+    rtt = rng.permutation(pool).astype(np.int32).reshape(1, -1)
+    seq = np.array([S], np.int32)
+    kw = dict(gamma=gamma, n_sink=n_sink, window=W, depth=gamma + 1, req_to_token=rtt)
+    tf, lf = oracle.build_draft_indices(seq, windowed=False, stride=pool, **kw)
+    tw, lw = oracle.build_draft_indices(seq, windowed=True, stride=n_sink + W, **kw)
+    tr, lr = oracle.build_far_indices(seq, gamma, n_sink, W, rtt)
+    for j in range(gamma):
+        of, lsf = oracle.draft_decode_attn(q, kp, vp, tf[j], lf[j], 0.4)
+        ow, lsw = oracle.draft_decode_attn(q, kp, vp, tw[j], lw[j], 0.4)
+        o_r, lsr = oracle.draft_decode_attn(q, kp, vp, tr[j], lr[j], 0.4)
+        a = 1.0 / (1.0 + np.exp(lsr - lsw))
+        b = 1.0 / (1.0 + np.exp(lsw - lsr))
+        merged = a[..., None] * ow + b[..., None] * o_r
+        assert np.allclose(merged, of, rtol=1e-12, atol=1e-14)
+        assert np.allclose(np.logaddexp(lsw, lsr), lsf, rtol=1e-13, atol=1e-13)
+        # and the diagnostics' tail fraction is b ||o_far|| / ||o_full||
+        ra, rp, rt = oracle.attn_mass(q, kp, vp, tf[j], lf[j], tw[j], lw[j], 0.4)
+        nf = np.linalg.norm(of, axis=-1)
+        assert np.allclose(rt, b * np.linalg.norm(o_r, axis=-1) / nf, rtol=1e-11)
+        assert np.allclose(rp, b * np.linalg.norm(o_r - ow, axis=-1) / nf, rtol=1e-11)
+        assert np.allclose(ra, a, rtol=1e-12)
