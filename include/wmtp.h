@@ -204,8 +204,9 @@ wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
  * lse      device fp32 [B][n_q][H_q] or NULL.
  * k_pool, v_pool 16-byte aligned; q 4-byte aligned.
  * workspace device, >= wmtp_attn_workspace_bytes(...) bytes, 256-byte
- *          aligned.  Its first bytes hold 16 merge counters per (request,
- *          query token, KV head); they must be zero when a call starts.
+ *          aligned.  Its first bytes hold max(16, 2 + n_split rounded up
+ *          to 16) merge counters per (request, query token, KV head); they
+ *          must be zero when a call starts.
  *          wmtp_attn_workspace_init() zeroes them, and every completed call
  *          leaves its own counters at zero, so a workspace serves any number
  *          of calls with the same B * n_q * H_kv.  Initialise again before
@@ -213,6 +214,16 @@ wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
  *          workspace must not overlap on the GPU.  Unused when n_split == 1,
  *          and when the splits merge through one thread-block cluster (up to
  *          16 splits, where the device can hold such a cluster).
+ * Merge paths (fixed by n_split, B * n_q * H_kv and the device, so results
+ * depend only on those and the inputs), in order of preference: one cluster
+ * (n_split <= 16, through distributed shared memory); whole clusters of up
+ * to 16 merged in two levels, when the device holds all of them at once;
+ * the slice merge, for more than 16 splits when the whole grid fits on the
+ * device at once (every split writes its partial, takes an arrival ticket
+ * and, once all have arrived -- a wait bounded at 50 us -- merges its own
+ * slice of the output; the last to arrive also merges any slice whose split
+ * gave up waiting, so the result never depends on co-residency); or the
+ * last split to finish merging all of them.
  * n_split  1 .. 1024; wmtp_attn_num_splits() gives a good value.
  * Errors: WMTP_EINVAL for null pointers, bad sizes, D not 128/256,
  * H_q % H_kv != 0, group > 8, misaligned pool/q pointers;
@@ -424,9 +435,10 @@ wmtp_status wmtp_tree_draft_attn(const uint16_t *q, int32_t B, int32_t H_q,
  *     call this entry point on that device again in the same process.
  *   - Results: the merge path is always the workspace ("last CTA merges")
  *     merge, so they are bit-identical to wmtp_draft_decode_attn with the
- *     same n_split whenever that call also merges through its workspace
- *     (no thread-block cluster fits the split plan); where it merges
- *     through a cluster instead, the two agree within rounding.
+ *     same n_split whenever that call takes the same merge (no thread-block
+ *     cluster fits the split plan and, above 16 splits, the grid is larger
+ *     than the device holds at once); where it merges through a cluster or
+ *     the slice merge instead, the two agree within rounding.
  *   - Every call shares the one array and it keeps the last call's
  *     contents; each call first zeroes the merge counters it uses (an
  *     async memset on `stream`).  Calls that overlap on the GPU (other

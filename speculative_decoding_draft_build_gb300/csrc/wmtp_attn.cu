@@ -67,6 +67,8 @@ constexpr int kMaxSplits = 1024;
 constexpr int kMaxClusterMerge = 16;  // splits merged through a cluster (non-portable size)
 constexpr int kMaxClusters = 8;       // clusters merged by the second level
 constexpr int kMaxNew = 4;            // rows one request appends in a fused call (one per warp)
+constexpr int kMinSliceSplits = kMaxClusterMerge + 1;  // the slice merge serves larger split counts
+constexpr uint64_t kSlicePollNs = 50000;  // a slice-merge wait gives up after 50 us (results stay exact)
 constexpr float kLn2 = 0.69314718055994530942f;
 
 #ifndef WMTP_FP8_STAGES
@@ -110,18 +112,26 @@ struct WorkspaceView {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline size_t counter_bytes(int64_t rows_kv) { return align256((size_t)rows_kv * kMaxClusterMerge * 4); }
+// int32 counters per (row, KV head): at least one cluster's worth, or the
+// slice merge's arrival and departure counts plus one claim word per split.
+inline int counter_stride(int n_split) {
+    const int need = (2 + n_split + 15) / 16 * 16;
+    return need > kMaxClusterMerge ? need : kMaxClusterMerge;
+}
+inline size_t counter_bytes(int64_t rows_kv, int n_split) {
+    return align256((size_t)rows_kv * counter_stride(n_split) * 4);
+}
 
 // Bytes for the split-order merge; the two-level merge (at most n_split / 2
 // clusters, each holding rows_q * D outputs and rows_q * D / 4 lse values)
 // never needs more.
 inline size_t workspace_bytes(int64_t rows_q, int64_t rows_kv, int D, int n_split) {
     if (n_split <= 1) return 0;
-    const size_t split_order =
-        counter_bytes(rows_kv) + align256((size_t)rows_q * n_split * 4) + (size_t)rows_q * n_split * D * 4;
+    const size_t split_order = counter_bytes(rows_kv, n_split) + align256((size_t)rows_q * n_split * 4) +
+                               (size_t)rows_q * n_split * D * 4;
     const int64_t m = n_split / 2 < kMaxClusters ? n_split / 2 : kMaxClusters;
     const size_t two_level =
-        counter_bytes(rows_kv) + align256((size_t)rows_q * m * D * 4) + (size_t)rows_q * m * D;
+        counter_bytes(rows_kv, n_split) + align256((size_t)rows_q * m * D * 4) + (size_t)rows_q * m * D;
     return split_order > two_level ? split_order : two_level;
 }
 
@@ -181,18 +191,18 @@ inline WorkspaceView carve(void *ws, int64_t rows_q, int64_t rows_kv, int n_spli
     uint8_t *p = static_cast<uint8_t *>(ws);
     WorkspaceView v;
     v.counters = reinterpret_cast<int32_t *>(p);
-    p += counter_bytes(rows_kv);
+    p += counter_bytes(rows_kv, n_split);
     v.lse_part = reinterpret_cast<float *>(p);
     p += align256((size_t)rows_q * n_split * 4);
     v.o_part = reinterpret_cast<float *>(p);
     return v;
 }
 
-inline WorkspaceView carve_two_level(void *ws, int64_t rows_q, int64_t rows_kv, int D, int clusters) {
+inline WorkspaceView carve_two_level(void *ws, int64_t rows_q, int64_t rows_kv, int D, int n_split, int clusters) {
     uint8_t *p = static_cast<uint8_t *>(ws);
     WorkspaceView v;
     v.counters = reinterpret_cast<int32_t *>(p);
-    p += counter_bytes(rows_kv);
+    p += counter_bytes(rows_kv, n_split);
     v.o_part = reinterpret_cast<float *>(p);
     p += align256((size_t)rows_q * clusters * D * 4);
     v.lse_part = reinterpret_cast<float *>(p);
@@ -205,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const void *__restrict__ k_pool, const void *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ table, int64_t table_stride,
     const int32_t *__restrict__ lens, float scale_log2, float *__restrict__ out,
-    float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t csz, AppendView ap,
-    ExtendView ev, Fp8View fv, RingView rv) {
+    float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t csz, int32_t slice_stride,
+    AppendView ap, ExtendView ev, Fp8View fv, RingView rv) {
     static_assert(!(kFp8 && (kAppend || kExtend)), "the fp8 path appends with its own kernel");
     static_assert(!(kRing && (kExtend || kFp8)), "ring launches are bf16 decode steps");
     using C = Cfg<D, kFp8>;
@@ -810,6 +820,136 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         return;
     }
 
+    if (slice_stride) {
+        // ------------------------------------------------- slice merge
+        // Every split has written its partial.  Each CTA takes an arrival
+        // ticket; all but the last wait (time-bounded) until every split has
+        // arrived and then merge their own slice of the G x D outputs, so the
+        // merge runs on all the launch's SMs at once.  The last to arrive
+        // never waits: it merges its own slice and then every slice still
+        // unclaimed (one whose CTA gave up waiting), so each slice is merged
+        // exactly once (claims are compare-and-swap) whatever the
+        // co-residency.  The last CTA to leave returns the counters to zero.
+        __threadfence();
+        __syncthreads();
+        int32_t *ctr = ws.counters + (bt * H_kv + g) * slice_stride;  // arrivals, departures, claims
+        if (tid == 0) {
+            const bool last = atomicAdd(ctr, 1) == n_split - 1;
+            const bool all_in = last || poll_geq_bounded(ctr, n_split, kSlicePollNs);
+            if (all_in) __threadfence();
+            flags[1] = last;
+            flags[2] = all_in && atomicCAS(ctr + 2 + split, 0, 1) == 0;
+        }
+        __syncthreads();
+        const bool last = flags[1] != 0;
+        const bool mine = flags[2] != 0;
+        const int total4 = G * D4;
+        const int per4 = (total4 + n_split - 1) / n_split;
+        float *sw = wts;                                    // [heads of the slice][n_split]
+        float4 *red = reinterpret_cast<float4 *>(part_o);   // [kThreads]
+        int32_t *claim = reinterpret_cast<int32_t *>(ow);   // [n_split]
+        // Merges slice s_idx: float4 outputs [lo4, hi4) of this (row, KV
+        // head); kThreads / nel threads per output, each summing a strided
+        // subset of the splits, then a fixed-order reduction.
+        auto slice_merge = [&](int s_idx) {
+            const int lo4 = s_idx * per4;
+            const int hi4 = lo4 + per4 < total4 ? lo4 + per4 : total4;
+            if (lo4 >= hi4) return;
+            const int nel = hi4 - lo4;
+            const int h0 = lo4 / D4;
+            const int nh = (hi4 - 1) / D4 - h0 + 1;
+            const int R = kThreads / nel;  // >= 1: nel <= ceil(G * D4 / 17) <= kThreads
+            const int r = tid / nel, el = tid - (tid / nel) * nel;
+            const int f = lo4 + el;
+            const int h = f / D4, d4 = f - h * D4;
+            const float4 *op = reinterpret_cast<const float4 *>(ws.o_part + (row_q0 + h) * n_split * D) + d4;
+            // the first batch of output partials is in flight while the lse
+            // values load and the weights are formed
+            constexpr int kBatch = 8;
+            float4 v[kBatch];
+            if (r < R) {
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int s2 = r + u * R;
+                    if (s2 < n_split) v[u] = __ldcg(op + (int64_t)s2 * D4);
+                }
+            }
+            for (int e = tid; e < nh * n_split; e += kThreads) {
+                const int hh = e / n_split, s2 = e - hh * n_split;
+                sw[e] = __ldcg(ws.lse_part + (row_q0 + h0 + hh) * n_split + s2);
+            }
+            __syncthreads();
+            for (int hh = warp; hh < nh; hh += kConsumerWarps) {
+                float *x = sw + hh * n_split;
+                float M = -INFINITY;
+                for (int s2 = lane; s2 < n_split; s2 += 32) M = fmaxf(M, x[s2]);
+#pragma unroll
+                for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
+                float sum = 0.f;
+                if (M != -INFINITY)
+                    for (int s2 = lane; s2 < n_split; s2 += 32) sum += x[s2] == -INFINITY ? 0.f : exp2f(x[s2] - M);
+#pragma unroll
+                for (int sh = 16; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+                const float lse_tot = sum > 0.f ? M + log2f(sum) : -INFINITY;
+                __syncwarp();
+                for (int s2 = lane; s2 < n_split; s2 += 32)
+                    x[s2] = (sum > 0.f && x[s2] != -INFINITY) ? exp2f(x[s2] - lse_tot) : 0.f;
+                if (lane == 0 && lse && (h0 + hh) * D4 >= lo4) lse[row_q0 + h0 + hh] = lse_tot * kLn2;
+            }
+            __syncthreads();
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < R) {
+                const float *wh = sw + (h - h0) * n_split;
+                for (int s0 = r; s0 < n_split; s0 += kBatch * R) {
+                    if (s0 != r) {
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) {
+                            const int s2 = s0 + u * R;
+                            if (s2 < n_split) v[u] = __ldcg(op + (int64_t)s2 * D4);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int s2 = s0 + u * R;
+                        if (s2 < n_split) {
+                            const float w = wh[s2];
+                            acc.x += w * v[u].x;
+                            acc.y += w * v[u].y;
+                            acc.z += w * v[u].z;
+                            acc.w += w * v[u].w;
+                        }
+                    }
+                }
+            }
+            red[tid] = acc;
+            __syncthreads();
+            if (tid < nel) {
+                float4 t = red[tid];
+                for (int rr = 1; rr < R; ++rr) {
+                    const float4 u = red[rr * nel + tid];
+                    t.x += u.x;
+                    t.y += u.y;
+                    t.z += u.z;
+                    t.w += u.w;
+                }
+                reinterpret_cast<float4 *>(out + (row_q0 + h) * D)[d4] = t;
+            }
+            __syncthreads();  // sw and red are reused by the next slice
+        };
+        if (mine) slice_merge(split);
+        if (last) {
+            for (int s2 = tid; s2 < n_split; s2 += kThreads)
+                claim[s2] = (s2 != split && atomicCAS(ctr + 2 + s2, 0, 2) == 0) ? 1 : 0;
+            __syncthreads();
+            for (int s2 = 0; s2 < n_split; ++s2)
+                if (claim[s2]) slice_merge(s2);
+        }
+        __syncthreads();
+        if (tid == 0 && atomicAdd(ctr + 1, 1) == n_split - 1)
+            for (int i = 0; i < 2 + n_split; ++i) ctr[i] = 0;  // ready for the next call
+        return;
+    }
+
     // ------------------------------------------ ticket; the last CTA merges
     __threadfence();
     __syncthreads();
@@ -933,6 +1073,24 @@ int cluster_capacity(int dev, int n) {
     return ok ? known[dev][n] : 0;
 }
 
+// CTAs of the plain instance the device holds at once (SMs x resident
+// blocks per SM; 0 if unknown), cached per device.
+template <int D, bool F = false>
+int resident_capacity(int dev) {
+    static int32_t known[64] = {};
+    if (dev < 0 || dev >= 64) return 0;
+    if (known[dev]) return known[dev] > 0 ? known[dev] : 0;
+    int sms = 0, per_sm = 0;
+    const bool ok = prepare_kernel<D, false, false, F>(dev) &&
+                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_decode_kernel<D, false, false, F>,
+                                                                  kThreads, Cfg<D, F>::kSmemBytes) == cudaSuccess &&
+                    sms > 0 && per_sm > 0;
+    cudaGetLastError();
+    known[dev] = ok ? sms * per_sm : -1;
+    return ok ? known[dev] : 0;
+}
+
 template <int D, bool F>
 wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
                                 int32_t H_kv, const void *k_pool, const void *v_pool,
@@ -982,9 +1140,17 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
             }
         }
     }
+    // No cluster plan: the slice merge when the whole grid fits on the
+    // device at once (its waits then end as soon as the last split
+    // arrives), else the last CTA merges.
+    int slice = 0;
+    if (csz == 0 && n_split >= kMinSliceSplits) {
+        const int cap = resident_capacity<D, F>(dev);
+        if (cap > 0 && rows_kv * n_split <= cap) slice = counter_stride(n_split);
+    }
     WorkspaceView ws{nullptr, nullptr, nullptr};
     if (n_split > 1 && csz == 0) ws = carve(workspace, rows_q, rows_kv, n_split);
-    if (csz && n_split / csz > 1) ws = carve_two_level(workspace, rows_q, rows_kv, D, n_split / csz);
+    if (csz && n_split / csz > 1) ws = carve_two_level(workspace, rows_q, rows_kv, D, n_split, n_split / csz);
     const float scale_log2 = scale * 1.4426950408889634f;
     PdlLaunch launch(dim3((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q)), dim3(kThreads),
                      C::kSmemBytes, stream);
@@ -998,7 +1164,8 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
                          : (extend ? split_decode_kernel<D, false, true, false>
                                    : split_decode_kernel<D, false, false, false>)),
         reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q, H_kv, H_q / H_kv, k_pool, v_pool,
-        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, ap, ev, fv, rv);
+        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, (int32_t)slice, ap, ev,
+        fv, rv);
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
@@ -1067,7 +1234,7 @@ wmtp_status launch_split_decode_noalloc(const uint16_t *q, int32_t B, int32_t n_
     const cudaError_t err = cudaLaunchKernelEx(
         &launch.cfg, split_decode_kernel<D, false, false, false>, reinterpret_cast<const __nv_bfloat16 *>(q), n_q,
         H_q, H_kv, H_q / H_kv, static_cast<const void *>(k_pool), static_cast<const void *>(v_pool), num_slots,
-        table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)0,
+        table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)0, (int32_t)0,
         AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0}, ExtendView{nullptr, nullptr, 0, 0, 0},
         Fp8View{nullptr, nullptr}, RingView{nullptr, nullptr, 0, 0, 0, 0, 0});
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
@@ -1128,7 +1295,8 @@ int32_t num_splits_for(int32_t B, int32_t n_q, int32_t H_kv, int64_t max_len, in
         // short rows: the launch is latency-bound and the load rate of one
         // SM is capped, so spread the row over the SMs, two key tiles per
         // split at least.  Above one cluster, keep to whole clusters of 16
-        // (two-level merge) that are all resident at once.
+        // (two-level merge) that are all resident at once: a merge through
+        // global memory costs more than the extra SMs save on such rows.
         const int64_t half = tiles / 2;
         n = by_sms < half ? by_sms : half;
         if (n > kMaxClusterMerge) {

@@ -83,6 +83,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// ------------------------------------------------------- global counters
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Polls the counter at p until it reaches `target`; gives up after
+// `limit_ns` nanoseconds and returns false.  Never spins without a bound.
+__device__ __forceinline__ bool poll_geq_bounded(const int32_t *p, int32_t target, uint64_t limit_ns) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ld_acquire_gpu(p) >= target) return true;
+        if ((i & 15u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // ------------------------------------------------------- bulk async copies
 // L2 policy: stream once, evict first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

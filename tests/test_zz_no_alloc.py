@@ -11,10 +11,11 @@ and check it against the regular entry point, which uses a caller-provided
 workspace, on several calls in a row with different shapes, so that each call
 runs on scratch left over by the one before.  The no-workspace call always
 merges through the scratch with the "last CTA merges" path; where the regular
-call takes that same path -- a prime split count above the largest cluster,
-or more rows than any cluster plan holds at once -- the two must agree bit
-for bit.  Where the regular call merges through a thread-block cluster, they
-must agree within the attention tolerance of the other parity tests.  One
+call takes that same path -- more splits than one cluster holds in a grid
+larger than the device holds at once, or no cluster plan that fits -- the two
+must agree bit for bit.  Where the regular call merges through a thread-block
+cluster, they must agree within the attention tolerance of the other parity
+tests.  One
 case is also checked against the fp64 oracle.  The file is named to be
 collected last.
 """
@@ -128,11 +129,11 @@ def test_noalloc_matches_workspace_entry_point_twice():
     cases = [
         # (B, H_q, H_kv, D, keys, pool, n_split, bit-exact expected)
         (2, 16, 2, 256, 20_000, 20_000, 9, False),   # regular call merges in a cluster of 9
-        (3, 8, 2, 128, 7_000, 7_000, 37, True),      # prime > 16: both merge through memory
-        (1, 16, 2, 256, LIMIT_SPLITS * 64, LIMIT_SPLITS * 64, LIMIT_SPLITS, True),  # scratch exactly full
+        (12, 8, 2, 128, 7_000, 7_000, 37, True),     # 888 CTAs, more than the device holds at once
+        (1, 16, 2, 256, LIMIT_SPLITS * 64, LIMIT_SPLITS * 64, LIMIT_SPLITS, True),  # scratch exactly full, 1018 CTAs
         (COUNTERS // 2, 2, 2, 128, 130, 5_000, 2, True),  # WMTP_NOALLOC_MAX_COUNTERS merge counters
         (2, 16, 2, 256, 3_000, 3_000, 1, True),      # one split: no scratch at all
-        (3, 8, 2, 128, 7_000, 7_000, 37, True),      # repeat: leftover counters and partials
+        (12, 8, 2, 128, 7_000, 7_000, 37, True),     # repeat: leftover counters and partials
     ]
     for i, (B, H_q, H_kv, D, L, pool, n_split, exact) in enumerate(cases):
         kp, vp, q, table, lens = _inputs(B, H_q, H_kv, D, L, pool, 500 + 10 * i, dev)
