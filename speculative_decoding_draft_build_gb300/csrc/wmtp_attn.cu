@@ -70,9 +70,19 @@ constexpr int kMaxNew = 4;            // rows one request appends in a fused cal
 constexpr int kMinSliceSplits = kMaxClusterMerge + 1;  // the slice merge serves larger split counts
 constexpr uint64_t kSlicePollNs = 50000;  // a slice-merge wait gives up after 50 us (results stay exact)
 constexpr float kLn2 = 0.69314718055994530942f;
+// Warp-specialised instances (long rows): one producer warp issues every
+// copy, the four consumer warps only compute; waits are time-bounded.
+constexpr int kWsProducers = 4;  // one producer warp per consumer warp (one of each per scheduler)
+constexpr int kWsThreads = kThreads + 32 * kWsProducers;
+constexpr int kWsMinKeysPerSplit = 4 * kTileKeys;  // rows with at least four key tiles per split
+constexpr uint64_t kWsWaitNs = 2000000000ull;
+
+// The consumer warps' CTA barrier (named barrier 1, 128 threads): in a
+// warp-specialised CTA the producer warp has left by then.
+__device__ __forceinline__ void sync_consumers() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 #ifndef WMTP_FP8_STAGES
-#define WMTP_FP8_STAGES 5
+#define WMTP_FP8_STAGES 6
 #endif
 
 template <int D, bool kFp8 = false>
@@ -95,7 +105,9 @@ struct Cfg {
     static constexpr int kRingOffset = kTilesBytes;  // int32 [warps][ring tiles][16]
     static constexpr int kMaskOffset = kRingOffset + kConsumerWarps * kRingTiles * kKeysPerWarp * 4;
     static constexpr int kFlagOffset = kMaskOffset + kConsumerWarps * kStages * 4;
-    static constexpr int kSmemBytes = kFlagOffset + 16;
+    // warp-specialised instances: a full and an empty mbarrier per stage
+    static constexpr int kBarOffset = (kFlagOffset + 16 + 7) / 8 * 8;
+    static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8;
 };
 
 // Workspace: a counter region of kMaxClusterMerge int32 per (row, KV head),
@@ -209,8 +221,8 @@ inline WorkspaceView carve_two_level(void *ws, int64_t rows_q, int64_t rows_kv, 
     return v;
 }
 
-template <int D, bool kAppend, bool kExtend, bool kFp8, bool kRing = false>
-__global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
+template <int D, bool kAppend, bool kExtend, bool kFp8, bool kRing = false, bool kWs = false>
+__global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_kernel(
     const __nv_bfloat16 *__restrict__ q, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t G,
     const void *__restrict__ k_pool, const void *__restrict__ v_pool,
     int64_t num_slots, const int32_t *__restrict__ table, int64_t table_stride,
@@ -225,8 +237,22 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *masks = reinterpret_cast<uint32_t *>(smem + C::kMaskOffset);
     volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(smem + C::kFlagOffset);
+    uint64_t *ws_bars = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);  // [S] full, then [S] empty
 
     griddep_launch_dependents();
+    if constexpr (kWs) {
+        // full: per producer warp, 32 copy-completion arrivals of its lanes
+        // and one after its key mask is stored; empty: one per consumer warp
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < S; ++i) {
+                mbar_init(smem_addr(ws_bars + i), kWsProducers * 33);
+                mbar_init(smem_addr(ws_bars + S + i), kConsumerWarps);
+            }
+            flags[3] = 0;
+            fence_mbar_init();
+        }
+        __syncthreads();  // all warps, before the roles split
+    }
 
     griddep_wait();
 
@@ -334,8 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const int64_t start_g = (int64_t)split * chunk_g;
     const int64_t cnt_g = table_stride - start_g < 0 ? 0 : (table_stride - start_g < chunk_g ? table_stride - start_g : chunk_g);
     const int n_tiles_g = (int)((cnt_g + kTileKeys - 1) / kTileKeys);
-    for (int t = 0; t < 2 * S - 1 && t < n_tiles_g; ++t) fetch_slots_from(t, table + b * table_stride + start_g, cnt_g);
-    cp_async_commit();
+    if constexpr (!kWs) {
+        for (int t = 0; t < 2 * S - 1 && t < n_tiles_g; ++t) fetch_slots_from(t, table + b * table_stride + start_g, cnt_g);
+        cp_async_commit();
+    }
 
     int64_t L = L_in;
     if (L < 0 || L > table_stride) {
@@ -366,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const int n_tiles = (int)((cnt + kTileKeys - 1) / kTileKeys);
     const int32_t *__restrict__ trow = table + b * table_stride + start;
     auto fetch_slots = [&](int t) { fetch_slots_from(t, trow, cnt); };
-    if (chunk != chunk_g) {  // a shorter row: fetch its own chunk
+    if (!kWs && chunk != chunk_g) {  // a shorter row: fetch its own chunk
         cp_async_wait<0>();
         __syncwarp();
         for (int t = 0; t < 2 * S - 1 && t < n_tiles; ++t) fetch_slots(t);
@@ -452,14 +480,95 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         }
     }
 
-    // Prologue: slots of the first 2S-1 tiles (fetched above), then K/V of
-    // the first S-1.
-    cp_async_wait<0>();
-    __syncwarp();
+    if constexpr (kWs) {
+        if (warp >= kConsumerWarps) {
+            // --------------------------------------------- producer warps
+            // Producer warp p copies, for every tile, the 16 keys that
+            // consumer warp p computes (lane l < 16: key 16p + l), with the
+            // slot (table entry loaded three tiles ahead, or the ring rule),
+            // validity and append substitution of the other instances'
+            // gathers.  The stage's full barrier completes when every
+            // producer's copies have landed and its key mask is stored.
+            const int pw = warp - kConsumerWarps;
+            auto slot_at = [&](int t) -> int32_t {
+                const int64_t k = (int64_t)t * kTileKeys + pw * kKeysPerWarp + lane;
+                return (!kRing && lane < kKeysPerWarp && k < cnt) ? __ldg(trow + k) : 0;
+            };
+            int32_t p0 = slot_at(0), p1 = slot_at(1), p2 = slot_at(2);
+            constexpr int kLanesPerRow = C::kRowBytes / 16;
+            constexpr int kRowsPerInst = 32 / kLanesPerRow;
+            const int sub = lane / kLanesPerRow;
+            const int col = (lane % kLanesPerRow) * 16;
+            const uint32_t wsm = smem_addr(smem + pw * C::kWarpBytes);
+            for (int t = 0; t < n_tiles; ++t) {
+                const int st = t % S;
+                const int32_t p3 = slot_at(t + 3);
+                if (t >= S && !__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(ws_bars + S + st),
+                                                                          ((t / S) - 1) & 1, kWsWaitNs))) {
+                    if (lane == 0) {
+                        latch(WMTP_DEV_WAIT_TIMEOUT);
+                        flags[3] = 1;
+                    }
+                    break;
+                }
+                const int64_t k = (int64_t)t * kTileKeys + pw * kKeysPerWarp + (lane & 15);
+                int32_t my_slot = p0;
+                if constexpr (kRing) {
+                    const int64_t e = start + k;
+                    const int64_t pos = (r_win && e >= rv.n_sink) ? r_lo + (e - rv.n_sink) : e;
+                    my_slot = (lane < kKeysPerWarp && k < cnt) ? ring_slot32(pos) : 0;
+                }
+                const bool in = lane < kKeysPerWarp && k < cnt;
+                const bool ok = in && my_slot >= 0 && my_slot < num_slots;
+                if (in && !ok) latch(WMTP_DEV_SLOT_RANGE);
+                int32_t src_slot = my_slot;
+                if constexpr (kAppend && kRing) {
+                    if (ok && start + k == L - 1) src_slot = -2;
+                } else if constexpr (kAppend) {
 #pragma unroll
-    for (int t = 0; t < S - 1; ++t) {
-        if (t < n_tiles) issue(t);
-        cp_async_commit();
+                    for (int i = kMaxNew - 1; i >= 0; --i)
+                        if (ok && my_slot == nslot[i]) src_slot = -2 - i;
+                }
+                const uint32_t vm = __ballot_sync(0xffffffffu, ok) & 0xffffu;
+                if (lane == 0) masks[pw * S + st] = vm;
+                const uint32_t kdst0 = wsm + st * C::kWarpStage;
+#pragma unroll
+                for (int r0 = 0; r0 < kKeysPerWarp; r0 += kRowsPerInst) {
+                    const int key = r0 + sub;
+                    const int32_t slot = __shfl_sync(0xffffffffu, src_slot, key);
+                    const bool kv = (vm >> key) & 1u;
+                    const uint8_t *ksrc, *vsrc;
+                    if (kAppend && slot < -1) {
+                        ksrc = knew + (size_t)(-2 - slot) * slot_bytes + col;
+                        vsrc = vnew + (size_t)(-2 - slot) * slot_bytes + col;
+                    } else {
+                        const size_t off = kv ? (size_t)slot * slot_bytes + col : 0;
+                        ksrc = kbase + off;
+                        vsrc = vbase + off;
+                    }
+                    cp_async_16(kdst0 + key * C::kPitch + col, ksrc, kv ? 16u : 0u, policy);
+                    cp_async_16(kdst0 + C::kWarpTile + key * C::kPitch + col, vsrc, kv ? 16u : 0u, policy);
+                }
+                cp_async_mbar_arrive(smem_addr(ws_bars + st));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(ws_bars + st));
+                p0 = p1;
+                p1 = p2;
+                p2 = p3;
+            }
+            cp_async_wait<0>();
+            return;
+        }
+    } else {
+        // Prologue: slots of the first 2S-1 tiles (fetched above), then K/V
+        // of the first S-1.
+        cp_async_wait<0>();
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < S - 1; ++t) {
+            if (t < n_tiles) issue(t);
+            cp_async_commit();
+        }
     }
 
 
@@ -474,13 +583,24 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     const uint32_t v_off = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * C::kPitch + ((lane >> 3) & 1) * 16);
 
     for (int it = 0; it < n_tiles; ++it) {
-        // Groups committed so far: slots, K/V of tiles 0..S-2, then one group
-        // per iteration; waiting for all but the newest S-1 makes tile `it`
-        // (and the slots of tile it+S) resident.
-        if (it + S - 1 < n_tiles) issue(it + S - 1);
-        if (it + 2 * S - 1 < n_tiles) fetch_slots(it + 2 * S - 1);
-        cp_async_commit();
-        cp_async_wait<S - 1>();
+        if constexpr (kWs) {
+            // the producer warp's copies of tile `it` have landed
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(ws_bars + it % S), (it / S) & 1, kWsWaitNs))) {
+                if (lane == 0) {
+                    latch(WMTP_DEV_WAIT_TIMEOUT);
+                    flags[3] = 1;
+                }
+                break;
+            }
+        } else {
+            // Groups committed so far: slots, K/V of tiles 0..S-2, then one
+            // group per iteration; waiting for all but the newest S-1 makes
+            // tile `it` (and the slots of tile it+S) resident.
+            if (it + S - 1 < n_tiles) issue(it + S - 1);
+            if (it + 2 * S - 1 < n_tiles) fetch_slots(it + 2 * S - 1);
+            cp_async_commit();
+            cp_async_wait<S - 1>();
+        }
         __syncwarp();
         const int st = it % S;
         const uint32_t wm = masks[warp * S + st];
@@ -589,6 +709,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
             }
         }
         __syncwarp();
+        if constexpr (kWs) {
+            if (lane == 0) mbar_arrive(smem_addr(ws_bars + S + st));  // stage st is free again
+        }
     }
     cp_async_wait<0>();
 
@@ -622,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
     }
 
     // ---------------------------------------------- combine the four warps
-    __syncthreads();  // every warp is done with its tiles
+    sync_consumers();  // every warp is done with its tiles
     float *ow = reinterpret_cast<float *>(smem);                       // [warp][head][kOPitch]
     float *mw = ow + kConsumerWarps * kMaxGroup * C::kOPitch;          // [warp][head]
     float *lw = mw + kConsumerWarps * kMaxGroup;                       // [warp][head]
@@ -650,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
             lw[warp * kMaxGroup + 2 * c + 1] = l1;
         }
     }
-    __syncthreads();
+    sync_consumers();
 
     const int tid = threadIdx.x;
     const int64_t row_q0 = bt * H_q + (int64_t)g * G;  // first query row of the group
@@ -674,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         for (int w = 0; w < kConsumerWarps; ++w) fac[h * kConsumerWarps + w] = f[w] * inv;
         cta_lse[h] = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
     }
-    __syncthreads();
+    sync_consumers();
     constexpr int D4 = D / 4;
     for (int e = tid; e < G * D4; e += kThreads) {
         const int h = e / D4, d4 = e - h * D4;
@@ -769,10 +892,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
             // -------------------- second level: the last cluster merges the
             // slice over all clusters, in cluster order
             __threadfence();
-            __syncthreads();
+            sync_consumers();
             int32_t *ctr = ws.counters + rk * kMaxClusterMerge + rank;
             if (tid == 0) flags[0] = (atomicAdd(ctr, 1) == n_cl - 1);
-            __syncthreads();
+            sync_consumers();
             if (flags[0]) {
                 __threadfence();
                 const float4 *o2 = reinterpret_cast<const float4 *>(ws.o_part) + rk * n_cl * total4;
@@ -831,7 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         // exactly once (claims are compare-and-swap) whatever the
         // co-residency.  The last CTA to leave returns the counters to zero.
         __threadfence();
-        __syncthreads();
+        sync_consumers();
         int32_t *ctr = ws.counters + (bt * H_kv + g) * slice_stride;  // arrivals, departures, claims
         if (tid == 0) {
             const bool last = atomicAdd(ctr, 1) == n_split - 1;
@@ -840,7 +963,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
             flags[1] = last;
             flags[2] = all_in && atomicCAS(ctr + 2 + split, 0, 1) == 0;
         }
-        __syncthreads();
+        sync_consumers();
         const bool last = flags[1] != 0;
         const bool mine = flags[2] != 0;
         const int total4 = G * D4;
@@ -878,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
                 const int hh = e / n_split, s2 = e - hh * n_split;
                 sw[e] = __ldcg(ws.lse_part + (row_q0 + h0 + hh) * n_split + s2);
             }
-            __syncthreads();
+            sync_consumers();
             for (int hh = warp; hh < nh; hh += kConsumerWarps) {
                 float *x = sw + hh * n_split;
                 float M = -INFINITY;
@@ -896,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
                     x[s2] = (sum > 0.f && x[s2] != -INFINITY) ? exp2f(x[s2] - lse_tot) : 0.f;
                 if (lane == 0 && lse && (h0 + hh) * D4 >= lo4) lse[row_q0 + h0 + hh] = lse_tot * kLn2;
             }
-            __syncthreads();
+            sync_consumers();
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             if (r < R) {
                 const float *wh = sw + (h - h0) * n_split;
@@ -922,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
                 }
             }
             red[tid] = acc;
-            __syncthreads();
+            sync_consumers();
             if (tid < nel) {
                 float4 t = red[tid];
                 for (int rr = 1; rr < R; ++rr) {
@@ -934,17 +1057,17 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
                 }
                 reinterpret_cast<float4 *>(out + (row_q0 + h) * D)[d4] = t;
             }
-            __syncthreads();  // sw and red are reused by the next slice
+            sync_consumers();  // sw and red are reused by the next slice
         };
         if (mine) slice_merge(split);
         if (last) {
             for (int s2 = tid; s2 < n_split; s2 += kThreads)
                 claim[s2] = (s2 != split && atomicCAS(ctr + 2 + s2, 0, 2) == 0) ? 1 : 0;
-            __syncthreads();
+            sync_consumers();
             for (int s2 = 0; s2 < n_split; ++s2)
                 if (claim[s2]) slice_merge(s2);
         }
-        __syncthreads();
+        sync_consumers();
         if (tid == 0 && atomicAdd(ctr + 1, 1) == n_split - 1)
             for (int i = 0; i < 2 + n_split; ++i) ctr[i] = 0;  // ready for the next call
         return;
@@ -952,12 +1075,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
 
     // ------------------------------------------ ticket; the last CTA merges
     __threadfence();
-    __syncthreads();
+    sync_consumers();
     if (tid == 0) {
         const int32_t ticket = atomicAdd(&ws.counters[bt * H_kv + g], 1);
         flags[0] = (ticket == n_split - 1);
     }
-    __syncthreads();
+    sync_consumers();
     if (!flags[0]) return;
     __threadfence();
 
@@ -966,7 +1089,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         const int h = e / n_split, s2 = e - h * n_split;
         wts[h * n_split + s2] = __ldcg(ws.lse_part + (row_q0 + h) * n_split + s2);
     }
-    __syncthreads();
+    sync_consumers();
     for (int h = warp; h < G; h += kConsumerWarps) {
         float M = -INFINITY;
         for (int s2 = lane; s2 < n_split; s2 += 32) M = fmaxf(M, wts[h * n_split + s2]);
@@ -990,7 +1113,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
         }
         if (lane == 0 && lse) lse[row_q0 + h] = lse_tot * kLn2;
     }
-    __syncthreads();
+    sync_consumers();
     constexpr int kUnroll = 8;
     for (int e = tid; e < G * D4; e += kThreads) {
         const int h = e / D4, d4 = e - h * D4;
@@ -1028,21 +1151,28 @@ __global__ void __launch_bounds__(kThreads, 1) split_decode_kernel(
 // device `dev` (0: none; cached per device and size).
 // Sets the kernel attributes (large dynamic shared memory, non-portable
 // cluster sizes) once per device for one kernel instance.
-template <int D, bool A, bool X, bool F = false, bool RG = false>
+template <int D, bool A, bool X, bool F = false, bool RG = false, bool WS = false>
 bool prepare_kernel(int dev) {
     static int8_t done[64] = {};
     if (dev < 0 || dev >= 64) return false;
     if (done[dev]) return done[dev] > 0;
-    const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG>,
+    const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<D, F>::kSmemBytes) == cudaSuccess &&
-                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG>,
+                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS>,
                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG>,
+                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS>,
                                          cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
     cudaGetLastError();
     done[dev] = ok ? 1 : -1;
     return ok;
+}
+
+// Sets the instance's attributes (once per device) and launches it.
+template <int D, bool A, bool X, bool F, bool RG, bool WS, typename... Args>
+cudaError_t launch_instance(int dev, const cudaLaunchConfig_t *cfg, Args... args) {
+    if (!prepare_kernel<D, A, X, F, RG, WS>(dev)) return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(cfg, split_decode_kernel<D, A, X, F, RG, WS>, args...);
 }
 
 template <int D, bool F = false>
@@ -1108,16 +1238,13 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     const bool append = ap.n_new > 0;
     const bool extend = ev.seq_lens != nullptr;
     const bool ring = rv.seq_lens != nullptr;
-    bool prepared;
-    if (F)
-        prepared = prepare_kernel<D, false, false, true>(dev);
-    else if (ring)
-        prepared = append ? prepare_kernel<D, true, false, false, true>(dev)
-                          : prepare_kernel<D, false, false, false, true>(dev);
-    else
-        prepared = append ? prepare_kernel<D, true, false>(dev)
-                          : (extend ? prepare_kernel<D, false, true>(dev) : prepare_kernel<D, false, false>(dev));
-    if (!prepared) return WMTP_ECUDA;
+    // fp8 rows of at least four key tiles per split: the warp-specialised
+    // instance (producer warps issue the copies, so the E4M3 widening and
+    // the MMAs never hold up the next copies); same results bit for bit.
+    // The bf16 instances keep their per-warp pipelines (measured faster:
+    // their math per byte is half the fp8 path's).
+    const bool use_ws = F && table_stride >= (int64_t)kWsMinKeysPerSplit * n_split;
+    if (!prepare_kernel<D, false, false, F>(dev)) return WMTP_ECUDA;  // cluster and residency queries
     // Cluster size: all splits in one cluster, else the largest cluster that
     // divides n_split into at most kMaxClusters clusters, provided the device
     // holds every cluster of the launch at once (clusters that wait for a
@@ -1152,20 +1279,27 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     if (n_split > 1 && csz == 0) ws = carve(workspace, rows_q, rows_kv, n_split);
     if (csz && n_split / csz > 1) ws = carve_two_level(workspace, rows_q, rows_kv, D, n_split, n_split / csz);
     const float scale_log2 = scale * 1.4426950408889634f;
-    PdlLaunch launch(dim3((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q)), dim3(kThreads),
+    PdlLaunch launch(dim3((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q)), dim3(use_ws ? kWsThreads : kThreads),
                      C::kSmemBytes, stream);
     if (csz) launch.add_cluster((unsigned)csz);
-    const cudaError_t err = cudaLaunchKernelEx(
-        &launch.cfg,
-        F      ? split_decode_kernel<D, false, false, true>
-        : ring ? (append ? split_decode_kernel<D, true, false, false, true>
-                         : split_decode_kernel<D, false, false, false, true>)
-               : (append ? split_decode_kernel<D, true, false, false>
-                         : (extend ? split_decode_kernel<D, false, true, false>
-                                   : split_decode_kernel<D, false, false, false>)),
-        reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q, H_kv, H_q / H_kv, k_pool, v_pool,
-        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, (int32_t)slice, ap, ev,
-        fv, rv);
+#define WMTP_ATTN_ARGS                                                                                          \
+    dev, &launch.cfg, reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q, H_kv, H_q / H_kv, k_pool, v_pool, \
+        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, (int32_t)slice, ap, ev, fv, rv
+    cudaError_t err;
+    if constexpr (F) {
+        err = use_ws ? launch_instance<D, false, false, true, false, true>(WMTP_ATTN_ARGS)
+                 : launch_instance<D, false, false, true, false, false>(WMTP_ATTN_ARGS);
+    } else if (ring) {
+        err = append ? launch_instance<D, true, false, false, true, false>(WMTP_ATTN_ARGS)
+                     : launch_instance<D, false, false, false, true, false>(WMTP_ATTN_ARGS);
+    } else if (append) {
+        err = launch_instance<D, true, false, false, false, false>(WMTP_ATTN_ARGS);
+    } else if (extend) {
+        err = launch_instance<D, false, true, false, false, false>(WMTP_ATTN_ARGS);
+    } else {
+        err = launch_instance<D, false, false, false, false, false>(WMTP_ATTN_ARGS);
+    }
+#undef WMTP_ATTN_ARGS
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
