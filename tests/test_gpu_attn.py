@@ -52,7 +52,9 @@ def test_attn_sizes_and_splits(D, H_q, H_kv):
         lens = torch.tensor([L, max(L - 7, 0), min(L + 5, num_slots)], dtype=torch.int32, device=DEV)
         # n_split <= 16 merges through one thread-block cluster; 18, 24, 64
         # and 128 in two levels (clusters of 9, 12, 16 and 16; 2 to 8
-        # clusters); 37 and 136 through the workspace ticket in split order
+        # clusters) where the device holds them; 37 and 136 have no cluster
+        # plan: the slice merge where the whole grid fits on the device, else
+        # the last CTA in split order
         for n_split in (1, 2, 3, 7, 16, 18, 24, 37, 64, 128, 136, None):
             out, lse, ro, rl = _run_both(q, kp, vp, table, lens, 1 / math.sqrt(D), n_split)
             assert_attn_close(out, lse, ro, rl, what=f"D={D} G={H_q // H_kv} L={L} split={n_split}")
@@ -71,6 +73,33 @@ def test_attn_many_query_tokens_and_empty_rows():
         out, lse, ro, rl = _run_both(q, kp, vp, table, lens, 0.0625, n_split)
         assert_attn_close(out, lse, ro, rl, what=f"n_q=3 split={n_split}")
         assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_attn_slice_merge_against_oracle_and_last_cta_merge(D):
+    """Split counts with no cluster plan at B = 1 (every split merging its
+    own output slice after the others arrive, when the grid fits on the
+    device), including plans that leave trailing splits empty, against the
+    fp64 oracle and against the last-CTA merge of the same partials (the
+    workspace-free entry point always merges that way)."""
+    H_q, H_kv = 16, 2
+    num_slots = 12_000
+    kp = synth.normal_bf16((num_slots, H_kv, D), 51, DEV)
+    vp = synth.normal_bf16((num_slots, H_kv, D), 52, DEV)
+    q = synth.normal_bf16((1, 1, H_q, D), 53, DEV)
+    table = synth.permutation(num_slots, 54, DEV).view(1, -1)
+    for L, n_split in ((11_999, 17), (11_999, 37), (9_000, 76), (4_000, 76), (11_999, 101), (5_000, 151)):
+        lens = torch.tensor([L], dtype=torch.int32, device=DEV)
+        out, lse, ro, rl = _run_both(q, kp, vp, table, lens, 1 / math.sqrt(D), n_split)
+        assert_attn_close(out, lse, ro, rl, what=f"D={D} L={L} split={n_split}")
+        o2 = torch.empty_like(out)
+        l2 = torch.empty_like(lse)
+        wm.draft_decode_attn_noalloc(q, kp, vp, table, lens, 1 / math.sqrt(D), o2, l2, n_split)
+        torch.testing.assert_close(out, o2, atol=2e-3, rtol=1e-2)
+        torch.testing.assert_close(lse, l2, atol=2e-3, rtol=1e-2)
+        # repeatable bit for bit (the counters are back at zero after each call)
+        out_b, lse_b = wm.draft_decode_attn(q, kp, vp, table, lens, 1 / math.sqrt(D), n_split=n_split)
+        assert torch.equal(out, out_b) and torch.equal(lse, lse_b)
 
 
 def test_attn_maximum_split_count():
