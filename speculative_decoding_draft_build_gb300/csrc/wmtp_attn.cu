@@ -85,10 +85,18 @@ __device__ __forceinline__ void sync_consumers() { asm volatile("bar.sync 1, 128
 #define WMTP_FP8_STAGES 6
 #endif
 
-template <int D, bool kFp8 = false>
+template <int D, bool kFp8 = false, bool kSwzTiles = false>
 struct Cfg {
     static constexpr int kRowBytes = D * (kFp8 ? 1 : 2);  // one K (or V) row of one head
-    static constexpr int kPitch = kRowBytes + 16;         // padded: conflict-free ldmatrix
+    // Ring instances (bf16): 16 rows per warp as D/64 blocks of 16 x 128
+    // bytes in the 128-byte-swizzled layout a TMA box writes (16-byte chunk c
+    // of row r at ((c ^ r % 8) << 4)), conflict-free for ldmatrix, so that a
+    // warp's keys in consecutive ring slots arrive as TMA boxes.  Table
+    // instances: rows padded by 16 bytes (every key a row copy: a random
+    // page table has no runs, and the padded layout measured faster there).
+    static constexpr bool kSwz = kSwzTiles && !kFp8;
+    static constexpr int kPitch = kSwz ? kRowBytes : kRowBytes + 16;
+    static constexpr int kBlockBytes = kKeysPerWarp * 128;  // one 64-dimension block of a warp tile
     // fp8 rows are half as long: more stages keep as many bytes in flight
     static constexpr int kStages = kFp8 ? WMTP_FP8_STAGES : 3;
     static constexpr int kWarpTile = kKeysPerWarp * kPitch;     // 16 rows of K (or V)
@@ -107,7 +115,10 @@ struct Cfg {
     static constexpr int kFlagOffset = kMaskOffset + kConsumerWarps * kStages * 4;
     // warp-specialised instances: a full and an empty mbarrier per stage
     static constexpr int kBarOffset = (kFlagOffset + 16 + 7) / 8 * 8;
-    static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8;
+    // swizzled tiles: one TMA mbarrier per warp and stage
+    static constexpr int kTmaBarOffset = kBarOffset + 2 * kStages * 8;
+    // + slack to align the base of the swizzled tiles to 1024 bytes
+    static constexpr int kSmemBytes = kTmaBarOffset + kConsumerWarps * kStages * 8 + (kSwz ? 1024 : 0);
 };
 
 // Workspace: a counter region of kMaxClusterMerge int32 per (row, KV head),
@@ -228,18 +239,31 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
     int64_t num_slots, const int32_t *__restrict__ table, int64_t table_stride,
     const int32_t *__restrict__ lens, float scale_log2, float *__restrict__ out,
     float *__restrict__ lse, WorkspaceView ws, int32_t n_split, int32_t csz, int32_t slice_stride,
-    AppendView ap, ExtendView ev, Fp8View fv, RingView rv) {
+    AppendView ap, ExtendView ev, Fp8View fv, RingView rv, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, int32_t tma_ok) {
     static_assert(!(kFp8 && (kAppend || kExtend)), "the fp8 path appends with its own kernel");
     static_assert(!(kRing && (kExtend || kFp8)), "ring launches are bf16 decode steps");
-    using C = Cfg<D, kFp8>;
+    using C = Cfg<D, kFp8, kRing>;
     constexpr int S = C::kStages;
     constexpr int R = C::kRingTiles;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = C::kSwz ? reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))
+                            : smem_raw;
     uint32_t *masks = reinterpret_cast<uint32_t *>(smem + C::kMaskOffset);
+    uint64_t *tma_bars = reinterpret_cast<uint64_t *>(smem + C::kTmaBarOffset);  // [warp][stage]
     volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(smem + C::kFlagOffset);
     uint64_t *ws_bars = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);  // [S] full, then [S] empty
 
     griddep_launch_dependents();
+    if constexpr (C::kSwz) {
+        // one arrival per use: the issuing lane's (with the TMA byte count
+        // when the warp's keys arrive as boxes)
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < kConsumerWarps * S; ++i) mbar_init(smem_addr(tma_bars + i), 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+    }
     if constexpr (kWs) {
         // full: per producer warp, 32 copy-completion arrivals of its lanes
         // and one after its key mask is stored; empty: one per consumer warp
@@ -439,6 +463,31 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
         if (lane == 0) masks[warp * S + st] = vm;
         const uint32_t kdst = wsm_addr + st * C::kWarpStage;
         const uint32_t vdst = kdst + C::kWarpTile;
+        if constexpr (C::kSwz) {
+            // 16 valid keys in 16 consecutive pool slots (a ring window, an
+            // identity page table), none of them appended by this launch:
+            // the warp's K and V rows come in as D/64 TMA boxes each (64
+            // dims x 1 head x 16 slots, 128-byte swizzle).  The stage's TMA
+            // barrier completes one phase per use either way.
+            const uint32_t tbar = smem_addr(tma_bars + warp * S + st);
+            const int32_t s0 = __shfl_sync(0xffffffffu, src_slot, 0);
+            const bool whole = tma_ok && vm == 0xffffu && s0 >= 0 &&
+                               __all_sync(0xffffffffu, lane >= kKeysPerWarp || src_slot == s0 + lane);
+            if (whole) {
+                fence_proxy_async_smem();  // this warp's reads of the stage's previous rows come first
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(tbar, 2u * kKeysPerWarp * C::kRowBytes);
+#pragma unroll
+                    for (int db = 0; db < D / 64; ++db) {
+                        tma_load_3d(kdst + db * C::kBlockBytes, &tm_k, db * 64, g, s0, tbar);
+                        tma_load_3d(vdst + db * C::kBlockBytes, &tm_v, db * 64, g, s0, tbar);
+                    }
+                }
+                return;
+            }
+            if (lane == 0) mbar_arrive(tbar);
+        }
         constexpr int kLanesPerRow = C::kRowBytes / 16;  // 32 (D=256) or 16 (D=128)
         constexpr int kRowsPerInst = 32 / kLanesPerRow;
         const int sub = lane / kLanesPerRow;
@@ -457,8 +506,12 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
                 ksrc = kbase + off;
                 vsrc = vbase + off;
             }
-            cp_async_16(kdst + key * C::kPitch + col, ksrc, kv ? 16u : 0u, policy);
-            cp_async_16(vdst + key * C::kPitch + col, vsrc, kv ? 16u : 0u, policy);
+            // swizzled: chunk c of row `key` in block c / 8 at ((c % 8) ^ (key % 8)) * 16
+            const int chunk = col >> 4;
+            const uint32_t dofs = C::kSwz ? (uint32_t)((chunk >> 3) * C::kBlockBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4))
+                                          : (uint32_t)(key * C::kPitch + col);
+            cp_async_16(kdst + dofs, ksrc, kv ? 16u : 0u, policy);
+            cp_async_16(vdst + dofs, vsrc, kv ? 16u : 0u, policy);
         }
     };
 
@@ -581,6 +634,19 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
 
     const uint32_t k_off = (uint32_t)((lane & 15) * C::kPitch + (lane >> 4) * 16);
     const uint32_t v_off = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * C::kPitch + ((lane >> 3) & 1) * 16);
+    // swizzled tiles: this lane's ldmatrix row address for the 16-dimension
+    // step kd lies in block kd / 4 at an in-block offset that repeats every
+    // four steps
+    uint32_t kso[4], vso[4];
+    if constexpr (C::kSwz) {
+        const int kr = lane & 15, ks = lane >> 4;
+        const int vr = (lane & 7) + ((lane >> 4) << 3), vs = (lane >> 3) & 1;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            kso[i] = (uint32_t)(kr * 128 + (((2 * i + ks) ^ (kr & 7)) << 4));
+            vso[i] = (uint32_t)(vr * 128 + (((2 * i + vs) ^ (vr & 7)) << 4));
+        }
+    }
 
     for (int it = 0; it < n_tiles; ++it) {
         if constexpr (kWs) {
@@ -600,6 +666,14 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
             if (it + 2 * S - 1 < n_tiles) fetch_slots(it + 2 * S - 1);
             cp_async_commit();
             cp_async_wait<S - 1>();
+            if constexpr (C::kSwz) {
+                // the stage's TMA boxes (if its keys came that way) have landed
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(tma_bars + warp * S + it % S), (it / S) & 1,
+                                                                kWsWaitNs))) {
+                    if (lane == 0) latch(WMTP_DEV_WAIT_TIMEOUT);
+                    break;
+                }
+            }
         }
         __syncwarp();
         const int st = it % S;
@@ -607,6 +681,8 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
         if (wm) {
             const uint32_t kaddr = wsm_addr + st * C::kWarpStage + k_off;
             const uint32_t vaddr = wsm_addr + st * C::kWarpStage + C::kWarpTile + (kFp8 ? k_off : v_off);
+            const uint32_t kbase_s = wsm_addr + st * C::kWarpStage;   // swizzled tiles
+            const uint32_t vbase_s = kbase_s + C::kWarpTile;
             // Four independent accumulation chains over the head dimension.
             float sacc[4][4] = {};
             if constexpr (kFp8) {
@@ -629,7 +705,10 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
 #pragma unroll
                 for (int kd = 0; kd < KD; ++kd) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kaddr + kd * 32, a0, a1, a2, a3);
+                    if constexpr (C::kSwz)
+                        ldsm_x4(kbase_s + (kd >> 2) * C::kBlockBytes + kso[kd & 3], a0, a1, a2, a3);
+                    else
+                        ldsm_x4(kaddr + kd * 32, a0, a1, a2, a3);
                     mma_bf16_16816(sacc[kd & 3], a0, a1, a2, a3, qf[kd][0], qf[kd][1]);
                 }
             }
@@ -702,7 +781,10 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
 #pragma unroll
                 for (int dt = 0; dt < KD; ++dt) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4_trans(vaddr + dt * 32, a0, a1, a2, a3);
+                    if constexpr (C::kSwz)
+                        ldsm_x4_trans(vbase_s + (dt >> 2) * C::kBlockBytes + vso[dt & 3], a0, a1, a2, a3);
+                    else
+                        ldsm_x4_trans(vaddr + dt * 32, a0, a1, a2, a3);
                     mma_bf16_16816(o[dt], a0, a1, a2, a3, ph0, ph1);
                     mma_bf16_16816(o[dt], a0, a1, a2, a3, pl0, pl1);
                 }
@@ -1158,7 +1240,7 @@ bool prepare_kernel(int dev) {
     if (done[dev]) return done[dev] > 0;
     const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<D, F>::kSmemBytes) == cudaSuccess &&
+                                         Cfg<D, F, RG>::kSmemBytes) == cudaSuccess &&
                     cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS>,
                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
                     cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS>,
@@ -1280,11 +1362,21 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     if (csz && n_split / csz > 1) ws = carve_two_level(workspace, rows_q, rows_kv, D, n_split, n_split / csz);
     const float scale_log2 = scale * 1.4426950408889634f;
     PdlLaunch launch(dim3((unsigned)n_split, (unsigned)H_kv, (unsigned)(B * n_q)), dim3(use_ws ? kWsThreads : kThreads),
-                     C::kSmemBytes, stream);
+                     ring ? Cfg<D, F, true>::kSmemBytes : C::kSmemBytes, stream);
     if (csz) launch.add_cluster((unsigned)csz);
+    // ring launches (bf16): TMA maps for warps whose 16 keys sit in
+    // consecutive ring slots
+    CUtensorMap tmk{}, tmv{};
+    int32_t tma_ok = 0;
+    if (!F && ring) {
+        if (num_slots <= INT32_MAX && pool_tensor_map(&tmk, k_pool, num_slots, H_kv, D, kKeysPerWarp) &&
+            pool_tensor_map(&tmv, v_pool, num_slots, H_kv, D, kKeysPerWarp))
+            tma_ok = 1;
+    }
 #define WMTP_ATTN_ARGS                                                                                          \
     dev, &launch.cfg, reinterpret_cast<const __nv_bfloat16 *>(q), n_q, H_q, H_kv, H_q / H_kv, k_pool, v_pool, \
-        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, (int32_t)slice, ap, ev, fv, rv
+        num_slots, table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)csz, (int32_t)slice, ap, ev, fv, rv, \
+        tmk, tmv, tma_ok
     cudaError_t err;
     if constexpr (F) {
         err = use_ws ? launch_instance<D, false, false, true, false, true>(WMTP_ATTN_ARGS)
@@ -1373,7 +1465,7 @@ wmtp_status launch_split_decode_noalloc(const uint16_t *q, int32_t B, int32_t n_
         H_q, H_kv, H_q / H_kv, static_cast<const void *>(k_pool), static_cast<const void *>(v_pool), num_slots,
         table, table_stride, lens, scale_log2, out, lse, ws, n_split, (int32_t)0, (int32_t)0,
         AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0}, ExtendView{nullptr, nullptr, 0, 0, 0},
-        Fp8View{nullptr, nullptr}, RingView{nullptr, nullptr, 0, 0, 0, 0, 0});
+        Fp8View{nullptr, nullptr}, RingView{nullptr, nullptr, 0, 0, 0, 0, 0}, CUtensorMap{}, CUtensorMap{}, (int32_t)0);
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 

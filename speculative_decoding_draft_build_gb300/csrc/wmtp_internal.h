@@ -2,12 +2,18 @@
 // units (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "wmtp.h"
 
 namespace wmtp {
+
+// 3-D TMA map of a [num_slots][H_kv][D] bf16 pool: boxes of 64 dims x 1 head
+// x `rows` consecutive slots, 128-byte swizzle (defined in wmtp_tree.cu).
+// False if the driver entry point is missing or the encoding is refused.
+bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t num_slots, int H_kv, int D, int rows);
 
 // Each translation unit keeps its own device error word (no relocatable
 // device code is needed); these read-and-optionally-clear them.

@@ -799,6 +799,11 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
+}  // namespace
+}  // namespace wmtp
+
+namespace wmtp {
+
 // 3-D map of a [num_slots][H_kv][D] bf16 pool: boxes of 64 dims x 1 head x
 // `rows` consecutive slots, 128-byte swizzle.
 bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t num_slots, int H_kv, int D, int rows) {
@@ -812,6 +817,11 @@ bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t num_slots, int 
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+}  // namespace wmtp
+
+namespace wmtp {
+namespace {
 
 template <int D>
 bool tree_cluster_ok(int dev, int n) {
