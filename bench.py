@@ -269,7 +269,12 @@ class Workload:
         self.flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize(dev)
 
-    def full_arm(self, events=None, attn_only=False, n_split=None):
+    # overlap=True: chained steps; steps after the first start their copies
+    # while the step before finishes (overlap_hold=2: the previous step's key
+    # and the step's own wait for it); step 0 follows the index build, which
+    # writes its table, so it reads nothing early (-1) but, like every
+    # chained step, releases the next step only after its own wait.
+    def full_arm(self, events=None, attn_only=False, n_split=None, overlap=False):
         import speculative_decoding_draft_build_gb300 as wm
         c = self.cfg
         if not attn_only:
@@ -282,11 +287,12 @@ class Workload:
             wm.draft_decode_attn_append(self.kn[j], self.vn[j], self.slots[j],
                                         self.q[j], self.kp, self.vp, self.tab_full[j], self.len_full[j],
                                         self.scale, out=self.out_full[j], lse=self.lse_full[j],
-                                        n_split=n_split or self.ns_full, workspace=self.ws_full)
+                                        n_split=n_split or self.ns_full, workspace=self.ws_full,
+                                        overlap_hold=(2 if j > 0 else -1) if overlap else None)
             if events is not None:
                 events[j][1].record()
 
-    def win_arm(self, events=None, attn_only=False, n_split=None):
+    def win_arm(self, events=None, attn_only=False, n_split=None, overlap=False):
         import speculative_decoding_draft_build_gb300 as wm
         c = self.cfg
         if not attn_only:
@@ -302,7 +308,8 @@ class Workload:
             wm.draft_decode_attn_append(self.kn[j], self.vn[j], self.slots[j],
                                         self.q[j], self.kp, self.vp, self.tab_win[j], self.len_win[j],
                                         self.scale, out=self.out_win[j], lse=self.lse_win[j],
-                                        n_split=n_split or self.ns_win, workspace=ws)
+                                        n_split=n_split or self.ns_win, workspace=ws,
+                                        overlap_hold=(2 if j > 0 else -1) if overlap else None)
             if events is not None:
                 events[j][1].record()
 
@@ -389,14 +396,18 @@ def run_ours(args, dist_ctx):
 
     # windowed arm as a CUDA graph (its kernels take microseconds)
     graph = graph_of(w.win_arm, dev)
+    # the same step as chained launches (bit-identical results)
+    graph_chain = graph_of(lambda: w.win_arm(overlap=True), dev)
     for _ in range(max(args.warmup, 1)):
         graph.replay()
+        graph_chain.replay()
     torch.cuda.synchronize(dev)
 
     K = args.steps
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     e_full = [[ev(), ev()] for _ in range(K)]
     e_win = [[ev(), ev()] for _ in range(K)]
+    e_chain = [[ev(), ev()] for _ in range(K)]
     e_attn = [[[ev(), ev()] for _ in range(g)] for _ in range(K)]
     sampler = ClockSampler(dev.index)
     dist_ctx.barrier()
@@ -412,6 +423,10 @@ def run_ours(args, dist_ctx):
         e_win[k][0].record()
         graph.replay()
         e_win[k][1].record()
+        w.flush.zero_()
+        e_chain[k][0].record()
+        graph_chain.replay()
+        e_chain[k][1].record()
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t0
     dist_ctx.barrier()
@@ -419,6 +434,7 @@ def run_ours(args, dist_ctx):
 
     full_ms = [a.elapsed_time(b) for a, b in e_full]
     win_ms = [a.elapsed_time(b) for a, b in e_win]
+    chain_ms = [a.elapsed_time(b) for a, b in e_chain]
     attn_full_ms = [[e_attn[k][j][0].elapsed_time(e_attn[k][j][1]) for j in range(g)] for k in range(K)]
     # median over the launches: the first launch of a step can start after a
     # host-side gap (its Python call is prepared while the index build runs)
@@ -436,9 +452,9 @@ def run_ours(args, dist_ctx):
     full_bytes = sum(w.bytes_full_attn(j) for j in range(g))
     win_bytes = sum(w.bytes_win_attn(j) for j in range(g))
     stats = [statistics.median(full_ms), statistics.median(win_ms), full_attn_mean_ms,
-             win_attn_mean_ms, wall]
+             win_attn_mean_ms, wall, statistics.median(chain_ms)]
     stats = dist_ctx.max(stats)
-    full_step_ms, win_step_ms, full_attn_ms_max, win_attn_ms_max, wall_max = stats
+    full_step_ms, win_step_ms, full_attn_ms_max, win_attn_ms_max, wall_max, chain_step_ms = stats
 
     peak, peak_kind = hbm_peak()
     full_gbs = (full_bytes / g) / (full_attn_ms_max * 1e-3) / 1e9
@@ -471,6 +487,7 @@ def run_ours(args, dist_ctx):
         "arms": {
             "windowed": {
                 "us_per_step": round(win_step_ms * 1e3, 3),
+                "us_per_step_chained": round(chain_step_ms * 1e3, 3),
                 "attn_us_per_launch": round(win_attn_ms_max * 1e3, 3),
                 "attn_us_per_step": round(win_attn_ms_max * 1e3 * g, 3),
                 "keys_per_launch": min(cfg["S"] + 1, cfg["n_sink"] + cfg["W"]),
@@ -488,7 +505,7 @@ def run_ours(args, dist_ctx):
                 "kv_gbs": round(full_gbs, 1),
                 "frac_of_hbm": round(full_gbs / peak, 4),
                 "n_split": w.ns_full,
-                "launch": "direct",
+                "launch": "direct, an event pair around each launch",
             },
         },
         "roofline": {
@@ -562,10 +579,16 @@ def measure_arms(w, args, dev, o=None):
         arm()
         torch.cuda.synchronize(dev)
         t_step = time_graph(graph_of(arm, dev), w.flush, reps, dev)
+        t_chain_step = time_graph(graph_of(lambda: arm(overlap=True), dev), w.flush, reps, dev)
+        # per launch: each launch's own duration (no overlap), and the time
+        # per launch of the chained launches
         t_attn = time_graph(graph_of(lambda: arm(attn_only=True), dev), w.flush, reps, dev) / g
+        t_chain = time_graph(graph_of(lambda: arm(attn_only=True, overlap=True), dev), w.flush, reps, dev) / g
         nbytes = sum(nbytes_fn(j) for j in range(g)) / g
         gbs = nbytes / (t_attn * 1e-6) / 1e9
-        res[name] = {"us_per_step": round(t_step, 3), "attn_us_per_launch": round(t_attn, 3),
+        res[name] = {"us_per_step": round(t_step, 3), "us_per_step_chained": round(t_chain_step, 3),
+                     "attn_us_per_launch": round(t_attn, 3),
+                     "attn_us_per_launch_chained": round(t_chain, 3),
                      "keys_per_launch": keys, "kv_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
                      "bytes_per_launch": int(nbytes), "n_split": ns}
         if o is not None:
@@ -574,7 +597,8 @@ def measure_arms(w, args, dev, o=None):
             res[name]["oracle_host_us_per_step"] = round((time.perf_counter() - t) * 1e6, 1)
     if o is not None:
         res["oracle_cores"] = o.num_threads()
-    res["timing"] = "CUDA graph replays, L2 flushed before each, median"
+    res["timing"] = ("CUDA graph replays, L2 flushed before each, median; *_chained: the same launches as "
+                     "chained steps (steps 2-6 copy their keys while the step before finishes)")
     return res
 
 
@@ -639,13 +663,15 @@ class RingBatch:
     def ring_steps(self):
         """The ring layout without tables: each step's slots come from the
         ring rule in the kernel (its window arrives in TMA boxes), the step's
-        own K/V appended in the same launch."""
+        own K/V appended in the same launch; chained steps (steps 2-6 copy
+        their keys while the step before finishes)."""
         import speculative_decoding_draft_build_gb300 as wm
         c = self.cfg
         for j in range(c["gamma"]):
             wm.draft_decode_attn_ring(self.q[j], self.ring_k, self.ring_v, self.seq, self.ring_base, j, c["n_sink"],
                                       c["W"], c["d"], self.scale, k_new=self.kn[j], v_new=self.vn[j],
-                                      out=self.out_ring[j], lse=self.lse_ring[j], n_split=self.ns, workspace=self.ws)
+                                      out=self.out_ring[j], lse=self.lse_ring[j], n_split=self.ns, workspace=self.ws,
+                                      overlap_hold=2 if j > 0 else -1)
 
     def arm(self, ring=True, attn_only=False):
         import speculative_decoding_draft_build_gb300 as wm
@@ -695,8 +721,9 @@ def measure_ring_batch(args, dev, o=None):
                        "W=4032, d=7, ring of 4103 slots per request at seeded ring bases, gamma=6",
            "S": rb.S_list, "us_per_step": round(t_step, 3), "us_per_launch": round(t_step / g, 3),
            "kv_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4), "bytes_per_launch": int(nbytes),
-           "n_split": rb.ns, "path": "table-free ring steps (slots from the ring rule, TMA boxes for runs of "
-                                     "consecutive ring slots), fused append",
+           "n_split": rb.ns, "path": "table-free chained ring steps (slots from the ring rule, TMA boxes for runs of "
+                                     "consecutive ring slots; steps 2-6 copy while the step before finishes), "
+                                     "fused append",
            "ring_via_tables_us_per_step": round(t_tab, 3),
            "unringed_flat_pool_us_per_step": round(t_flat, 3),
            "ring_equals_unringed_bitwise": same and same_tables,
@@ -985,7 +1012,7 @@ def measure_ring(w, args, dev):
         for j in range(g):
             wm.draft_decode_attn_ring(w.q[j], ring_k, ring_v, w.seq, ring_base, j, n_sink, W, d, w.scale,
                                       k_new=w.kn[j], v_new=w.vn[j], out=out[j], lse=lse[j], n_split=ns,
-                                      workspace=ws)
+                                      workspace=ws, overlap_hold=2 if j > 0 else -1)
     for _ in range(3):
         step()
     torch.cuda.synchronize(dev)
@@ -1012,7 +1039,7 @@ def measure_ring(w, args, dev):
             "step": {"us_per_step": round(t_step, 3), "us_per_launch": round(t_step / g, 3),
                      "launches": g, "kv_gbs": round(step_bytes / (t_step * 1e-6) / 1e9, 1),
                      "frac_of_hbm": round(step_bytes / (t_step * 1e-6) / 1e9 / peak, 4),
-                     "launch": "cuda graph, no index build, no table"},
+                     "launch": "cuda graph, no index build, no table; chained steps (steps 2-6 copy while the step before finishes)"},
             "timing": "CUDA events, L2 flushed before each, median"}
 
 

@@ -282,6 +282,43 @@ wmtp_status wmtp_draft_decode_attn_append(const uint16_t *k_new,
                                           void *workspace, size_t workspace_bytes,
                                           int32_t n_split, void *stream);
 
+/* A chained draft step: wmtp_draft_decode_attn_append whose launch starts
+ * copying keys while the preceding kernel on the stream is still running.
+ * The draft forwards of one decode step run back to back (§3 Eq. (1): gamma
+ * forwards, each re-reading the draft KV), and step j + 1 reads the same
+ * kept keys as step j except the newest one or two, so their copies need
+ * not wait for step j to finish.
+ *
+ * Ordering (programmatic dependent launch): a launch may begin once the
+ * preceding kernel on the stream has released its dependents.  This call
+ * releases them only after it has waited for its own predecessor, so the
+ * launch that follows it overlaps this launch alone; the other calls of
+ * this library release them as soon as they start.
+ * hold = -1: nothing is read before the preceding kernel has completed (a
+ *            safe first step of a chain, e.g. after the index builder).
+ * hold >= 0: lens, table, new_slots and the K/V rows of the entries below
+ *            lens[b] - hold of every row b are read before the preceding
+ *            kernel has completed; q, k_new / v_new, the rows of the last
+ *            `hold` entries and of any key whose slot is a new slot are
+ *            read, and every output written, only after it.  The caller
+ *            guarantees that no kernel that may still be running when the
+ *            launch begins writes what is read early: the preceding kernel
+ *            and, if it is not a chained launch of this library, the ones
+ *            it may overlap.  For fused steps j >= 1 of one decode step on
+ *            the same table, each issued by this call (step 0 with
+ *            hold = -1), the preceding kernel is step j - 1, which writes
+ *            the row of position S + j - 1 (entry lens[b] - 2): hold = 2.
+ * Results are bit-identical to wmtp_draft_decode_attn_append with the same
+ * arguments: only the moment of the copies changes.  Other arguments and
+ * errors as wmtp_draft_decode_attn_append; WMTP_EINVAL for hold < -1. */
+wmtp_status wmtp_draft_decode_attn_append_overlap(
+    const uint16_t *k_new, const uint16_t *v_new, const int32_t *new_slots,
+    int32_t n_new, const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
+    int32_t H_kv, int32_t D, uint16_t *k_pool, uint16_t *v_pool,
+    int64_t num_slots, const int32_t *table, int64_t table_stride,
+    const int32_t *lens, float scale, float *out, float *lse, void *workspace,
+    size_t workspace_bytes, int32_t n_split, int32_t hold, void *stream);
+
 /* Draft-extend attention: the draft forward over the n = n_new[b] tokens a
  * request accepted (positions S..S+n-1, K/V already appended), in one
  * launch.  Row t < n of request b is the attention of its query heads over
@@ -508,6 +545,22 @@ wmtp_status wmtp_draft_decode_attn_ring(
     int32_t step, int32_t n_sink, int32_t window, int32_t depth,
     int32_t tree_k, float scale, float *out, float *lse, void *workspace,
     size_t workspace_bytes, int32_t n_split, void *stream);
+
+/* wmtp_draft_decode_attn_ring as a chained step, with the ordering and
+ * the hold rule of wmtp_draft_decode_attn_append_overlap: with hold >= 0,
+ * seq_lens, ring_base and the ring rows of the kept entries below the row
+ * length minus hold are read before the preceding kernel has completed, q,
+ * k_new / v_new and the last `hold` entries after it (hold = 2 for steps
+ * >= 1 of a chain of fused ring steps, -1 for its first step).  k_new /
+ * v_new are required.  Bit-identical to wmtp_draft_decode_attn_ring;
+ * WMTP_EINVAL for hold < -1 or no k_new / v_new. */
+wmtp_status wmtp_draft_decode_attn_ring_overlap(
+    const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q, int32_t B,
+    int32_t H_q, int32_t H_kv, int32_t D, uint16_t *k_pool, uint16_t *v_pool,
+    int64_t num_slots, const int32_t *seq_lens, const int32_t *ring_base,
+    int32_t step, int32_t n_sink, int32_t window, int32_t depth,
+    int32_t tree_k, float scale, float *out, float *lse, void *workspace,
+    size_t workspace_bytes, int32_t n_split, int32_t hold, void *stream);
 
 /* ------------------------------------------------------------------------
  * fp8 KV ("Windowed-MTP", §6 "Robustness to KV-cache quantization": the

@@ -129,6 +129,11 @@ def load():
             _vp, _vp, _vp, _i32,
             _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, ctypes.c_float,
             _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
+        lib.wmtp_draft_decode_attn_append_overlap.restype = _i32
+        lib.wmtp_draft_decode_attn_append_overlap.argtypes = [
+            _vp, _vp, _vp, _i32,
+            _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, ctypes.c_float,
+            _vp, _vp, _vp, ctypes.c_size_t, _i32, _i32, _vp]
         lib.wmtp_tree_workspace_bytes.restype = ctypes.c_size_t
         lib.wmtp_tree_workspace_bytes.argtypes = [_i32] * 7
         lib.wmtp_tree_num_splits.restype = _i32
@@ -157,6 +162,10 @@ def load():
         lib.wmtp_draft_decode_attn_ring.argtypes = [
             _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
             ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _i32, _vp]
+        lib.wmtp_draft_decode_attn_ring_overlap.restype = _i32
+        lib.wmtp_draft_decode_attn_ring_overlap.argtypes = [
+            _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+            ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _i32, _i32, _vp]
         lib.wmtp_draft_decode_attn_noalloc.restype = _i32
         lib.wmtp_draft_decode_attn_noalloc.argtypes = [
             _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i64, _vp, _i64, _vp, ctypes.c_float,
@@ -464,14 +473,22 @@ def draft_decode_attn_append(k_new: torch.Tensor, v_new: torch.Tensor, new_slots
                              table: torch.Tensor, lens: torch.Tensor, scale: float,
                              out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
                              n_split: int | None = None, max_len: int | None = None,
-                             workspace: AttnWorkspace | None = None, stream=None):
+                             workspace: AttnWorkspace | None = None, stream=None,
+                             overlap_hold: int | None = None):
     """``append_kv`` then ``draft_decode_attn`` in one launch
     (``wmtp_draft_decode_attn_append``).
 
     k_new/v_new: [B, n_new, H_kv, D] bf16 (or [B, H_kv, D] for n_new = 1);
     new_slots: [B, n_new] (or [B]) int32 pool slots.  Other arguments and the
-    result as :func:`draft_decode_attn`; the pools are written."""
-    return _attn((k_new, v_new, new_slots), q, k_pool, v_pool, table, lens, scale, out, lse,
+    result as :func:`draft_decode_attn`; the pools are written.
+    ``overlap_hold`` not None: a chained step (``wmtp_draft_decode_attn_append_overlap``):
+    -1 for the first step of a chain (nothing read early), >= 0 to start the
+    copies of every entry but the last ``overlap_hold`` of a row while the
+    preceding kernel on the stream finishes (2 for steps >= 1 of consecutive
+    fused steps); same results bit for bit."""
+    if overlap_hold is not None and int(overlap_hold) < -1:
+        raise ValueError("overlap_hold must be -1 or >= 0 (None: not a chained step)")
+    return _attn((k_new, v_new, new_slots, overlap_hold), q, k_pool, v_pool, table, lens, scale, out, lse,
                  n_split, max_len, workspace, stream)
 
 
@@ -598,7 +615,7 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
                 float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf), workspace.nbytes, n_split,
                 _stream(stream)), "draft_extend_attn")
         return out, lse
-    k_new, v_new, new_slots = append
+    k_new, v_new, new_slots, hold = append
     _need(k_new, "k_new", torch.bfloat16, dev)
     _need(v_new, "v_new", torch.bfloat16, dev)
     _need(new_slots, "new_slots", torch.int32, dev)
@@ -607,11 +624,18 @@ def _attn(append, q, k_pool, v_pool, table, lens, scale, out, lse, n_split, max_
             or v_new.shape != k_new.shape or k_new.shape[-2:] != (H_kv, D)):
         raise ValueError("draft_decode_attn_append: k_new/v_new/new_slots shape mismatch")
     with _on(dev):
-        _check(load().wmtp_draft_decode_attn_append(
-            _ptr(k_new), _ptr(v_new), _ptr(new_slots), n_new,
-            _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
-            stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf),
-            workspace.nbytes, n_split, _stream(stream)), "draft_decode_attn_append")
+        if hold is None:
+            _check(load().wmtp_draft_decode_attn_append(
+                _ptr(k_new), _ptr(v_new), _ptr(new_slots), n_new,
+                _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
+                stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf),
+                workspace.nbytes, n_split, _stream(stream)), "draft_decode_attn_append")
+        else:
+            _check(load().wmtp_draft_decode_attn_append_overlap(
+                _ptr(k_new), _ptr(v_new), _ptr(new_slots), n_new,
+                _ptr(q), B, n_q, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots, _ptr(table),
+                stride, _ptr(lens), float(scale), _ptr(out), _ptr(lse), _ptr(workspace.buf),
+                workspace.nbytes, n_split, int(hold), _stream(stream)), "draft_decode_attn_append_overlap")
     return out, lse
 
 
@@ -789,10 +813,16 @@ def draft_decode_attn_ring(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
                            v_new: torch.Tensor | None = None, tree_k: int = 1,
                            out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
                            n_split: int | None = None, workspace: AttnWorkspace | None = None,
-                           stream=None):
+                           stream=None, overlap_hold: int | None = None):
     """Draft step ``step`` over the ring with no table (``wmtp_draft_decode_attn_ring``):
     q [B, 1, H_q, D] (or [B, H_q, D]) bf16; k_new/v_new [B, H_kv, D] bf16 appended at
-    position S + step first (optional).  Returns ``(out [B, 1, H_q, D], lse [B, 1, H_q])``."""
+    position S + step first (optional).  Returns ``(out [B, 1, H_q, D], lse [B, 1, H_q])``.
+    ``overlap_hold`` not None: a chained step as in :func:`draft_decode_attn_append`
+    (``wmtp_draft_decode_attn_ring_overlap``; needs k_new / v_new)."""
+    if overlap_hold is not None and int(overlap_hold) < -1:
+        raise ValueError("overlap_hold must be -1 or >= 0 (None: not a chained step)")
+    if overlap_hold is not None and k_new is None:
+        raise ValueError("draft_decode_attn_ring: a chained step appends (give k_new and v_new)")
     _need(q, "q", torch.bfloat16)
     dev = q.device
     for t, nm in ((k_pool, "k_pool"), (v_pool, "v_pool")):
@@ -831,9 +861,16 @@ def draft_decode_attn_ring(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     elif workspace.nbytes < need:
         raise ValueError(f"workspace holds {workspace.nbytes} bytes, {need} needed")
     with _on(dev):
-        _check(load().wmtp_draft_decode_attn_ring(
-            _ptr(k_new), _ptr(v_new), _ptr(q), B, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots,
-            _ptr(seq_lens), _ptr(ring_base), int(step), n_sink, window, depth, tree_k, float(scale),
-            _ptr(out), _ptr(lse), _ptr(workspace.buf), workspace.nbytes, n_split, _stream(stream)),
-            "draft_decode_attn_ring")
+        if overlap_hold is None:
+            _check(load().wmtp_draft_decode_attn_ring(
+                _ptr(k_new), _ptr(v_new), _ptr(q), B, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots,
+                _ptr(seq_lens), _ptr(ring_base), int(step), n_sink, window, depth, tree_k, float(scale),
+                _ptr(out), _ptr(lse), _ptr(workspace.buf), workspace.nbytes, n_split, _stream(stream)),
+                "draft_decode_attn_ring")
+        else:
+            _check(load().wmtp_draft_decode_attn_ring_overlap(
+                _ptr(k_new), _ptr(v_new), _ptr(q), B, H_q, H_kv, D, _ptr(k_pool), _ptr(v_pool), num_slots,
+                _ptr(seq_lens), _ptr(ring_base), int(step), n_sink, window, depth, tree_k, float(scale),
+                _ptr(out), _ptr(lse), _ptr(workspace.buf), workspace.nbytes, n_split, int(overlap_hold),
+                _stream(stream)), "draft_decode_attn_ring_overlap")
     return out, lse

@@ -46,6 +46,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "wmtp.h"
 #include "wmtp_internal.h"
@@ -163,6 +164,11 @@ inline size_t workspace_bytes(int64_t rows_q, int64_t rows_kv, int D, int n_spli
 // append.  Gathers of a key whose slot is one of its request's appended
 // slots read the new row itself, so no CTA reads a pool slot that this
 // launch writes.
+// Chained steps (chain != 0: the overlapped bf16 table and ring steps)
+// release their dependents only after their own wait.  With hold >= 0 the
+// table, lengths, slots and the K/V rows of entries below L - hold are read
+// before the preceding kernel has completed (copied while it finishes); q,
+// the new rows and the last `hold` entries of each row only after it.
 struct AppendView {
     const __nv_bfloat16 *k_new;
     const __nv_bfloat16 *v_new;
@@ -170,6 +176,8 @@ struct AppendView {
     __nv_bfloat16 *k_pool;
     __nv_bfloat16 *v_pool;
     int32_t n_new;
+    int32_t chain;
+    int32_t hold;
 };
 // Draft-extend pass: the n_q rows of request b are its new tokens at
 // positions S..S+n-1 (n = n_new[b]; rows t >= n are empty), all reading the
@@ -232,7 +240,8 @@ inline WorkspaceView carve_two_level(void *ws, int64_t rows_q, int64_t rows_kv, 
     return v;
 }
 
-template <int D, bool kAppend, bool kExtend, bool kFp8, bool kRing = false, bool kWs = false>
+template <int D, bool kAppend, bool kExtend, bool kFp8, bool kRing = false, bool kWs = false,
+          bool kChain = false>
 __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_kernel(
     const __nv_bfloat16 *__restrict__ q, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t G,
     const void *__restrict__ k_pool, const void *__restrict__ v_pool,
@@ -243,6 +252,7 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
     const __grid_constant__ CUtensorMap tm_v, int32_t tma_ok) {
     static_assert(!(kFp8 && (kAppend || kExtend)), "the fp8 path appends with its own kernel");
     static_assert(!(kRing && (kExtend || kFp8)), "ring launches are bf16 decode steps");
+    static_assert(!kChain || (kAppend && !kExtend && !kFp8 && !kWs), "chained launches are fused bf16 steps");
     using C = Cfg<D, kFp8, kRing>;
     constexpr int S = C::kStages;
     constexpr int R = C::kRingTiles;
@@ -254,7 +264,7 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
     volatile int32_t *flags = reinterpret_cast<volatile int32_t *>(smem + C::kFlagOffset);
     uint64_t *ws_bars = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);  // [S] full, then [S] empty
 
-    griddep_launch_dependents();
+    if constexpr (!kChain) griddep_launch_dependents();
     if constexpr (C::kSwz) {
         // one arrival per use: the issuing lane's (with the TMA byte count
         // when the warp's keys arrive as boxes)
@@ -278,7 +288,13 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
         __syncthreads();  // all warps, before the roles split
     }
 
-    griddep_wait();
+    // A chained launch releases its dependents only after its own wait, so
+    // a dependent that reads early overlaps with this kernel alone.
+    const bool early = kChain && ap.hold >= 0;
+    if (!early) {
+        griddep_wait();
+        if constexpr (kChain) griddep_launch_dependents();
+    }
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -302,7 +318,7 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
     // dimension in the order the E4M3 key fragments come in (k index 2c+e of
     // step kd is dimension 16kd + 4c + e, k index 2c+8+e is 16kd + 4c+2+e).
     uint32_t qf[KD][2];
-    {
+    auto load_q = [&]() {
         const bool live = r < G;
         const __nv_bfloat16 *qrow = q + (bt * H_q + (int64_t)g * G + (live ? r : 0)) * D;
 #pragma unroll
@@ -317,7 +333,8 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
                 qf[kd][1] = live ? __ldg(reinterpret_cast<const uint32_t *>(qrow + kd * 16 + 2 * c + 8)) : 0u;
             }
         }
-    }
+    };
+    if (!early) load_q();
     float sl2 = scale_log2;  // softmax scale in base 2 (times k_scale for fp8 keys)
     float out_scale = 1.f;   // v_scale / P scale for fp8 values
     if constexpr (kFp8) {
@@ -426,11 +443,16 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
     }
 
     // Issue the K/V gathers of tile t (stage t % S); its slots are in the ring.
+    // Pass 0: every key.  A chained launch that reads early issues its
+    // first tiles in two passes: 1 before its wait (every key not held) and
+    // 2 after it (the held keys: the last `hold` entries of the row and keys
+    // read from the new rows; `issued` is set if there were any).
     const uint8_t *knew = reinterpret_cast<const uint8_t *>(ap.k_new) +
                           ((size_t)b * ap.n_new * H_kv + g) * C::kRowBytes;
     const uint8_t *vnew = reinterpret_cast<const uint8_t *>(ap.v_new) +
                           ((size_t)b * ap.n_new * H_kv + g) * C::kRowBytes;
-    auto issue = [&](int t) {
+    auto issue_p = [&](int t, auto phase_c, bool &issued) {
+        constexpr int P = decltype(phase_c)::value;
         const int st = t % S;
         const int64_t k = (int64_t)t * kTileKeys + warp * kKeysPerWarp + (lane & 15);
         int32_t my_slot = 0;
@@ -443,7 +465,7 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
         }
         const bool in = lane < kKeysPerWarp && k < cnt;
         bool ok = in && my_slot >= 0 && my_slot < num_slots;
-        if (in && !ok) latch(WMTP_DEV_SLOT_RANGE);
+        if (P != 2 && in && !ok) latch(WMTP_DEV_SLOT_RANGE);
         if constexpr (kExtend) {
             const int64_t e = start + k;
             const int64_t pos = (x_win_u && e >= ev.n_sink) ? x_lo_u + (e - ev.n_sink) : e;
@@ -459,11 +481,17 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
             for (int i = kMaxNew - 1; i >= 0; --i)
                 if (ok && my_slot == nslot[i]) src_slot = -2 - i;
         }
+        uint32_t held = 0;  // keys of the second pass
+        if constexpr (P != 0) {
+            held = __ballot_sync(0xffffffffu, ok && (start + k >= L - ap.hold || src_slot < -1)) & 0xffffu;
+            if (P == 2 && held == 0) return;
+            issued = true;
+        }
         const uint32_t vm = __ballot_sync(0xffffffffu, ok) & 0xffffu;
-        if (lane == 0) masks[warp * S + st] = vm;
+        if (P != 2 && lane == 0) masks[warp * S + st] = vm;
         const uint32_t kdst = wsm_addr + st * C::kWarpStage;
         const uint32_t vdst = kdst + C::kWarpTile;
-        if constexpr (C::kSwz) {
+        if constexpr (C::kSwz && P != 2) {
             // 16 valid keys in 16 consecutive pool slots (a ring window, an
             // identity page table), none of them appended by this launch:
             // the warp's K and V rows come in as D/64 TMA boxes each (64
@@ -471,7 +499,7 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
             // barrier completes one phase per use either way.
             const uint32_t tbar = smem_addr(tma_bars + warp * S + st);
             const int32_t s0 = __shfl_sync(0xffffffffu, src_slot, 0);
-            const bool whole = tma_ok && vm == 0xffffu && s0 >= 0 &&
+            const bool whole = tma_ok && vm == 0xffffu && held == 0 && s0 >= 0 &&
                                __all_sync(0xffffffffu, lane >= kKeysPerWarp || src_slot == s0 + lane);
             if (whole) {
                 fence_proxy_async_smem();  // this warp's reads of the stage's previous rows come first
@@ -510,9 +538,21 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
             const int chunk = col >> 4;
             const uint32_t dofs = C::kSwz ? (uint32_t)((chunk >> 3) * C::kBlockBytes + key * 128 + (((chunk & 7) ^ (key & 7)) << 4))
                                           : (uint32_t)(key * C::kPitch + col);
-            cp_async_16(kdst + dofs, ksrc, kv ? 16u : 0u, policy);
-            cp_async_16(vdst + dofs, vsrc, kv ? 16u : 0u, policy);
+            if constexpr (P == 0) {
+                cp_async_16(kdst + dofs, ksrc, kv ? 16u : 0u, policy);
+                cp_async_16(vdst + dofs, vsrc, kv ? 16u : 0u, policy);
+            } else {
+                const bool hr = (held >> key) & 1u;
+                if (P == 1 ? !hr : hr) {
+                    cp_async_16(kdst + dofs, ksrc, kv ? 16u : 0u, policy);
+                    cp_async_16(vdst + dofs, vsrc, kv ? 16u : 0u, policy);
+                }
+            }
         }
+    };
+    auto issue = [&](int t) {
+        bool unused = false;
+        issue_p(t, std::integral_constant<int, 0>{}, unused);
     };
 
     // Append: the first split of each (request, KV head) writes the new rows
@@ -522,7 +562,7 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
     constexpr int kNewPerLane = (C::kRowBytes + 32 * 16 - 1) / (32 * 16);  // 16-byte pieces
     const bool writer = kAppend && split == 0 && (bt % n_q) == 0 && warp < ap.n_new;
     int4 new_k[kNewPerLane], new_v[kNewPerLane];
-    if (writer) {
+    auto load_new = [&]() {
 #pragma unroll
         for (int u = 0; u < kNewPerLane; ++u) {
             const int off = (u * 32 + lane) * 16;
@@ -531,7 +571,8 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
                 new_v[u] = *reinterpret_cast<const int4 *>(vnew + (size_t)warp * slot_bytes + off);
             }
         }
-    }
+    };
+    if (writer && !early) load_new();
 
     if constexpr (kWs) {
         if (warp >= kConsumerWarps) {
@@ -619,8 +660,32 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
         __syncwarp();
 #pragma unroll
         for (int t = 0; t < S - 1; ++t) {
-            if (t < n_tiles) issue(t);
+            if (t < n_tiles) {
+                if constexpr (kChain) {
+                    bool unused = false;
+                    if (early)
+                        issue_p(t, std::integral_constant<int, 1>{}, unused);
+                    else
+                        issue(t);
+                } else {
+                    issue(t);
+                }
+            }
             cp_async_commit();
+        }
+        if (early) {
+            // the preceding kernel has completed: q, the new rows and the
+            // held keys (in a group of their own, complete before tile 0)
+            griddep_wait();
+            griddep_launch_dependents();
+            load_q();
+            if (writer) load_new();
+            bool any = false;
+#pragma unroll
+            for (int t = 0; t < S - 1; ++t)
+                if (t < n_tiles) issue_p(t, std::integral_constant<int, 2>{}, any);
+            cp_async_commit();
+            if (any) cp_async_wait<0>();
         }
     }
 
@@ -1233,17 +1298,17 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
 // device `dev` (0: none; cached per device and size).
 // Sets the kernel attributes (large dynamic shared memory, non-portable
 // cluster sizes) once per device for one kernel instance.
-template <int D, bool A, bool X, bool F = false, bool RG = false, bool WS = false>
+template <int D, bool A, bool X, bool F = false, bool RG = false, bool WS = false, bool CH = false>
 bool prepare_kernel(int dev) {
     static int8_t done[64] = {};
     if (dev < 0 || dev >= 64) return false;
     if (done[dev]) return done[dev] > 0;
-    const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS>,
+    const bool ok = cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS, CH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<D, F, RG>::kSmemBytes) == cudaSuccess &&
-                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS>,
+                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS, CH>,
                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS>,
+                    cudaFuncSetAttribute(split_decode_kernel<D, A, X, F, RG, WS, CH>,
                                          cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
     cudaGetLastError();
     done[dev] = ok ? 1 : -1;
@@ -1251,10 +1316,10 @@ bool prepare_kernel(int dev) {
 }
 
 // Sets the instance's attributes (once per device) and launches it.
-template <int D, bool A, bool X, bool F, bool RG, bool WS, typename... Args>
+template <int D, bool A, bool X, bool F, bool RG, bool WS, bool CH = false, typename... Args>
 cudaError_t launch_instance(int dev, const cudaLaunchConfig_t *cfg, Args... args) {
-    if (!prepare_kernel<D, A, X, F, RG, WS>(dev)) return cudaErrorInvalidValue;
-    return cudaLaunchKernelEx(cfg, split_decode_kernel<D, A, X, F, RG, WS>, args...);
+    if (!prepare_kernel<D, A, X, F, RG, WS, CH>(dev)) return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(cfg, split_decode_kernel<D, A, X, F, RG, WS, CH>, args...);
 }
 
 template <int D, bool F = false>
@@ -1318,6 +1383,7 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WMTP_ECUDA;
     const bool append = ap.n_new > 0;
+    const bool chain = append && ap.chain != 0 && !F;
     const bool extend = ev.seq_lens != nullptr;
     const bool ring = rv.seq_lens != nullptr;
     // fp8 rows of at least four key tiles per split: the warp-specialised
@@ -1382,8 +1448,9 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
         err = use_ws ? launch_instance<D, false, false, true, false, true>(WMTP_ATTN_ARGS)
                  : launch_instance<D, false, false, true, false, false>(WMTP_ATTN_ARGS);
     } else if (ring) {
-        err = append ? launch_instance<D, true, false, false, true, false>(WMTP_ATTN_ARGS)
-                     : launch_instance<D, false, false, false, true, false>(WMTP_ATTN_ARGS);
+        err = chain    ? launch_instance<D, true, false, false, true, false, true>(WMTP_ATTN_ARGS)
+              : append ? launch_instance<D, true, false, false, true, false>(WMTP_ATTN_ARGS)
+                       : launch_instance<D, false, false, false, true, false>(WMTP_ATTN_ARGS);
     } else if (extend) {
         err = launch_instance<D, false, true, false, false, false>(WMTP_ATTN_ARGS);
     } else {
@@ -1391,7 +1458,8 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
         // it substitutes nothing and writes nothing).  Its arithmetic is the
         // plain instance's, and it runs measurably faster (360 against 480
         // us for a 1M-key row), so the plain table-path instance is not used.
-        err = launch_instance<D, true, false, false, false, false>(WMTP_ATTN_ARGS);
+        err = chain ? launch_instance<D, true, false, false, false, false, true>(WMTP_ATTN_ARGS)
+                    : launch_instance<D, true, false, false, false, false>(WMTP_ATTN_ARGS);
     }
 #undef WMTP_ATTN_ARGS
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
@@ -1640,6 +1708,48 @@ wmtp_status draft_decode_attn_checked(const uint16_t *q, int32_t B, int32_t n_q,
                                            fv, rv);
 }
 
+wmtp_status append_entry(const uint16_t *k_new, const uint16_t *v_new, const int32_t *new_slots, int32_t n_new,
+                         const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q, int32_t H_kv, int32_t D,
+                         uint16_t *k_pool, uint16_t *v_pool, int64_t num_slots, const int32_t *table,
+                         int64_t table_stride, const int32_t *lens, float scale, float *out, float *lse,
+                         void *workspace, size_t workspace_bytes_, int32_t n_split, int32_t chain,
+                         int32_t hold, void *stream) {
+    if (n_new < 1) return WMTP_EINVAL;
+    const AppendView ap{reinterpret_cast<const __nv_bfloat16 *>(k_new),
+                        reinterpret_cast<const __nv_bfloat16 *>(v_new), new_slots,
+                        reinterpret_cast<__nv_bfloat16 *>(k_pool),
+                        reinterpret_cast<__nv_bfloat16 *>(v_pool), n_new, chain, hold};
+    return draft_decode_attn_checked(q, B, n_q, H_q, H_kv, D, k_pool, v_pool, num_slots, table,
+                                     table_stride, lens, scale, out, lse, workspace,
+                                     workspace_bytes_, n_split, stream, ap);
+}
+
+wmtp_status ring_entry(const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q, int32_t B, int32_t H_q,
+                       int32_t H_kv, int32_t D, uint16_t *k_pool, uint16_t *v_pool, int64_t num_slots,
+                       const int32_t *seq_lens, const int32_t *ring_base, int32_t step, int32_t n_sink,
+                       int32_t window, int32_t depth, int32_t tree_k, float scale, float *out, float *lse,
+                       void *workspace, size_t workspace_bytes_, int32_t n_split, int32_t chain, int32_t hold,
+                       void *stream) {
+    if (n_sink < 0 || window < 1 || depth < 1 || tree_k < 1 || step < 0) return WMTP_EINVAL;
+    // ring slots and positions stay below 2^31 (the kernel maps them in
+    // 32-bit arithmetic)
+    if ((int64_t)n_sink + window + (int64_t)depth * tree_k > (int64_t)1 << 30 || num_slots > INT32_MAX)
+        return WMTP_EINVAL;
+    if ((k_new == nullptr) != (v_new == nullptr)) return WMTP_EINVAL;
+    if (chain && k_new == nullptr) return WMTP_EINVAL;  // chained steps append
+    if (B > 0 && (!seq_lens || !ring_base)) return WMTP_EINVAL;
+    const AppendView ap = k_new ? AppendView{reinterpret_cast<const __nv_bfloat16 *>(k_new),
+                                             reinterpret_cast<const __nv_bfloat16 *>(v_new), nullptr,
+                                             reinterpret_cast<__nv_bfloat16 *>(k_pool),
+                                             reinterpret_cast<__nv_bfloat16 *>(v_pool), 1, chain, hold}
+                                : AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0, 0, 0};
+    return draft_decode_attn_checked(q, B, 1, H_q, H_kv, D, k_pool, v_pool, num_slots, nullptr,
+                                     (int64_t)n_sink + window, nullptr, scale, out, lse, workspace,
+                                     workspace_bytes_, n_split, stream, ap, ExtendView{nullptr, nullptr, 0, 0, 0},
+                                     Fp8View{nullptr, nullptr},
+                                     RingView{seq_lens, ring_base, n_sink, window, depth, tree_k, step});
+}
+
 }  // namespace
 }  // namespace wmtp
 
@@ -1667,14 +1777,24 @@ wmtp_status wmtp_draft_decode_attn_append(const uint16_t *k_new, const uint16_t 
                                           const int32_t *lens, float scale, float *out,
                                           float *lse, void *workspace, size_t workspace_bytes_,
                                           int32_t n_split, void *stream) {
-    if (n_new < 1) return WMTP_EINVAL;
-    const AppendView ap{reinterpret_cast<const __nv_bfloat16 *>(k_new),
-                        reinterpret_cast<const __nv_bfloat16 *>(v_new), new_slots,
-                        reinterpret_cast<__nv_bfloat16 *>(k_pool),
-                        reinterpret_cast<__nv_bfloat16 *>(v_pool), n_new};
-    return draft_decode_attn_checked(q, B, n_q, H_q, H_kv, D, k_pool, v_pool, num_slots, table,
-                                     table_stride, lens, scale, out, lse, workspace,
-                                     workspace_bytes_, n_split, stream, ap);
+    return wmtp::append_entry(k_new, v_new, new_slots, n_new, q, B, n_q, H_q, H_kv, D, k_pool, v_pool,
+                              num_slots, table, table_stride, lens, scale, out, lse, workspace,
+                              workspace_bytes_, n_split, 0, 0, stream);
+}
+
+wmtp_status wmtp_draft_decode_attn_append_overlap(const uint16_t *k_new, const uint16_t *v_new,
+                                                  const int32_t *new_slots, int32_t n_new,
+                                                  const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
+                                                  int32_t H_kv, int32_t D, uint16_t *k_pool,
+                                                  uint16_t *v_pool, int64_t num_slots,
+                                                  const int32_t *table, int64_t table_stride,
+                                                  const int32_t *lens, float scale, float *out,
+                                                  float *lse, void *workspace, size_t workspace_bytes_,
+                                                  int32_t n_split, int32_t hold, void *stream) {
+    if (hold < -1) return WMTP_EINVAL;
+    return wmtp::append_entry(k_new, v_new, new_slots, n_new, q, B, n_q, H_q, H_kv, D, k_pool, v_pool,
+                              num_slots, table, table_stride, lens, scale, out, lse, workspace,
+                              workspace_bytes_, n_split, 1, hold, stream);
 }
 
 wmtp_status wmtp_draft_extend_attn(const uint16_t *q, int32_t B, int32_t n_q, int32_t H_q,
@@ -1757,23 +1877,23 @@ wmtp_status wmtp_draft_decode_attn_ring(const uint16_t *k_new, const uint16_t *v
                                         int32_t window, int32_t depth, int32_t tree_k, float scale,
                                         float *out, float *lse, void *workspace, size_t workspace_bytes_,
                                         int32_t n_split, void *stream) {
-    if (n_sink < 0 || window < 1 || depth < 1 || tree_k < 1 || step < 0) return WMTP_EINVAL;
-    // ring slots and positions stay below 2^31 (the kernel maps them in
-    // 32-bit arithmetic)
-    if ((int64_t)n_sink + window + (int64_t)depth * tree_k > (int64_t)1 << 30 || num_slots > INT32_MAX)
-        return WMTP_EINVAL;
-    if ((k_new == nullptr) != (v_new == nullptr)) return WMTP_EINVAL;
-    if (B > 0 && (!seq_lens || !ring_base)) return WMTP_EINVAL;
-    const AppendView ap = k_new ? AppendView{reinterpret_cast<const __nv_bfloat16 *>(k_new),
-                                             reinterpret_cast<const __nv_bfloat16 *>(v_new), nullptr,
-                                             reinterpret_cast<__nv_bfloat16 *>(k_pool),
-                                             reinterpret_cast<__nv_bfloat16 *>(v_pool), 1}
-                                : AppendView{nullptr, nullptr, nullptr, nullptr, nullptr, 0};
-    return draft_decode_attn_checked(q, B, 1, H_q, H_kv, D, k_pool, v_pool, num_slots, nullptr,
-                                     (int64_t)n_sink + window, nullptr, scale, out, lse, workspace,
-                                     workspace_bytes_, n_split, stream, ap, ExtendView{nullptr, nullptr, 0, 0, 0},
-                                     Fp8View{nullptr, nullptr},
-                                     RingView{seq_lens, ring_base, n_sink, window, depth, tree_k, step});
+    return wmtp::ring_entry(k_new, v_new, q, B, H_q, H_kv, D, k_pool, v_pool, num_slots, seq_lens, ring_base,
+                            step, n_sink, window, depth, tree_k, scale, out, lse, workspace, workspace_bytes_,
+                            n_split, 0, 0, stream);
+}
+
+wmtp_status wmtp_draft_decode_attn_ring_overlap(const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q,
+                                                int32_t B, int32_t H_q, int32_t H_kv, int32_t D, uint16_t *k_pool,
+                                                uint16_t *v_pool, int64_t num_slots, const int32_t *seq_lens,
+                                                const int32_t *ring_base, int32_t step, int32_t n_sink,
+                                                int32_t window, int32_t depth, int32_t tree_k, float scale,
+                                                float *out, float *lse, void *workspace,
+                                                size_t workspace_bytes_, int32_t n_split, int32_t hold,
+                                                void *stream) {
+    if (hold < -1) return WMTP_EINVAL;
+    return wmtp::ring_entry(k_new, v_new, q, B, H_q, H_kv, D, k_pool, v_pool, num_slots, seq_lens, ring_base,
+                            step, n_sink, window, depth, tree_k, scale, out, lse, workspace, workspace_bytes_,
+                            n_split, 1, hold, stream);
 }
 
 }  // extern "C"

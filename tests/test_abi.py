@@ -145,3 +145,31 @@ def test_builder_and_ring_argument_checks(lib):
     a = lib.wmtp_append_kv
     assert a(P, P, P, 3, 2, 250, P, P, 10, NULL) == wm.WMTP_EINVAL  # D % 8
     assert a(ctypes.c_void_p(20), P, P, 3, 2, 256, P, P, 10, NULL) == wm.WMTP_EINVAL
+
+
+def test_overlapped_step_argument_checks(lib):
+    f = lib.wmtp_draft_decode_attn_append_overlap
+    args = dict(kn=P, vn=P, slots=P, n_new=1, q=P, B=1, n_q=1, H_q=16, H_kv=2, D=256, k=P, v=P,
+                num_slots=10, table=P, stride=10, lens=P, scale=0.1, out=P, lse=NULL, ws=P,
+                ws_bytes=1 << 20, n_split=1, hold=2, stream=NULL)
+
+    def call(**over):
+        a = dict(args, **over)
+        return f(a["kn"], a["vn"], a["slots"], a["n_new"], a["q"], a["B"], a["n_q"], a["H_q"], a["H_kv"],
+                 a["D"], a["k"], a["v"], a["num_slots"], a["table"], a["stride"], a["lens"], a["scale"],
+                 a["out"], a["lse"], a["ws"], a["ws_bytes"], a["n_split"], a["hold"], a["stream"])
+
+    assert call(hold=-2) == wm.WMTP_EINVAL           # -1 is "no overlap", below that is an error
+    assert call(n_new=0) == wm.WMTP_EINVAL
+    assert call(D=64) == wm.WMTP_EINVAL
+    assert call(kn=ctypes.c_void_p(24)) == wm.WMTP_EINVAL  # new rows not 16-byte aligned
+    assert call(B=0) == wm.WMTP_OK
+    assert call(B=0, hold=-1) == wm.WMTP_OK
+    r = lib.wmtp_draft_decode_attn_ring_overlap
+    # k_new, v_new, q, B, H_q, H_kv, D, k, v, num_slots, seq_lens, ring_base, step, n_sink, W,
+    # depth, tree_k, scale, out, lse, ws, ws_bytes, n_split, hold, stream
+    ring = [P, P, P, 1, 16, 2, 256, P, P, 4200, P, P, 0, 64, 4032, 7, 1, 0.1, P, NULL, P, 1 << 20, 1]
+    assert r(*ring, -2, NULL) == wm.WMTP_EINVAL
+    assert r(*ring[:12], -1, *ring[13:], 2, NULL) == wm.WMTP_EINVAL  # step < 0
+    assert r(*ring[:3], 0, *ring[4:], 2, NULL) == wm.WMTP_OK          # B = 0
+    assert r(NULL, NULL, *ring[2:], 2, NULL) == wm.WMTP_EINVAL      # a chained ring step appends
