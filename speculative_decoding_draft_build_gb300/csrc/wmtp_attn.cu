@@ -26,7 +26,7 @@
 //     shuffles; the accumulator is rescaled only when a running max moves.
 //   * at the end the four warps combine through shared memory (per-head
 //     factors computed once).  The splits of a (row, KV head) then merge in
-//     one of three ways:
+//     one of four ways:
 //       - up to 16 splits run as one thread-block cluster and merge through
 //         distributed shared memory, each CTA producing a slice of the
 //         output;
@@ -34,12 +34,19 @@
 //         cluster merges as above into a per-cluster partial of its slice,
 //         takes a ticket for that slice, and the last cluster's CTA merges
 //         the slice over the clusters in cluster order;
+//       - without a cluster plan, when the whole grid is resident at once,
+//         every split writes its partial, takes an arrival ticket and merges
+//         its own slice of the output once all have arrived (slice merge);
 //       - otherwise every split writes its partial to the workspace, takes a
 //         ticket, and the last CTA merges all splits in split order.
-//     No CTA ever spins on another.
-//   * every kernel waits on its predecessor with griddepcontrol.wait before
-//     touching global memory and is launched with programmatic stream
-//     serialization, so consecutive launches overlap only their start-up.
+//     Only the slice merge waits on other CTAs, and only for a bounded time
+//     (the last CTA to arrive merges whatever the others left).
+//   * every kernel is launched with programmatic stream serialization and
+//     waits on its predecessor with griddepcontrol.wait before touching
+//     global memory, so consecutive launches overlap only their start-up;
+//     chained draft steps (the _overlap entry points) instead copy the keys
+//     their predecessor cannot be writing before that wait, and release
+//     their own dependents only after it.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
