@@ -14,6 +14,9 @@
  *     the caller owns every buffer.  The library allocates nothing and never
  *     synchronises; every call is asynchronous on `stream` (a cudaStream_t,
  *     NULL = the legacy default stream) and may be captured in a CUDA graph.
+ *     A captured call keeps its pointers: every buffer it was given, the
+ *     workspace included, must stay allocated while the graph may be
+ *     replayed (a replay after the memory is freed is an invalid access).
  *   - bf16 values travel as their 16-bit patterns (uint16_t).
  *   - Positions and slots are 0-based.  A request's KV pool has the layout
  *     [num_slots][H_kv][D]: the K (or V) row of KV head g for slot s starts at

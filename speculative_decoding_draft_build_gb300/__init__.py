@@ -434,6 +434,10 @@ class AttnWorkspace:
 
     Every completed ``draft_decode_attn`` call leaves the merge counters at
     zero, so one workspace serves any number of calls (not concurrent ones).
+    A CUDA graph that captured a call keeps the workspace's address: keep the
+    object alive as long as the graph (``torch.cuda.graph`` empties the
+    allocator cache when a capture starts, so a dropped workspace can be
+    unmapped before the replay).
     """
 
     def __init__(self, nbytes: int, device, stream=None):
