@@ -427,7 +427,11 @@ wmtp_status wmtp_attn_mass_diagnostics(const float *o_win, const float *lse_win,
  *           zeroes a whole workspace) and every completed call leaves them
  *           zero.  Unused when n_split == 1, and when the key chunks merge
  *           through a thread-block cluster (n_split <= 8, where the device
- *           holds such clusters).
+ *           holds such clusters).  Otherwise, when the whole grid fits on
+ *           the device at once, every chunk merges its own slice of the
+ *           output after all have arrived (a wait bounded at 50 us; the last
+ *           to arrive merges any slice left over), else the last chunk to
+ *           finish merges them all.
  * n_split   1 .. 128 key chunks per request; wmtp_tree_num_splits() gives one.
  * Errors: WMTP_EINVAL for null or misaligned pointers, bad sizes, D not
  * 128/256, H_q % H_kv != 0, W < 1, d < 1, k < 1; WMTP_ECAPACITY for a small

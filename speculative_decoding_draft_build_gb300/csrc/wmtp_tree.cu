@@ -41,8 +41,10 @@
 // same key sets as node (0, i) above.
 // Key chunks are split over CTAs; up to 8 chunks of a (request, KV head,
 // row block) run as one cluster and merge through distributed shared memory,
-// more through the workspace (the last CTA merges in split order).  Every
-// wait has a time limit; tensor memory is always released.
+// more through the workspace: when the whole grid is resident, every chunk
+// merges its own slice of the outputs once all have arrived (slice merge),
+// else the last CTA merges in split order.  Every wait has a time limit;
+// tensor memory is always released.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -74,6 +76,7 @@ constexpr int kMmaWarp = kSoftWarps + kLoadWarps;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr int kMaxSplits = 128;
 constexpr int kMaxClusterSplits = 8;  // key chunks merged through one (portable) cluster
+constexpr uint64_t kSlicePollNs = 50000;  // a slice-merge wait gives up after 50 us (results stay exact)
 constexpr float kLazyRescale = 8.f;  // log2 of the growth tolerated before rescaling O
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     int64_t num_slots, const int32_t *__restrict__ seq_lens, const int32_t *__restrict__ ring_base,
     int32_t n_sink, int32_t window, int32_t depth, int32_t tree_k, float scale_log2,
     float *__restrict__ out, float *__restrict__ lse, TreeWs ws, TreeTable tt, int32_t n_split, int32_t n_rb,
-    int32_t cluster_merge, const __grid_constant__ CUtensorMap tm_k32, const __grid_constant__ CUtensorMap tm_v32,
+    int32_t cluster_merge, int32_t slice_stride, const __grid_constant__ CUtensorMap tm_k32, const __grid_constant__ CUtensorMap tm_v32,
     const __grid_constant__ CUtensorMap tm_k8, const __grid_constant__ CUtensorMap tm_v8) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -730,10 +733,136 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         return;
     }
 
+    const int64_t cidx = (b * H_kv + g) * n_rb + rb;
+    if (slice_stride) {
+        // ------------------------------------------------- slice merge
+        // Every split has written its partial.  Each CTA takes an arrival
+        // ticket; all but the last wait (time-bounded) until every split has
+        // arrived and then merge their own slice of the rows x D outputs, so
+        // the merge runs on all the launch's SMs at once.  The last to arrive
+        // never waits: it merges its own slice and then every slice still
+        // unclaimed (one whose CTA gave up waiting), so each slice is merged
+        // exactly once (claims are compare-and-swap) whatever the
+        // co-residency.  The last CTA to leave returns the counters to zero.
+        __threadfence();
+        __syncthreads();
+        int32_t *ctr = ws.counters + cidx * slice_stride;  // arrivals, departures, claims
+        if (tid == 0) {
+            const bool is_last = atomicAdd(ctr, 1) == n_split - 1;
+            const bool all_in = is_last || poll_geq_bounded(ctr, n_split, kSlicePollNs);
+            if (all_in) __threadfence();
+            flags[1] = is_last;
+            flags[2] = all_in && atomicCAS(ctr + 2 + split, 0, 1) == 0;
+        }
+        __syncthreads();
+        const bool is_last = flags[1] != 0;
+        const bool mine = flags[2] != 0;
+        const int total4 = n_rows * D4;
+        const int per4 = (total4 + n_split - 1) / n_split;
+        constexpr int kWarps = kThreads / 32;
+        float *sw = reinterpret_cast<float *>(smem + C::kKvOff);                  // [rows of the slice][n_split]
+        float4 *red = reinterpret_cast<float4 *>(smem + C::kKvOff + 65536);       // [kThreads]
+        int32_t *claim = reinterpret_cast<int32_t *>(smem + C::kKvOff + 65536 + kThreads * 16);  // [n_split]
+        const int64_t prow0 = (b * H_kv + g) * R + row0;
+        // Merges slice s_idx: float4 outputs [lo4, hi4) of this row block;
+        // rr_n threads per output, each summing a strided subset of the
+        // splits, then a fixed-order reduction.
+        auto slice_merge = [&](int s_idx) {
+            const int lo4 = s_idx * per4;
+            const int hi4 = lo4 + per4 < total4 ? lo4 + per4 : total4;
+            if (lo4 >= hi4) return;
+            const int nel = hi4 - lo4;
+            const int i0 = lo4 / D4;
+            const int nh = (hi4 - 1) / D4 - i0 + 1;
+            for (int e = tid; e < nh * n_split; e += kThreads) sw[e] = __ldcg(ws.lse_part + (prow0 + i0) * n_split + e);
+            __syncthreads();
+            for (int hh = warp; hh < nh; hh += kWarps) {
+                float *x = sw + hh * n_split;
+                float M = -INFINITY;
+                for (int s2 = lane; s2 < n_split; s2 += 32) M = fmaxf(M, x[s2]);
+#pragma unroll
+                for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
+                float sum = 0.f;
+                if (M != -INFINITY)
+                    for (int s2 = lane; s2 < n_split; s2 += 32) sum += x[s2] == -INFINITY ? 0.f : exp2f(x[s2] - M);
+#pragma unroll
+                for (int sh = 16; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+                const float lt = sum > 0.f ? M + log2f(sum) : -INFINITY;
+                __syncwarp();
+                for (int s2 = lane; s2 < n_split; s2 += 32)
+                    x[s2] = (sum > 0.f && x[s2] != -INFINITY) ? exp2f(x[s2] - lt) : 0.f;
+                const int rq = row0 + i0 + hh;
+                if (lane == 0 && lse && (i0 + hh) * D4 >= lo4)
+                    lse[(b * n_nodes + rq / G) * H_q + g * G + rq % G] = lt * kLn2;
+            }
+            __syncthreads();
+            const int per_round = nel < kThreads ? nel : kThreads;
+            const int rr_n = kThreads / per_round;  // >= 1
+            for (int base = 0; base < nel; base += per_round) {
+                const int sub = tid / per_round, el = base + (tid - sub * per_round);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (sub < rr_n && el < nel) {
+                    const int f = lo4 + el;
+                    const int i = f / D4, d4 = f - i * D4;
+                    const float *wh = sw + (i - i0) * n_split;
+                    const float4 *op = reinterpret_cast<const float4 *>(ws.o_part + (prow0 + i) * n_split * D) + d4;
+                    constexpr int kBatch = 8;
+                    for (int s0 = sub; s0 < n_split; s0 += kBatch * rr_n) {
+                        float4 v[kBatch];
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) {
+                            const int s2 = s0 + u * rr_n;
+                            if (s2 < n_split) v[u] = __ldcg(op + (int64_t)s2 * D4);
+                        }
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) {
+                            const int s2 = s0 + u * rr_n;
+                            if (s2 < n_split) {
+                                const float w = wh[s2];
+                                acc.x += w * v[u].x;
+                                acc.y += w * v[u].y;
+                                acc.z += w * v[u].z;
+                                acc.w += w * v[u].w;
+                            }
+                        }
+                    }
+                }
+                red[tid] = acc;
+                __syncthreads();
+                if (tid < per_round && base + tid < nel) {
+                    float4 t = red[tid];
+                    for (int k2 = 1; k2 < rr_n; ++k2) {
+                        const float4 u = red[k2 * per_round + tid];
+                        t.x += u.x;
+                        t.y += u.y;
+                        t.z += u.z;
+                        t.w += u.w;
+                    }
+                    const int f = lo4 + base + tid;
+                    const int i = f / D4, d4 = f - i * D4;
+                    const int rq = row0 + i;
+                    reinterpret_cast<float4 *>(out + ((b * n_nodes + rq / G) * H_q + g * G + rq % G) * D)[d4] = t;
+                }
+                __syncthreads();  // red is reused by the next round
+            }
+        };
+        if (mine) slice_merge(split);
+        if (is_last) {
+            for (int s2 = tid; s2 < n_split; s2 += kThreads)
+                claim[s2] = (s2 != split && atomicCAS(ctr + 2 + s2, 0, 2) == 0) ? 1 : 0;
+            __syncthreads();
+            for (int s2 = 0; s2 < n_split; ++s2)
+                if (claim[s2]) slice_merge(s2);
+        }
+        __syncthreads();
+        if (tid == 0 && atomicAdd(ctr + 1, 1) == n_split - 1)
+            for (int i = 0; i < 2 + n_split; ++i) ctr[i] = 0;  // ready for the next call
+        return;
+    }
+
     // ------------------------------------------ ticket; the last CTA merges
     __threadfence();
     __syncthreads();
-    const int64_t cidx = (b * H_kv + g) * n_rb + rb;
     if (tid == 0) {
         const int32_t ticket = atomicAdd(&ws.counters[cidx], 1);
         flags[1] = (ticket == n_split - 1);
@@ -823,6 +952,31 @@ bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t num_slots, int 
 namespace wmtp {
 namespace {
 
+// Merge counters per (request, KV head, row block) for the slice merge:
+// arrivals, departures and one claim per split, rounded to 16 (the same
+// stride as the decode attention's workspace, whose counters the draft-extend
+// pass shares).
+inline int tree_counter_stride(int n_split) {
+    const int n = 2 + n_split;
+    return n < 16 ? 16 : (n + 15) / 16 * 16;
+}
+
+// CTAs of the tree kernel the device holds at once (0 if unknown).
+template <int D>
+int tree_resident_capacity(int dev) {
+    static int32_t known[64] = {};
+    if (dev < 0 || dev >= 64) return 0;
+    if (known[dev]) return known[dev] > 0 ? known[dev] : 0;
+    int sms = 0, per_sm = 0;
+    const bool ok = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tree_tc_kernel<D>, kThreads,
+                                                                  Cfg<D>::kSmemBytes) == cudaSuccess &&
+                    sms > 0 && per_sm > 0;
+    cudaGetLastError();
+    known[dev] = ok ? sms * per_sm : -1;
+    return ok ? known[dev] : 0;
+}
+
 template <int D>
 bool tree_cluster_ok(int dev, int n) {
     static int8_t known[64][kMaxClusterSplits + 1] = {};
@@ -869,13 +1023,21 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
         opted_in[dev] = 1;
     }
     const bool use_cluster = n_split > 1 && tree_cluster_ok<D>(dev, n_split);
+    // without a cluster: the slice merge when the whole grid is resident at
+    // once (its waits then end as soon as the last split arrives), else the
+    // last CTA merges
+    int32_t slice = 0;
+    if (n_split > 1 && !use_cluster) {
+        const int cap = tree_resident_capacity<D>(dev);
+        if (cap > 0 && (int64_t)n_split * H_kv * n_rb * B <= cap) slice = tree_counter_stride(n_split);
+    }
     TreeWs ws{nullptr, nullptr, nullptr};
     if (n_split > 1 && !use_cluster && ws_given.counters) {
         ws = ws_given;
     } else if (n_split > 1 && !use_cluster) {
         uint8_t *p = static_cast<uint8_t *>(workspace);
         ws.counters = reinterpret_cast<int32_t *>(p);
-        p += align256((size_t)B * H_kv * n_rb * 4);
+        p += align256((size_t)B * H_kv * n_rb * tree_counter_stride(n_split) * 4);
         ws.lse_part = reinterpret_cast<float *>(p);
         p += align256((size_t)B * H_kv * R * n_split * 4);
         ws.o_part = reinterpret_cast<float *>(p);
@@ -894,7 +1056,7 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
         n_nodes, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
         reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, seq_lens, ring_base, n_sink,
         window, depth, tree_k, scale * 1.4426950408889634f, out, lse, ws, tt, n_split, n_rb,
-        (int32_t)(use_cluster ? 1 : 0), tm_k32, tm_v32, tm_k8, tm_v8);
+        (int32_t)(use_cluster ? 1 : 0), slice, tm_k32, tm_v32, tm_k8, tm_v8);
     return err == cudaSuccess ? WMTP_OK : WMTP_ECUDA;
 }
 
@@ -910,7 +1072,8 @@ cudaError_t read_tree_tc_error(int32_t *code, bool clear) {
 size_t tree_tc_workspace_bytes(int64_t B, int64_t H_kv, int64_t R, int D, int n_split) {
     if (n_split <= 1) return 0;
     const int64_t n_rb = (R + kRows - 1) / kRows;
-    return align256((size_t)B * H_kv * n_rb * 4) + align256((size_t)B * H_kv * R * n_split * 4) +
+    return align256((size_t)B * H_kv * n_rb * tree_counter_stride(n_split) * 4) +
+           align256((size_t)B * H_kv * R * n_split * 4) +
            (size_t)B * H_kv * R * n_split * D * 4;
 }
 

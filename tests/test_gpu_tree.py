@@ -105,3 +105,18 @@ def test_tree_bad_ring_base_is_latched():
     out, lse = wm.tree_draft_attn(q, kp, kp, seq, rb, n_sink, W, d, k, 0.1)
     torch.cuda.synchronize()
     assert wm.device_error(clear=True) == 1
+
+
+@pytest.mark.parametrize("D,H_q,H_kv", [(256, 16, 2), (128, 8, 2)])
+def test_tree_workspace_merges(D, H_q, H_kv):
+    # one request, k = 4, d = 7 (224 query rows: two row blocks), more key
+    # chunks than a cluster holds: 12, 19 and 37 chunks put the whole grid on
+    # the device (every chunk merges its own slice of the outputs; 19 chunks
+    # give slices longer than the CTA's threads), 100 do not (the last chunk
+    # merges all); against the oracle, and bitwise repeatable
+    n_sink, W, d, k = 64, 4096, 7, 4
+    S_list = [300_000]
+    for n_split in (12, 19, 37, 100):
+        out, lse = _check(S_list, n_sink, W, d, k, H_q, H_kv, D, seed=900 + n_split, n_split=n_split)
+        out2, lse2 = _check(S_list, n_sink, W, d, k, H_q, H_kv, D, seed=900 + n_split, n_split=n_split)
+        assert torch.equal(out, out2) and torch.equal(lse, lse2), f"split={n_split} not repeatable"
