@@ -1117,6 +1117,8 @@ def measure_e2e(w, args, dev):
             fn()
         times = []
         for _ in range(reps):
+            w.flush.zero_()  # L2 flushed before each step, outside the timed interval
+            torch.cuda.synchronize(dev)
             t = time.perf_counter()
             fn()
             times.append(time.perf_counter() - t)
@@ -1155,9 +1157,10 @@ def measure_e2e(w, args, dev):
             "eager_us": round(eager_s * 1e6, 3),
             "full": {"value": round(full_s * 1e6, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                      "d2h_bytes_per_step": int(out_full_h.numel())},
-            "how": "each arm with pinned host I/O, host-timed: one CUDA graph per step (packed copy in, "
-                   "index build, 6 fused launches, packed copy out); value = windowed arm, full.value = "
-                   "full-context arm; eager_us = windowed arm by direct calls"}
+            "how": "each arm with pinned host I/O, host-timed (L2 flushed before each step, outside the "
+                   "interval): one CUDA graph per step (packed copy in, index build, 6 fused launches, packed "
+                   "copy out); value = windowed arm, full.value = full-context arm; eager_us = windowed arm by "
+                   "direct calls"}
 
 
 # ------------------------------------------------------------------ oracle legs
