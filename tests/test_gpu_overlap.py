@@ -209,3 +209,68 @@ def test_overlap_hold_range():
     with pytest.raises(ValueError):
         wm.draft_decode_attn_append(ch.kn[1], ch.vn[1], ch.slots[1], ch.q[1], ch.kp, ch.vp, ch.tab[1],
                                     ch.lens[1], ch.scale, n_split=1, overlap_hold=-2)
+
+
+@pytest.mark.parametrize("hold", [0, 1, 3, 9])
+def test_overlap_two_new_rows_and_hold_values(hold):
+    # one launch, two new rows per request (their slots are the last two
+    # entries of each row), every hold value giving the same bits as the
+    # plain call: keys read from the new rows are always held, the rest
+    # follow `hold`
+    B, H_q, H_kv, D, n_new = 3, 8, 2, 128, 2
+    lens_list = [3000, 130, 2]
+    num_slots = 8000
+    kp = synth.normal_bf16((num_slots, H_kv, D), 71, DEV)
+    vp = synth.normal_bf16((num_slots, H_kv, D), 72, DEV)
+    q = synth.normal_bf16((B, 1, H_q, D), 73, DEV)
+    perm = synth.permutation(num_slots, 74, DEV)
+    stride = max(lens_list)
+    table = torch.full((B, stride), -1, dtype=torch.int32, device=DEV)
+    off = 0
+    for b, L in enumerate(lens_list):
+        table[b, :L] = perm[off:off + L]
+        off += L
+    lens = torch.tensor(lens_list, dtype=torch.int32, device=DEV)
+    new_slots = torch.stack([table[b, L - n_new:L] for b, L in enumerate(lens_list)]).contiguous()
+    kn = synth.normal_bf16((B, n_new, H_kv, D), 75, DEV)
+    vn = synth.normal_bf16((B, n_new, H_kv, D), 76, DEV)
+    for n_split in (1, 7, 37):
+        a_k, a_v = kp.clone(), vp.clone()
+        b_k, b_v = kp.clone(), vp.clone()
+        oa, la = wm.draft_decode_attn_append(kn, vn, new_slots, q, a_k, a_v, table, lens, 0.09, n_split=n_split)
+        ob, lb = wm.draft_decode_attn_append(kn, vn, new_slots, q, b_k, b_v, table, lens, 0.09, n_split=n_split,
+                                             overlap_hold=hold)
+        assert torch.equal(oa, ob) and torch.equal(la, lb), f"hold={hold} n_split={n_split}"
+        assert torch.equal(a_k, b_k) and torch.equal(a_v, b_v)
+
+
+def test_overlapped_tree_ring_layout_chain():
+    # ring of a k = 4 tree layout (modulus W + d*k); chained fused steps on
+    # branch 0 equal the plain ones
+    n_sink, W, d, k = 64, 1024, 7, 4
+    D, H_q, H_kv = 256, 16, 2
+    S_list = [5, 1100, 70_000]
+    B = len(S_list)
+    R = n_sink + W + d * k
+    rb = synth.ring_bases(B, R, B + 1, 81)
+    ring_base = torch.tensor(rb, dtype=torch.int32, device=DEV)
+    kp0 = synth.normal_bf16(((B + 1) * R, H_kv, D), 82, DEV)
+    vp0 = synth.normal_bf16(((B + 1) * R, H_kv, D), 83, DEV)
+    seq = torch.tensor(S_list, dtype=torch.int32, device=DEV)
+    kn = synth.normal_bf16((GAMMA, B, H_kv, D), 84, DEV)
+    vn = synth.normal_bf16((GAMMA, B, H_kv, D), 85, DEV)
+    qs = synth.normal_bf16((GAMMA, B, 1, H_q, D), 86, DEV)
+    res = []
+    for hold in (None, 2):
+        kp, vp = kp0.clone(), vp0.clone()
+        outs = []
+        for j in range(GAMMA):
+            o, l = wm.draft_decode_attn_ring(qs[j], kp, vp, seq, ring_base, j, n_sink, W, d, 1 / 16, k_new=kn[j],
+                                             v_new=vn[j], tree_k=k,
+                                             overlap_hold=None if hold is None else (hold if j > 0 else -1))
+            outs.append((o, l))
+        torch.cuda.synchronize()
+        res.append((outs, kp, vp))
+    for j in range(GAMMA):
+        assert torch.equal(res[0][0][j][0], res[1][0][j][0]) and torch.equal(res[0][0][j][1], res[1][0][j][1])
+    assert torch.equal(res[0][1], res[1][1]) and torch.equal(res[0][2], res[1][2])
