@@ -250,7 +250,11 @@ class Workload:
         self.vn.copy_(synth.normal_bf16((g, B, H_kv, D), seed + 4, dev))
         self.q.copy_(synth.normal_bf16((g, B, 1, H_q, D), seed + 5, dev))
         self.seq.fill_(S)
-        self.rtt = synth.permutation(pool, seed + 6, dev).view(B, S + g)
+        if cfg.get("identity"):
+            # identity page table: request b's positions in consecutive slots
+            self.rtt = torch.arange(pool, dtype=torch.int32, device=dev).view(B, S + g)
+        else:
+            self.rtt = synth.permutation(pool, seed + 6, dev).view(B, S + g)
         self.slots = torch.stack([self.rtt[:, S + j] for j in range(g)]).contiguous()  # [g, B]
         self.full_stride = S + g
         self.win_stride = cfg["n_sink"] + cfg["W"]
@@ -776,6 +780,18 @@ def measure_configs(args, dev, w3, result, o=None):
     res["3_1m"] = {"see": "arms, roofline, roofline_windowed (the headline workload)",
                    "windowed_us_per_step": result["arms"]["windowed"]["us_per_step"],
                    "full_us_per_step": result["arms"]["full"]["us_per_step"]}
+    # the same 131K and 1M steps over an identity page table (each request's
+    # positions in consecutive slots) instead of a permuted one
+    for key, cfg, oo in (("2_131k_identity", dict(WORKLOADS["131k"], identity=True), o),
+                         ("3_1m_identity", dict(WORKLOADS["1m"], identity=True), None)):
+        w = Workload(cfg, dev)
+        res[key] = measure_arms(w, args, dev, oo)
+        res[key]["workload"] = (f"{cfg['name']}: B={cfg['B']}, S={cfg['S']}, H_q={cfg['H_q']}, "
+                                f"H_kv={cfg['H_kv']}, D={cfg['D']}, n_sink={cfg['n_sink']}, W={cfg['W']}, "
+                                f"gamma={cfg['gamma']}, identity page table"
+                                + (f", {cfg['outlier_frac']:.0%} of K rows x4" if cfg["outlier_frac"] else ""))
+        del w
+        torch.cuda.empty_cache()
     res["4_ring_batch"] = measure_ring_batch(args, dev, o)
     if "tree" in result:
         res["5_tree"] = {"see": "tree (per window W)"}
