@@ -534,7 +534,9 @@ def run_ours(args, dist_ctx):
             "bytes_per_launch": int(win_bytes / g),
             "traffic": profiled_traffic("windowed_4096") if args.workload == "1m" else None,
         },
-        "gpu_launches": K * 2 * (1 + g),
+        # per timed iteration: the full arm, the windowed step and the same
+        # step as chained launches, each an index build and g attention launches
+        "gpu_launches": K * 3 * (1 + g),
         "clocks": sampler.summary(),
         "timed_region_s": round(wall_max, 4),
     }
