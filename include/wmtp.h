@@ -221,8 +221,9 @@ wmtp_status wmtp_append_kv(const uint16_t *k_new, const uint16_t *v_new,
  * depend only on those and the inputs), in order of preference: one cluster
  * (n_split <= 16, through distributed shared memory); whole clusters of up
  * to 16 merged in two levels, when the device holds all of them at once;
- * the slice merge, for more than 16 splits when the whole grid fits on the
- * device at once (every split writes its partial, takes an arrival ticket
+ * the slice merge, when no cluster plan fits, the whole grid fits on the
+ * device at once and no split's slice holds more than 128 float4 outputs
+ * (ceil(G * D / 4 / n_split) <= 128) (every split writes its partial, takes an arrival ticket
  * and, once all have arrived -- a wait bounded at 50 us -- merges its own
  * slice of the output; the last to arrive also merges any slice whose split
  * gave up waiting, so the result never depends on co-residency); or the

@@ -75,7 +75,6 @@ constexpr int kMaxSplits = 1024;
 constexpr int kMaxClusterMerge = 16;  // splits merged through a cluster (non-portable size)
 constexpr int kMaxClusters = 8;       // clusters merged by the second level
 constexpr int kMaxNew = 4;            // rows one request appends in a fused call (one per warp)
-constexpr int kMinSliceSplits = kMaxClusterMerge + 1;  // the slice merge serves larger split counts
 constexpr uint64_t kSlicePollNs = 50000;  // a slice-merge wait gives up after 50 us (results stay exact)
 constexpr float kLn2 = 0.69314718055994530942f;
 // Warp-specialised instances (long rows): one producer warp issues every
@@ -1135,7 +1134,7 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
             const int nel = hi4 - lo4;
             const int h0 = lo4 / D4;
             const int nh = (hi4 - 1) / D4 - h0 + 1;
-            const int R = kThreads / nel;  // >= 1: nel <= ceil(G * D4 / 17) <= kThreads
+            const int R = kThreads / nel;  // >= 1: the host takes this path only when nel <= kThreads
             const int r = tid / nel, el = tid - (tid / nel) * nel;
             const int f = lo4 + el;
             const int h = f / D4, d4 = f - h * D4;
@@ -1424,11 +1423,14 @@ wmtp_status launch_split_decode(const uint16_t *q, int32_t B, int32_t n_q, int32
     }
     // No cluster plan: the slice merge when the whole grid fits on the
     // device at once (its waits then end as soon as the last split
-    // arrives), else the last CTA merges.
+    // arrives) and no slice holds more outputs than the CTA has threads,
+    // else the last CTA merges.
     int slice = 0;
-    if (csz == 0 && n_split >= kMinSliceSplits) {
+    if (csz == 0 && n_split > 1) {
+        const int64_t total4 = (int64_t)(H_q / H_kv) * (D / 4);
         const int cap = resident_capacity<D, F>(dev);
-        if (cap > 0 && rows_kv * n_split <= cap) slice = counter_stride(n_split);
+        if ((total4 + n_split - 1) / n_split <= kThreads && cap > 0 && rows_kv * n_split <= cap)
+            slice = counter_stride(n_split);
     }
     WorkspaceView ws{nullptr, nullptr, nullptr};
     if (n_split > 1 && csz == 0) ws = carve(workspace, rows_q, rows_kv, n_split);
