@@ -24,6 +24,11 @@ Calls (same names as the C ABI without the ``wmtp_`` prefix):
                        positions and their KV written into the ring
   draft_decode_attn_ring  a draft step over the ring with no table (slots
                        from the ring rule in the kernel), append fused
+  (overlap_hold=...)   draft_decode_attn_append / draft_decode_attn_ring as
+                       chained steps (``*_overlap`` in the C ABI): copies of
+                       every key but the last few start while the previous
+                       step on the stream finishes; the same bits
+  draft_decode_attn_noalloc  the attention without a caller workspace
   tree_draft_attn      tree-draft attention over the ring (tree-causal mask)
 """
 from __future__ import annotations
