@@ -28,7 +28,11 @@
 //              copy stages of consecutive slots arrive as TMA boxes (64 dims
 //              x 1 head x 32 or 8 slots, 128-byte swizzle), other keys
 //              through 16-byte cp.async into the same swizzled layout, each
-//              warp one 8-key group; six stages, two per MMA tile.
+//              warp one 8-key group; six stages, two per MMA tile.  Ring
+//              chunks of 16 or more MMA tiles take the split instance: two
+//              warps copy K rows, two V rows (one 8-key group in two each),
+//              against separate K and V stage barriers, so that K is
+//              refilled once its QK product is done, before V is free.
 //   warp 8     one thread issues the MMAs: S(t) = Q K(t)^T (M=128, N=64,
 //              K=D) into one of two S buffers, then O += P_hi V + P_lo V
 //              (M=128, N=D, K=64); completion is signalled through mbarriers
@@ -68,6 +72,9 @@ constexpr int kRows = 128;  // query rows per CTA (MMA M)
 constexpr int kKeys = 64;      // keys per MMA tile (N of QK^T, K of PV)
 constexpr int kCopyKeys = 32;  // keys per copy stage: two stages make one MMA tile
 constexpr int kKvStages = 6;   // copy stages (even: an MMA tile never wraps the ring)
+// ring-mode chunks of at least this many MMA tiles take the split-role
+// instance (K rows refilled once QK is done); shorter ones the combined one
+constexpr int kSplitMinTiles = 16;
 static_assert(kKeys == 2 * kCopyKeys && kKvStages % 2 == 0, "stage pairing");
 constexpr int kSoftWarps = 4;
 constexpr int kLoadWarps = 4;  // gather warps: warp w copies the 8-key groups w, w + 4, ...
@@ -84,9 +91,11 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // Barrier slots: K/V copy stages, S buffers (2), P (2, written over S), PV
 // done (2, which also frees the S buffer), Q.
 enum {
-    kKvFull = 0,
-    kKvEmpty = kKvFull + kKvStages,
-    kSFull = kKvEmpty + kKvStages,
+    kKFull = 0,                      // K rows of a copy stage landed (table instance: K and V)
+    kVFull = kKFull + kKvStages,     // V rows of a copy stage landed (ring instance)
+    kKEmpty = kVFull + kKvStages,    // QK done with a stage's K rows (table instance: PV done with it)
+    kVEmpty = kKEmpty + kKvStages,   // PV done with a stage's V rows (ring instance)
+    kSFull = kVEmpty + kKvStages,
     kPFull = kSFull + 2,
     kPvDone = kPFull + 2,
     kQFull = kPvDone + 2,
@@ -208,7 +217,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
-template <int D>
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     const __nv_bfloat16 *__restrict__ q, int32_t H_q, int32_t H_kv, int32_t G, int32_t n_nodes,
     const __nv_bfloat16 *__restrict__ k_pool, const __nv_bfloat16 *__restrict__ v_pool,
@@ -261,10 +270,19 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
     const int64_t cnt = geo.U - start < 0 ? 0 : (geo.U - start < chunk ? geo.U - start : chunk);
     const int n_tiles = (int)((cnt + kKeys - 1) / kKeys);
 
+    // kSplit (ring mode, long chunks): two gather warps copy K rows and two
+    // V rows, so that a stage's K is refilled as soon as its QK product is
+    // done, before its V.  Table mode and short chunks keep every gather
+    // warp on both (the split roles measured slower there).
     if (tid == 0) {
         for (int i = 0; i < kKvStages; ++i) {
-            mbar_init(smem_addr(&bars[kKvFull + i]), kLoadThreads + kLoadWarps);  // + one byte-count arrival per warp
-            mbar_init(smem_addr(&bars[kKvEmpty + i]), 1);
+            // cp.async completions of the warps feeding the barrier plus one
+            // byte-count arrival per such warp
+            constexpr uint32_t n_full = kSplit ? kLoadThreads / 2 + kLoadWarps / 2 : kLoadThreads + kLoadWarps;
+            mbar_init(smem_addr(&bars[kKFull + i]), n_full);
+            mbar_init(smem_addr(&bars[kVFull + i]), n_full);
+            mbar_init(smem_addr(&bars[kKEmpty + i]), 1);
+            mbar_init(smem_addr(&bars[kVEmpty + i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_addr(&bars[kSFull + i]), 1);
@@ -300,6 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         // swizzled layout.  The stage barrier counts the 128 cp.async
         // arrivals and one byte-count arrival per warp.
         const int lw = warp - kSoftWarps;  // gather warp index
+        // split: warps 0-1 copy K, 2-3 V, each one 8-key group in two;
+        // otherwise every warp copies K and V of one 8-key group in four
+        const bool is_v = kSplit && lw >= kLoadWarps / 2;
+        constexpr int n_roles = kSplit ? kLoadWarps / 2 : kLoadWarps;
+        const int hw = kSplit ? lw % (kLoadWarps / 2) : lw;
         const uint8_t *kbase = reinterpret_cast<const uint8_t *>(k_pool) + (size_t)g * D * 2;
         const uint8_t *vbase = reinterpret_cast<const uint8_t *>(v_pool) + (size_t)g * D * 2;
         const size_t slot_bytes = (size_t)H_kv * D * 2;
@@ -330,12 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         for (int t = 0; t < 2 * n_tiles; ++t) {  // copy stages; keys past cnt are zero-filled
             const int st = t % kKvStages;
             if (t >= kKvStages &&
-                !mbar_wait(&bars[kKvEmpty + st], ((t / kKvStages) - 1) & 1, flags))
+                !mbar_wait(&bars[(is_v ? kVEmpty : kKEmpty) + st], ((t / kKvStages) - 1) & 1, flags))
                 break;
             if (flags[0]) break;
             const uint32_t kt = sbase + C::kKOff + st * (kCopyKeys * 128);
             const uint32_t vt = sbase + C::kVOff + st * (kCopyKeys * 128);
-            const uint32_t bar = smem_addr(&bars[kKvFull + st]);
+            const uint32_t bar = smem_addr(&bars[(is_v ? kVFull : kKFull) + st]);
+            // split: this warp's operand (xt, its pool and maps); both otherwise
+            const uint32_t xt = is_v ? vt : kt;
             const int64_t kk = (int64_t)t * kCopyKeys + lane;
             int64_t slot = 0;
             bool ok = false;
@@ -353,12 +378,20 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
             const bool whole = __all_sync(0xffffffffu, ok && (lane == 0 || slot == prev + 1));
             if (whole) {
                 const int64_t slot0 = __shfl_sync(0xffffffffu, slot, 0);
-                if (lane == 0 && lw == 0) {
-                    mbar_arrive_expect_tx(bar, 2u * C::kCopyBytes);
+                if (lane == 0 && hw == 0) {
+                    if constexpr (kSplit) {
+                        mbar_arrive_expect_tx(bar, (uint32_t)C::kCopyBytes);
 #pragma unroll
-                    for (int db = 0; db < C::kDimBlocks; ++db) {
-                        tma_load_3d(kt + db * C::kRingBlockBytes, &tm_k32, db * 64, g, (int32_t)slot0, bar);
-                        tma_load_3d(vt + db * C::kRingBlockBytes, &tm_v32, db * 64, g, (int32_t)slot0, bar);
+                        for (int db = 0; db < C::kDimBlocks; ++db)
+                            tma_load_3d(xt + db * C::kRingBlockBytes, is_v ? &tm_v32 : &tm_k32, db * 64, g,
+                                        (int32_t)slot0, bar);
+                    } else {
+                        mbar_arrive_expect_tx(bar, 2u * C::kCopyBytes);
+#pragma unroll
+                        for (int db = 0; db < C::kDimBlocks; ++db) {
+                            tma_load_3d(kt + db * C::kRingBlockBytes, &tm_k32, db * 64, g, (int32_t)slot0, bar);
+                            tma_load_3d(vt + db * C::kRingBlockBytes, &tm_v32, db * 64, g, (int32_t)slot0, bar);
+                        }
                     }
                 } else if (lane == 0) {
                     mbar_arrive(bar);
@@ -373,20 +406,28 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
 #pragma unroll
                 for (int gi = 0; gi < kCopyKeys / 8; ++gi) {
                     const uint32_t gm = 0xffu << (gi * 8);
-                    if (gi % kLoadWarps == lw && (okm & gm) == gm && (contm & gm) == gm) tma_groups |= 1u << gi;
+                    if (gi % n_roles == hw && (okm & gm) == gm && (contm & gm) == gm) tma_groups |= 1u << gi;
                 }
                 if (lane == 0)
-                    mbar_arrive_expect_tx(bar, (uint32_t)__popc(tma_groups) * 2u * 8u * (uint32_t)(D * 2));
+                    mbar_arrive_expect_tx(bar, (uint32_t)__popc(tma_groups) * (kSplit ? 1u : 2u) * 8u *
+                                                   (uint32_t)(D * 2));
 #pragma unroll
                 for (int gi = 0; gi < kCopyKeys / 8; ++gi) {
-                    if (gi % kLoadWarps != lw) continue;
+                    if (gi % n_roles != hw) continue;
                     if ((tma_groups >> gi) & 1u) {
                         const int64_t gs = __shfl_sync(0xffffffffu, slot, gi * 8);
                         if (lane == 0) {
 #pragma unroll
                             for (int db = 0; db < C::kDimBlocks; ++db) {
-                                tma_load_3d(kt + db * C::kRingBlockBytes + gi * 1024, &tm_k8, db * 64, g, (int32_t)gs, bar);
-                                tma_load_3d(vt + db * C::kRingBlockBytes + gi * 1024, &tm_v8, db * 64, g, (int32_t)gs, bar);
+                                if constexpr (kSplit) {
+                                    tma_load_3d(xt + db * C::kRingBlockBytes + gi * 1024, is_v ? &tm_v8 : &tm_k8,
+                                                db * 64, g, (int32_t)gs, bar);
+                                } else {
+                                    tma_load_3d(kt + db * C::kRingBlockBytes + gi * 1024, &tm_k8, db * 64, g,
+                                                (int32_t)gs, bar);
+                                    tma_load_3d(vt + db * C::kRingBlockBytes + gi * 1024, &tm_v8, db * 64, g,
+                                                (int32_t)gs, bar);
+                                }
                             }
                         }
                     } else {
@@ -400,8 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                             const size_t off = kok ? (size_t)sl * slot_bytes + c * 16 : 0;
                             const int db = c >> 3, cb = c & 7;
                             const uint32_t dst = db * C::kRingBlockBytes + kr * 128 + ((cb ^ (kr & 7)) << 4);
-                            cp_async_16(kt + dst, kbase + off, kok ? 16u : 0u, keep);
-                            cp_async_16(vt + dst, vbase + off, kok ? 16u : 0u, keep);
+                            if constexpr (kSplit) {
+                                cp_async_16(xt + dst, (is_v ? vbase : kbase) + off, kok ? 16u : 0u, keep);
+                            } else {
+                                cp_async_16(kt + dst, kbase + off, kok ? 16u : 0u, keep);
+                                cp_async_16(vt + dst, vbase + off, kok ? 16u : 0u, keep);
+                            }
                         }
                     }
                 }
@@ -419,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                 const int s0 = (2 * t) % kKvStages, sb = t & 1;
                 const uint32_t ph = (uint32_t)((2 * t) / kKvStages) & 1u;
                 if (t == 0 && !mbar_wait(&bars[kQFull], 0, flags)) return false;
-                if (!mbar_wait(&bars[kKvFull + s0], ph, flags)) return false;
-                if (!mbar_wait(&bars[kKvFull + s0 + 1], ph, flags)) return false;
+                if (!mbar_wait(&bars[kKFull + s0], ph, flags)) return false;
+                if (!mbar_wait(&bars[kKFull + s0 + 1], ph, flags)) return false;
                 // S buffer sb last held P of tile t-2: its PV must be done
                 if (t >= 2 && !mbar_wait(&bars[kPvDone + sb], ((t >> 1) - 1) & 1, flags)) return false;
                 fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
@@ -432,6 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                                    tc_smem_desc_sw128(kt + (kk / 4) * C::kRingBlockBytes + (kk % 4) * 32, 16, 1024),
                                    idesc_qk, kk > 0);
                 tc_commit(smem_addr(&bars[kSFull + sb]));
+                if constexpr (kSplit) {
+                    // the stage pair's K rows are free once this product is done
+                    tc_commit(smem_addr(&bars[kKEmpty + s0]));
+                    tc_commit(smem_addr(&bars[kKEmpty + s0 + 1]));
+                }
                 return true;
             };
             bool live = n_tiles == 0 || issue_qk(0);
@@ -439,8 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                 if (t + 1 < n_tiles && !issue_qk(t + 1)) break;
                 const int pb = t & 1;
                 if (!mbar_wait(&bars[kPFull + pb], (t >> 1) & 1, flags)) break;
-                tc_fence_after();
                 const int s0 = (2 * t) % kKvStages;
+                if constexpr (kSplit) {
+                    const uint32_t vph = (uint32_t)((2 * t) / kKvStages) & 1u;
+                    if (!mbar_wait(&bars[kVFull + s0], vph, flags)) break;
+                    if (!mbar_wait(&bars[kVFull + s0 + 1], vph, flags)) break;
+                    fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
+                }
+                tc_fence_after();
                 const uint32_t vt = sbase + C::kVOff + s0 * (kCopyKeys * 128);
                 // P was written over S buffer pb: head in its first half, tail in the second
                 const uint32_t p_hi = tmem + pb * kKeys, p_lo = p_hi + kKeys / 2;
@@ -451,8 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                     tc_mma_bf16_ta(tmem + C::kOCol, p_lo + kk * 8, vd, idesc_pv, 1);
                 }
                 tc_commit(smem_addr(&bars[kPvDone + pb]));
-                tc_commit(smem_addr(&bars[kKvEmpty + s0]));
-                tc_commit(smem_addr(&bars[kKvEmpty + s0 + 1]));
+                tc_commit(smem_addr(&bars[(kSplit ? kVEmpty : kKEmpty) + s0]));
+                tc_commit(smem_addr(&bars[(kSplit ? kVEmpty : kKEmpty) + s0 + 1]));
             }
         }
     } else {
@@ -969,7 +1025,7 @@ int tree_resident_capacity(int dev) {
     if (known[dev]) return known[dev] > 0 ? known[dev] : 0;
     int sms = 0, per_sm = 0;
     const bool ok = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tree_tc_kernel<D>, kThreads,
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tree_tc_kernel<D, true>, kThreads,
                                                                   Cfg<D>::kSmemBytes) == cudaSuccess &&
                     sms > 0 && per_sm > 0;
     cudaGetLastError();
@@ -994,7 +1050,7 @@ bool tree_cluster_ok(int dev, int n) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    const bool ok = cudaOccupancyMaxActiveClusters(&clusters, tree_tc_kernel<D>, &cfg) == cudaSuccess &&
+    const bool ok = cudaOccupancyMaxActiveClusters(&clusters, tree_tc_kernel<D, true>, &cfg) == cudaSuccess &&
                     clusters > 0;
     cudaGetLastError();  // a refused query is not an error of this call
     known[dev][n] = ok ? 1 : -1;
@@ -1017,7 +1073,9 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return WMTP_ECUDA;
     if (!opted_in[dev]) {
-        if (cudaFuncSetAttribute(tree_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(tree_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(tree_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes) != cudaSuccess)
             return WMTP_ECUDA;
         opted_in[dev] = 1;
@@ -1051,8 +1109,12 @@ wmtp_status launch_tree_tc(const uint16_t *q, int32_t B, int32_t H_q, int32_t H_
     PdlLaunch launch(dim3((unsigned)n_split, (unsigned)(H_kv * n_rb), (unsigned)B), dim3(kThreads),
                      C::kSmemBytes, stream);
     if (use_cluster) launch.add_cluster((unsigned)n_split);
+    // ring mode with long chunks: the instance with split K / V gather roles
+    const int64_t ring_keys = (int64_t)n_sink + window + (int64_t)depth * tree_k;
+    const int64_t chunk_tiles = (ring_keys + (int64_t)n_split * kKeys - 1) / ((int64_t)n_split * kKeys);
+    auto kernel = !tt.table && chunk_tiles >= kSplitMinTiles ? tree_tc_kernel<D, true> : tree_tc_kernel<D, false>;
     const cudaError_t err = cudaLaunchKernelEx(
-        &launch.cfg, tree_tc_kernel<D>, reinterpret_cast<const __nv_bfloat16 *>(q), H_q, H_kv, G,
+        &launch.cfg, kernel, reinterpret_cast<const __nv_bfloat16 *>(q), H_q, H_kv, G,
         n_nodes, reinterpret_cast<const __nv_bfloat16 *>(k_pool),
         reinterpret_cast<const __nv_bfloat16 *>(v_pool), num_slots, seq_lens, ring_base, n_sink,
         window, depth, tree_k, scale * 1.4426950408889634f, out, lse, ws, tt, n_split, n_rb,

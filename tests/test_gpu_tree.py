@@ -120,3 +120,17 @@ def test_tree_workspace_merges(D, H_q, H_kv):
         out, lse = _check(S_list, n_sink, W, d, k, H_q, H_kv, D, seed=900 + n_split, n_split=n_split)
         out2, lse2 = _check(S_list, n_sink, W, d, k, H_q, H_kv, D, seed=900 + n_split, n_split=n_split)
         assert torch.equal(out, out2) and torch.equal(lse, lse2), f"split={n_split} not repeatable"
+
+
+@pytest.mark.parametrize("D,H_q,H_kv", [(256, 16, 2), (128, 8, 2)])
+def test_tree_long_chunks(D, H_q, H_kv):
+    # chunks of 16 MMA tiles or more (the instance whose gather warps copy K
+    # and V rows separately): one chunk, cluster-merged chunks, and 12 / 16
+    # chunks merged slice by slice; a request past the window and one inside
+    # it (its chunks end early or are empty); sampled rows against the oracle
+    n_sink, W, d, k = 64, 16_384, 7, 4
+    S_list = [300_000, 9_000]
+    n_rows = len(S_list) * k * d * H_q
+    rows = np.random.default_rng(D).choice(n_rows, 384, replace=False)
+    for n_split in (1, 5, 12, 16):
+        _check(S_list, n_sink, W, d, k, H_q, H_kv, D, seed=1300 + n_split, n_split=n_split, rows=rows)
