@@ -87,6 +87,16 @@ constexpr uint64_t kWsWaitNs = 2000000000ull;
 // The consumer warps' CTA barrier (named barrier 1, 128 threads): in a
 // warp-specialised CTA the producer warp has left by then.
 __device__ __forceinline__ void sync_consumers() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// The same barrier, returning how many of the consumer threads passed p.
+__device__ __forceinline__ int sync_consumers_count(bool p) {
+    int n;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.popc.u32 %0, 1, 128, q;\n\t}"
+        : "=r"(n)
+        : "r"((uint32_t)p)
+        : "memory");
+    return n;
+}
 
 #ifndef WMTP_FP8_STAGES
 #define WMTP_FP8_STAGES 6
@@ -1214,11 +1224,21 @@ __global__ void __launch_bounds__(kWs ? kWsThreads : kThreads, 1) split_decode_k
         };
         if (mine) slice_merge(split);
         if (last) {
-            for (int s2 = tid; s2 < n_split; s2 += kThreads)
-                claim[s2] = (s2 != split && atomicCAS(ctr + 2 + s2, 0, 2) == 0) ? 1 : 0;
-            sync_consumers();
-            for (int s2 = 0; s2 < n_split; ++s2)
-                if (claim[s2]) slice_merge(s2);
+            // a plain load first: a claimed word (every one, unless a CTA
+            // gave up waiting) needs no compare-and-swap
+            bool any = false;
+            for (int s2 = tid; s2 < n_split; s2 += kThreads) {
+                const bool c = s2 != split && ld_acquire_gpu(ctr + 2 + s2) == 0 &&
+                               atomicCAS(ctr + 2 + s2, 0, 2) == 0;
+                claim[s2] = c ? 1 : 0;
+                any |= c;
+            }
+            // normally nothing is left: then skip the scan over the slices
+            // (n_split iterations around an inlined merge took ~5 us on the
+            // launch's critical path even when none was claimed)
+            if (sync_consumers_count(any) > 0)
+                for (int s2 = 0; s2 < n_split; ++s2)
+                    if (claim[s2]) slice_merge(s2);
         }
         sync_consumers();
         if (tid == 0 && atomicAdd(ctr + 1, 1) == n_split - 1)

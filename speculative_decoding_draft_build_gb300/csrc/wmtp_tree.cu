@@ -904,11 +904,21 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
         };
         if (mine) slice_merge(split);
         if (is_last) {
-            for (int s2 = tid; s2 < n_split; s2 += kThreads)
-                claim[s2] = (s2 != split && atomicCAS(ctr + 2 + s2, 0, 2) == 0) ? 1 : 0;
-            __syncthreads();
-            for (int s2 = 0; s2 < n_split; ++s2)
-                if (claim[s2]) slice_merge(s2);
+            // a plain load first: a claimed word (every one, unless a CTA
+            // gave up waiting) needs no compare-and-swap
+            bool any = false;
+            for (int s2 = tid; s2 < n_split; s2 += kThreads) {
+                const bool c = s2 != split && ld_acquire_gpu(ctr + 2 + s2) == 0 &&
+                               atomicCAS(ctr + 2 + s2, 0, 2) == 0;
+                claim[s2] = c ? 1 : 0;
+                any |= c;
+            }
+            // normally nothing is left: then skip the scan over the slices
+            // (n_split iterations around an inlined merge took ~5 us on the
+            // launch's critical path even when none was claimed)
+            if (__syncthreads_count(any) > 0)
+                for (int s2 = 0; s2 < n_split; ++s2)
+                    if (claim[s2]) slice_merge(s2);
         }
         __syncthreads();
         if (tid == 0 && atomicAdd(ctr + 1, 1) == n_split - 1)
