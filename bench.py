@@ -545,7 +545,7 @@ def run_ours(args, dist_ctx):
     result["mass_diagnostics"] = measure_mass(w, dev)
     if args.workload == "1m" and not args.no_tree:
         result["tree"] = measure_tree(args, dev)
-    if args.workload == "1m" and not args.no_extend:
+    if not args.no_extend:
         result["extend"] = measure_extend(w, args, dev)
     if not args.no_fp8:
         result["fp8"] = measure_fp8(w, args, dev)
@@ -842,9 +842,9 @@ def measure_mass(w, dev):
 
 
 def measure_extend(w, args, dev):
-    """Draft-extend pass on the million-token workload: the draft forward over
-    n_new = 5 accepted tokens (positions S..S+4) in one launch, windowed and
-    full-context.  Event-timed with L2 flushed before each launch; algorithmic
+    """Draft-extend pass on the bench's workload (the million-token one by
+    default): the draft forward over n_new = 5 accepted tokens (positions
+    S..S+4) in one launch, windowed and full-context.  Event-timed with L2 flushed before each launch; algorithmic
     bytes are the pass's unique bytes: K and V of every key of the union table
     once (every KV head), the table, q, out and lse.  `token_reads_gbs` counts
     instead each token's own key set (the tokens of a request share most of
@@ -891,7 +891,7 @@ def measure_extend(w, args, dev):
         token_bytes = B * (keys * H_kv * D * 2 * 2 + rest)
         stride = tab.shape[-1]
         if 2 <= n <= 8 and ns <= 128 and stride >= 65536:
-            kernel = f"tree_tc_kernel<{D}> (tcgen05, union table row)"
+            kernel = f"tree_tc_kernel<{D}, false> (tcgen05, union table row, combined gather roles)"
         elif 2 <= n <= 8 and ns <= 128 and stride >= 1024 * ns:
             kernel = f"extend_kernel<{D}> (one K/V read for all tokens)"
         else:
