@@ -431,8 +431,11 @@ __global__ void __launch_bounds__(kThreads, 1) tree_tc_kernel(
                             }
                         }
                     } else {
-                        // 8 keys x D/8 16-byte chunks over 32 lanes
-#pragma unroll 4
+                        // 8 keys x D/8 16-byte chunks over 32 lanes; kept
+                        // rolled: its code shares the instruction cache with
+                        // the other roles' (unrolled by four, the table-mode
+                        // pass over a 1M union ran ~20% slower)
+#pragma unroll 1
                         for (int idx = lane; idx < 8 * (D / 8); idx += 32) {
                             const int kr = gi * 8 + (idx >> (D == 256 ? 5 : 4));
                             const int c = idx & (D / 8 - 1);
